@@ -1,0 +1,138 @@
+"""fp64 CPU oracle for Parallax attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference arm may import this package.  The CUDA product path never imports
+it, and it imports nothing from the product package.
+
+The arithmetic lives in ``parallax_oracle.c`` (plain loops, fp64, OpenMP over
+rows); this module only marshals numpy arrays.  Each function follows the
+definition in the Parallax news pages ("Parallax mantem softmax ...",
+paragraph 2; "Parallax garde softmax ...", paragraph 2): the output is softmax
+attention minus the key/value covariance multiplied by the probe
+``rho_i = W_R x_i``; ``W_R = 0`` (``rho=None``) gives plain softmax attention.
+
+Forms: ``"explicit"`` (d x d covariance, centered two-pass), ``"contracted"``
+(rho contracted into the centered key side first, O(n d) per row) and
+``"uncentered"`` (one pass of raw moments).  All three are the same function
+of the inputs up to rounding.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "parallax_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+FORMS = {"explicit": 0, "contracted": 1, "uncentered": 2}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``parallax_oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            dp = ctypes.POINTER(ctypes.c_double)
+            i64 = ctypes.c_int64
+            lib.oracle_rows.argtypes = [dp, dp, dp, dp, ctypes.POINTER(i64), i64, i64, i64,
+                                        ctypes.c_double, ctypes.c_int, dp]
+            lib.oracle_prefill.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64, ctypes.c_int,
+                                           ctypes.c_double, ctypes.c_int, dp]
+            lib.oracle_decode.argtypes = [dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int32), i64,
+                                          i64, i64, i64, ctypes.c_double, ctypes.c_int, dp]
+            for f in (lib.oracle_rows, lib.oracle_prefill, lib.oracle_decode):
+                f.restype = ctypes.c_int
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x):
+    """Widen to a contiguous float64 numpy array (torch tensors are moved to the CPU)."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor: widen exactly on the host
+        import torch
+
+        x = x.detach().to("cpu", torch.float64).contiguous().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops use on this host."""
+    return int(_load().oracle_num_threads())
+
+
+def prefill(q, rho, k, v, causal: bool = True, scale: float | None = None,
+            form: str = "explicit") -> np.ndarray:
+    """Parallax prefill rows; q, rho, k, v are [B, H, L, d]; rho=None means W_R = 0."""
+    q, rho, k, v = _f64(q), _f64(rho), _f64(k), _f64(v)
+    B, H, L, d = q.shape
+    assert k.shape == v.shape == q.shape and (rho is None or rho.shape == q.shape)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.empty_like(q)
+    rc = _load().oracle_prefill(_ptr(q), _ptr(rho), _ptr(k), _ptr(v), B, H, L, d,
+                                1 if causal else 0, float(scale), FORMS[form], _ptr(o))
+    if rc != 0:
+        raise RuntimeError(f"oracle_prefill failed ({rc})")
+    return o
+
+
+def decode(q, rho, k_cache, v_cache, seqlens, scale: float | None = None,
+           form: str = "explicit") -> np.ndarray:
+    """Parallax single-token decode; q, rho [B, H, d], caches [B, H, Lmax, d], seqlens [B]."""
+    q, rho, kc, vc = _f64(q), _f64(rho), _f64(k_cache), _f64(v_cache)
+    if hasattr(seqlens, "detach"):
+        seqlens = seqlens.detach().cpu().numpy()
+    sl = np.ascontiguousarray(seqlens, dtype=np.int32)
+    B, H, Lmax, d = kc.shape
+    assert q.shape == (B, H, d) and vc.shape == kc.shape and sl.shape == (B,)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.empty_like(q)
+    rc = _load().oracle_decode(_ptr(q), _ptr(rho), _ptr(kc), _ptr(vc),
+                               sl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), B, H, Lmax, d,
+                               float(scale), FORMS[form], _ptr(o))
+    if rc != 0:
+        raise RuntimeError(f"oracle_decode failed ({rc})")
+    return o
+
+
+def rows(q, rho, k, v, nkeys, scale: float, form: str = "explicit") -> np.ndarray:
+    """Rows that share one key set: q, rho [nq, d]; k, v [nk, d]; row i uses keys < nkeys[i]."""
+    q, rho, k, v = _f64(q), _f64(rho), _f64(k), _f64(v)
+    nq, d = q.shape
+    nk = k.shape[0]
+    nkeys = np.ascontiguousarray(nkeys, dtype=np.int64)
+    assert nkeys.shape == (nq,) and k.shape == v.shape == (nk, d)
+    o = np.empty_like(q)
+    rc = _load().oracle_rows(_ptr(q), _ptr(rho), _ptr(k), _ptr(v),
+                             nkeys.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), nq, nk, d,
+                             float(scale), FORMS[form], _ptr(o))
+    if rc != 0:
+        raise RuntimeError(f"oracle_rows failed ({rc})")
+    return o
