@@ -1,0 +1,449 @@
+#!/usr/bin/env python3
+"""Benchmark of the Parallax attention forward hot path (one JSON line on stdout).
+
+A step is one pass of the whole hot path over synthetic inputs resident in HBM:
+  * single-token decode, bf16 KV cache, B=64, H=16, d=128, 8192 keys per head
+    (split-KV decode kernel + log-sum-exp combine), and
+  * causal prefill, bf16, B=8, H=16, L=4096, d=128, with q, k, v, rho produced
+    by random projections of x (width 2048) (tcgen05 tensor-core kernel).
+`value` is the decode KV-stream bandwidth (GB/s); the prefill throughput
+(TFLOP/s) is reported in the `prefill` object.  Both kernels also get a
+roofline entry against the measured B300 peaks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on the host cores, on bounded samples of the same decode workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode KV-stream GB/s (% B300 HBM peak); causal prefill TFLOP/s (% TC peak)"
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
+# ncu captures summarised in profiles/; None until a capture of the current
+# kernel exists.
+TRAFFIC_BYTES = {"decode": None, "prefill": None}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- workloads
+def decode_bytes(B, H, n, d, elem=2):
+    kv = 2 * B * H * n * d * elem                 # K and V rows streamed once
+    io = 2 * B * H * d * elem + B * H * d * 4 + B * 4  # q, rho in; o out; seqlens
+    return kv, kv + io
+
+
+def prefill_flops(B, H, L, d):
+    # four causal contractions (S, R, U, W), each 2*d flop per (query, visible key)
+    return 8.0 * d * (L * (L + 1) / 2) * B * H
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock / throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", self.gpu_id], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self, max_mhz_hint=None):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": max_mhz_hint, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v == "Active"})
+        busy = [r for r in rows if r[2] > 250.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": rows[0][1],
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def cpu_oracle_decode_sample(inp, target_s: float, max_batches: int = 64):
+    """Time the fp64 oracle (explicit covariance form, OpenMP over heads) on the first
+    b sequences of the decode workload; b grows until about target_s of CPU work."""
+    import numpy as np
+
+    import oracle
+
+    B, H, Lmax, d = inp.k_cache.shape
+    n = int(inp.seqlens[0])
+
+    def host(b):
+        return [np.ascontiguousarray(t[:b].to("cpu").double().numpy()) for t in
+                (inp.q, inp.rho, inp.k_cache, inp.v_cache)] + [inp.seqlens[:b].cpu().numpy()]
+
+    b = 1
+    while True:
+        q, rho, kc, vc, sl = host(b)
+        t0 = time.perf_counter()
+        oracle.decode(q, rho, kc, vc, sl, form="explicit")
+        dt = time.perf_counter() - t0
+        if dt >= 0.25 * target_s or b >= max_batches:
+            break
+        b = min(max_batches, max(b + 1, int(b * min(8.0, 0.6 * target_s / max(dt, 1e-3)))))
+    _, total = decode_bytes(b, H, n, d)
+    return {"value": total / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{b * H} of {B * H} heads x {n} keys (explicit d x d covariance, fp64), "
+                      f"{dt:.2f} s"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    import oracle
+    from softmax_covariance_correction_pass_b300 import configs
+
+    c = configs.DECODE_UNIFORM
+    B, H, d, n = c["B"], c["H"], c["d"], c["ctx"]
+    # the same seeded workload, drawn on the host
+    inp = configs.decode_inputs(B, H, d, n, n, c["seed"], c["rho_std"], device="cpu")
+    q = inp.q.double().numpy()
+    rho = inp.rho.double().numpy()
+    # per step: one sequence (H heads) of the workload, cycling through the batch;
+    # keep the whole run to about two minutes
+    t0 = time.perf_counter()
+    oracle.decode(q[:1], rho[:1], inp.k_cache[:1].double().numpy(),
+                  inp.v_cache[:1].double().numpy(), inp.seqlens[:1].numpy(), form="explicit")
+    t_one = time.perf_counter() - t0
+    heads_per_step = H
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    keys = n if t_one <= budget else max(256, int(n * budget / t_one) // 256 * 256)
+    kh = [inp.k_cache[b:b + 1, :, :keys].double().numpy() for b in range(min(B, 8))]
+    vh = [inp.v_cache[b:b + 1, :, :keys].double().numpy() for b in range(min(B, 8))]
+    sl = np.full(1, keys, dtype=np.int32)
+    times = []
+    for s in range(args.warmup + args.steps):
+        b = s % len(kh)
+        t0 = time.perf_counter()
+        oracle.decode(q[b:b + 1], rho[b:b + 1], kh[b], vh[b], sl, form="explicit")
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    _, per_step = decode_bytes(1, H, keys, d)
+    total_t = sum(times)
+    value = per_step * len(times) / total_t / 1e9
+    sample = (f"per step {heads_per_step} heads x {keys} keys of the B=64 H=16 d=128 ctx=8192 "
+              "decode workload (explicit covariance, fp64)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_t / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": configs.DECODE_UNIFORM["name"], "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import softmax_covariance_correction_pass_b300 as px
+    from softmax_covariance_correction_pass_b300 import configs
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    px.load_library()
+    peaks = load_peaks()
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if ws == 1:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- inputs resident in HBM
+    dc = configs.DECODE_UNIFORM
+    dinp = configs.decode_uniform_inputs(dev)
+    B, H, d, n = dc["B"], dc["H"], dc["d"], dc["ctx"]
+    do = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    pc = configs.LAYER_PREFILL
+    pinp = configs.layer_prefill_inputs(dev)
+    PB, PH, PL, Pd = pc["B"], pc["H"], pc["L"], pc["d"]
+    po = torch.empty((PB, PH, PL, Pd), dtype=torch.float32, device=dev)
+    kv_bytes, dec_bytes = decode_bytes(B, H, n, d)
+    pre_flops = prefill_flops(PB, PH, PL, Pd)
+    chunk = px.parallax_attn_decode_chunk_keys(B, H, n, d, 2)
+    dec_launches = 2 if chunk < n else 1
+
+    def decode():
+        px.parallax_attn_decode(dinp.q, dinp.rho, dinp.k_cache, dinp.v_cache, dinp.seqlens, do)
+
+    def prefill():
+        px.parallax_attn_prefill(pinp.q, pinp.rho, pinp.k, pinp.v, po, causal=True,
+                                 scale=pinp.scale)
+
+    for _ in range(max(args.warmup, 3)):
+        decode()
+        prefill()
+    torch.cuda.synchronize()
+    if px.parallax_check_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- timed region: K steps, per-kernel events on the launching stream
+    K = args.steps
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(dev.index)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as clocks:
+        t_start.record(stream)
+        for k in range(K):
+            ev[k][0].record(stream)
+            decode()
+            ev[k][1].record(stream)
+            ev[k][2].record(stream)
+            prefill()
+            ev[k][3].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    pre_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / K
+    total_ms = max_over_ranks(total_ms)
+    dec_ms = max_over_ranks(dec_ms)
+    pre_ms = max_over_ranks(pre_ms)
+    if px.parallax_check_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    pre_tflops = pre_flops / (pre_ms * 1e-3) / 1e12
+    value = ws * dec_bytes / (dec_ms * 1e-3) / 1e9  # whole job: all replicas' bytes / max time
+
+    roof_dec = {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": dec_gbs / peaks["hbm_gbs"], "traffic": TRAFFIC_BYTES["decode"],
+                "kernel": "decode_kernel (+ combine_kernel)",
+                "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_ms,
+                "peak_source": peaks["source"]}
+    roof_pre = {"bound": "tensor", "achieved": pre_tflops, "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": pre_tflops / peaks["bf16_tflops_sustained"],
+                "traffic": TRAFFIC_BYTES["prefill"], "kernel": "prefill_tc_kernel",
+                "algorithmic_flops_per_launch": pre_flops, "avg_launch_ms": pre_ms,
+                "peak_burst": peaks["bf16_tflops"],
+                "frac_burst": pre_tflops / peaks["bf16_tflops"],
+                "peak_source": peaks["source"] + " (sustained)"}
+    dominant = roof_pre if pre_ms >= dec_ms else roof_dec
+
+    # ---- W_R = 0 fast paths (rho = NULL), for context
+    f0 = {}
+    for name, fn, units in (
+            ("decode_gbs", lambda: px.parallax_attn_decode(dinp.q, None, dinp.k_cache,
+                                                           dinp.v_cache, dinp.seqlens, do),
+             dec_bytes / 1e9),
+            ("prefill_tflops_softmax_only", lambda: px.parallax_attn_prefill(
+                pinp.q, None, pinp.k, pinp.v, po, causal=True, scale=pinp.scale),
+             pre_flops / 2 / 1e12)):
+        fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(20):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        f0[name] = units / (a.elapsed_time(b) / 20 * 1e-3)
+
+    # ---- end to end through the public call, host buffers (pinned), copies timed
+    e2e = None
+    e2e_prefill = None
+    if not args.no_e2e:
+        hq = [t.to("cpu").pin_memory() for t in (dinp.q, dinp.rho, dinp.k_cache, dinp.v_cache,
+                                                  dinp.seqlens)]
+        ho = torch.empty((B, H, d), dtype=torch.float32).pin_memory()
+        dq = [torch.empty_like(t, device=dev) for t in hq]
+        h2d = sum(t.numel() * t.element_size() for t in hq)
+        d2h = ho.numel() * ho.element_size()
+
+        def e2e_step():
+            for src, dst in zip(hq, dq):
+                dst.copy_(src, non_blocking=True)
+            px.parallax_attn_decode(dq[0], dq[1], dq[2], dq[3], dq[4], do)
+            ho.copy_(do, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / args.e2e_steps)
+        e2e = {"value": ws * dec_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        del hq, dq
+
+        hp = [t.to("cpu").pin_memory() for t in (pinp.q, pinp.rho, pinp.k, pinp.v)]
+        hpo = torch.empty_like(po, device="cpu").pin_memory()
+        dp = [torch.empty_like(t, device=dev) for t in hp]
+
+        def e2e_prefill_step():
+            for src, dst in zip(hp, dp):
+                dst.copy_(src, non_blocking=True)
+            px.parallax_attn_prefill(dp[0], dp[1], dp[2], dp[3], po, causal=True,
+                                     scale=pinp.scale)
+            hpo.copy_(po, non_blocking=True)
+
+        e2e_prefill_step()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_prefill_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ep_ms = max_over_ranks(a.elapsed_time(b) / args.e2e_steps)
+        e2e_prefill = {"value": ws * pre_flops / (ep_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hp),
+                       "d2h_bytes_per_step": hpo.numel() * hpo.element_size(),
+                       "ms_per_step": ep_ms}
+        del hp, dp
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_decode_sample(dinp, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": configs.DECODE_UNIFORM["name"] + " + " + configs.LAYER_PREFILL["name"],
+                "decode": {"B": B, "H": H, "d": d, "context": n, "chunk_keys": chunk,
+                           "kv_bytes": kv_bytes, "tokens_per_s": ws * B / (dec_ms * 1e-3)},
+                "prefill": {"B": PB, "H": PH, "L": PL, "d": Pd, "causal": True,
+                            "tokens_per_s": ws * PB * PL / (pre_ms * 1e-3)},
+                "l2": "inputs larger than L2 (4.3 GB KV cache; 1.07 GB of prefill tensors)",
+                "parallelism": f"replicas x{ws} (no collectives)"},
+            "roofline": dominant,
+            "roofline_decode": roof_dec,
+            "roofline_prefill": roof_pre,
+            "prefill": {"metric": "causal prefill TFLOP/s", "value": ws * pre_tflops,
+                        "unit": "TFLOP/s", "frac_of_peak": roof_pre["frac"],
+                        "ms_per_launch": pre_ms, "e2e": e2e_prefill},
+            "decode": {"metric": "decode KV-stream GB/s", "value": value, "unit": "GB/s",
+                       "frac_of_peak": roof_dec["frac"], "ms_per_call": dec_ms},
+            "w_r_zero_fast_path": f0,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clocks.summary(),
+            "gpu_launches": K * (dec_launches + 1),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

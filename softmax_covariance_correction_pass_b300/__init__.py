@@ -1,0 +1,181 @@
+"""Parallax attention forward hot path for B300 (sm_103a).
+
+Thin ctypes binding over ``libparallax_attn.so`` (C ABI declared in
+``include/parallax_attn.h``).  This module only marshals arguments: every step
+of the computation runs in the library's CUDA kernels.  There is no CPU path;
+if the library is missing the import of the binding fails loudly.
+
+Functions carry the C names (``parallax_attn_prefill``, ...), with short
+aliases ``prefill`` / ``decode``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libparallax_attn.so")
+
+PARALLAX_OK = 0
+PARALLAX_ERR_INVALID = -1
+PARALLAX_ERR_UNSUPPORTED = -2
+PARALLAX_ERR_CUDA = -3
+PARALLAX_ERR_DEVICE = -4
+DEVERR_SEQLEN_CLAMPED = 0x1
+DEVERR_WAIT_TIMEOUT = 0x2
+
+_lib = None
+
+
+class ParallaxError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"parallax error {code}: {msg}")
+        self.code = code
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the in-tree CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m softmax_covariance_correction_pass_b300.build` (no CPU fallback exists)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.parallax_attn_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+    lib.parallax_attn_prefill_f32.argtypes = lib.parallax_attn_prefill.argtypes
+    lib.parallax_attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    lib.parallax_attn_decode_f32.argtypes = lib.parallax_attn_decode.argtypes
+    lib.parallax_attn_decode_chunk_keys.argtypes = [i32, i32, i32, i32, i32]
+    lib.parallax_attn_set_decode_chunk_keys.argtypes = [i32]
+    lib.parallax_attn_workspace_bytes.restype = ctypes.c_size_t
+    lib.parallax_last_error.restype = ctypes.c_char_p
+    lib.parallax_check_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    for name in ("parallax_attn_prefill", "parallax_attn_prefill_f32", "parallax_attn_decode",
+                 "parallax_attn_decode_f32", "parallax_attn_decode_chunk_keys",
+                 "parallax_attn_set_decode_chunk_keys", "parallax_attn_release_workspace",
+                 "parallax_check_device_error", "parallax_version"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def last_error() -> str:
+    return load_library().parallax_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != PARALLAX_OK:
+        raise ParallaxError(rc, last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t, name, dtype, shape):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def parallax_attn_prefill(q, rho, k, v, o=None, causal: bool = True, scale: float | None = None,
+                          stream=None):
+    """Prefill over [B, H, L, d] tensors (bf16 -> tensor-core kernel, fp32 -> fp32 kernel).
+
+    ``rho=None`` is the W_R = 0 path (plain softmax attention).  Returns ``o``
+    (fp32 [B, H, L, d]).
+    """
+    B, H, L, d = q.shape
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("q must be bf16 or fp32")
+    for name, t in (("q", q), ("k", k), ("v", v)) + ((("rho", rho),) if rho is not None else ()):
+        _need(t, name, dt, (B, H, L, d))
+    if o is None:
+        o = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.float32, (B, H, L, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    fn = load_library().parallax_attn_prefill if dt == torch.bfloat16 else \
+        load_library().parallax_attn_prefill_f32
+    _check(fn(_ptr(q), _ptr(rho), _ptr(k), _ptr(v), _ptr(o), B, H, L, d, 1 if causal else 0,
+              float(scale), _stream(stream)))
+    return o
+
+
+def parallax_attn_decode(q, rho, k_cache, v_cache, seqlens, o=None, stream=None):
+    """Single-token decode; q/rho [B, H, d], caches [B, H, Lmax, d], seqlens int32 [B].
+
+    Returns ``o`` (fp32 [B, H, d]).  The softmax scale is 1/sqrt(d).
+    """
+    B, H, Lmax, d = k_cache.shape
+    dt = k_cache.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("caches must be bf16 or fp32")
+    _need(q, "q", dt, (B, H, d))
+    if rho is not None:
+        _need(rho, "rho", dt, (B, H, d))
+    _need(k_cache, "k_cache", dt, (B, H, Lmax, d))
+    _need(v_cache, "v_cache", dt, (B, H, Lmax, d))
+    _need(seqlens, "seqlens", torch.int32, (B,))
+    if o is None:
+        o = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.float32, (B, H, d))
+    fn = load_library().parallax_attn_decode if dt == torch.bfloat16 else \
+        load_library().parallax_attn_decode_f32
+    _check(fn(_ptr(q), _ptr(rho), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o), B, H,
+              Lmax, d, _stream(stream)))
+    return o
+
+
+def parallax_attn_decode_chunk_keys(B: int, H: int, Lmax: int, d: int, elem_bytes: int) -> int:
+    rc = load_library().parallax_attn_decode_chunk_keys(B, H, Lmax, d, elem_bytes)
+    if rc < 0:
+        raise ParallaxError(rc, last_error())
+    return rc
+
+
+def parallax_attn_set_decode_chunk_keys(keys: int) -> None:
+    _check(load_library().parallax_attn_set_decode_chunk_keys(int(keys)))
+
+
+def parallax_attn_workspace_bytes() -> int:
+    return int(load_library().parallax_attn_workspace_bytes())
+
+
+def parallax_attn_release_workspace() -> None:
+    _check(load_library().parallax_attn_release_workspace())
+
+
+def parallax_check_device_error(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device error bits (0 = none)."""
+    bits = ctypes.c_uint(0)
+    rc = load_library().parallax_check_device_error(_stream(stream), ctypes.byref(bits))
+    if rc not in (PARALLAX_OK, PARALLAX_ERR_DEVICE):
+        raise ParallaxError(rc, last_error())
+    return int(bits.value)
+
+
+def parallax_version() -> int:
+    return int(load_library().parallax_version())
+
+
+prefill = parallax_attn_prefill
+decode = parallax_attn_decode

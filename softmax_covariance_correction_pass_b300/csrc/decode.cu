@@ -1,0 +1,332 @@
+// Parallax split-KV decode (one query token per sequence and head).
+//
+// Kernel 1 (decode_kernel): a persistent CTA walks work items (head, key
+// chunk).  One producer warp streams the chunk's K and V rows -- contiguous
+// in the [B, H, Lmax, d] cache -- into a ring of shared-memory stages with
+// bulk asynchronous copies (cp.async.bulk, completion on mbarriers, L2
+// evict-first), eight consumer warps each take an eighth of every stage and
+// update the online state of BOTH Parallax branches from the same bytes
+// (Parallax, "Parallax mantem softmax ...", paragraph 2: one KV stream feeds
+// the softmax and the covariance branch).  At the end of an item the warps'
+// states are merged in shared memory; the result is either the finished
+// output (a single chunk per head) or a partial state (m, l, A, U, W) in the
+// workspace.
+// Kernel 2 (combine_kernel): per head, rescales the partial states to a common
+// maximum (log-sum-exp), sums them and finishes o = U/l - (W/l - (A/l)(U/l)).
+#include "warp_stream.cuh"
+#include "kernels.h"
+
+namespace parallax {
+namespace {
+
+__device__ unsigned g_decode_err = 0;
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 4;
+constexpr int kStageRowBytes = 16384;  // bytes of K (and of V) per stage
+
+template <typename T, int D>
+struct DecodeShape {
+    using KL = KeyLayout<T, D>;
+    static constexpr int STAGE_KEYS = kStageRowBytes / KL::ROW_BYTES;
+    static constexpr int KEYS_PER_WARP = STAGE_KEYS / kConsumerWarps;
+    static constexpr int BLOCKS_PER_WARP = KEYS_PER_WARP / KL::BLOCK_KEYS;
+    static_assert(BLOCKS_PER_WARP >= 1 && KEYS_PER_WARP % KL::BLOCK_KEYS == 0, "stage shape");
+    static constexpr int MERGE_FLOATS = kConsumerWarps * (4 + 2 * D);
+    static constexpr size_t SMEM_BYTES =
+        (size_t)kStages * 2 * kStageRowBytes + MERGE_FLOATS * sizeof(float) + 2 * kStages * 8 + 16;
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* rho;
+    const void* kc;
+    const void* vc;
+    const int32_t* seqlens;
+    float* o;
+    float4* ws_stats;  // [B*H][nsplit]   (m, l, A, -)
+    float* ws_uw;      // [B*H][nsplit][2][D]
+    int B, H, Lmax, chunk, nsplit;
+    float qscale;  // softmax scale * log2(e)
+};
+
+__device__ __forceinline__ int clamp_seqlen(const int32_t* seqlens, int b, int Lmax) {
+    int n = seqlens[b];
+    if (n < 0 || n > Lmax) {
+        raise_error(&g_decode_err, PARALLAX_DEVERR_SEQLEN_CLAMPED);
+        n = n < 0 ? 0 : Lmax;
+    }
+    return n;
+}
+
+// Item (head bh, chunk ch) -> key range [start, end); returns false if the item is empty
+// and produces nothing.  Without split every head has exactly one item (it may be
+// empty: a zero-length sequence still writes o = 0).
+__device__ __forceinline__ bool item_range(const DecodeArgs& a, int slot, int BH, int& bh,
+                                           int& ch, int& start, int& end, bool split) {
+    ch = slot / BH;
+    bh = slot - ch * BH;
+    const int n = clamp_seqlen(a.seqlens, bh / a.H, a.Lmax);
+    start = ch * a.chunk;
+    end = min(start + a.chunk, n);
+    return split ? start < n : true;
+}
+
+template <typename T, int D, bool RHO, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
+    using KL = KeyLayout<T, D>;
+    using SH = DecodeShape<T, D>;
+    constexpr int VEC = KL::VEC;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    T* stage_k = reinterpret_cast<T*>(smem);                               // [kStages][STAGE_KEYS][D]
+    T* stage_v = reinterpret_cast<T*>(smem + kStages * kStageRowBytes);    // [kStages][STAGE_KEYS][D]
+    float* merge = reinterpret_cast<float*>(smem + 2 * kStages * kStageRowBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(merge + SH::MERGE_FLOATS);
+    uint64_t* empty = full + kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int BH = a.B * a.H;
+    const int total = BH * a.nsplit;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (*(volatile unsigned*)&g_decode_err & PARALLAX_DEVERR_WAIT_TIMEOUT) return;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        const uint64_t pol = l2_evict_first_policy();
+        uint32_t it = 0;
+        bool ok = true;
+        for (int slot = blockIdx.x; slot < total && ok; slot += gridDim.x) {
+            int bh, ch, start, end;
+            if (!item_range(a, slot, BH, bh, ch, start, end, SPLIT)) continue;
+            const size_t head = (size_t)bh * a.Lmax;
+            for (int t0 = start; t0 < end; t0 += SH::STAGE_KEYS, ++it) {
+                const int s = it % kStages;
+                if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, &g_decode_err)) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                const int nk = min(SH::STAGE_KEYS, end - t0);
+                const uint32_t bytes = (uint32_t)nk * KL::ROW_BYTES;
+                mbar_arrive_expect_tx(&full[s], 2 * bytes);
+                bulk_copy_g2s(stage_k + (size_t)s * SH::STAGE_KEYS * D,
+                              static_cast<const T*>(a.kc) + (head + t0) * D, bytes, &full[s], pol);
+                bulk_copy_g2s(stage_v + (size_t)s * SH::STAGE_KEYS * D,
+                              static_cast<const T*>(a.vc) + (head + t0) * D, bytes, &full[s], pol);
+            }
+        }
+        if (!ok) {
+            // drain the copies still in flight into this CTA's shared memory
+            for (uint32_t k = (it >= kStages ? it - kStages : 0); k < it; ++k)
+                mbar_wait(&full[k % kStages], (k / kStages) & 1, &g_decode_err);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int g = lane / KL::LPK, e = lane % KL::LPK;
+    uint32_t it = 0;
+    for (int slot = blockIdx.x; slot < total; slot += gridDim.x) {
+        int bh, ch, start, end;
+        if (!item_range(a, slot, BH, bh, ch, start, end, SPLIT)) continue;
+        float qf[VEC], rf[VEC];
+        load_row_slice<T, D>(static_cast<const T*>(a.q) + (size_t)bh * D, e, a.qscale, qf);
+        if (RHO) load_row_slice<T, D>(static_cast<const T*>(a.rho) + (size_t)bh * D, e, 1.f, rf);
+        else
+#pragma unroll
+            for (int x = 0; x < VEC; ++x) rf[x] = 0.f;
+
+        RowState<T, D> st;
+        st.reset();
+        bool ok = true;
+        for (int t0 = start; t0 < end; t0 += SH::STAGE_KEYS, ++it) {
+            const int s = it % kStages;
+            if (*abort_flag || !mbar_wait(&full[s], (it / kStages) & 1, &g_decode_err)) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            const int nk = min(SH::STAGE_KEYS, end - t0);
+            const T* sK = stage_k + (size_t)s * SH::STAGE_KEYS * D;
+            const T* sV = stage_v + (size_t)s * SH::STAGE_KEYS * D;
+#pragma unroll
+            for (int blk = 0; blk < SH::BLOCKS_PER_WARP; ++blk) {
+                const int kb = warp * SH::KEYS_PER_WARP + blk * KL::BLOCK_KEYS;
+                if (kb < nk) warp_block<T, D, RHO>(st, qf, rf, sK, sV, kb, nk, lane);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        // After a timeout every warp still walks the remaining items (without
+        // waiting) so that all of them meet at the same named barriers; nothing
+        // is written.
+        warp_merge_groups<T, D, RHO>(st);
+
+        // ---- merge the consumer warps' states
+        float* mw = merge + warp * (4 + 2 * D);
+        if (lane == 0) {
+            mw[0] = st.m;
+            mw[1] = st.l;
+            mw[2] = st.A;
+        }
+        if (g == 0) {
+#pragma unroll
+            for (int x = 0; x < VEC; ++x) {
+                mw[4 + e * VEC + x] = st.U[x];
+                mw[4 + D + e * VEC + x] = st.W[x];
+            }
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+        const int c = threadIdx.x;
+        if (c < D && ok && !*abort_flag) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge[w * (4 + 2 * D)]);
+            float l = 0.f, A = 0.f, U = 0.f, W = 0.f;
+            if (M > -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float* m2 = merge + w * (4 + 2 * D);
+                    const float f = fast_exp2(m2[0] - M);
+                    l = fmaf(f, m2[1], l);
+                    A = fmaf(f, m2[2], A);
+                    U = fmaf(f, m2[4 + c], U);
+                    W = fmaf(f, m2[4 + D + c], W);
+                }
+            }
+            if (SPLIT) {
+                const size_t idx = (size_t)bh * a.nsplit + ch;
+                a.ws_uw[idx * 2 * D + c] = U;
+                a.ws_uw[idx * 2 * D + D + c] = W;
+                if (c == 0) a.ws_stats[idx] = make_float4(M, l, A, 0.f);
+            } else {
+                const float inv_l = l > 0.f ? 1.f / l : 0.f;
+                const float mu = U * inv_l;
+                a.o[(size_t)bh * D + c] = RHO ? mu - (W * inv_l - (A * inv_l) * mu) : mu;
+            }
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+    }
+}
+
+template <int D, bool RHO>
+__global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a) {
+    const int bh = blockIdx.x, c = threadIdx.x;
+    const int n = clamp_seqlen(a.seqlens, bh / a.H, a.Lmax);
+    const int nch = (n + a.chunk - 1) / a.chunk;
+    const float4* stats = a.ws_stats + (size_t)bh * a.nsplit;
+    const float* uw = a.ws_uw + (size_t)bh * a.nsplit * 2 * D;
+    float M = -INFINITY;
+    for (int k = 0; k < nch; ++k) M = fmaxf(M, stats[k].x);
+    float l = 0.f, A = 0.f, U = 0.f, W = 0.f;
+    for (int k = 0; k < nch; ++k) {
+        const float4 s = stats[k];
+        const float f = fast_exp2(s.x - M);
+        l = fmaf(f, s.y, l);
+        A = fmaf(f, s.z, A);
+        U = fmaf(f, uw[(size_t)k * 2 * D + c], U);
+        if (RHO) W = fmaf(f, uw[(size_t)k * 2 * D + D + c], W);
+    }
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const float mu = U * inv_l;
+    a.o[(size_t)bh * D + c] = RHO ? mu - (W * inv_l - (A * inv_l) * mu) : mu;
+}
+
+template <typename T, int D, bool RHO, bool SPLIT>
+cudaError_t launch_decode_kernel(const DecodeArgs& a, int grid, cudaStream_t stream) {
+    using SH = DecodeShape<T, D>;
+    auto kern = decode_kernel<T, D, RHO, SPLIT>;
+    static bool configured = false;  // per process; the attribute is per function
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SH::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    kern<<<grid, kThreads, SH::SMEM_BYTES, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int D, bool RHO>
+cudaError_t run_decode(const DecodePlan& plan, const void* q, const void* rho, const void* kc,
+                       const void* vc, const int32_t* seqlens, float* o, void* ws,
+                       cudaStream_t stream) {
+    DecodeArgs a;
+    a.q = q;
+    a.rho = rho;
+    a.kc = kc;
+    a.vc = vc;
+    a.seqlens = seqlens;
+    a.o = o;
+    a.B = plan.B;
+    a.H = plan.H;
+    a.Lmax = plan.Lmax;
+    a.chunk = plan.chunk;
+    a.nsplit = plan.nsplit;
+    a.qscale = plan.scale * kLog2e;
+    const size_t BH = (size_t)plan.B * plan.H;
+    a.ws_stats = static_cast<float4*>(ws);
+    a.ws_uw = reinterpret_cast<float*>(static_cast<char*>(ws) + BH * plan.nsplit * sizeof(float4));
+    cudaError_t e;
+    if (plan.nsplit > 1) {
+        e = launch_decode_kernel<T, D, RHO, true>(a, plan.grid, stream);
+        if (e != cudaSuccess) return e;
+        combine_kernel<D, RHO><<<(unsigned)BH, D, 0, stream>>>(a);
+    } else {
+        e = launch_decode_kernel<T, D, RHO, false>(a, plan.grid, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(const DecodePlan& plan) {
+    if (plan.nsplit <= 1) return 0;
+    const size_t items = (size_t)plan.B * plan.H * plan.nsplit;
+    return items * sizeof(float4) + items * 2 * plan.d * sizeof(float);
+}
+
+int decode_stage_keys(int d, int elem_bytes) { return kStageRowBytes / (d * elem_bytes); }
+
+int decode_threads() { return kThreads; }
+
+cudaError_t decode_launch(const DecodePlan& plan, bool bf16, const void* q, const void* rho,
+                          const void* kc, const void* vc, const int32_t* seqlens, float* o,
+                          void* ws, cudaStream_t stream) {
+    const bool r = rho != nullptr;
+#define PARALLAX_DECODE_CASE(T, DD)                                                              \
+    if (plan.d == DD)                                                                            \
+        return r ? run_decode<T, DD, true>(plan, q, rho, kc, vc, seqlens, o, ws, stream)         \
+                 : run_decode<T, DD, false>(plan, q, rho, kc, vc, seqlens, o, ws, stream);
+    if (bf16) {
+        PARALLAX_DECODE_CASE(__nv_bfloat16, 64)
+        PARALLAX_DECODE_CASE(__nv_bfloat16, 128)
+    } else {
+        PARALLAX_DECODE_CASE(float, 64)
+        PARALLAX_DECODE_CASE(float, 128)
+    }
+#undef PARALLAX_DECODE_CASE
+    return cudaErrorInvalidValue;
+}
+
+unsigned decode_take_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_decode_err, sizeof(v)) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_decode_err, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace parallax

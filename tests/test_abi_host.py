@@ -1,0 +1,132 @@
+"""Host-side checks of the C-ABI library: it loads without a GPU, exports every
+symbol include/parallax_attn.h declares, and rejects bad arguments before it
+touches CUDA.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import softmax_covariance_correction_pass_b300 as px
+from softmax_covariance_correction_pass_b300 import build as pxbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "parallax_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pxbuild.build()
+    return px.load_library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(parallax_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("parallax_attn_prefill", "parallax_attn_decode", "parallax_attn_prefill_f32",
+                     "parallax_attn_decode_f32", "parallax_last_error",
+                     "parallax_check_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version(lib):
+    assert px.parallax_version() >= 100
+
+
+FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced by the checks below
+
+
+def _prefill(lib, q=FAKE, rho=None, k=FAKE, v=FAKE, o=FAKE, B=1, H=1, L=8, d=64, causal=1,
+             scale=0.125, f32=False):
+    fn = lib.parallax_attn_prefill_f32 if f32 else lib.parallax_attn_prefill
+    vp = ctypes.c_void_p
+    return fn(vp(q), vp(rho), vp(k), vp(v), vp(o), B, H, L, d, causal, ctypes.c_float(scale), None)
+
+
+def _decode(lib, q=FAKE, rho=None, k=FAKE, v=FAKE, sl=FAKE, o=FAKE, B=1, H=1, Lmax=8, d=128,
+            f32=False):
+    fn = lib.parallax_attn_decode_f32 if f32 else lib.parallax_attn_decode
+    vp = ctypes.c_void_p
+    return fn(vp(q), vp(rho), vp(k), vp(v), vp(sl), vp(o), B, H, Lmax, d, None)
+
+
+@pytest.mark.parametrize("f32", [False, True])
+def test_prefill_argument_errors(lib, f32):
+    E, U = px.PARALLAX_ERR_INVALID, px.PARALLAX_ERR_UNSUPPORTED
+    assert _prefill(lib, q=None, f32=f32) == E
+    assert _prefill(lib, k=None, f32=f32) == E
+    assert _prefill(lib, v=None, f32=f32) == E
+    assert _prefill(lib, o=None, f32=f32) == E
+    assert _prefill(lib, B=0, f32=f32) == E
+    assert _prefill(lib, H=-1, f32=f32) == E
+    assert _prefill(lib, L=0, f32=f32) == E
+    assert _prefill(lib, d=96, f32=f32) == U
+    assert _prefill(lib, d=256, f32=f32) == U
+    assert _prefill(lib, q=FAKE + 8, f32=f32) == E
+    assert _prefill(lib, rho=FAKE + 4, f32=f32) == E
+    assert _prefill(lib, causal=2, f32=f32) == E
+    assert _prefill(lib, scale=float("nan"), f32=f32) == E
+    assert _prefill(lib, scale=float("inf"), f32=f32) == E
+    assert "causal" in px.last_error() or "scale" in px.last_error()
+
+
+@pytest.mark.parametrize("f32", [False, True])
+def test_decode_argument_errors(lib, f32):
+    E, U = px.PARALLAX_ERR_INVALID, px.PARALLAX_ERR_UNSUPPORTED
+    assert _decode(lib, q=None, f32=f32) == E
+    assert _decode(lib, sl=None, f32=f32) == E
+    assert _decode(lib, o=None, f32=f32) == E
+    assert _decode(lib, Lmax=0, f32=f32) == E
+    assert _decode(lib, B=0, f32=f32) == E
+    assert _decode(lib, d=32, f32=f32) == U
+    assert _decode(lib, k=FAKE + 2, f32=f32) == E
+
+
+def test_last_error_is_thread_local(lib):
+    import threading
+
+    assert _prefill(lib, d=96) == px.PARALLAX_ERR_UNSUPPORTED
+    seen = {}
+
+    def other():
+        seen["msg"] = px.last_error()
+
+    t = threading.Thread(target=other)
+    t.start()
+    t.join()
+    assert seen["msg"] == ""
+    assert "d=96" in px.last_error()
+
+
+def test_chunk_plan(lib):
+    # split-KV plan: chunk is a multiple of 256 keys (or the whole cache), more
+    # splits for few heads and long caches, none when every head is short
+    f = px.parallax_attn_decode_chunk_keys
+    assert f(64, 16, 8192, 128, 2) % 256 == 0
+    assert f(1, 16, 128, 128, 2) == 128                      # no split: whole cache
+    assert f(1, 16, 32768, 128, 2) == 256                    # few heads: smallest chunks
+    assert f(2048, 16, 1024, 128, 2) == 1024                 # many heads: no split
+    assert 256 <= f(512, 16, 16384, 128, 2) <= 4096
+    with pytest.raises(px.ParallaxError):
+        f(0, 16, 128, 128, 2)
+    with pytest.raises(px.ParallaxError):
+        f(1, 16, 128, 128, 3)
+
+
+def test_forced_chunk_validation(lib):
+    with pytest.raises(px.ParallaxError):
+        px.parallax_attn_set_decode_chunk_keys(100)
+    px.parallax_attn_set_decode_chunk_keys(512)
+    assert px.parallax_attn_decode_chunk_keys(1, 1, 4096, 128, 2) == 512
+    assert px.parallax_attn_decode_chunk_keys(1, 1, 300, 128, 2) == 300  # >= Lmax: no split
+    px.parallax_attn_set_decode_chunk_keys(0)
