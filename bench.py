@@ -48,6 +48,12 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+                    help="time one kernel alone (profiling runs); the default times both")
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="override the decode batch (profiling runs on smaller cases)")
+    ap.add_argument("--prefill-batch", type=int, default=None,
+                    help="override the prefill batch (profiling runs on smaller cases)")
     return ap.parse_args(argv)
 
 
@@ -252,24 +258,30 @@ def run_ours(args):
 
     # ---- inputs resident in HBM
     dc = configs.DECODE_UNIFORM
-    dinp = configs.decode_uniform_inputs(dev)
-    B, H, d, n = dc["B"], dc["H"], dc["d"], dc["ctx"]
+    B, H, d, n = args.decode_batch or dc["B"], dc["H"], dc["d"], dc["ctx"]
+    dinp = configs.decode_uniform_inputs(dev, B=B)
     do = torch.empty((B, H, d), dtype=torch.float32, device=dev)
     pc = configs.LAYER_PREFILL
-    pinp = configs.layer_prefill_inputs(dev)
-    PB, PH, PL, Pd = pc["B"], pc["H"], pc["L"], pc["d"]
+    PB, PH, PL, Pd = args.prefill_batch or pc["B"], pc["H"], pc["L"], pc["d"]
+    pinp = configs.layer_prefill_inputs(dev, B=PB)
     po = torch.empty((PB, PH, PL, Pd), dtype=torch.float32, device=dev)
     kv_bytes, dec_bytes = decode_bytes(B, H, n, d)
     pre_flops = prefill_flops(PB, PH, PL, Pd)
     chunk = px.parallax_attn_decode_chunk_keys(B, H, n, d, 2)
     dec_launches = 2 if chunk < n else 1
 
+    run_decode = args.only in (None, "decode")
+    run_prefill = args.only in (None, "prefill")
+
     def decode():
-        px.parallax_attn_decode(dinp.q, dinp.rho, dinp.k_cache, dinp.v_cache, dinp.seqlens, do)
+        if run_decode:
+            px.parallax_attn_decode(dinp.q, dinp.rho, dinp.k_cache, dinp.v_cache, dinp.seqlens,
+                                    do)
 
     def prefill():
-        px.parallax_attn_prefill(pinp.q, pinp.rho, pinp.k, pinp.v, po, causal=True,
-                                 scale=pinp.scale)
+        if run_prefill:
+            px.parallax_attn_prefill(pinp.q, pinp.rho, pinp.k, pinp.v, po, causal=True,
+                                     scale=pinp.scale)
 
     for _ in range(max(args.warmup, 3)):
         decode()
@@ -308,6 +320,8 @@ def run_ours(args):
     if px.parallax_check_device_error() != 0:
         raise RuntimeError("device error in the timed region")
 
+    dec_ms = max(dec_ms, 1e-9)
+    pre_ms = max(pre_ms, 1e-9)
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
     pre_tflops = pre_flops / (pre_ms * 1e-3) / 1e12
     value = ws * dec_bytes / (dec_ms * 1e-3) / 1e9  # whole job: all replicas' bytes / max time
@@ -324,11 +338,11 @@ def run_ours(args):
                 "peak_burst": peaks["bf16_tflops"],
                 "frac_burst": pre_tflops / peaks["bf16_tflops"],
                 "peak_source": peaks["source"] + " (sustained)"}
-    dominant = roof_pre if pre_ms >= dec_ms else roof_dec
+    dominant = roof_pre if (run_prefill and (pre_ms >= dec_ms or not run_decode)) else roof_dec
 
     # ---- W_R = 0 fast paths (rho = NULL), for context
     f0 = {}
-    for name, fn, units in (
+    for name, fn, units in () if args.only else (
             ("decode_gbs", lambda: px.parallax_attn_decode(dinp.q, None, dinp.k_cache,
                                                            dinp.v_cache, dinp.seqlens, do),
              dec_bytes / 1e9),
@@ -347,7 +361,7 @@ def run_ours(args):
     # ---- end to end through the public call, host buffers (pinned), copies timed
     e2e = None
     e2e_prefill = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.only:
         hq = [t.to("cpu").pin_memory() for t in (dinp.q, dinp.rho, dinp.k_cache, dinp.v_cache,
                                                   dinp.seqlens)]
         ho = torch.empty((B, H, d), dtype=torch.float32).pin_memory()
@@ -417,6 +431,7 @@ def run_ours(args):
                 "prefill": {"B": PB, "H": PH, "L": PL, "d": Pd, "causal": True,
                             "tokens_per_s": ws * PB * PL / (pre_ms * 1e-3)},
                 "l2": "inputs larger than L2 (4.3 GB KV cache; 1.07 GB of prefill tensors)",
+                "only": args.only,
                 "parallelism": f"replicas x{ws} (no collectives)"},
             "roofline": dominant,
             "roofline_decode": roof_dec,
@@ -430,7 +445,7 @@ def run_ours(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks.summary(),
-            "gpu_launches": K * (dec_launches + 1),
+            "gpu_launches": K * ((dec_launches if run_decode else 0) + (1 if run_prefill else 0)),
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

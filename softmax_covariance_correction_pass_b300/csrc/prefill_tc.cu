@@ -24,7 +24,9 @@
 //  * the row shift c (Cov_p(r - c, v) = Cov_p(r, v) for any constant c) is set
 //    to the p-weighted mean of r over the first key tile processed, so PR is
 //    centred and its bf16 rounding error stays proportional to the spread of
-//    r rather than its size;
+//    r rather than its size.  Key tiles are processed in order 0, 1, ..., with
+//    the causal diagonal tile last, so that the first tile is a full one and c
+//    is a mean over 128 keys (for the first query tile it is the only tile);
 //  * rows that see few keys (the first query tile of a causal head, or a
 //    non-causal head with L <= 128) also feed the bf16 rounding residual of PR
 //    (PR - bf16(PR), stored in S columns [64,128)) through one more MMA, so the
@@ -57,8 +59,7 @@ struct TcLayout {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K then V
     static constexpr int BAR_OFF = KV_OFF + kStages * STAGE_BYTES;
     static constexpr int NBARS = 1 + 3 * kStages + 3;
-    // + alignment slack, + 4 KB so that no operand read can leave the allocation
-    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024 + 4096;
+    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + alignment slack
     static constexpr uint32_t S_COL = 0;
     static constexpr uint32_t R_COL = 128;
     static constexpr uint32_t U_COL = RHO ? 256 : 128;
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     q_full);
             }
             for (; it < n_kv; ++it) {
-                const int j = CAUSAL ? qt - it : it;
+                const int j = it;
                 const int s = it % kStages;
                 if (it >= kStages &&
                     !mbar_wait(&kv_empty[s], ((it / kStages) - 1) & 1, &g_tc_err)) {
@@ -190,42 +191,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdescV = tc::idesc_bf16_f32(BM, D, true);
             bool ok = mbar_wait(q_full, 0, &g_tc_err);
             tc::fence_after_sync();
-            const uint32_t sQ = smem_u32(smem + LY::Q_OFF);
-            const uint32_t sR = smem_u32(smem + LY::RHO_OFF);
+            // Descriptors are built once; a K-step only adds a constant to the
+            // start-address field (bits 0..13, in 16-byte units).
+            const uint64_t dQ = tc::smem_desc_sw128(smem_u32(smem + LY::Q_OFF), 16, 1024);
+            const uint64_t dR = tc::smem_desc_sw128(smem_u32(smem + LY::RHO_OFF), 16, 1024);
+            const uint32_t kv0 = smem_u32(smem + LY::KV_OFF);
             for (int it = 0; it < n_kv && ok; ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1;
-                const uint32_t sK = smem_u32(smem + LY::KV_OFF + s * LY::STAGE_BYTES);
-                const uint32_t sV = sK + LY::TILE_BYTES;
+                const uint32_t sK = kv0 + s * LY::STAGE_BYTES;
+                const uint64_t dK = tc::smem_desc_sw128(sK, 16, 1024);
+                const uint64_t dV = tc::smem_desc_sw128(sK + LY::TILE_BYTES, LY::SUB_BYTES, 1024);
                 if (!mbar_wait(&k_full[s], ph, &g_tc_err)) { ok = false; break; }
                 tc::fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * LY::SUB_BYTES + (kk % 4) * 32;
-                    const uint64_t bdesc = tc::smem_desc_sw128(sK + off, 16, 1024);
-                    tc::mma_ss(tmem + LY::S_COL, tc::smem_desc_sw128(sQ + off, 16, 1024), bdesc,
-                               kIdescS, kk > 0);
-                    if (RHO)
-                        tc::mma_ss(tmem + LY::R_COL, tc::smem_desc_sw128(sR + off, 16, 1024), bdesc,
-                                   kIdescS, kk > 0);
+                    const uint32_t off = ((kk / 4) * LY::SUB_BYTES + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem + LY::S_COL, dQ + off, dK + off, kIdescS, kk > 0);
+                    if (RHO) tc::mma_ss(tmem + LY::R_COL, dR + off, dK + off, kIdescS, kk > 0);
                 }
                 tc::commit(s_full);
                 if (!mbar_wait(p_full, it & 1, &g_tc_err)) { ok = false; break; }
                 tc::fence_after_sync();
                 if (!mbar_wait(&v_full[s], ph, &g_tc_err)) { ok = false; break; }
                 tc::fence_after_sync();
+                const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     // 16 keys = 16 rows of 128 bytes in each 64-column block; the second
                     // column block of V (d >= 64) sits LBO = one block further on.
-                    const uint64_t bdesc =
-                        tc::smem_desc_sw128(sV + kk * 16 * 128, LY::SUB_BYTES, 1024);
-                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    tc::mma_ts(tmem + LY::U_COL, tmem + LY::S_COL + kk * 8, bdesc, kIdescV, acc);
+                    const uint32_t off = (kk * 16 * 128) >> 4;
+                    const uint32_t acc = kk > 0 ? 1u : acc0;
+                    tc::mma_ts(tmem + LY::U_COL, tmem + LY::S_COL + kk * 8, dV + off, kIdescV, acc);
                     if (RHO) {
-                        tc::mma_ts(tmem + LY::W_COL, tmem + LY::R_COL + kk * 8, bdesc, kIdescV, acc);
+                        tc::mma_ts(tmem + LY::W_COL, tmem + LY::R_COL + kk * 8, dV + off, kIdescV, acc);
                         if (precise)
-                            tc::mma_ts(tmem + LY::W_COL, tmem + LY::S_COL + 64 + kk * 8, bdesc,
+                            tc::mma_ts(tmem + LY::W_COL, tmem + LY::S_COL + 64 + kk * 8, dV + off,
                                        kIdescV, 1u);
                     }
                 }
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m = -INFINITY, l = 0.f, A = 0.f, c = 0.f;
         bool ok = !skip;
         for (int it = 0; it < n_kv && ok; ++it) {
-            const int k0 = (CAUSAL ? qt - it : it) * BN;
+            const int k0 = it * BN;
             const bool got = !*abort_flag && mbar_wait(s_full, it & 1, &g_tc_err);
             if (!__all_sync(kFullMask, got)) { ok = false; break; }  // warp-uniform exit
             tc::fence_after_sync();
