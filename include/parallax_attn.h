@@ -100,6 +100,27 @@ int parallax_attn_decode_f32(const void* q, const void* rho, const void* k_cache
                              int Lmax, int d, cudaStream_t stream);
 
 /*
+ * parallax_attn_decode without any device allocation (bf16 inputs, fp32 o).
+ * This entry point has no counterpart in the Parallax paper; it exists for
+ * callers that cannot let a library call cudaMalloc -- serving engines that
+ * reserve nearly all device memory for their own KV-cache pool up front, and
+ * latency-critical decode loops where an allocation's implicit device
+ * synchronisation would stall every other stream.
+ * Arguments, layout, result and split plan are those of parallax_attn_decode;
+ * only the split-KV partial states live in a fixed array inside the library:
+ * 8 MiB per device (2 * 4 B * d + 16 B per head per key chunk), held by every
+ * GPU that loads the library until the process exits.  A shape whose split
+ * needs more returns PARALLAX_ERR_UNSUPPORTED before anything is launched
+ * (parallax_attn_decode handles it).  The first call on a device looks up
+ * the array's device address (no allocation); make that first call before
+ * any stream capture.  All calls on a device share the array, so calls that
+ * may overlap on the GPU (other streams, other host threads) race on it.
+ */
+int parallax_attn_decode_noalloc(const void* q, const void* rho, const void* k_cache,
+                                 const void* v_cache, const int32_t* seqlens, void* o, int B,
+                                 int H, int Lmax, int d, cudaStream_t stream);
+
+/*
  * Keys per split-KV chunk that parallax_attn_decode{,_f32} would use for this
  * shape (elem_bytes = 2 for bf16, 4 for fp32).  Returns a negative
  * parallax_status for invalid arguments.  A result >= Lmax means no split.

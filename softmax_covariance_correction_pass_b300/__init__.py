@@ -145,6 +145,26 @@ def parallax_attn_decode(q, rho, k_cache, v_cache, seqlens, o=None, stream=None)
     return o
 
 
+def parallax_attn_decode_noalloc(q, rho, k_cache, v_cache, seqlens, o, stream=None):
+    """parallax_attn_decode (bf16) with the split-KV partials in the library's fixed
+    device array: the call allocates nothing (``o`` must be supplied)."""
+    B, H, Lmax, d = k_cache.shape
+    _need(q, "q", torch.bfloat16, (B, H, d))
+    if rho is not None:
+        _need(rho, "rho", torch.bfloat16, (B, H, d))
+    _need(k_cache, "k_cache", torch.bfloat16, (B, H, Lmax, d))
+    _need(v_cache, "v_cache", torch.bfloat16, (B, H, Lmax, d))
+    _need(seqlens, "seqlens", torch.int32, (B,))
+    _need(o, "o", torch.float32, (B, H, d))
+    lib = load_library()
+    fn = lib.parallax_attn_decode_noalloc
+    fn.argtypes = lib.parallax_attn_decode.argtypes
+    fn.restype = ctypes.c_int
+    _check(fn(_ptr(q), _ptr(rho), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o), B, H,
+              Lmax, d, _stream(stream)))
+    return o
+
+
 def parallax_attn_decode_chunk_keys(B: int, H: int, Lmax: int, d: int, elem_bytes: int) -> int:
     rc = load_library().parallax_attn_decode_chunk_keys(B, H, Lmax, d, elem_bytes)
     if rc < 0:

@@ -193,6 +193,38 @@ int parallax_attn_decode_f32(const void* q, const void* rho, const void* k_cache
     return decode_common(q, rho, k_cache, v_cache, seqlens, o, B, H, Lmax, d, stream, false);
 }
 
+int parallax_attn_decode_noalloc(const void* q, const void* rho, const void* k_cache,
+                                 const void* v_cache, const int32_t* seqlens, void* o, int B,
+                                 int H, int Lmax, int d, cudaStream_t stream) {
+    int rc = validate_common(q, k_cache, v_cache, o, rho, B, H, Lmax, d, "Lmax");
+    if (rc != PARALLAX_OK) return rc;
+    if (!seqlens) return fail(PARALLAX_ERR_INVALID, "null seqlens pointer");
+    DeviceState* ds = device_state(nullptr);
+    if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
+    // the same split plan as parallax_attn_decode, so both give the same result
+    parallax::DecodePlan plan;
+    plan.B = B;
+    plan.H = H;
+    plan.Lmax = Lmax;
+    plan.d = d;
+    plan.scale = 1.0f / std::sqrt((float)d);
+    plan.chunk = plan_chunk(B, H, Lmax, ds->num_sms);
+    plan.nsplit = (Lmax + plan.chunk - 1) / plan.chunk;
+    plan.grid = (int)std::min<long long>((long long)B * H * plan.nsplit, (long long)ds->num_sms);
+    const size_t need = parallax::decode_workspace_bytes(plan);
+    const size_t cap = parallax::decode_noalloc_capacity();
+    if (need > cap)
+        return fail(PARALLAX_ERR_UNSUPPORTED,
+                    "decode of B=%d H=%d Lmax=%d d=%d needs %zu bytes of split-KV scratch; the "
+                    "no-allocation entry point holds at most %zu bytes (use "
+                    "parallax_attn_decode for this size)",
+                    B, H, Lmax, d, need, cap);
+    cudaError_t e = parallax::decode_launch_noalloc(plan, true, q, rho, k_cache, v_cache,
+                                                    seqlens, static_cast<float*>(o), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode (no-allocation) launch");
+    return succeed();
+}
+
 int parallax_attn_decode_chunk_keys(int B, int H, int Lmax, int d, int elem_bytes) {
     if (B <= 0 || H <= 0 || Lmax <= 0)
         return fail(PARALLAX_ERR_INVALID, "B, H, Lmax must be >= 1");

@@ -13,6 +13,8 @@
 // workspace.
 // Kernel 2 (combine_kernel): per head, rescales the partial states to a common
 // maximum (log-sum-exp), sums them and finishes o = U/l - (W/l - (A/l)(U/l)).
+#include <mutex>
+
 #include "warp_stream.cuh"
 #include "kernels.h"
 
@@ -320,6 +322,53 @@ cudaError_t decode_launch(const DecodePlan& plan, bool bf16, const void* q, cons
     }
 #undef PARALLAX_DECODE_CASE
     return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for decode callers that cannot allocate device memory.
+//
+// Some callers cannot let a library call cudaMalloc: serving engines that
+// reserve nearly all device memory for their own KV-cache pool up front (a
+// late allocation would fail or eat into the pool), and latency-critical
+// decode loops where cudaMalloc/cudaFree would synchronise the device and
+// stall every other stream.  For them the split-KV partial states go to this
+// file-scope array instead of the grown-on-demand workspace.  It exists once
+// per device that loads the library and stays until the process exits.
+// Nothing in it needs to start at zero: the combine kernel reads only the
+// partial states that the decode kernel of the same call wrote.  All calls on
+// a device share it, so calls that overlap on the GPU race on it.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+}  // namespace
+
+size_t decode_noalloc_capacity() { return kNoAllocScratchBytes; }
+
+cudaError_t decode_launch_noalloc(const DecodePlan& plan, bool bf16, const void* q,
+                                  const void* rho, const void* kc, const void* vc,
+                                  const int32_t* seqlens, float* o, cudaStream_t stream) {
+    if (decode_workspace_bytes(plan) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void* ptr = nullptr;
+    {
+        // Set-up, once per device, with that device current: the symbol's name
+        // is only a host-side stand-in, so fetch the device address of the array.
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_addr[dev]) {
+            e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess) return e;
+            g_noalloc_addr[dev] = ptr;
+        }
+        ptr = g_noalloc_addr[dev];
+    }
+    return decode_launch(plan, bf16, q, rho, kc, vc, seqlens, o, ptr, stream);
 }
 
 unsigned decode_take_error() {

@@ -23,6 +23,13 @@ cudaError_t decode_launch(const DecodePlan& plan, bool bf16, const void* q, cons
                           const void* kc, const void* vc, const int32_t* seqlens, float* o,
                           void* ws, cudaStream_t stream);
 unsigned decode_take_error();
+// Same as decode_launch with the split-KV partials in a fixed device array
+// (no allocation).  Fails with cudaErrorInvalidValue if the plan needs more
+// than decode_noalloc_capacity() bytes.
+size_t decode_noalloc_capacity();
+cudaError_t decode_launch_noalloc(const DecodePlan& plan, bool bf16, const void* q,
+                                  const void* rho, const void* kc, const void* vc,
+                                  const int32_t* seqlens, float* o, cudaStream_t stream);
 
 // ---------------------------------------------------------------- prefill
 struct PrefillShape {
