@@ -393,6 +393,423 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ============================================================================
+// Correction path (rho != NULL): two 64-query sub-tiles in ping-pong.
+//
+// The A operand of MMA-1 stacks, per 16-query group g of a sub-tile, the 16
+// query rows (operand rows 32g..32g+15) and the same 16 queries' probe rows
+// (rows 32g+16..32g+31).  One M=128 MMA per sub-tile therefore yields S and
+// R for 64 queries, and one M=128 MMA with A = [P; PR] (read from TMEM) yields
+// U and W.  TMEM lane 32g+i holds query 16g+i's S row (then P, then U) and
+// lane 32g+16+i its R row (then PR, then W), so each softmax warp (one TMEM
+// lane quarter) owns 16 queries, and the half-split TMEM access gives thread t
+// (t < 16) and thread t+16 the same query's rows, each with half of the key
+// columns: every thread computes s, r, p and p(r - c) for the same 64 keys of
+// one query with no data exchange, and the exponentials are spread over all
+// four SM sub-partitions.  While the softmax warps of one sub-tile work, the
+// tensor core runs the other sub-tile's MMAs.
+//
+// TMEM columns: D_sub at 128*sub (S|R, then P|PR packed into its first 64
+// columns, the few-key residuals into the next 64), O_sub at 256 + sub*d (U|W).
+// ============================================================================
+constexpr int kThreads2 = 320;  // warp 0 TMA, warp 1 TMEM + MMA, warps 2-5 / 6-9: sub-tile 0 / 1
+constexpr int kHeadGroup = 16;  // heads per CTA-scheduling group (keeps their K/V in L2)
+
+template <int D>
+struct PairLayout {
+    static constexpr int SUB_BYTES = 128 * 128;         // [128 rows x 64 cols] bf16, 128B-swizzled
+    static constexpr int NCB = D / 64;                  // 64-column blocks per row
+    static constexpr int OP_BYTES = NCB * SUB_BYTES;    // one 128 x D bf16 operand
+    static constexpr int QR_OFF = 0;                    // [Q;rho] stacked, sub-tiles 0 and 1
+    static constexpr int K_OFF = 2 * OP_BYTES;          // K ring, 2 stages
+    static constexpr int V_OFF = K_OFF + 2 * OP_BYTES;  // V ring, 2 stages
+    static constexpr int BAR_OFF = V_OFF + 2 * OP_BYTES;
+    // q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2], p_full[2], o_full
+    static constexpr int NBARS = 14;
+    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    __host__ __device__ static constexpr uint32_t dcol(int sub) { return 128u * sub; }
+    __host__ __device__ static constexpr uint32_t ocol(int sub) { return 256u + (uint32_t)(D * sub); }
+};
+
+// Pack 32 fp32 values (this thread's key block b) to bf16 and store them in
+// the packed columns 16b.. of this thread's half of the row (split 32); with
+// `residual`, also store bf16(x - bf16(x)) 64 columns further on.
+__device__ __forceinline__ void store_pr_block(uint32_t taddr, const uint32_t (&v)[32], int b,
+                                               bool residual) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int y = 0; y < 16; ++y)
+        pk[y] = tc::pack_bf16(__uint_as_float(v[2 * y]), __uint_as_float(v[2 * y + 1]));
+    tc::tmem_st16_split<32>(taddr + 16 * b, pk);
+    if (residual) {
+#pragma unroll
+        for (int y = 0; y < 16; ++y)
+            pk[y] = tc::pack_bf16(__uint_as_float(v[2 * y]) - tc::bf16_lo_to_f32(pk[y]),
+                                  __uint_as_float(v[2 * y + 1]) - tc::bf16_hi_to_f32(pk[y]));
+        tc::tmem_st16_split<32>(taddr + 64 + 16 * b, pk);
+    }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads2, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmR,
+                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const TcArgs a) {
+    using LY = PairLayout<D>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* v_full = bars + 3;
+    uint64_t* k_empty = bars + 5;
+    uint64_t* v_empty = bars + 7;
+    uint64_t* s_full = bars + 9;
+    uint64_t* p_full = bars + 11;
+    uint64_t* o_full = bars + 13;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    // CTA -> (head, 128-query block): heads in groups of kHeadGroup, heaviest
+    // block (most key tiles) first within a group, so that the CTAs resident
+    // at any time share the K/V of a few heads in L2.
+    const int n_qb = a.n_qt;
+    const int group = blockIdx.x / (kHeadGroup * n_qb);
+    const int gsize = min(kHeadGroup, a.BH - group * kHeadGroup);
+    const int r_in = blockIdx.x - group * kHeadGroup * n_qb;
+    const int qb = CAUSAL ? n_qb - 1 - r_in / gsize : r_in / gsize;
+    const int bh = group * kHeadGroup + r_in % gsize;
+    const int q0 = qb * 128;
+    const int n_kv = CAUSAL ? qb + 1 : (a.L + BN - 1) / BN;
+    const bool precise = CAUSAL ? qb == 0 : n_kv == 1;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], (b == 11 || b == 12) ? 128 : 1);
+        *abort_flag = (*(volatile unsigned*)&g_tc_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&tmQ);
+        tc::prefetch_tmap(&tmR);
+        tc::prefetch_tmap(&tmK);
+        tc::prefetch_tmap(&tmV);
+    }
+    if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort_flag != 0;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0 && !skip) {
+            const int z = bh;
+            bool ok = true;
+            int kj = 0, vj = 0;  // K / V tiles issued
+            mbar_arrive_expect_tx(q_full, 2 * LY::OP_BYTES);
+            for (int sub = 0; sub < 2; ++sub)
+                for (int g = 0; g < 4; ++g)
+                    for (int cb = 0; cb < LY::NCB; ++cb) {
+                        unsigned char* dst =
+                            smem + LY::QR_OFF + sub * LY::OP_BYTES + cb * LY::SUB_BYTES;
+                        const int row = q0 + 64 * sub + 16 * g;
+                        tc::tma_load_3d(dst + (32 * g) * 128, &tmQ, cb * 64, row, z, q_full);
+                        tc::tma_load_3d(dst + (32 * g + 16) * 128, &tmR, cb * 64, row, z, q_full);
+                    }
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait(&k_empty[st], ((j >> 1) - 1) & 1, &g_tc_err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&k_full[st], LY::OP_BYTES);
+                for (int cb = 0; cb < LY::NCB; ++cb)
+                    tc::tma_load_3d(smem + LY::K_OFF + st * LY::OP_BYTES + cb * LY::SUB_BYTES, &tmK,
+                                    cb * 64, j * BN, z, &k_full[st]);
+                kj = j + 1;
+                if (j >= 2 && !mbar_wait(&v_empty[st], ((j >> 1) - 1) & 1, &g_tc_err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&v_full[st], LY::OP_BYTES);
+                for (int cb = 0; cb < LY::NCB; ++cb)
+                    tc::tma_load_3d(smem + LY::V_OFF + st * LY::OP_BYTES + cb * LY::SUB_BYTES, &tmV,
+                                    cb * 64, j * BN, z, &v_full[st]);
+                vj = j + 1;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                // wait (bounded) for the copies already issued into this CTA's shared memory
+                mbar_wait(q_full, 0, &g_tc_err);
+                for (int k = (kj >= 2 ? kj - 2 : 0); k < kj; ++k)
+                    mbar_wait(&k_full[k & 1], (k >> 1) & 1, &g_tc_err);
+                for (int k = (vj >= 2 ? vj - 2 : 0); k < vj; ++k)
+                    mbar_wait(&v_full[k & 1], (k >> 1) & 1, &g_tc_err);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0 && !skip) {
+            constexpr uint32_t kIdesc1 = tc::idesc_bf16_f32(128, BN, false);
+            constexpr uint32_t kIdesc2 = tc::idesc_bf16_f32(128, D, true);
+            const uint32_t sbase = smem_u32(smem);
+            // descriptors: one base each; a stage / sub-tile / K-step only adds a
+            // constant to the 16-byte start-address field
+            const uint64_t dQR0 = tc::smem_desc_sw128(sbase + LY::QR_OFF, 16, 1024);
+            const uint64_t dK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, 16, 1024);
+            const uint64_t dV0 = tc::smem_desc_sw128(sbase + LY::V_OFF, LY::SUB_BYTES, 1024);
+            constexpr uint32_t kOpStep = LY::OP_BYTES >> 4;
+            auto mma1 = [&](int sub, int st) {  // D_sub = [Q;rho]_sub K^T
+                const uint64_t dA = dQR0 + (uint32_t)sub * kOpStep;
+                const uint64_t dB = dK0 + (uint32_t)st * kOpStep;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk / 4) * LY::SUB_BYTES + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem + LY::dcol(sub), dA + off, dB + off, kIdesc1, kk > 0);
+                }
+            };
+            auto mma2 = [&](int sub, int st, bool first) {  // O_sub += [P;PR]_sub V
+                const uint64_t dB = dV0 + (uint32_t)st * kOpStep;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint32_t off = (kk * 16 * 128) >> 4;
+                    tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + kk * 8, dB + off,
+                               kIdesc2, (first && kk == 0) ? 0u : 1u);
+                    if (precise)
+                        tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + 64 + kk * 8,
+                                   dB + off, kIdesc2, 1u);
+                }
+            };
+            bool ok = mbar_wait(q_full, 0, &g_tc_err) && mbar_wait(&k_full[0], 0, &g_tc_err);
+            tc::fence_after_sync();
+            if (ok) {
+                mma1(0, 0);
+                tc::commit(&s_full[0]);
+                mma1(1, 0);
+                tc::commit(&s_full[1]);
+                tc::commit(&k_empty[0]);
+            }
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int st = j & 1;
+                const bool more = j + 1 < n_kv;
+                if (!mbar_wait(&p_full[0], j & 1, &g_tc_err) ||
+                    !mbar_wait(&v_full[st], (j >> 1) & 1, &g_tc_err)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                mma2(0, st, j == 0);
+                if (more) {
+                    if (!mbar_wait(&k_full[st ^ 1], ((j + 1) >> 1) & 1, &g_tc_err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    mma1(0, st ^ 1);  // in-order after mma2(0): P_0 is consumed before D_0 is rewritten
+                    tc::commit(&s_full[0]);
+                }
+                if (!mbar_wait(&p_full[1], j & 1, &g_tc_err)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                mma2(1, st, j == 0);
+                tc::commit(&v_empty[st]);
+                if (more) {
+                    mma1(1, st ^ 1);
+                    tc::commit(&s_full[1]);
+                    tc::commit(&k_empty[st ^ 1]);
+                }
+            }
+            tc::commit(o_full);
+            if (!ok) {
+                *abort_flag = 1;
+                mbar_wait(o_full, 0, &g_tc_err);  // the MMAs already issued have drained
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax / epilogue
+        const int sub = (warp - 2) >> 2;
+        const int g = warp & 3;               // TMEM lane quarter of this warp
+        const int h = lane >> 4;              // which half of the key (and d) columns
+        const int qi = 16 * g + (lane & 15);  // query within the sub-tile
+        const int i = q0 + 64 * sub + qi;     // query index
+        const uint32_t rowS = tmem + ((uint32_t)(32 * g) << 16);
+        const uint32_t rowR = tmem + ((uint32_t)(32 * g + 16) << 16);
+        const uint32_t tS = rowS + LY::dcol(sub), tR = rowR + LY::dcol(sub);
+        const uint32_t tU = rowS + LY::ocol(sub), tW = rowR + LY::ocol(sub);
+        const float qs = a.qscale;
+        float m = -INFINITY, l = 0.f, A = 0.f, c = 0.f;
+        bool ok = !skip;
+        for (int it = 0; it < n_kv && ok; ++it) {
+            // this thread owns keys it*128 + 64h + 32b + x, b in {0,1}, x in [0,32)
+            const int k0 = it * BN + 64 * h;
+            const bool got = !*abort_flag && mbar_wait(&s_full[sub], it & 1, &g_tc_err);
+            if (!__all_sync(kFullMask, got)) {  // warp-uniform exit
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            uint32_t sv[2][32];
+            tc::tmem_ld32_split<64>(tS, sv[0]);
+            tc::tmem_ld32_split<64>(tS + 32, sv[1]);
+            tc::tmem_ld_wait();
+
+            const bool need_mask = (it * BN + BN > a.L) || (CAUSAL && it == n_kv - 1);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    float f = __uint_as_float(sv[b][x]);
+                    if (need_mask) {
+                        const int key = k0 + 32 * b + x;
+                        f = (key < a.L && (!CAUSAL || key <= i)) ? f : -INFINITY;
+                        sv[b][x] = __float_as_uint(f);
+                    }
+                    mx = fmaxf(mx, f);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16)) * qs;
+            if (it == 0) {
+                m = mx;
+            } else if (__any_sync(kFullMask, mx > m + kRescaleThreshold)) {
+                // TMEM accesses are warp-collective: the whole warp rescales, rows
+                // whose max did not grow use alpha = 1
+                const float m_new = fmaxf(m, mx);
+                const float alpha = fast_exp2(m - m_new);
+                l *= alpha;
+                A *= alpha;
+#pragma unroll 1
+                for (int b = 0; b < D / 64; ++b) {
+                    uint32_t u[32];
+                    tc::tmem_ld32_split<D / 2>(tU + 32 * b, u);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
+                    tc::tmem_st32_split<D / 2>(tU + 32 * b, u);
+                    tc::tmem_ld32_split<D / 2>(tW + 32 * b, u);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
+                    tc::tmem_st32_split<D / 2>(tW + 32 * b, u);
+                }
+                m = m_new;
+            }
+            const float nm = -m;
+            float lsum = 0.f;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    const float p = fast_exp2(fmaf(__uint_as_float(sv[b][x]), qs, nm));
+                    sv[b][x] = __float_as_uint(p);
+                    lsum += p;
+                }
+                // P (bf16) -> packed columns 16b.. of this thread's half (split 32)
+                uint32_t pk[16];
+#pragma unroll
+                for (int y = 0; y < 16; ++y)
+                    pk[y] = tc::pack_bf16(__uint_as_float(sv[b][2 * y]),
+                                          __uint_as_float(sv[b][2 * y + 1]));
+                tc::tmem_st16_split<32>(tS + 16 * b, pk);
+                if (precise) {
+#pragma unroll
+                    for (int y = 0; y < 16; ++y)
+                        pk[y] = tc::pack_bf16(
+                            __uint_as_float(sv[b][2 * y]) - tc::bf16_lo_to_f32(pk[y]),
+                            __uint_as_float(sv[b][2 * y + 1]) - tc::bf16_hi_to_f32(pk[y]));
+                    tc::tmem_st16_split<32>(tS + 64 + 16 * b, pk);
+                }
+            }
+            if (it == 0) {  // row shift: p-weighted mean of r over the first (full) key tile
+                float prs = 0.f;
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    uint32_t rv[32];
+                    tc::tmem_ld32_split<64>(tR + 32 * b, rv);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        prs = fmaf(__uint_as_float(sv[b][x]), __uint_as_float(rv[x]), prs);
+                }
+                prs += __shfl_xor_sync(kFullMask, prs, 16);
+                c = prs / (lsum + __shfl_xor_sync(kFullMask, lsum, 16));
+            }
+            // PR = p (r - c).  Both R blocks are read before the first PR store: the
+            // packed output of one half of a row lands in columns that the other
+            // half reads as R.
+            float asum = 0.f;
+            uint32_t r0[32], r1[32];
+            tc::tmem_ld32_split<64>(tR, r0);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                const float pr = __uint_as_float(sv[0][x]) * (__uint_as_float(r0[x]) - c);
+                r0[x] = __float_as_uint(pr);
+                asum += pr;
+            }
+            tc::tmem_ld32_split<64>(tR + 32, r1);
+            tc::tmem_ld_wait();
+            store_pr_block(tR, r0, 0, precise);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                const float pr = __uint_as_float(sv[1][x]) * (__uint_as_float(r1[x]) - c);
+                r1[x] = __float_as_uint(pr);
+                asum += pr;
+            }
+            store_pr_block(tR, r1, 1, precise);
+            l += lsum;
+            A += asum;
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            mbar_arrive(&p_full[sub]);
+        }
+
+        // ---- epilogue: o = U/l - (W/l - (A/l)(U/l)) = ((U (1 + A/l)) - W) / l
+        const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_tc_err);
+        if (__all_sync(kFullMask, done)) {
+            tc::fence_after_sync();
+            const float lt = l + __shfl_xor_sync(kFullMask, l, 16);
+            const float At = A + __shfl_xor_sync(kFullMask, A, 16);
+            const float inv_l = 1.f / lt;
+            const float gain = 1.f + At * inv_l;
+            float* orow = a.o + ((size_t)bh * a.L + i) * D + h * (D / 2);
+#pragma unroll 1
+            for (int b = 0; b < D / 64; ++b) {
+                uint32_t u[32], w[32];
+                tc::tmem_ld32_split<D / 2>(tU + 32 * b, u);
+                tc::tmem_ld32_split<D / 2>(tW + 32 * b, w);
+                tc::tmem_ld_wait();
+                if (i < a.L) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 4) {
+                        float out[4];
+#pragma unroll
+                        for (int y = 0; y < 4; ++y)
+                            out[y] = (__uint_as_float(u[x + y]) * gain - __uint_as_float(w[x + y])) *
+                                     inv_l;
+                        *reinterpret_cast<float4*>(orow + 32 * b + x) =
+                            make_float4(out[0], out[1], out[2], out[3]);
+                    }
+                }
+            }
+        } else {
+            *abort_flag = 1;
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -412,14 +829,14 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [B*H, L, D] bf16 viewed as a 3-D tensor; box = 64 columns (128 bytes) x 128 rows x 1 head,
+// [B*H, L, D] bf16 viewed as a 3-D tensor; box = 64 columns (128 bytes) x box_rows rows x 1 head,
 // 128-byte swizzle; rows past L read as zeros.
-bool make_map(CUtensorMap* m, const void* base, int BH, int L, int D) {
+bool make_map(CUtensorMap* m, const void* base, int BH, int L, int D, int box_rows = 128) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * D * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -443,6 +860,23 @@ cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mr, const CUtensorM
     return cudaGetLastError();
 }
 
+template <int D, bool CAUSAL>
+cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mr, const CUtensorMap& mk,
+                        const CUtensorMap& mv, const TcArgs& a, cudaStream_t stream) {
+    using LY = PairLayout<D>;
+    auto kern = prefill_pair_kernel<D, CAUSAL>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             LY::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const unsigned grid = (unsigned)((size_t)a.n_qt * a.BH);
+    kern<<<grid, kThreads2, LY::SMEM_BYTES, stream>>>(mq, mr, mk, mv, a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t prefill_tc_launch(const PrefillShape& s, const void* q, const void* rho,
@@ -460,6 +894,18 @@ cudaError_t prefill_tc_launch(const PrefillShape& s, const void* q, const void* 
     }
     TcArgs a{o, s.L, BH, (s.L + BM - 1) / BM, s.scale * kLog2e};
     const bool r = rho != nullptr;
+    if (r) {
+        // correction path: query and probe maps use 16-row boxes (stacked operand)
+        if (!make_map(&mq, q, BH, s.L, s.d, 16) || !make_map(&mr, rho, BH, s.L, s.d, 16))
+            return cudaErrorInvalidValue;
+        if (s.d == 64)
+            return s.causal ? launch_pair<64, true>(mq, mr, mk, mv, a, stream)
+                            : launch_pair<64, false>(mq, mr, mk, mv, a, stream);
+        if (s.d == 128)
+            return s.causal ? launch_pair<128, true>(mq, mr, mk, mv, a, stream)
+                            : launch_pair<128, false>(mq, mr, mk, mv, a, stream);
+        return cudaErrorInvalidValue;
+    }
 #define PARALLAX_TC_CASE(DD)                                                               \
     if (s.d == DD) {                                                                       \
         if (r) return s.causal ? launch<DD, true, true>(mq, mr, mk, mv, a, stream)         \
