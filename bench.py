@@ -338,7 +338,11 @@ def run_ours(args):
                 "peak_burst": peaks["bf16_tflops"],
                 "frac_burst": pre_tflops / peaks["bf16_tflops"],
                 "peak_source": peaks["source"] + " (sustained)"}
-    dominant = roof_pre if (run_prefill and (pre_ms >= dec_ms or not run_decode)) else roof_dec
+    if not run_decode:
+        roof_dec = None
+    if not run_prefill:
+        roof_pre = None
+    dominant = roof_pre if (run_prefill and (not run_decode or pre_ms >= dec_ms)) else roof_dec
 
     # ---- W_R = 0 fast paths (rho = NULL), for context
     f0 = {}
@@ -436,11 +440,12 @@ def run_ours(args):
             "roofline": dominant,
             "roofline_decode": roof_dec,
             "roofline_prefill": roof_pre,
-            "prefill": {"metric": "causal prefill TFLOP/s", "value": ws * pre_tflops,
-                        "unit": "TFLOP/s", "frac_of_peak": roof_pre["frac"],
-                        "ms_per_launch": pre_ms, "e2e": e2e_prefill},
-            "decode": {"metric": "decode KV-stream GB/s", "value": value, "unit": "GB/s",
-                       "frac_of_peak": roof_dec["frac"], "ms_per_call": dec_ms},
+            "prefill": None if roof_pre is None else {
+                "metric": "causal prefill TFLOP/s", "value": ws * pre_tflops, "unit": "TFLOP/s",
+                "frac_of_peak": roof_pre["frac"], "ms_per_launch": pre_ms, "e2e": e2e_prefill},
+            "decode": None if roof_dec is None else {
+                "metric": "decode KV-stream GB/s", "value": value, "unit": "GB/s",
+                "frac_of_peak": roof_dec["frac"], "ms_per_call": dec_ms},
             "w_r_zero_fast_path": f0,
             "e2e": e2e,
             "cpu_baseline": cpu,

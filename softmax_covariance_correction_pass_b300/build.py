@@ -62,6 +62,36 @@ def _compile(src: str) -> tuple[str, str]:
     return obj, r.stdout + r.stderr
 
 
+# Kernels that hand registers between warpgroups (setmaxnreg) must be launched
+# with exactly the per-thread register count their hand-over arithmetic assumes;
+# a smaller launch allocation would make the raising warpgroups wait forever.
+LAUNCH_REGISTERS = {"prefill_pair_kernel": 168}
+
+
+def kernel_registers(log: str) -> dict:
+    """Map each compiled kernel (mangled name) to the registers ptxas assigned."""
+    regs, name = {}, None
+    for line in log.splitlines():
+        if "Compiling entry function" in line:
+            name = line.split("'")[1]
+        elif name and "Used" in line and "registers" in line:
+            regs[name] = int(line.split("Used")[1].split("registers")[0])
+            name = None
+    return regs
+
+
+def check_registers(log: str) -> None:
+    regs = kernel_registers(log)
+    for key, want in LAUNCH_REGISTERS.items():
+        found = {n: r for n, r in regs.items() if key in n}
+        if not found:
+            raise RuntimeError(f"no kernel matching {key} in the ptxas report")
+        bad = {n: r for n, r in found.items() if r != want}
+        if bad:
+            raise RuntimeError(f"{key}: ptxas assigned {sorted(set(bad.values()))} registers, "
+                               f"the register hand-over needs exactly {want}")
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
@@ -72,6 +102,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     log = "\n".join(r[1] for r in results)
     with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
         f.write(log)
+    check_registers(log)
     if verbose:
         print(log)
     tmp = LIB + f".tmp{os.getpid()}"

@@ -82,6 +82,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     }
 }
 
+// Warp-collective form of mbar_wait for code that the whole warp runs (the
+// MMA issuer): every lane polls, and the result is the same on all lanes, so
+// that a timeout seen by one lane takes the whole warp down the same path.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned* err) {
+    return __all_sync(kFullMask, mbar_wait(bar, parity, err));
+}
+
 // ----------------------------------------------------------------------------
 // bulk (non-tensor) asynchronous copies global -> shared, completing on an mbarrier
 // ----------------------------------------------------------------------------
@@ -109,6 +116,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// max(a, b, c) in one instruction (three-input max of the sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

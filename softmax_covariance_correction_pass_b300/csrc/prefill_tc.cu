@@ -186,10 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0 && !skip) {
+        // (the whole warp runs this; one elected lane issues each MMA and commit)
+        if (!skip) {
             constexpr uint32_t kIdescS = tc::idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t kIdescV = tc::idesc_bf16_f32(BM, D, true);
-            bool ok = mbar_wait(q_full, 0, &g_tc_err);
+            bool ok = mbar_wait_warp(q_full, 0, &g_tc_err);
             tc::fence_after_sync();
             // Descriptors are built once; a K-step only adds a constant to the
             // start-address field (bits 0..13, in 16-byte units).
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sK = kv0 + s * LY::STAGE_BYTES;
                 const uint64_t dK = tc::smem_desc_sw128(sK, 16, 1024);
                 const uint64_t dV = tc::smem_desc_sw128(sK + LY::TILE_BYTES, LY::SUB_BYTES, 1024);
-                if (!mbar_wait(&k_full[s], ph, &g_tc_err)) { ok = false; break; }
+                if (!mbar_wait_warp(&k_full[s], ph, &g_tc_err)) { ok = false; break; }
                 tc::fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -211,9 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (RHO) tc::mma_ss(tmem + LY::R_COL, dR + off, dK + off, kIdescS, kk > 0);
                 }
                 tc::commit(s_full);
-                if (!mbar_wait(p_full, it & 1, &g_tc_err)) { ok = false; break; }
+                if (!mbar_wait_warp(p_full, it & 1, &g_tc_err)) { ok = false; break; }
                 tc::fence_after_sync();
-                if (!mbar_wait(&v_full[s], ph, &g_tc_err)) { ok = false; break; }
+                if (!mbar_wait_warp(&v_full[s], ph, &g_tc_err)) { ok = false; break; }
                 tc::fence_after_sync();
                 const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::commit(o_full);
             if (!ok) {
                 *abort_flag = 1;
-                mbar_wait(o_full, 0, &g_tc_err);  // MMAs already issued have drained
+                mbar_wait_warp(o_full, 0, &g_tc_err);  // MMAs already issued have drained
             }
         }
     } else {
@@ -412,7 +413,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 // TMEM columns: D_sub at 128*sub (S|R, then P|PR packed into its first 64
 // columns, the few-key residuals into the next 64), O_sub at 256 + sub*d (U|W).
 // ============================================================================
-constexpr int kThreads2 = 320;  // warp 0 TMA, warp 1 TMEM + MMA, warps 2-5 / 6-9: sub-tile 0 / 1
+// 12 warps = 3 warpgroups: warp 0 TMA, warp 1 TMEM + MMA (warps 2-3 idle),
+// warps 4-7 / 8-11: softmax of sub-tile 0 / 1.  The first warpgroup hands
+// registers to the other two (setmaxnreg): the launch gives every thread
+// kRegsLaunch registers (3 warps per SM sub-partition x 32 x 168 <= 16384);
+// afterwards 4 warps x 64 + 8 warps x 216 use no more than that total.  The
+// build checks that ptxas assigned kRegsLaunch registers to this kernel.
+constexpr int kThreads2 = 384;
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsSupport = 64;
+constexpr int kRegsSoftmax = 216;
+static_assert(128 * kRegsSupport + 256 * kRegsSoftmax <= kThreads2 * kRegsLaunch,
+              "register hand-over exceeds the launch allocation");
 constexpr int kHeadGroup = 16;  // heads per CTA-scheduling group (keeps their K/V in L2)
 
 template <int D>
@@ -430,25 +442,6 @@ struct PairLayout {
     __host__ __device__ static constexpr uint32_t dcol(int sub) { return 128u * sub; }
     __host__ __device__ static constexpr uint32_t ocol(int sub) { return 256u + (uint32_t)(D * sub); }
 };
-
-// Pack 32 fp32 values (this thread's key block b) to bf16 and store them in
-// the packed columns 16b.. of this thread's half of the row (split 32); with
-// `residual`, also store bf16(x - bf16(x)) 64 columns further on.
-__device__ __forceinline__ void store_pr_block(uint32_t taddr, const uint32_t (&v)[32], int b,
-                                               bool residual) {
-    uint32_t pk[16];
-#pragma unroll
-    for (int y = 0; y < 16; ++y)
-        pk[y] = tc::pack_bf16(__uint_as_float(v[2 * y]), __uint_as_float(v[2 * y + 1]));
-    tc::tmem_st16_split<32>(taddr + 16 * b, pk);
-    if (residual) {
-#pragma unroll
-        for (int y = 0; y < 16; ++y)
-            pk[y] = tc::pack_bf16(__uint_as_float(v[2 * y]) - tc::bf16_lo_to_f32(pk[y]),
-                                  __uint_as_float(v[2 * y + 1]) - tc::bf16_hi_to_f32(pk[y]));
-        tc::tmem_st16_split<32>(taddr + 64 + 16 * b, pk);
-    }
-}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads2, 1)
@@ -503,7 +496,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const bool skip = *abort_flag != 0;
-
+    if (warp < 4) {
+        tc::setmaxnreg_dec<kRegsSupport>();
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0 && !skip) {
@@ -553,7 +547,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0 && !skip) {
+        // (the whole warp runs this; one elected lane issues each MMA and commit)
+        if (!skip) {
             constexpr uint32_t kIdesc1 = tc::idesc_bf16_f32(128, BN, false);
             constexpr uint32_t kIdesc2 = tc::idesc_bf16_f32(128, D, true);
             const uint32_t sbase = smem_u32(smem);
@@ -563,9 +558,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
             const uint64_t dK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, 16, 1024);
             const uint64_t dV0 = tc::smem_desc_sw128(sbase + LY::V_OFF, LY::SUB_BYTES, 1024);
             constexpr uint32_t kOpStep = LY::OP_BYTES >> 4;
+            // (the per-call bases pass through tc::opaque so that the compiler does
+            // not hoist every K-step's descriptor out of the tile loop and keep them
+            // all live in registers)
             auto mma1 = [&](int sub, int st) {  // D_sub = [Q;rho]_sub K^T
-                const uint64_t dA = dQR0 + (uint32_t)sub * kOpStep;
-                const uint64_t dB = dK0 + (uint32_t)st * kOpStep;
+                const uint64_t dA = tc::opaque(dQR0 + (uint32_t)sub * kOpStep);
+                const uint64_t dB = tc::opaque(dK0 + (uint32_t)st * kOpStep);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk / 4) * LY::SUB_BYTES + (kk % 4) * 32) >> 4;
@@ -573,18 +571,27 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 }
             };
             auto mma2 = [&](int sub, int st, bool first) {  // O_sub += [P;PR]_sub V
-                const uint64_t dB = dV0 + (uint32_t)st * kOpStep;
+                const uint64_t dB = tc::opaque(dV0 + (uint32_t)st * kOpStep);
+                const uint32_t acc0 = first ? 0u : 1u;
+                if (precise) {
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint32_t off = (kk * 16 * 128) >> 4;
-                    tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + kk * 8, dB + off,
-                               kIdesc2, (first && kk == 0) ? 0u : 1u);
-                    if (precise)
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint32_t off = (kk * 16 * 128) >> 4;
+                        tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + kk * 8, dB + off,
+                                   kIdesc2, kk == 0 ? acc0 : 1u);
                         tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + 64 + kk * 8,
                                    dB + off, kIdesc2, 1u);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint32_t off = (kk * 16 * 128) >> 4;
+                        tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + kk * 8, dB + off,
+                                   kIdesc2, kk == 0 ? acc0 : 1u);
+                    }
                 }
             };
-            bool ok = mbar_wait(q_full, 0, &g_tc_err) && mbar_wait(&k_full[0], 0, &g_tc_err);
+            bool ok = mbar_wait_warp(q_full, 0, &g_tc_err) && mbar_wait_warp(&k_full[0], 0, &g_tc_err);
             tc::fence_after_sync();
             if (ok) {
                 mma1(0, 0);
@@ -596,15 +603,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int st = j & 1;
                 const bool more = j + 1 < n_kv;
-                if (!mbar_wait(&p_full[0], j & 1, &g_tc_err) ||
-                    !mbar_wait(&v_full[st], (j >> 1) & 1, &g_tc_err)) {
+                if (!mbar_wait_warp(&p_full[0], j & 1, &g_tc_err) ||
+                    !mbar_wait_warp(&v_full[st], (j >> 1) & 1, &g_tc_err)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
                 mma2(0, st, j == 0);
                 if (more) {
-                    if (!mbar_wait(&k_full[st ^ 1], ((j + 1) >> 1) & 1, &g_tc_err)) {
+                    if (!mbar_wait_warp(&k_full[st ^ 1], ((j + 1) >> 1) & 1, &g_tc_err)) {
                         ok = false;
                         break;
                     }
@@ -612,7 +619,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     mma1(0, st ^ 1);  // in-order after mma2(0): P_0 is consumed before D_0 is rewritten
                     tc::commit(&s_full[0]);
                 }
-                if (!mbar_wait(&p_full[1], j & 1, &g_tc_err)) {
+                if (!mbar_wait_warp(&p_full[1], j & 1, &g_tc_err)) {
                     ok = false;
                     break;
                 }
@@ -628,12 +635,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
             tc::commit(o_full);
             if (!ok) {
                 *abort_flag = 1;
-                mbar_wait(o_full, 0, &g_tc_err);  // the MMAs already issued have drained
+                mbar_wait_warp(o_full, 0, &g_tc_err);  // the MMAs already issued have drained
             }
         }
+    }
     } else {
+        tc::setmaxnreg_inc<kRegsSoftmax>();
         // ---------------------------------------------------------------- softmax / epilogue
-        const int sub = (warp - 2) >> 2;
+        const int sub = (warp - 4) >> 2;
         const int g = warp & 3;               // TMEM lane quarter of this warp
         const int h = lane >> 4;              // which half of the key (and d) columns
         const int qi = 16 * g + (lane & 15);  // query within the sub-tile
@@ -645,6 +654,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const float qs = a.qscale;
         float m = -INFINITY, l = 0.f, A = 0.f, c = 0.f;
         bool ok = !skip;
+        const float2 qs2 = make_float2(qs, qs);
         for (int it = 0; it < n_kv && ok; ++it) {
             // this thread owns keys it*128 + 64h + 32b + x, b in {0,1}, x in [0,32)
             const int k0 = it * BN + 64 * h;
@@ -654,25 +664,37 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 break;
             }
             tc::fence_after_sync();
-            uint32_t sv[2][32];
+            // S and R of this thread's 64 keys, behind a single wait
+            uint32_t sv[2][32], rv[2][32];
             tc::tmem_ld32_split<64>(tS, sv[0]);
             tc::tmem_ld32_split<64>(tS + 32, sv[1]);
+            tc::tmem_ld32_split<64>(tR, rv[0]);
+            tc::tmem_ld32_split<64>(tR + 32, rv[1]);
             tc::tmem_ld_wait();
 
             const bool need_mask = (it * BN + BN > a.L) || (CAUSAL && it == n_kv - 1);
-            float mx = -INFINITY;
+            if (need_mask) {
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        const int key = k0 + 32 * b + x;
+                        if (!(key < a.L && (!CAUSAL || key <= i)))
+                            sv[b][x] = __float_as_uint(-INFINITY);
+                    }
+            }
+            // row max: four independent chains of three-input max
+            float c0 = -INFINITY, c1 = -INFINITY, c2 = -INFINITY, c3 = -INFINITY;
 #pragma unroll
             for (int b = 0; b < 2; ++b)
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    float f = __uint_as_float(sv[b][x]);
-                    if (need_mask) {
-                        const int key = k0 + 32 * b + x;
-                        f = (key < a.L && (!CAUSAL || key <= i)) ? f : -INFINITY;
-                        sv[b][x] = __float_as_uint(f);
-                    }
-                    mx = fmaxf(mx, f);
+                for (int x = 0; x < 32; x += 8) {
+                    c0 = fmax3(c0, __uint_as_float(sv[b][x]), __uint_as_float(sv[b][x + 1]));
+                    c1 = fmax3(c1, __uint_as_float(sv[b][x + 2]), __uint_as_float(sv[b][x + 3]));
+                    c2 = fmax3(c2, __uint_as_float(sv[b][x + 4]), __uint_as_float(sv[b][x + 5]));
+                    c3 = fmax3(c3, __uint_as_float(sv[b][x + 6]), __uint_as_float(sv[b][x + 7]));
                 }
+            float mx = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3));
             mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16)) * qs;
             if (it == 0) {
                 m = mx;
@@ -699,22 +721,25 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 }
                 m = m_new;
             }
-            const float nm = -m;
-            float lsum = 0.f;
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-#pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const float p = fast_exp2(fmaf(__uint_as_float(sv[b][x]), qs, nm));
-                    sv[b][x] = __float_as_uint(p);
-                    lsum += p;
-                }
-                // P (bf16) -> packed columns 16b.. of this thread's half (split 32)
+            // P = 2^(S*scale*log2e - m) (packed fp32x2 FMA, SFU exponentials), P (bf16)
+            // -> packed columns 16b.. of this thread's half of the row (split 32);
+            // p overwrites s in registers
+            const float2 nm2 = make_float2(-m, -m);
+            float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
+            auto do_p = [&](int b) {
                 uint32_t pk[16];
 #pragma unroll
-                for (int y = 0; y < 16; ++y)
-                    pk[y] = tc::pack_bf16(__uint_as_float(sv[b][2 * y]),
-                                          __uint_as_float(sv[b][2 * y + 1]));
+                for (int y = 0; y < 16; ++y) {
+                    const float2 t = __ffma2_rn(
+                        make_float2(__uint_as_float(sv[b][2 * y]), __uint_as_float(sv[b][2 * y + 1])),
+                        qs2, nm2);
+                    const float2 p2 = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+                    sv[b][2 * y] = __float_as_uint(p2.x);
+                    sv[b][2 * y + 1] = __float_as_uint(p2.y);
+                    if (y & 1) ls1 = __fadd2_rn(ls1, p2);
+                    else ls0 = __fadd2_rn(ls0, p2);
+                    pk[y] = tc::pack_bf16(p2.x, p2.y);
+                }
                 tc::tmem_st16_split<32>(tS + 16 * b, pk);
                 if (precise) {
 #pragma unroll
@@ -724,46 +749,73 @@ __global__ void __launch_bounds__(kThreads2, 1)
                             __uint_as_float(sv[b][2 * y + 1]) - tc::bf16_hi_to_f32(pk[y]));
                     tc::tmem_st16_split<32>(tS + 64 + 16 * b, pk);
                 }
-            }
-            if (it == 0) {  // row shift: p-weighted mean of r over the first (full) key tile
-                float prs = 0.f;
+            };
+            // PR = p (r - c) -> packed columns of the R rows.  R was read in full
+            // above, so these stores may land on columns that the other half of
+            // the row read as R.
+            float2 as0 = make_float2(0.f, 0.f), as1 = make_float2(0.f, 0.f);
+            auto do_pr = [&](int b) {
+                const float2 nc2 = make_float2(-c, -c);
+                uint32_t pk[16];
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    uint32_t rv[32];
-                    tc::tmem_ld32_split<64>(tR + 32 * b, rv);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int x = 0; x < 32; ++x)
-                        prs = fmaf(__uint_as_float(sv[b][x]), __uint_as_float(rv[x]), prs);
+                for (int y = 0; y < 16; ++y) {
+                    const float2 p2 = make_float2(__uint_as_float(sv[b][2 * y]),
+                                                  __uint_as_float(sv[b][2 * y + 1]));
+                    const float2 r2 = make_float2(__uint_as_float(rv[b][2 * y]),
+                                                  __uint_as_float(rv[b][2 * y + 1]));
+                    const float2 pr = __fmul2_rn(p2, __fadd2_rn(r2, nc2));
+                    rv[b][2 * y] = __float_as_uint(pr.x);
+                    rv[b][2 * y + 1] = __float_as_uint(pr.y);
+                    if (y & 1) as1 = __fadd2_rn(as1, pr);
+                    else as0 = __fadd2_rn(as0, pr);
+                    pk[y] = tc::pack_bf16(pr.x, pr.y);
                 }
+                tc::tmem_st16_split<32>(tR + 16 * b, pk);
+                if (precise) {
+#pragma unroll
+                    for (int y = 0; y < 16; ++y)
+                        pk[y] = tc::pack_bf16(
+                            __uint_as_float(rv[b][2 * y]) - tc::bf16_lo_to_f32(pk[y]),
+                            __uint_as_float(rv[b][2 * y + 1]) - tc::bf16_hi_to_f32(pk[y]));
+                    tc::tmem_st16_split<32>(tR + 64 + 16 * b, pk);
+                }
+            };
+            if (it == 0) {
+                // row shift c: p-weighted mean of r over the first (full) key tile,
+                // needed before any PR
+                do_p(0);
+                do_p(1);
+                float2 pr0 = make_float2(0.f, 0.f), pr1 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+#pragma unroll
+                    for (int y = 0; y < 16; ++y) {
+                        const float2 p2 = make_float2(__uint_as_float(sv[b][2 * y]),
+                                                      __uint_as_float(sv[b][2 * y + 1]));
+                        const float2 r2 = make_float2(__uint_as_float(rv[b][2 * y]),
+                                                      __uint_as_float(rv[b][2 * y + 1]));
+                        if (y & 1) pr1 = __ffma2_rn(p2, r2, pr1);
+                        else pr0 = __ffma2_rn(p2, r2, pr0);
+                    }
+                const float2 ls = __fadd2_rn(ls0, ls1);
+                const float2 pr = __fadd2_rn(pr0, pr1);
+                float prs = pr.x + pr.y;
                 prs += __shfl_xor_sync(kFullMask, prs, 16);
-                c = prs / (lsum + __shfl_xor_sync(kFullMask, lsum, 16));
+                c = prs / (ls.x + ls.y + __shfl_xor_sync(kFullMask, ls.x + ls.y, 16));
+                do_pr(0);
+                do_pr(1);
+            } else {
+                // one pass per 32-key block keeps fewer values live
+                do_p(0);
+                do_pr(0);
+                do_p(1);
+                do_pr(1);
             }
-            // PR = p (r - c).  Both R blocks are read before the first PR store: the
-            // packed output of one half of a row lands in columns that the other
-            // half reads as R.
-            float asum = 0.f;
-            uint32_t r0[32], r1[32];
-            tc::tmem_ld32_split<64>(tR, r0);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                const float pr = __uint_as_float(sv[0][x]) * (__uint_as_float(r0[x]) - c);
-                r0[x] = __float_as_uint(pr);
-                asum += pr;
-            }
-            tc::tmem_ld32_split<64>(tR + 32, r1);
-            tc::tmem_ld_wait();
-            store_pr_block(tR, r0, 0, precise);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                const float pr = __uint_as_float(sv[1][x]) * (__uint_as_float(r1[x]) - c);
-                r1[x] = __float_as_uint(pr);
-                asum += pr;
-            }
-            store_pr_block(tR, r1, 1, precise);
+            const float2 ls = __fadd2_rn(ls0, ls1);
+            const float lsum = ls.x + ls.y;
+            const float2 as = __fadd2_rn(as0, as1);
             l += lsum;
-            A += asum;
+            A += as.x + as.y;
             tc::tmem_st_wait();
             tc::fence_before_sync();
             mbar_arrive(&p_full[sub]);

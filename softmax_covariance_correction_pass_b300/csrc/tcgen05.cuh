@@ -76,13 +76,29 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
 }
 
 // ---------------------------------------------------------------- MMA
+// Returns x unchanged, but the compiler cannot see through it (it is not
+// hoisted or constant-folded).
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+    uint64_t y;
+    asm volatile("mov.b64 %0, %1;" : "=l"(y) : "l"(x));
+    return y;
+}
+
+// tcgen05.mma and tcgen05.commit are issued by a single thread.  These
+// wrappers are called by ALL 32 lanes of a converged warp and let one lane,
+// chosen by elect.sync, issue the instruction: the operands are then
+// warp-uniform values, which the compiler keeps on the uniform datapath, so
+// back-to-back MMAs issue as fast as the tensor core retires them (a
+// lane-0-only issue loop was measured at about twice the MMA time per MMA).
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T  (M x N x 16)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -91,19 +107,35 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// Arrive once on *bar when every tcgen05.mma issued so far by this thread has completed.
+// Arrive once on *bar when every tcgen05.mma issued so far by this warp's
+// elected lane has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
             smem_u32(bar))
         : "memory");
+}
+
+// ---------------------------------------------------------------- register hand-over
+// Warpgroup-collective (all 4 warps of an aligned warpgroup execute it):
+// lower / raise this warpgroup's per-thread register allocation to N.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- TMEM <-> registers
