@@ -31,10 +31,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode KV-stream GB/s (% B300 HBM peak); causal prefill TFLOP/s (% TC peak)"
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
-# ncu captures summarised in profiles/; None until a capture of the current
-# kernel exists.
-TRAFFIC_BYTES = {"decode": None, "prefill": None}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# bench-size launch, from the ncu captures summarised in profiles/ (taken on
+# smaller cases and scaled by the units processed; see those files).  None when
+# the kernel has changed since its counters were taken.
+TRAFFIC_BYTES = {
+    # B=8 capture: 536.98 MB read (x8 heads' worth at B=64) + ~5.9 MB partials and o
+    "decode": 8 * 536.98e6 + 5.9e6,
+    # B=2 capture: 135.58 MB read (x4 at B=8) + the 268.4 MB fp32 output written
+    "prefill": 4 * 135.58e6 + 268.4e6,
+}
 
 
 def parse_args(argv=None):
