@@ -118,6 +118,32 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// 2^x for a pair of x <= 0 (-inf allowed) on the FMA/ALU pipes, to take part of
+// the exponentials off the SFU.  Method: Cody-Waite style split x = n + f with
+// n = round(x) (added to a 1.5 * 2^23 bias, whose low mantissa bits then hold
+// n) and f in [-1/2, 1/2]; 2^f from a degree-3 polynomial whose coefficients
+// are a minimax fit of the relative error on [-1/2, 1/2] (Lawson's iteratively
+// reweighted least squares, computed offline); 2^n is added to the exponent
+// field.  Maximum relative error 7.5e-5 (the product path rounds P to bf16,
+// 3.9e-3).  x is clamped to -125, so 2^x underflows to ~2.4e-38, not to 0.
+constexpr float kExp2C0 = 0.99992806f;
+constexpr float kExp2C1 = 0.69326097f;
+constexpr float kExp2C2 = 0.24261114f;
+constexpr float kExp2C3 = 0.055171669f;
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+    x.x = fmaxf(x.x, -125.f);
+    x.y = fmaxf(x.y, -125.f);
+    const float2 bias = make_float2(12582912.f, 12582912.f);  // 1.5 * 2^23
+    const float2 j = __fadd2_rn(x, bias);
+    const float2 n = __fadd2_rn(j, make_float2(-12582912.f, -12582912.f));
+    const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
+    float2 p = __ffma2_rn(f, make_float2(kExp2C3, kExp2C3), make_float2(kExp2C2, kExp2C2));
+    p = __ffma2_rn(p, f, make_float2(kExp2C1, kExp2C1));
+    p = __ffma2_rn(p, f, make_float2(kExp2C0, kExp2C0));
+    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(j.x) << 23)),
+                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(j.y) << 23)));
+}
+
 // max(a, b, c) in one instruction (three-input max of the sm_100 family).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;

@@ -1,8 +1,8 @@
 // Parallax prefill on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// One CTA computes a 128-query tile of one head.  For every 128-key tile of
-// K and V (fetched once by TMA and shared by both branches -- the pages' "same
-// KV stream for both branches", "Parallax mantem softmax ...", paragraph 2):
+// For every 128-key tile of K and V (fetched once by TMA and shared by both
+// branches -- the pages' "same KV stream for both branches", "Parallax mantem
+// softmax ...", paragraph 2) a CTA computes, for its query rows,
 //
 //   MMA-1   S = Q K^T   and   R = rho K^T            (bf16 in, fp32 in TMEM)
 //   softmax P = 2^(S*scale*log2e - m)  (row max m, lazily rescaled),
@@ -10,30 +10,49 @@
 //   MMA-2   U += P V    and   W += PR V               (P, PR read from TMEM)
 //
 // and at the end o = U/l - (W/l - (A/l)(U/l)) with l = sum P, A = sum PR.
+// With rho == NULL (W_R = 0) only S, P and U exist and o = U/l: plain softmax
+// attention.
 //
-// Roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
-// the MMAs (one elected thread), warps 2-5 (one TMEM lane quarter each, one
-// query row per thread) do the softmax, the correction-branch elementwise
-// work and the epilogue.
+// A CTA owns two query sub-tiles that take turns on the tensor core: while
+// the softmax warps of one sub-tile work, the MMAs of the other run.
 //
-// TMEM (512 columns x 128 lanes): S [0,128), R [128,256), U [256,256+d),
-// W [256+d, 256+2d).  P (bf16) overwrites S columns [0,64) and PR overwrites R
-// columns [0,64) after the softmax threads have read S and R.
+//  * correction path (RHO): a sub-tile is 64 queries and the A operand of
+//    MMA-1 stacks, per 16-query group g, the 16 query rows (operand rows
+//    32g..32g+15) and the same 16 queries' probe rows (rows 32g+16..32g+31).
+//    One M=128 MMA per sub-tile yields S and R for its 64 queries, and one
+//    M=128 MMA with A = [P; PR] (from TMEM) yields U and W.  TMEM lane 32g+i
+//    holds query 16g+i's S row (then P, then U) and lane 32g+16+i its R row
+//    (then PR, then W).  The half-split TMEM access (.16x32bx2) gives thread
+//    t < 16 and thread t + 16 of a softmax warp the same query's S and R rows,
+//    each with half of the key columns, so every thread computes s, r, p and
+//    p(r - c) for 64 keys of one query with no data exchange.
+//  * W_R = 0 path: a sub-tile is 128 queries (one per TMEM lane and softmax
+//    thread), A of MMA-1 is the Q tile, A of MMA-2 is P.
 //
-// Numerics:
+// TMEM columns: D_sub at 128*sub (S|R, then P|PR packed into its first 64
+// columns, the few-key residuals into the next 64), O_sub at 256 + sub*d.
+//
+// Warps (12 = 3 warpgroups): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs (warps 2-3 idle), warps 4-7 / 8-11 are the softmax and
+// epilogue warps of sub-tile 0 / 1.  The first warpgroup hands registers to
+// the other two (setmaxnreg).
+//
+// Numerics of the correction path:
 //  * the row shift c (Cov_p(r - c, v) = Cov_p(r, v) for any constant c) is set
 //    to the p-weighted mean of r over the first key tile processed, so PR is
 //    centred and its bf16 rounding error stays proportional to the spread of
 //    r rather than its size.  Key tiles are processed in order 0, 1, ..., with
 //    the causal diagonal tile last, so that the first tile is a full one and c
-//    is a mean over 128 keys (for the first query tile it is the only tile);
-//  * rows that see few keys (the first query tile of a causal head, or a
-//    non-causal head with L <= 128) also feed the bf16 rounding residual of PR
-//    (PR - bf16(PR), stored in S columns [64,128)) through one more MMA, so the
-//    correction branch is accurate to ~2^-16 there;
+//    is a mean over 128 keys (for the first query block it is the only tile);
+//  * rows that see few keys (the first query block of a causal head, or a
+//    non-causal head with L <= 128) also feed the bf16 rounding residuals of
+//    P and PR (stored in D columns [64,128)) through one more MMA, so U and W
+//    are accurate to ~2^-16 there;
 //  * the running max m is only moved when a tile's max exceeds it by more
 //    than 2^8 (lazy rescale); the final normalisation uses the same m, so the
 //    result is exact in exact arithmetic.
+// A quarter of the exponentials are evaluated by a polynomial on the FMA
+// pipes (exp2_poly2) to take load off the SFU.
 #include "tcgen05.cuh"
 #include "kernels.h"
 
@@ -42,397 +61,29 @@ namespace {
 
 __device__ unsigned g_tc_err = 0;
 
-constexpr int BM = 128;  // queries per tile
 constexpr int BN = 128;  // keys per tile
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
-
-template <int D, bool RHO>
-struct TcLayout {
-    static constexpr int SUB = D / 64;                // 128-byte swizzle column blocks per row
-    static constexpr int SUB_BYTES = BM * 128;        // one [128 rows x 64] bf16 block
-    static constexpr int TILE_BYTES = BM * D * 2;     // one [128 x D] bf16 tile
-    static constexpr int Q_OFF = 0;
-    static constexpr int RHO_OFF = Q_OFF + TILE_BYTES;
-    static constexpr int KV_OFF = RHO_OFF + (RHO ? TILE_BYTES : 0);
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K then V
-    static constexpr int BAR_OFF = KV_OFF + kStages * STAGE_BYTES;
-    static constexpr int NBARS = 1 + 3 * kStages + 3;
-    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + alignment slack
-    static constexpr uint32_t S_COL = 0;
-    static constexpr uint32_t R_COL = 128;
-    static constexpr uint32_t U_COL = RHO ? 256 : 128;
-    static constexpr uint32_t W_COL = U_COL + D;
-    static constexpr uint32_t TMEM_COLS = RHO ? 512 : 256;
-};
-
-struct TcArgs {
-    float* o;
-    int L;
-    int BH;
-    int n_qt;
-    float qscale;  // scale * log2(e)
-};
-
-__device__ __forceinline__ void tmem_scale_cols(uint32_t addr, int ncols, float alpha) {
-    for (int c0 = 0; c0 < ncols; c0 += 32) {
-        uint32_t v[32];
-        tc::tmem_ld32(addr + c0, v);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha);
-        tc::tmem_st32(addr + c0, v);
-    }
-}
-
-template <int D, bool RHO, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmR,
-                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                      const TcArgs a) {
-    using LY = TcLayout<D, RHO>;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
-    uint64_t* q_full = bars;
-    uint64_t* k_full = bars + 1;
-    uint64_t* v_full = k_full + kStages;
-    uint64_t* kv_empty = v_full + kStages;
-    uint64_t* s_full = kv_empty + kStages;
-    uint64_t* p_full = s_full + 1;
-    uint64_t* o_full = s_full + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int tile = blockIdx.x;
-    // heaviest (most key tiles) first when causal
-    const int qt = CAUSAL ? a.n_qt - 1 - tile / a.BH : tile / a.BH;
-    const int bh = tile % a.BH;
-    const int q0 = qt * BM;
-    const int n_kv = CAUSAL ? qt + 1 : (a.L + BN - 1) / BN;
-    const bool precise = RHO && (CAUSAL ? qt == 0 : n_kv == 1);
-
-    if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
-        }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
-        mbar_init(o_full, 1);
-        *abort_flag = (*(volatile unsigned*)&g_tc_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        tc::prefetch_tmap(&tmQ);
-        tc::prefetch_tmap(&tmK);
-        tc::prefetch_tmap(&tmV);
-        if (RHO) tc::prefetch_tmap(&tmR);
-    }
-    if (warp == 1) tc::tmem_alloc(tmem_slot, LY::TMEM_COLS);
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-    const bool skip = *abort_flag != 0;
-
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0 && !skip) {
-            const int z = bh;
-            int it = 0;
-            bool ok = true;
-            mbar_arrive_expect_tx(q_full, (RHO ? 2 : 1) * LY::TILE_BYTES);
-#pragma unroll
-            for (int sub = 0; sub < LY::SUB; ++sub) {
-                tc::tma_load_3d(smem + LY::Q_OFF + sub * LY::SUB_BYTES, &tmQ, sub * 64, q0, z, q_full);
-                if (RHO)
-                    tc::tma_load_3d(smem + LY::RHO_OFF + sub * LY::SUB_BYTES, &tmR, sub * 64, q0, z,
-                                    q_full);
-            }
-            for (; it < n_kv; ++it) {
-                const int j = it;
-                const int s = it % kStages;
-                if (it >= kStages &&
-                    !mbar_wait(&kv_empty[s], ((it / kStages) - 1) & 1, &g_tc_err)) {
-                    ok = false;
-                    break;
-                }
-                unsigned char* kb = smem + LY::KV_OFF + s * LY::STAGE_BYTES;
-                unsigned char* vb = kb + LY::TILE_BYTES;
-                mbar_arrive_expect_tx(&k_full[s], LY::TILE_BYTES);
-#pragma unroll
-                for (int sub = 0; sub < LY::SUB; ++sub)
-                    tc::tma_load_3d(kb + sub * LY::SUB_BYTES, &tmK, sub * 64, j * BN, z, &k_full[s]);
-                mbar_arrive_expect_tx(&v_full[s], LY::TILE_BYTES);
-#pragma unroll
-                for (int sub = 0; sub < LY::SUB; ++sub)
-                    tc::tma_load_3d(vb + sub * LY::SUB_BYTES, &tmV, sub * 64, j * BN, z, &v_full[s]);
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                // wait (bounded) for the copies already issued into this CTA's shared memory
-                mbar_wait(q_full, 0, &g_tc_err);
-                for (int k = (it >= kStages ? it - kStages : 0); k < it; ++k) {
-                    mbar_wait(&k_full[k % kStages], (k / kStages) & 1, &g_tc_err);
-                    mbar_wait(&v_full[k % kStages], (k / kStages) & 1, &g_tc_err);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        // (the whole warp runs this; one elected lane issues each MMA and commit)
-        if (!skip) {
-            constexpr uint32_t kIdescS = tc::idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t kIdescV = tc::idesc_bf16_f32(BM, D, true);
-            bool ok = mbar_wait_warp(q_full, 0, &g_tc_err);
-            tc::fence_after_sync();
-            // Descriptors are built once; a K-step only adds a constant to the
-            // start-address field (bits 0..13, in 16-byte units).
-            const uint64_t dQ = tc::smem_desc_sw128(smem_u32(smem + LY::Q_OFF), 16, 1024);
-            const uint64_t dR = tc::smem_desc_sw128(smem_u32(smem + LY::RHO_OFF), 16, 1024);
-            const uint32_t kv0 = smem_u32(smem + LY::KV_OFF);
-            for (int it = 0; it < n_kv && ok; ++it) {
-                const int s = it % kStages;
-                const uint32_t ph = (it / kStages) & 1;
-                const uint32_t sK = kv0 + s * LY::STAGE_BYTES;
-                const uint64_t dK = tc::smem_desc_sw128(sK, 16, 1024);
-                const uint64_t dV = tc::smem_desc_sw128(sK + LY::TILE_BYTES, LY::SUB_BYTES, 1024);
-                if (!mbar_wait_warp(&k_full[s], ph, &g_tc_err)) { ok = false; break; }
-                tc::fence_after_sync();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk / 4) * LY::SUB_BYTES + (kk % 4) * 32) >> 4;
-                    tc::mma_ss(tmem + LY::S_COL, dQ + off, dK + off, kIdescS, kk > 0);
-                    if (RHO) tc::mma_ss(tmem + LY::R_COL, dR + off, dK + off, kIdescS, kk > 0);
-                }
-                tc::commit(s_full);
-                if (!mbar_wait_warp(p_full, it & 1, &g_tc_err)) { ok = false; break; }
-                tc::fence_after_sync();
-                if (!mbar_wait_warp(&v_full[s], ph, &g_tc_err)) { ok = false; break; }
-                tc::fence_after_sync();
-                const uint32_t acc0 = it > 0 ? 1u : 0u;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // 16 keys = 16 rows of 128 bytes in each 64-column block; the second
-                    // column block of V (d >= 64) sits LBO = one block further on.
-                    const uint32_t off = (kk * 16 * 128) >> 4;
-                    const uint32_t acc = kk > 0 ? 1u : acc0;
-                    tc::mma_ts(tmem + LY::U_COL, tmem + LY::S_COL + kk * 8, dV + off, kIdescV, acc);
-                    if (RHO) {
-                        tc::mma_ts(tmem + LY::W_COL, tmem + LY::R_COL + kk * 8, dV + off, kIdescV, acc);
-                        if (precise)
-                            tc::mma_ts(tmem + LY::W_COL, tmem + LY::S_COL + 64 + kk * 8, dV + off,
-                                       kIdescV, 1u);
-                    }
-                }
-                tc::commit(&kv_empty[s]);
-            }
-            tc::commit(o_full);
-            if (!ok) {
-                *abort_flag = 1;
-                mbar_wait_warp(o_full, 0, &g_tc_err);  // MMAs already issued have drained
-            }
-        }
-    } else {
-        // ---------------------------------------------------------------- softmax / epilogue
-        const int quarter = warp % 4;  // TMEM lanes this warp may touch
-        const int row = quarter * 32 + lane;
-        const int i = q0 + row;
-        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float qscale = a.qscale;
-        float m = -INFINITY, l = 0.f, A = 0.f, c = 0.f;
-        bool ok = !skip;
-        for (int it = 0; it < n_kv && ok; ++it) {
-            const int k0 = it * BN;
-            const bool got = !*abort_flag && mbar_wait(s_full, it & 1, &g_tc_err);
-            if (!__all_sync(kFullMask, got)) { ok = false; break; }  // warp-uniform exit
-            tc::fence_after_sync();
-            uint32_t sv[4][32];
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(taddr + LY::S_COL + ch * 32, sv[ch]);
-            tc::tmem_ld_wait();
-
-            // scale, mask, tile max
-            const bool need_mask = (k0 + BN > a.L) || (CAUSAL && k0 + BN > q0);
-            float mx = -INFINITY;
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    float f = __uint_as_float(sv[ch][x]) * qscale;
-                    if (need_mask) {
-                        const int key = k0 + ch * 32 + x;
-                        const bool valid = key < a.L && (!CAUSAL || key <= i);
-                        f = valid ? f : -INFINITY;
-                    }
-                    sv[ch][x] = __float_as_uint(f);
-                    mx = fmaxf(mx, f);
-                }
-            if (it == 0) {
-                m = mx;
-            } else if (__any_sync(kFullMask, mx > m + kRescaleThreshold)) {
-                // the TMEM accesses are warp-collective, so the whole warp rescales;
-                // rows whose max did not grow keep alpha = 1
-                const float m_new = fmaxf(m, mx);
-                const float alpha = fast_exp2(m - m_new);
-                l *= alpha;
-                A *= alpha;
-                tmem_scale_cols(taddr + LY::U_COL, D, alpha);
-                if (RHO) tmem_scale_cols(taddr + LY::W_COL, D, alpha);
-                m = m_new;
-            }
-
-            // P = 2^(s - m), row sum, P -> bf16 into S columns [0, 64)
-            float lsum = 0.f;
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t packed[16];
-#pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const float p = fast_exp2(__uint_as_float(sv[ch][x]) - m);
-                    sv[ch][x] = __float_as_uint(p);
-                    lsum += p;
-                }
-#pragma unroll
-                for (int y = 0; y < 16; ++y)
-                    packed[y] = tc::pack_bf16(__uint_as_float(sv[ch][2 * y]),
-                                              __uint_as_float(sv[ch][2 * y + 1]));
-                tc::tmem_st16(taddr + LY::S_COL + ch * 16, packed);
-            }
-            l += lsum;
-
-            if (RHO) {
-                if (it == 0) {  // row shift: p-weighted mean of r over this first tile
-                    float prs = 0.f;
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t rr[32];
-                        tc::tmem_ld32(taddr + LY::R_COL + ch * 32, rr);
-                        tc::tmem_ld_wait();
-#pragma unroll
-                        for (int x = 0; x < 32; ++x)
-                            prs = fmaf(__uint_as_float(sv[ch][x]), __uint_as_float(rr[x]), prs);
-                    }
-                    c = prs / lsum;
-                }
-                float asum = 0.f;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t rr[32];
-                    tc::tmem_ld32(taddr + LY::R_COL + ch * 32, rr);
-                    tc::tmem_ld_wait();
-                    float pr[32];
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        pr[x] = __uint_as_float(sv[ch][x]) * (__uint_as_float(rr[x]) - c);
-                        asum += pr[x];
-                    }
-                    uint32_t hi[16];
-#pragma unroll
-                    for (int y = 0; y < 16; ++y) hi[y] = tc::pack_bf16(pr[2 * y], pr[2 * y + 1]);
-                    // columns [16ch, 16ch+16) of R were read above (chunk ch/2 <= ch)
-                    tc::tmem_st16(taddr + LY::R_COL + ch * 16, hi);
-                    if (precise) {
-                        uint32_t lo[16];
-#pragma unroll
-                        for (int y = 0; y < 16; ++y)
-                            lo[y] = tc::pack_bf16(pr[2 * y] - tc::bf16_lo_to_f32(hi[y]),
-                                                  pr[2 * y + 1] - tc::bf16_hi_to_f32(hi[y]));
-                        tc::tmem_st16(taddr + LY::S_COL + 64 + ch * 16, lo);
-                    }
-                }
-                A += asum;
-            }
-            tc::tmem_st_wait();
-            tc::fence_before_sync();
-            mbar_arrive(p_full);
-        }
-
-        // ---- epilogue: o = U/l - (W/l - (A/l)(U/l))
-        const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_tc_err);
-        if (__all_sync(kFullMask, done)) {
-            tc::fence_after_sync();
-            const float inv_l = 1.f / l;
-            const float rbar = A * inv_l;
-            float* orow = a.o + ((size_t)bh * a.L + i) * D;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t u[32], w[32];
-                tc::tmem_ld32(taddr + LY::U_COL + c0, u);
-                if (RHO) tc::tmem_ld32(taddr + LY::W_COL + c0, w);
-                tc::tmem_ld_wait();
-                if (i < a.L) {
-#pragma unroll
-                    for (int x = 0; x < 32; x += 4) {
-                        float out[4];
-#pragma unroll
-                        for (int y = 0; y < 4; ++y) {
-                            const float mu = __uint_as_float(u[x + y]) * inv_l;
-                            out[y] = RHO ? mu - (__uint_as_float(w[x + y]) * inv_l - rbar * mu) : mu;
-                        }
-                        *reinterpret_cast<float4*>(orow + c0 + x) =
-                            make_float4(out[0], out[1], out[2], out[3]);
-                    }
-                }
-            }
-        } else {
-            *abort_flag = 1;
-        }
-    }
-
-    tc::fence_before_sync();
-    __syncthreads();
-    if (warp == 1) {
-        tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, LY::TMEM_COLS);
-    }
-}
-
-// ============================================================================
-// Correction path (rho != NULL): two 64-query sub-tiles in ping-pong.
-//
-// The A operand of MMA-1 stacks, per 16-query group g of a sub-tile, the 16
-// query rows (operand rows 32g..32g+15) and the same 16 queries' probe rows
-// (rows 32g+16..32g+31).  One M=128 MMA per sub-tile therefore yields S and
-// R for 64 queries, and one M=128 MMA with A = [P; PR] (read from TMEM) yields
-// U and W.  TMEM lane 32g+i holds query 16g+i's S row (then P, then U) and
-// lane 32g+16+i its R row (then PR, then W), so each softmax warp (one TMEM
-// lane quarter) owns 16 queries, and the half-split TMEM access gives thread t
-// (t < 16) and thread t+16 the same query's rows, each with half of the key
-// columns: every thread computes s, r, p and p(r - c) for the same 64 keys of
-// one query with no data exchange, and the exponentials are spread over all
-// four SM sub-partitions.  While the softmax warps of one sub-tile work, the
-// tensor core runs the other sub-tile's MMAs.
-//
-// TMEM columns: D_sub at 128*sub (S|R, then P|PR packed into its first 64
-// columns, the few-key residuals into the next 64), O_sub at 256 + sub*d (U|W).
-// ============================================================================
-// 12 warps = 3 warpgroups: warp 0 TMA, warp 1 TMEM + MMA (warps 2-3 idle),
-// warps 4-7 / 8-11: softmax of sub-tile 0 / 1.  The first warpgroup hands
-// registers to the other two (setmaxnreg): the launch gives every thread
-// kRegsLaunch registers (3 warps per SM sub-partition x 32 x 168 <= 16384);
-// afterwards 4 warps x 64 + 8 warps x 216 use no more than that total.  The
-// build checks that ptxas assigned kRegsLaunch registers to this kernel.
-constexpr int kThreads2 = 384;
+constexpr int kThreads = 384;
+// Register hand-over: the launch gives every thread kRegsLaunch registers
+// (3 warps per SM sub-partition x 32 x 168 <= 16384); afterwards 4 warps x 64
+// + 8 warps x 216 use no more than that total.  The build checks that ptxas
+// assigned kRegsLaunch registers to this kernel: with fewer, the raising
+// warpgroups would wait forever.
 constexpr int kRegsLaunch = 168;
 constexpr int kRegsSupport = 64;
 constexpr int kRegsSoftmax = 216;
-static_assert(128 * kRegsSupport + 256 * kRegsSoftmax <= kThreads2 * kRegsLaunch,
+static_assert(128 * kRegsSupport + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register hand-over exceeds the launch allocation");
 constexpr int kHeadGroup = 16;  // heads per CTA-scheduling group (keeps their K/V in L2)
 
-template <int D>
+template <int D, bool RHO>
 struct PairLayout {
+    static constexpr int QROWS = RHO ? 64 : 128;        // queries per sub-tile
+    static constexpr int BLOCK = 2 * QROWS;             // queries per CTA
     static constexpr int SUB_BYTES = 128 * 128;         // [128 rows x 64 cols] bf16, 128B-swizzled
     static constexpr int NCB = D / 64;                  // 64-column blocks per row
     static constexpr int OP_BYTES = NCB * SUB_BYTES;    // one 128 x D bf16 operand
-    static constexpr int QR_OFF = 0;                    // [Q;rho] stacked, sub-tiles 0 and 1
+    static constexpr int QR_OFF = 0;                    // A operands of MMA-1, sub-tiles 0 and 1
     static constexpr int K_OFF = 2 * OP_BYTES;          // K ring, 2 stages
     static constexpr int V_OFF = K_OFF + 2 * OP_BYTES;  // V ring, 2 stages
     static constexpr int BAR_OFF = V_OFF + 2 * OP_BYTES;
@@ -443,12 +94,46 @@ struct PairLayout {
     __host__ __device__ static constexpr uint32_t ocol(int sub) { return 256u + (uint32_t)(D * sub); }
 };
 
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads2, 1)
+struct TcArgs {
+    float* o;
+    int L;
+    int BH;
+    int n_qb;      // query blocks per head
+    float qscale;  // scale * log2(e)
+};
+
+// p = 2^(s*qs - m) for 32 consecutive values (in place), their sum into ls0/ls1,
+// and the bf16 pairs into pk; one pair in four through exp2_poly2, the rest on
+// the SFU.
+__device__ __forceinline__ void exp_block32(uint32_t (&v)[32], float2 qs2, float2 nm2,
+                                            float2& ls0, float2& ls1, uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int y = 0; y < 16; ++y) {
+        const float2 t = __ffma2_rn(
+            make_float2(__uint_as_float(v[2 * y]), __uint_as_float(v[2 * y + 1])), qs2, nm2);
+        const float2 p2 = (y & 3) == 3 ? exp2_poly2(t) : make_float2(fast_exp2(t.x), fast_exp2(t.y));
+        v[2 * y] = __float_as_uint(p2.x);
+        v[2 * y + 1] = __float_as_uint(p2.y);
+        if (y & 1) ls1 = __fadd2_rn(ls1, p2);
+        else ls0 = __fadd2_rn(ls0, p2);
+        pk[y] = tc::pack_bf16(p2.x, p2.y);
+    }
+}
+
+// bf16 rounding residual of the 32 values packed in pk.
+__device__ __forceinline__ void residual_block32(const uint32_t (&v)[32], uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int y = 0; y < 16; ++y)
+        pk[y] = tc::pack_bf16(__uint_as_float(v[2 * y]) - tc::bf16_lo_to_f32(pk[y]),
+                              __uint_as_float(v[2 * y + 1]) - tc::bf16_hi_to_f32(pk[y]));
+}
+
+template <int D, bool CAUSAL, bool RHO>
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmR,
                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const TcArgs a) {
-    using LY = PairLayout<D>;
+    using LY = PairLayout<D, RHO>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -466,18 +151,23 @@ __global__ void __launch_bounds__(kThreads2, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // CTA -> (head, 128-query block): heads in groups of kHeadGroup, heaviest
+    // CTA -> (head, query block): heads in groups of kHeadGroup, heaviest
     // block (most key tiles) first within a group, so that the CTAs resident
     // at any time share the K/V of a few heads in L2.
-    const int n_qb = a.n_qt;
+    const int n_qb = a.n_qb;
     const int group = blockIdx.x / (kHeadGroup * n_qb);
     const int gsize = min(kHeadGroup, a.BH - group * kHeadGroup);
     const int r_in = blockIdx.x - group * kHeadGroup * n_qb;
     const int qb = CAUSAL ? n_qb - 1 - r_in / gsize : r_in / gsize;
     const int bh = group * kHeadGroup + r_in % gsize;
-    const int q0 = qb * 128;
-    const int n_kv = CAUSAL ? qb + 1 : (a.L + BN - 1) / BN;
-    const bool precise = CAUSAL ? qb == 0 : n_kv == 1;
+    const int q0 = qb * LY::BLOCK;
+    // key tiles of each sub-tile: causal rows q0 + QROWS*sub .. see keys up to
+    // their own index (the last tile is the diagonal one); sub-tile 0 may need
+    // one tile fewer than sub-tile 1
+    const int n_all = (a.L + BN - 1) / BN;
+    const int n1 = CAUSAL ? min(n_all, (q0 + LY::BLOCK - 1) / BN + 1) : n_all;
+    const int n0 = CAUSAL ? min(n1, (q0 + LY::QROWS - 1) / BN + 1) : n_all;
+    const bool precise = RHO && n1 == 1;
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], (b == 11 || b == 12) ? 128 : 1);
@@ -486,7 +176,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     }
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tmQ);
-        tc::prefetch_tmap(&tmR);
+        if (RHO) tc::prefetch_tmap(&tmR);
         tc::prefetch_tmap(&tmK);
         tc::prefetch_tmap(&tmV);
     }
@@ -498,359 +188,446 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const bool skip = *abort_flag != 0;
     if (warp < 4) {
         tc::setmaxnreg_dec<kRegsSupport>();
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0 && !skip) {
-            const int z = bh;
-            bool ok = true;
-            int kj = 0, vj = 0;  // K / V tiles issued
-            mbar_arrive_expect_tx(q_full, 2 * LY::OP_BYTES);
-            for (int sub = 0; sub < 2; ++sub)
-                for (int g = 0; g < 4; ++g)
+        if (warp == 0) {
+            // ------------------------------------------------------------ TMA producer
+            if (lane == 0 && !skip) {
+                const int z = bh;
+                bool ok = true;
+                int kj = 0, vj = 0;  // K / V tiles issued
+                mbar_arrive_expect_tx(q_full, 2 * LY::OP_BYTES);
+                for (int sub = 0; sub < 2; ++sub)
                     for (int cb = 0; cb < LY::NCB; ++cb) {
-                        unsigned char* dst =
-                            smem + LY::QR_OFF + sub * LY::OP_BYTES + cb * LY::SUB_BYTES;
-                        const int row = q0 + 64 * sub + 16 * g;
-                        tc::tma_load_3d(dst + (32 * g) * 128, &tmQ, cb * 64, row, z, q_full);
-                        tc::tma_load_3d(dst + (32 * g + 16) * 128, &tmR, cb * 64, row, z, q_full);
+                        unsigned char* dst = smem + LY::QR_OFF + sub * LY::OP_BYTES + cb * LY::SUB_BYTES;
+                        if (RHO) {
+                            for (int g = 0; g < 4; ++g) {
+                                const int row = q0 + 64 * sub + 16 * g;
+                                tc::tma_load_3d(dst + (32 * g) * 128, &tmQ, cb * 64, row, z, q_full);
+                                tc::tma_load_3d(dst + (32 * g + 16) * 128, &tmR, cb * 64, row, z,
+                                                q_full);
+                            }
+                        } else {
+                            tc::tma_load_3d(dst, &tmQ, cb * 64, q0 + 128 * sub, z, q_full);
+                        }
                     }
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait(&k_empty[st], ((j >> 1) - 1) & 1, &g_tc_err)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&k_full[st], LY::OP_BYTES);
-                for (int cb = 0; cb < LY::NCB; ++cb)
-                    tc::tma_load_3d(smem + LY::K_OFF + st * LY::OP_BYTES + cb * LY::SUB_BYTES, &tmK,
-                                    cb * 64, j * BN, z, &k_full[st]);
-                kj = j + 1;
-                if (j >= 2 && !mbar_wait(&v_empty[st], ((j >> 1) - 1) & 1, &g_tc_err)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&v_full[st], LY::OP_BYTES);
-                for (int cb = 0; cb < LY::NCB; ++cb)
-                    tc::tma_load_3d(smem + LY::V_OFF + st * LY::OP_BYTES + cb * LY::SUB_BYTES, &tmV,
-                                    cb * 64, j * BN, z, &v_full[st]);
-                vj = j + 1;
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                // wait (bounded) for the copies already issued into this CTA's shared memory
-                mbar_wait(q_full, 0, &g_tc_err);
-                for (int k = (kj >= 2 ? kj - 2 : 0); k < kj; ++k)
-                    mbar_wait(&k_full[k & 1], (k >> 1) & 1, &g_tc_err);
-                for (int k = (vj >= 2 ? vj - 2 : 0); k < vj; ++k)
-                    mbar_wait(&v_full[k & 1], (k >> 1) & 1, &g_tc_err);
-            }
-        }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        // (the whole warp runs this; one elected lane issues each MMA and commit)
-        if (!skip) {
-            constexpr uint32_t kIdesc1 = tc::idesc_bf16_f32(128, BN, false);
-            constexpr uint32_t kIdesc2 = tc::idesc_bf16_f32(128, D, true);
-            const uint32_t sbase = smem_u32(smem);
-            // descriptors: one base each; a stage / sub-tile / K-step only adds a
-            // constant to the 16-byte start-address field
-            const uint64_t dQR0 = tc::smem_desc_sw128(sbase + LY::QR_OFF, 16, 1024);
-            const uint64_t dK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, 16, 1024);
-            const uint64_t dV0 = tc::smem_desc_sw128(sbase + LY::V_OFF, LY::SUB_BYTES, 1024);
-            constexpr uint32_t kOpStep = LY::OP_BYTES >> 4;
-            // (the per-call bases pass through tc::opaque so that the compiler does
-            // not hoist every K-step's descriptor out of the tile loop and keep them
-            // all live in registers)
-            auto mma1 = [&](int sub, int st) {  // D_sub = [Q;rho]_sub K^T
-                const uint64_t dA = tc::opaque(dQR0 + (uint32_t)sub * kOpStep);
-                const uint64_t dB = tc::opaque(dK0 + (uint32_t)st * kOpStep);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk / 4) * LY::SUB_BYTES + (kk % 4) * 32) >> 4;
-                    tc::mma_ss(tmem + LY::dcol(sub), dA + off, dB + off, kIdesc1, kk > 0);
-                }
-            };
-            auto mma2 = [&](int sub, int st, bool first) {  // O_sub += [P;PR]_sub V
-                const uint64_t dB = tc::opaque(dV0 + (uint32_t)st * kOpStep);
-                const uint32_t acc0 = first ? 0u : 1u;
-                if (precise) {
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint32_t off = (kk * 16 * 128) >> 4;
-                        tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + kk * 8, dB + off,
-                                   kIdesc2, kk == 0 ? acc0 : 1u);
-                        tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + 64 + kk * 8,
-                                   dB + off, kIdesc2, 1u);
+                for (int j = 0; j < n1 && ok; ++j) {
+                    const int st = j & 1;
+                    if (j >= 2 && !mbar_wait(&k_empty[st], ((j >> 1) - 1) & 1, &g_tc_err)) {
+                        ok = false;
+                        break;
                     }
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint32_t off = (kk * 16 * 128) >> 4;
-                        tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + kk * 8, dB + off,
-                                   kIdesc2, kk == 0 ? acc0 : 1u);
+                    mbar_arrive_expect_tx(&k_full[st], LY::OP_BYTES);
+                    for (int cb = 0; cb < LY::NCB; ++cb)
+                        tc::tma_load_3d(smem + LY::K_OFF + st * LY::OP_BYTES + cb * LY::SUB_BYTES,
+                                        &tmK, cb * 64, j * BN, z, &k_full[st]);
+                    kj = j + 1;
+                    if (j >= 2 && !mbar_wait(&v_empty[st], ((j >> 1) - 1) & 1, &g_tc_err)) {
+                        ok = false;
+                        break;
                     }
+                    mbar_arrive_expect_tx(&v_full[st], LY::OP_BYTES);
+                    for (int cb = 0; cb < LY::NCB; ++cb)
+                        tc::tma_load_3d(smem + LY::V_OFF + st * LY::OP_BYTES + cb * LY::SUB_BYTES,
+                                        &tmV, cb * 64, j * BN, z, &v_full[st]);
+                    vj = j + 1;
                 }
-            };
-            bool ok = mbar_wait_warp(q_full, 0, &g_tc_err) && mbar_wait_warp(&k_full[0], 0, &g_tc_err);
-            tc::fence_after_sync();
-            if (ok) {
-                mma1(0, 0);
-                tc::commit(&s_full[0]);
-                mma1(1, 0);
-                tc::commit(&s_full[1]);
-                tc::commit(&k_empty[0]);
+                if (!ok) {
+                    *abort_flag = 1;
+                    // wait (bounded) for the copies already issued into this CTA's shared memory
+                    mbar_wait(q_full, 0, &g_tc_err);
+                    for (int k = (kj >= 2 ? kj - 2 : 0); k < kj; ++k)
+                        mbar_wait(&k_full[k & 1], (k >> 1) & 1, &g_tc_err);
+                    for (int k = (vj >= 2 ? vj - 2 : 0); k < vj; ++k)
+                        mbar_wait(&v_full[k & 1], (k >> 1) & 1, &g_tc_err);
+                }
             }
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j & 1;
-                const bool more = j + 1 < n_kv;
-                if (!mbar_wait_warp(&p_full[0], j & 1, &g_tc_err) ||
-                    !mbar_wait_warp(&v_full[st], (j >> 1) & 1, &g_tc_err)) {
-                    ok = false;
-                    break;
-                }
+        } else if (warp == 1) {
+            // ------------------------------------------------------------ MMA issuer
+            // (the whole warp runs this; one elected lane issues each MMA and commit)
+            if (!skip) {
+                constexpr uint32_t kIdesc1 = tc::idesc_bf16_f32(128, BN, false);
+                constexpr uint32_t kIdesc2 = tc::idesc_bf16_f32(128, D, true);
+                const uint32_t sbase = smem_u32(smem);
+                // descriptors: one base each; a stage / sub-tile / K-step only adds a
+                // constant to the 16-byte start-address field
+                const uint64_t dQR0 = tc::smem_desc_sw128(sbase + LY::QR_OFF, 16, 1024);
+                const uint64_t dK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, 16, 1024);
+                const uint64_t dV0 = tc::smem_desc_sw128(sbase + LY::V_OFF, LY::SUB_BYTES, 1024);
+                constexpr uint32_t kOpStep = LY::OP_BYTES >> 4;
+                // (the per-call bases pass through tc::opaque so that the compiler
+                // does not hoist every K-step's descriptor out of the tile loop and
+                // keep them all live in registers)
+                auto mma1 = [&](int sub, int st) {  // D_sub = A_sub K^T
+                    const uint64_t dA = tc::opaque(dQR0 + (uint32_t)sub * kOpStep);
+                    const uint64_t dB = tc::opaque(dK0 + (uint32_t)st * kOpStep);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk / 4) * LY::SUB_BYTES + (kk % 4) * 32) >> 4;
+                        tc::mma_ss(tmem + LY::dcol(sub), dA + off, dB + off, kIdesc1, kk > 0);
+                    }
+                };
+                auto mma2 = [&](int sub, int st, bool first) {  // O_sub += [P;PR]_sub V
+                    const uint64_t dB = tc::opaque(dV0 + (uint32_t)st * kOpStep);
+                    const uint32_t acc0 = first ? 0u : 1u;
+                    if (precise) {
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            const uint32_t off = (kk * 16 * 128) >> 4;
+                            tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + kk * 8,
+                                       dB + off, kIdesc2, kk == 0 ? acc0 : 1u);
+                            tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + 64 + kk * 8,
+                                       dB + off, kIdesc2, 1u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            const uint32_t off = (kk * 16 * 128) >> 4;
+                            tc::mma_ts(tmem + LY::ocol(sub), tmem + LY::dcol(sub) + kk * 8,
+                                       dB + off, kIdesc2, kk == 0 ? acc0 : 1u);
+                        }
+                    }
+                };
+                bool ok = mbar_wait_warp(q_full, 0, &g_tc_err) &&
+                          mbar_wait_warp(&k_full[0], 0, &g_tc_err);
                 tc::fence_after_sync();
-                mma2(0, st, j == 0);
-                if (more) {
-                    if (!mbar_wait_warp(&k_full[st ^ 1], ((j + 1) >> 1) & 1, &g_tc_err)) {
+                if (ok) {
+                    mma1(0, 0);
+                    tc::commit(&s_full[0]);
+                    mma1(1, 0);
+                    tc::commit(&s_full[1]);
+                    tc::commit(&k_empty[0]);
+                }
+                for (int j = 0; j < n1 && ok; ++j) {
+                    const int st = j & 1;
+                    const bool do0 = j < n0, more0 = j + 1 < n0, more1 = j + 1 < n1;
+                    // V first: it is normally resident long before P is ready
+                    if (!mbar_wait_warp(&v_full[st], (j >> 1) & 1, &g_tc_err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (do0) {
+                        if (!mbar_wait_warp(&p_full[0], j & 1, &g_tc_err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        mma2(0, st, j == 0);
+                    }
+                    if (more1 && !mbar_wait_warp(&k_full[st ^ 1], ((j + 1) >> 1) & 1, &g_tc_err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (more0) {
+                        tc::fence_after_sync();
+                        mma1(0, st ^ 1);  // in order after mma2(0): P_0 is read before D_0 is rewritten
+                        tc::commit(&s_full[0]);
+                    }
+                    if (!mbar_wait_warp(&p_full[1], j & 1, &g_tc_err)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-                    mma1(0, st ^ 1);  // in-order after mma2(0): P_0 is consumed before D_0 is rewritten
-                    tc::commit(&s_full[0]);
+                    mma2(1, st, j == 0);
+                    tc::commit(&v_empty[st]);
+                    if (more1) {
+                        mma1(1, st ^ 1);
+                        tc::commit(&s_full[1]);
+                        tc::commit(&k_empty[st ^ 1]);
+                    }
                 }
-                if (!mbar_wait_warp(&p_full[1], j & 1, &g_tc_err)) {
-                    ok = false;
-                    break;
+                tc::commit(o_full);
+                if (!ok) {
+                    *abort_flag = 1;
+                    mbar_wait_warp(o_full, 0, &g_tc_err);  // the MMAs already issued have drained
                 }
-                tc::fence_after_sync();
-                mma2(1, st, j == 0);
-                tc::commit(&v_empty[st]);
-                if (more) {
-                    mma1(1, st ^ 1);
-                    tc::commit(&s_full[1]);
-                    tc::commit(&k_empty[st ^ 1]);
-                }
-            }
-            tc::commit(o_full);
-            if (!ok) {
-                *abort_flag = 1;
-                mbar_wait_warp(o_full, 0, &g_tc_err);  // the MMAs already issued have drained
             }
         }
-    }
     } else {
         tc::setmaxnreg_inc<kRegsSoftmax>();
         // ---------------------------------------------------------------- softmax / epilogue
         const int sub = (warp - 4) >> 2;
-        const int g = warp & 3;               // TMEM lane quarter of this warp
-        const int h = lane >> 4;              // which half of the key (and d) columns
-        const int qi = 16 * g + (lane & 15);  // query within the sub-tile
-        const int i = q0 + 64 * sub + qi;     // query index
-        const uint32_t rowS = tmem + ((uint32_t)(32 * g) << 16);
-        const uint32_t rowR = tmem + ((uint32_t)(32 * g + 16) << 16);
-        const uint32_t tS = rowS + LY::dcol(sub), tR = rowR + LY::dcol(sub);
-        const uint32_t tU = rowS + LY::ocol(sub), tW = rowR + LY::ocol(sub);
+        const int g = warp & 3;  // TMEM lane quarter of this warp
+        const int n_tiles = sub ? n1 : n0;
+        const int first_row = q0 + LY::QROWS * sub;  // first query of this sub-tile
         const float qs = a.qscale;
-        float m = -INFINITY, l = 0.f, A = 0.f, c = 0.f;
-        bool ok = !skip;
         const float2 qs2 = make_float2(qs, qs);
-        for (int it = 0; it < n_kv && ok; ++it) {
-            // this thread owns keys it*128 + 64h + 32b + x, b in {0,1}, x in [0,32)
-            const int k0 = it * BN + 64 * h;
-            const bool got = !*abort_flag && mbar_wait(&s_full[sub], it & 1, &g_tc_err);
-            if (!__all_sync(kFullMask, got)) {  // warp-uniform exit
-                ok = false;
-                break;
-            }
-            tc::fence_after_sync();
-            // S and R of this thread's 64 keys, behind a single wait
-            uint32_t sv[2][32], rv[2][32];
-            tc::tmem_ld32_split<64>(tS, sv[0]);
-            tc::tmem_ld32_split<64>(tS + 32, sv[1]);
-            tc::tmem_ld32_split<64>(tR, rv[0]);
-            tc::tmem_ld32_split<64>(tR + 32, rv[1]);
-            tc::tmem_ld_wait();
+        float m = -INFINITY, l = 0.f;
+        bool ok = !skip;
+        if constexpr (RHO) {
+            const int h = lane >> 4;              // which half of the key (and d) columns
+            const int i = first_row + 16 * g + (lane & 15);  // query index
+            const uint32_t rowS = tmem + ((uint32_t)(32 * g) << 16);
+            const uint32_t rowR = tmem + ((uint32_t)(32 * g + 16) << 16);
+            const uint32_t tS = rowS + LY::dcol(sub), tR = rowR + LY::dcol(sub);
+            const uint32_t tU = rowS + LY::ocol(sub), tW = rowR + LY::ocol(sub);
+            float A = 0.f, c = 0.f;
+            for (int it = 0; it < n_tiles && ok; ++it) {
+                // this thread owns keys it*128 + 64h + 32b + x, b in {0,1}, x in [0,32)
+                const int k0 = it * BN + 64 * h;
+                const bool got = !*abort_flag && mbar_wait(&s_full[sub], it & 1, &g_tc_err);
+                if (!__all_sync(kFullMask, got)) {  // warp-uniform exit
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                // S and R of this thread's 64 keys, behind a single wait
+                uint32_t sv[2][32], rv[2][32];
+                tc::tmem_ld32_split<64>(tS, sv[0]);
+                tc::tmem_ld32_split<64>(tS + 32, sv[1]);
+                tc::tmem_ld32_split<64>(tR, rv[0]);
+                tc::tmem_ld32_split<64>(tR + 32, rv[1]);
+                tc::tmem_ld_wait();
 
-            const bool need_mask = (it * BN + BN > a.L) || (CAUSAL && it == n_kv - 1);
-            if (need_mask) {
+                const bool need_mask = (it * BN + BN > a.L) || (CAUSAL && it * BN + BN - 1 > first_row);
+                if (need_mask) {
+#pragma unroll
+                    for (int b = 0; b < 2; ++b)
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            const int key = k0 + 32 * b + x;
+                            if (!(key < a.L && (!CAUSAL || key <= i)))
+                                sv[b][x] = __float_as_uint(-INFINITY);
+                        }
+                }
+                // row max: four independent chains of three-input max
+                float c0 = -INFINITY, c1 = -INFINITY, c2 = -INFINITY, c3 = -INFINITY;
 #pragma unroll
                 for (int b = 0; b < 2; ++b)
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        const int key = k0 + 32 * b + x;
-                        if (!(key < a.L && (!CAUSAL || key <= i)))
-                            sv[b][x] = __float_as_uint(-INFINITY);
+                    for (int x = 0; x < 32; x += 8) {
+                        c0 = fmax3(c0, __uint_as_float(sv[b][x]), __uint_as_float(sv[b][x + 1]));
+                        c1 = fmax3(c1, __uint_as_float(sv[b][x + 2]), __uint_as_float(sv[b][x + 3]));
+                        c2 = fmax3(c2, __uint_as_float(sv[b][x + 4]), __uint_as_float(sv[b][x + 5]));
+                        c3 = fmax3(c3, __uint_as_float(sv[b][x + 6]), __uint_as_float(sv[b][x + 7]));
                     }
-            }
-            // row max: four independent chains of three-input max
-            float c0 = -INFINITY, c1 = -INFINITY, c2 = -INFINITY, c3 = -INFINITY;
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-#pragma unroll
-                for (int x = 0; x < 32; x += 8) {
-                    c0 = fmax3(c0, __uint_as_float(sv[b][x]), __uint_as_float(sv[b][x + 1]));
-                    c1 = fmax3(c1, __uint_as_float(sv[b][x + 2]), __uint_as_float(sv[b][x + 3]));
-                    c2 = fmax3(c2, __uint_as_float(sv[b][x + 4]), __uint_as_float(sv[b][x + 5]));
-                    c3 = fmax3(c3, __uint_as_float(sv[b][x + 6]), __uint_as_float(sv[b][x + 7]));
-                }
-            float mx = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3));
-            mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16)) * qs;
-            if (it == 0) {
-                m = mx;
-            } else if (__any_sync(kFullMask, mx > m + kRescaleThreshold)) {
-                // TMEM accesses are warp-collective: the whole warp rescales, rows
-                // whose max did not grow use alpha = 1
-                const float m_new = fmaxf(m, mx);
-                const float alpha = fast_exp2(m - m_new);
-                l *= alpha;
-                A *= alpha;
+                float mx = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3));
+                mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16)) * qs;
+                if (it == 0) {
+                    m = mx;
+                } else if (__any_sync(kFullMask, mx > m + kRescaleThreshold)) {
+                    // TMEM accesses are warp-collective: the whole warp rescales, rows
+                    // whose max did not grow use alpha = 1
+                    const float m_new = fmaxf(m, mx);
+                    const float alpha = fast_exp2(m - m_new);
+                    l *= alpha;
+                    A *= alpha;
 #pragma unroll 1
-                for (int b = 0; b < D / 64; ++b) {
-                    uint32_t u[32];
-                    tc::tmem_ld32_split<D / 2>(tU + 32 * b, u);
-                    tc::tmem_ld_wait();
+                    for (int b = 0; b < D / 64; ++b) {
+                        uint32_t u[32];
+                        tc::tmem_ld32_split<D / 2>(tU + 32 * b, u);
+                        tc::tmem_ld_wait();
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
-                    tc::tmem_st32_split<D / 2>(tU + 32 * b, u);
-                    tc::tmem_ld32_split<D / 2>(tW + 32 * b, u);
-                    tc::tmem_ld_wait();
+                        for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
+                        tc::tmem_st32_split<D / 2>(tU + 32 * b, u);
+                        tc::tmem_ld32_split<D / 2>(tW + 32 * b, u);
+                        tc::tmem_ld_wait();
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
-                    tc::tmem_st32_split<D / 2>(tW + 32 * b, u);
+                        for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
+                        tc::tmem_st32_split<D / 2>(tW + 32 * b, u);
+                    }
+                    m = m_new;
                 }
-                m = m_new;
-            }
-            // P = 2^(S*scale*log2e - m) (packed fp32x2 FMA, SFU exponentials), P (bf16)
-            // -> packed columns 16b.. of this thread's half of the row (split 32);
-            // p overwrites s in registers
-            const float2 nm2 = make_float2(-m, -m);
-            float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
-            auto do_p = [&](int b) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int y = 0; y < 16; ++y) {
-                    const float2 t = __ffma2_rn(
-                        make_float2(__uint_as_float(sv[b][2 * y]), __uint_as_float(sv[b][2 * y + 1])),
-                        qs2, nm2);
-                    const float2 p2 = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-                    sv[b][2 * y] = __float_as_uint(p2.x);
-                    sv[b][2 * y + 1] = __float_as_uint(p2.y);
-                    if (y & 1) ls1 = __fadd2_rn(ls1, p2);
-                    else ls0 = __fadd2_rn(ls0, p2);
-                    pk[y] = tc::pack_bf16(p2.x, p2.y);
-                }
-                tc::tmem_st16_split<32>(tS + 16 * b, pk);
-                if (precise) {
-#pragma unroll
-                    for (int y = 0; y < 16; ++y)
-                        pk[y] = tc::pack_bf16(
-                            __uint_as_float(sv[b][2 * y]) - tc::bf16_lo_to_f32(pk[y]),
-                            __uint_as_float(sv[b][2 * y + 1]) - tc::bf16_hi_to_f32(pk[y]));
-                    tc::tmem_st16_split<32>(tS + 64 + 16 * b, pk);
-                }
-            };
-            // PR = p (r - c) -> packed columns of the R rows.  R was read in full
-            // above, so these stores may land on columns that the other half of
-            // the row read as R.
-            float2 as0 = make_float2(0.f, 0.f), as1 = make_float2(0.f, 0.f);
-            auto do_pr = [&](int b) {
-                const float2 nc2 = make_float2(-c, -c);
-                uint32_t pk[16];
-#pragma unroll
-                for (int y = 0; y < 16; ++y) {
-                    const float2 p2 = make_float2(__uint_as_float(sv[b][2 * y]),
-                                                  __uint_as_float(sv[b][2 * y + 1]));
-                    const float2 r2 = make_float2(__uint_as_float(rv[b][2 * y]),
-                                                  __uint_as_float(rv[b][2 * y + 1]));
-                    const float2 pr = __fmul2_rn(p2, __fadd2_rn(r2, nc2));
-                    rv[b][2 * y] = __float_as_uint(pr.x);
-                    rv[b][2 * y + 1] = __float_as_uint(pr.y);
-                    if (y & 1) as1 = __fadd2_rn(as1, pr);
-                    else as0 = __fadd2_rn(as0, pr);
-                    pk[y] = tc::pack_bf16(pr.x, pr.y);
-                }
-                tc::tmem_st16_split<32>(tR + 16 * b, pk);
-                if (precise) {
-#pragma unroll
-                    for (int y = 0; y < 16; ++y)
-                        pk[y] = tc::pack_bf16(
-                            __uint_as_float(rv[b][2 * y]) - tc::bf16_lo_to_f32(pk[y]),
-                            __uint_as_float(rv[b][2 * y + 1]) - tc::bf16_hi_to_f32(pk[y]));
-                    tc::tmem_st16_split<32>(tR + 64 + 16 * b, pk);
-                }
-            };
-            if (it == 0) {
-                // row shift c: p-weighted mean of r over the first (full) key tile,
-                // needed before any PR
-                do_p(0);
-                do_p(1);
-                float2 pr0 = make_float2(0.f, 0.f), pr1 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int b = 0; b < 2; ++b)
+                // P -> packed columns 16b.. of this thread's half of the row (split 32);
+                // p overwrites s in registers
+                const float2 nm2 = make_float2(-m, -m);
+                float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
+                auto do_p = [&](int b) {
+                    uint32_t pk[16];
+                    exp_block32(sv[b], qs2, nm2, ls0, ls1, pk);
+                    tc::tmem_st16_split<32>(tS + 16 * b, pk);
+                    if (precise) {
+                        residual_block32(sv[b], pk);
+                        tc::tmem_st16_split<32>(tS + 64 + 16 * b, pk);
+                    }
+                };
+                // PR = p (r - c) -> packed columns of the R rows.  R was read in full
+                // above, so these stores may land on columns that the other half of
+                // the row read as R.
+                float2 as0 = make_float2(0.f, 0.f), as1 = make_float2(0.f, 0.f);
+                auto do_pr = [&](int b) {
+                    const float2 nc2 = make_float2(-c, -c);
+                    uint32_t pk[16];
 #pragma unroll
                     for (int y = 0; y < 16; ++y) {
                         const float2 p2 = make_float2(__uint_as_float(sv[b][2 * y]),
                                                       __uint_as_float(sv[b][2 * y + 1]));
                         const float2 r2 = make_float2(__uint_as_float(rv[b][2 * y]),
                                                       __uint_as_float(rv[b][2 * y + 1]));
-                        if (y & 1) pr1 = __ffma2_rn(p2, r2, pr1);
-                        else pr0 = __ffma2_rn(p2, r2, pr0);
+                        const float2 pr = __fmul2_rn(p2, __fadd2_rn(r2, nc2));
+                        rv[b][2 * y] = __float_as_uint(pr.x);
+                        rv[b][2 * y + 1] = __float_as_uint(pr.y);
+                        if (y & 1) as1 = __fadd2_rn(as1, pr);
+                        else as0 = __fadd2_rn(as0, pr);
+                        pk[y] = tc::pack_bf16(pr.x, pr.y);
                     }
+                    tc::tmem_st16_split<32>(tR + 16 * b, pk);
+                    if (precise) {
+                        residual_block32(rv[b], pk);
+                        tc::tmem_st16_split<32>(tR + 64 + 16 * b, pk);
+                    }
+                };
+                if (it == 0) {
+                    // row shift c: p-weighted mean of r over the first (full) key tile,
+                    // needed before any PR
+                    do_p(0);
+                    do_p(1);
+                    float2 pr0 = make_float2(0.f, 0.f), pr1 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int b = 0; b < 2; ++b)
+#pragma unroll
+                        for (int y = 0; y < 16; ++y) {
+                            const float2 p2 = make_float2(__uint_as_float(sv[b][2 * y]),
+                                                          __uint_as_float(sv[b][2 * y + 1]));
+                            const float2 r2 = make_float2(__uint_as_float(rv[b][2 * y]),
+                                                          __uint_as_float(rv[b][2 * y + 1]));
+                            if (y & 1) pr1 = __ffma2_rn(p2, r2, pr1);
+                            else pr0 = __ffma2_rn(p2, r2, pr0);
+                        }
+                    const float2 ls = __fadd2_rn(ls0, ls1);
+                    const float2 pr = __fadd2_rn(pr0, pr1);
+                    float prs = pr.x + pr.y;
+                    prs += __shfl_xor_sync(kFullMask, prs, 16);
+                    c = prs / (ls.x + ls.y + __shfl_xor_sync(kFullMask, ls.x + ls.y, 16));
+                    do_pr(0);
+                    do_pr(1);
+                } else {
+                    // one pass per 32-key block keeps fewer values live
+                    do_p(0);
+                    do_pr(0);
+                    do_p(1);
+                    do_pr(1);
+                }
                 const float2 ls = __fadd2_rn(ls0, ls1);
-                const float2 pr = __fadd2_rn(pr0, pr1);
-                float prs = pr.x + pr.y;
-                prs += __shfl_xor_sync(kFullMask, prs, 16);
-                c = prs / (ls.x + ls.y + __shfl_xor_sync(kFullMask, ls.x + ls.y, 16));
-                do_pr(0);
-                do_pr(1);
-            } else {
-                // one pass per 32-key block keeps fewer values live
-                do_p(0);
-                do_pr(0);
-                do_p(1);
-                do_pr(1);
+                const float2 as = __fadd2_rn(as0, as1);
+                l += ls.x + ls.y;
+                A += as.x + as.y;
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+                mbar_arrive(&p_full[sub]);
             }
-            const float2 ls = __fadd2_rn(ls0, ls1);
-            const float lsum = ls.x + ls.y;
-            const float2 as = __fadd2_rn(as0, as1);
-            l += lsum;
-            A += as.x + as.y;
-            tc::tmem_st_wait();
-            tc::fence_before_sync();
-            mbar_arrive(&p_full[sub]);
-        }
 
-        // ---- epilogue: o = U/l - (W/l - (A/l)(U/l)) = ((U (1 + A/l)) - W) / l
-        const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_tc_err);
-        if (__all_sync(kFullMask, done)) {
-            tc::fence_after_sync();
-            const float lt = l + __shfl_xor_sync(kFullMask, l, 16);
-            const float At = A + __shfl_xor_sync(kFullMask, A, 16);
-            const float inv_l = 1.f / lt;
-            const float gain = 1.f + At * inv_l;
-            float* orow = a.o + ((size_t)bh * a.L + i) * D + h * (D / 2);
+            // ---- epilogue: o = U/l - (W/l - (A/l)(U/l)) = ((U (1 + A/l)) - W) / l
+            const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_tc_err);
+            if (__all_sync(kFullMask, done)) {
+                tc::fence_after_sync();
+                const float lt = l + __shfl_xor_sync(kFullMask, l, 16);
+                const float At = A + __shfl_xor_sync(kFullMask, A, 16);
+                const float inv_l = 1.f / lt;
+                const float gain = 1.f + At * inv_l;
+                float* orow = a.o + ((size_t)bh * a.L + i) * D + h * (D / 2);
 #pragma unroll 1
-            for (int b = 0; b < D / 64; ++b) {
-                uint32_t u[32], w[32];
-                tc::tmem_ld32_split<D / 2>(tU + 32 * b, u);
-                tc::tmem_ld32_split<D / 2>(tW + 32 * b, w);
-                tc::tmem_ld_wait();
-                if (i < a.L) {
+                for (int b = 0; b < D / 64; ++b) {
+                    uint32_t u[32], w[32];
+                    tc::tmem_ld32_split<D / 2>(tU + 32 * b, u);
+                    tc::tmem_ld32_split<D / 2>(tW + 32 * b, w);
+                    tc::tmem_ld_wait();
+                    if (i < a.L) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 4) {
-                        float out[4];
+                        for (int x = 0; x < 32; x += 4) {
+                            float out[4];
 #pragma unroll
-                        for (int y = 0; y < 4; ++y)
-                            out[y] = (__uint_as_float(u[x + y]) * gain - __uint_as_float(w[x + y])) *
-                                     inv_l;
-                        *reinterpret_cast<float4*>(orow + 32 * b + x) =
-                            make_float4(out[0], out[1], out[2], out[3]);
+                            for (int y = 0; y < 4; ++y)
+                                out[y] = (__uint_as_float(u[x + y]) * gain - __uint_as_float(w[x + y])) *
+                                         inv_l;
+                            *reinterpret_cast<float4*>(orow + 32 * b + x) =
+                                make_float4(out[0], out[1], out[2], out[3]);
+                        }
                     }
                 }
+            } else {
+                *abort_flag = 1;
             }
         } else {
-            *abort_flag = 1;
+            // ------------------------------------------------ W_R = 0: one query row per thread
+            const int i = first_row + 32 * g + lane;
+            const uint32_t row = tmem + ((uint32_t)(32 * g) << 16);
+            const uint32_t tS = row + LY::dcol(sub), tU = row + LY::ocol(sub);
+            for (int it = 0; it < n_tiles && ok; ++it) {
+                const int k0 = it * BN;
+                const bool got = !*abort_flag && mbar_wait(&s_full[sub], it & 1, &g_tc_err);
+                if (!__all_sync(kFullMask, got)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                uint32_t sv[4][32];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) tc::tmem_ld32(tS + 32 * b, sv[b]);
+                tc::tmem_ld_wait();
+                const bool need_mask = (k0 + BN > a.L) || (CAUSAL && k0 + BN - 1 > first_row);
+                if (need_mask) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            const int key = k0 + 32 * b + x;
+                            if (!(key < a.L && (!CAUSAL || key <= i)))
+                                sv[b][x] = __float_as_uint(-INFINITY);
+                        }
+                }
+                float c0 = -INFINITY, c1 = -INFINITY, c2 = -INFINITY, c3 = -INFINITY;
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+#pragma unroll
+                    for (int x = 0; x < 32; x += 8) {
+                        c0 = fmax3(c0, __uint_as_float(sv[b][x]), __uint_as_float(sv[b][x + 1]));
+                        c1 = fmax3(c1, __uint_as_float(sv[b][x + 2]), __uint_as_float(sv[b][x + 3]));
+                        c2 = fmax3(c2, __uint_as_float(sv[b][x + 4]), __uint_as_float(sv[b][x + 5]));
+                        c3 = fmax3(c3, __uint_as_float(sv[b][x + 6]), __uint_as_float(sv[b][x + 7]));
+                    }
+                const float mx = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * qs;
+                if (it == 0) {
+                    m = mx;
+                } else if (__any_sync(kFullMask, mx > m + kRescaleThreshold)) {
+                    const float m_new = fmaxf(m, mx);
+                    const float alpha = fast_exp2(m - m_new);
+                    l *= alpha;
+#pragma unroll 1
+                    for (int b = 0; b < D / 32; ++b) {
+                        uint32_t u[32];
+                        tc::tmem_ld32(tU + 32 * b, u);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
+                        tc::tmem_st32(tU + 32 * b, u);
+                    }
+                    m = m_new;
+                }
+                const float2 nm2 = make_float2(-m, -m);
+                float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    uint32_t pk[16];
+                    exp_block32(sv[b], qs2, nm2, ls0, ls1, pk);
+                    tc::tmem_st16(tS + 16 * b, pk);  // packed: keys 32b.. -> columns 16b..
+                }
+                const float2 ls = __fadd2_rn(ls0, ls1);
+                l += ls.x + ls.y;
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+                mbar_arrive(&p_full[sub]);
+            }
+            // ---- epilogue: o = U / l
+            const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_tc_err);
+            if (__all_sync(kFullMask, done)) {
+                tc::fence_after_sync();
+                const float inv_l = 1.f / l;
+                float* orow = a.o + ((size_t)bh * a.L + i) * D;
+#pragma unroll 1
+                for (int b = 0; b < D / 32; ++b) {
+                    uint32_t u[32];
+                    tc::tmem_ld32(tU + 32 * b, u);
+                    tc::tmem_ld_wait();
+                    if (i < a.L) {
+#pragma unroll
+                        for (int x = 0; x < 32; x += 4)
+                            *reinterpret_cast<float4*>(orow + 32 * b + x) = make_float4(
+                                __uint_as_float(u[x]) * inv_l, __uint_as_float(u[x + 1]) * inv_l,
+                                __uint_as_float(u[x + 2]) * inv_l, __uint_as_float(u[x + 3]) * inv_l);
+                    }
+                }
+            } else {
+                *abort_flag = 1;
+            }
         }
     }
 
@@ -895,11 +672,11 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int L, int D, int box_ro
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool RHO, bool CAUSAL>
+template <int D, bool CAUSAL, bool RHO>
 cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mr, const CUtensorMap& mk,
                    const CUtensorMap& mv, const TcArgs& a, cudaStream_t stream) {
-    using LY = TcLayout<D, RHO>;
-    auto kern = prefill_tc_kernel<D, RHO, CAUSAL>;
+    using LY = PairLayout<D, RHO>;
+    auto kern = prefill_pair_kernel<D, CAUSAL, RHO>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -907,26 +684,18 @@ cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mr, const CUtensorM
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const unsigned grid = (unsigned)((size_t)a.n_qt * a.BH);
+    const unsigned grid = (unsigned)((size_t)a.n_qb * a.BH);
     kern<<<grid, kThreads, LY::SMEM_BYTES, stream>>>(mq, mr, mk, mv, a);
     return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
-cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mr, const CUtensorMap& mk,
-                        const CUtensorMap& mv, const TcArgs& a, cudaStream_t stream) {
-    using LY = PairLayout<D>;
-    auto kern = prefill_pair_kernel<D, CAUSAL>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             LY::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    const unsigned grid = (unsigned)((size_t)a.n_qt * a.BH);
-    kern<<<grid, kThreads2, LY::SMEM_BYTES, stream>>>(mq, mr, mk, mv, a);
-    return cudaGetLastError();
+template <int D, bool RHO>
+cudaError_t launch_d(const PrefillShape& s, const CUtensorMap& mq, const CUtensorMap& mr,
+                     const CUtensorMap& mk, const CUtensorMap& mv, float* o, cudaStream_t stream) {
+    using LY = PairLayout<D, RHO>;
+    const TcArgs a{o, s.L, s.B * s.H, (s.L + LY::BLOCK - 1) / LY::BLOCK, s.scale * kLog2e};
+    return s.causal ? launch<D, true, RHO>(mq, mr, mk, mv, a, stream)
+                    : launch<D, false, RHO>(mq, mr, mk, mv, a, stream);
 }
 
 }  // namespace
@@ -936,38 +705,20 @@ cudaError_t prefill_tc_launch(const PrefillShape& s, const void* q, const void* 
                               cudaStream_t stream) {
     const int BH = s.B * s.H;
     CUtensorMap mq, mr, mk, mv;
-    if (!make_map(&mq, q, BH, s.L, s.d) || !make_map(&mk, k, BH, s.L, s.d) ||
-        !make_map(&mv, v, BH, s.L, s.d))
+    if (!make_map(&mk, k, BH, s.L, s.d) || !make_map(&mv, v, BH, s.L, s.d))
         return cudaErrorInvalidValue;
     if (rho) {
-        if (!make_map(&mr, rho, BH, s.L, s.d)) return cudaErrorInvalidValue;
-    } else {
-        mr = mq;
-    }
-    TcArgs a{o, s.L, BH, (s.L + BM - 1) / BM, s.scale * kLog2e};
-    const bool r = rho != nullptr;
-    if (r) {
         // correction path: query and probe maps use 16-row boxes (stacked operand)
         if (!make_map(&mq, q, BH, s.L, s.d, 16) || !make_map(&mr, rho, BH, s.L, s.d, 16))
             return cudaErrorInvalidValue;
-        if (s.d == 64)
-            return s.causal ? launch_pair<64, true>(mq, mr, mk, mv, a, stream)
-                            : launch_pair<64, false>(mq, mr, mk, mv, a, stream);
-        if (s.d == 128)
-            return s.causal ? launch_pair<128, true>(mq, mr, mk, mv, a, stream)
-                            : launch_pair<128, false>(mq, mr, mk, mv, a, stream);
+        if (s.d == 64) return launch_d<64, true>(s, mq, mr, mk, mv, o, stream);
+        if (s.d == 128) return launch_d<128, true>(s, mq, mr, mk, mv, o, stream);
         return cudaErrorInvalidValue;
     }
-#define PARALLAX_TC_CASE(DD)                                                               \
-    if (s.d == DD) {                                                                       \
-        if (r) return s.causal ? launch<DD, true, true>(mq, mr, mk, mv, a, stream)         \
-                               : launch<DD, true, false>(mq, mr, mk, mv, a, stream);       \
-        return s.causal ? launch<DD, false, true>(mq, mr, mk, mv, a, stream)               \
-                        : launch<DD, false, false>(mq, mr, mk, mv, a, stream);             \
-    }
-    PARALLAX_TC_CASE(64)
-    PARALLAX_TC_CASE(128)
-#undef PARALLAX_TC_CASE
+    if (!make_map(&mq, q, BH, s.L, s.d)) return cudaErrorInvalidValue;
+    mr = mq;  // unused
+    if (s.d == 64) return launch_d<64, false>(s, mq, mr, mk, mv, o, stream);
+    if (s.d == 128) return launch_d<128, false>(s, mq, mr, mk, mv, o, stream);
     return cudaErrorInvalidValue;
 }
 
