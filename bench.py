@@ -38,8 +38,8 @@ METRIC = "decode KV-stream GB/s (% B300 HBM peak); causal prefill TFLOP/s (% TC 
 TRAFFIC_BYTES = {
     # B=8 capture: 536.98 MB read (x8 heads' worth at B=64) + ~5.9 MB partials and o
     "decode": 8 * 536.98e6 + 5.9e6,
-    # B=2 capture: 135.58 MB read (x4 at B=8) + the 268.4 MB fp32 output written
-    "prefill": 4 * 135.58e6 + 268.4e6,
+    # the prefill kernel changed after its capture; re-measure before quoting
+    "prefill": None,
 }
 
 
@@ -60,6 +60,9 @@ def parse_args(argv=None):
                     help="override the decode batch (profiling runs on smaller cases)")
     ap.add_argument("--prefill-batch", type=int, default=None,
                     help="override the prefill batch (profiling runs on smaller cases)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the step: time the decode sweep cells and the ragged-batch "
+                         "decode, one JSON line per case (plus a markdown table on stderr)")
     return ap.parse_args(argv)
 
 
@@ -464,10 +467,88 @@ def run_ours(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- decode sweep
+def run_sweep(args):
+    """Decode over the sweep grid (batch x context, caches up to 64e9 bytes, plus the
+    64 GiB boundary cell, flagged) and the ragged batch.  Each case is timed with CUDA
+    events per call; caches smaller than twice the L2 are evicted before every call by
+    writing a 512 MB buffer (not timed), larger ones are timed back to back."""
+    import torch
+
+    import softmax_covariance_correction_pass_b300 as px
+    from softmax_covariance_correction_pass_b300 import configs
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    px.load_library()
+    peaks = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sw = configs.DECODE_SWEEP
+    cases = [("sweep", B, L, False) for B, L in configs.decode_sweep_cells()]
+    cases += [("sweep", B, L, True) for B, L in configs.decode_sweep_cells(include_boundary=True)
+              if (B, L) not in configs.decode_sweep_cells()]
+    cases.append(("ragged", configs.DECODE_RAGGED["B"], configs.DECODE_RAGGED["hi"], False))
+    rows = []
+    for kind, B, L, boundary in cases:
+        if kind == "sweep":
+            inp = configs.decode_sweep_inputs(B, L, dev)
+        else:
+            inp = configs.decode_ragged_inputs(dev)
+        H, d = sw["H"], sw["d"]
+        keys = int(inp.seqlens.sum().item())
+        kv = keys * H * d * 2 * 2
+        total = kv + 2 * B * H * d * 2 + B * H * d * 4 + B * 4
+        o = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+        call = lambda: px.parallax_attn_decode(inp.q, inp.rho, inp.k_cache, inp.v_cache,
+                                               inp.seqlens, o)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        cold = kv < 2 * l2
+        reps = 20 if cold else max(5, min(50, int(2e10 / max(total, 1))))
+        times = []
+        for _ in range(reps):
+            if cold:
+                flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            torch.cuda.synchronize() if cold else None
+            times.append((a, b))
+        torch.cuda.synchronize()
+        if px.parallax_check_device_error() != 0:
+            raise RuntimeError(f"device error in decode case {kind} B={B} L={L}")
+        ms = statistics.median(a.elapsed_time(b) for a, b in times)
+        gbs = total / (ms * 1e-3) / 1e9
+        chunk = px.parallax_attn_decode_chunk_keys(B, H, int(inp.k_cache.shape[2]), d, 2)
+        row = {"case": kind, "B": B, "context": L if kind == "sweep" else f"U[128,{L}]",
+               "keys": keys, "kv_bytes": kv, "ms": ms, "GB/s": gbs,
+               "frac_of_hbm_peak": gbs / peaks["hbm_gbs"], "tokens_per_s": B / (ms * 1e-3),
+               "chunk_keys": chunk, "l2": "evicted before each call" if cold else "larger than L2",
+               "boundary_cell_64GiB": boundary}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+        del inp, o
+        torch.cuda.empty_cache()
+    print("| case | B | context | KV bytes | ms | GB/s | % of HBM peak | tokens/s | chunk |",
+          file=sys.stderr)
+    print("|---|---|---|---|---|---|---|---|---|", file=sys.stderr)
+    for r in rows:
+        tag = " (64 GiB, flagged)" if r["boundary_cell_64GiB"] else ""
+        print(f"| {r['case']}{tag} | {r['B']} | {r['context']} | {r['kv_bytes'] / 1e9:.3f} GB | "
+              f"{r['ms']:.4f} | {r['GB/s']:.0f} | {100 * r['frac_of_hbm_peak']:.1f}% | "
+              f"{r['tokens_per_s']:.0f} | {r['chunk_keys']} |", file=sys.stderr)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 
