@@ -136,3 +136,27 @@ def rows(q, rho, k, v, nkeys, scale: float, form: str = "explicit") -> np.ndarra
     if rc != 0:
         raise RuntimeError(f"oracle_rows failed ({rc})")
     return o
+
+
+def qkvr_projection(x, w, H: int, d: int) -> list:
+    """The layer's input projections: q, k, v and the probe rho = W_R x.
+
+    The probe is a learned linear map of the layer input x_i ("Parallax mantem
+    softmax ...", paragraph 2: rho_i = W_R x_i); q, k and v are the usual
+    attention projections of the same x_i.  Here they are one product with the
+    stacked weight:
+
+      x : [B, L, width]            (one row per token)
+      w : [n_out * H * d, width]   rows = output features, blocks W_q; W_k; W_v; (W_R)
+      y = x w^T                    [B, L, n_out * H * d]      (fp64, numpy matmul)
+      out[t][b, h, l, c] = y[b, l, t*H*d + h*d + c]           (t = 0: q, 1: k, 2: v, 3: rho)
+
+    Returns the n_out arrays [B, H, L, d] in fp64 (n_out = rows of w / (H*d)).
+    """
+    x, w = _f64(x), _f64(w)
+    B, L, width = x.shape
+    n_out, rem = divmod(w.shape[0], H * d)
+    assert rem == 0 and w.shape[1] == width
+    y = x.reshape(B * L, width) @ w.T
+    y = y.reshape(B, L, n_out, H, d)
+    return [np.ascontiguousarray(y[:, :, t].transpose(0, 2, 1, 3)) for t in range(n_out)]
