@@ -160,3 +160,48 @@ def qkvr_projection(x, w, H: int, d: int) -> list:
     y = x.reshape(B * L, width) @ w.T
     y = y.reshape(B, L, n_out, H, d)
     return [np.ascontiguousarray(y[:, :, t].transpose(0, 2, 1, 3)) for t in range(n_out)]
+
+
+def decode_gqa(q, rho, k_cache, v_cache, seqlens, scale: float | None = None,
+               form: str = "explicit") -> np.ndarray:
+    """Decode with key/value heads shared by groups of query heads (grouped-query
+    attention): q, rho [B, H, d]; caches [B, H_kv, Lmax, d] with H a multiple of
+    H_kv; query head h reads key/value head h // (H // H_kv).  Each query head's
+    output is the Parallax decode of its own q and rho against that cache."""
+    q, rho, kc, vc = _f64(q), _f64(rho), _f64(k_cache), _f64(v_cache)
+    B, H, d = q.shape
+    Hkv = kc.shape[1]
+    G, rem = divmod(H, Hkv)
+    assert rem == 0
+    heads = [h // G for h in range(H)]
+    return decode(q, rho, kc[:, heads], vc[:, heads], seqlens, scale=scale, form=form)
+
+
+def gather_pages(pages, block_table, seqlens, page_size: int) -> np.ndarray:
+    """The contiguous cache [B, H_kv, Lmax, d] that a paged cache stands for:
+    key t of sequence b lives in page block_table[b, t // page_size], row
+    t % page_size, of pages [num_pages, H_kv, page_size, d].  Rows at or past
+    seqlens[b] are left zero; Lmax = block_table.shape[1] * page_size."""
+    pages = _f64(pages)
+    if hasattr(block_table, "detach"):
+        block_table = block_table.detach().cpu().numpy()
+    if hasattr(seqlens, "detach"):
+        seqlens = seqlens.detach().cpu().numpy()
+    bt = np.asarray(block_table)
+    B, max_pages = bt.shape
+    _, Hkv, P, d = pages.shape
+    assert P == page_size
+    out = np.zeros((B, Hkv, max_pages * P, d))
+    for b in range(B):
+        for t in range(int(seqlens[b])):
+            out[b, :, t] = pages[bt[b, t // P], :, t % P]
+    return out
+
+
+def decode_paged(q, rho, k_pages, v_pages, block_table, seqlens, page_size: int,
+                 scale: float | None = None, form: str = "explicit") -> np.ndarray:
+    """Decode against a paged key/value cache (see gather_pages), with grouped
+    query heads when the pages hold fewer heads than q (see decode_gqa)."""
+    kc = gather_pages(k_pages, block_table, seqlens, page_size)
+    vc = gather_pages(v_pages, block_table, seqlens, page_size)
+    return decode_gqa(q, rho, kc, vc, seqlens, scale=scale, form=form)
