@@ -38,8 +38,10 @@ METRIC = "decode KV-stream GB/s (% B300 HBM peak); causal prefill TFLOP/s (% TC 
 TRAFFIC_BYTES = {
     # B=8 capture: 536.98 MB read (x8 heads' worth at B=64) + ~5.9 MB partials and o
     "decode": 8 * 536.98e6 + 5.9e6,
-    # the prefill kernel changed after its capture; re-measure before quoting
-    "prefill": None,
+    # B=2 capture of prefill_pair_kernel<128,1,1>: 135.49 MB read (x4 at B=8) + the 268.4 MB
+    # fp32 output written
+    "prefill": 4 * 135.49e6 + 268.4e6,
+    "projection": None,
 }
 
 
@@ -54,12 +56,17 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "projection"], default=None,
                     help="time one kernel alone (profiling runs); the default times both")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="override the decode batch (profiling runs on smaller cases)")
     ap.add_argument("--prefill-batch", type=int, default=None,
                     help="override the prefill batch (profiling runs on smaller cases)")
+    ap.add_argument("--no-projection", action="store_true",
+                    help="skip the q/k/v/probe projection leg")
+    ap.add_argument("--wr-zero", action="store_true",
+                    help="time the W_R = 0 path (rho = NULL) in the step instead of the "
+                         "correction path (profiling runs)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the step: time the decode sweep cells and the ragged-batch "
                          "decode, one JSON line per case (plus a markdown table on stderr)")
@@ -236,6 +243,61 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
     return 0
 
+def time_projection(args, dev, peaks, max_over_ranks, n_rep=20):
+    """The layer-shaped projection x [B, L, 2048] -> q, k, v, rho [B, H, L, d] (one tcgen05
+    GEMM, 4*H*d output features), `n_rep` launches back to back after 3 warm-ups."""
+    import torch
+
+    import softmax_covariance_correction_pass_b300 as px
+    from softmax_covariance_correction_pass_b300 import configs
+
+    pc = configs.LAYER_PREFILL
+    PB, PH, PL, Pd = args.prefill_batch or pc["B"], pc["H"], pc["L"], pc["d"]
+    stream = torch.cuda.current_stream()
+    x, w = configs.layer_projection_inputs(dev, B=PB)
+    pq = [torch.empty((PB, PH, PL, Pd), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    width = x.shape[-1]
+    proj_flops = 2.0 * PB * PL * width * 4 * PH * Pd
+
+    def project():
+        px.parallax_attn_qkvr_projection(x, w, PH, Pd, *pq)
+
+    for _ in range(max(args.warmup, 3)):
+        project()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n_rep):
+        project()
+    b.record(stream)
+    torch.cuda.synchronize()
+    proj_ms = max_over_ranks(a.elapsed_time(b) / n_rep)
+    if px.parallax_check_device_error() != 0:
+        raise RuntimeError("device error in the projection")
+    proj_tf = proj_flops / (proj_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": proj_tf, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": proj_tf / peaks["bf16_tflops"],
+            "traffic": TRAFFIC_BYTES.get("projection"), "kernel": "proj_kernel",
+            "algorithmic_flops_per_launch": proj_flops, "avg_launch_ms": proj_ms,
+            "launches": n_rep,
+            "shape": f"x [{PB},{PL},{width}] x W^T [{width},{4 * PH * Pd}] -> q,k,v,rho "
+                     f"[{PB},{PH},{PL},{Pd}] bf16",
+            "peak_source": peaks["source"] + f" (burst: timed alone, {n_rep} launches)"}
+
+
+def run_projection_only(args):
+    """--only projection: the projection leg alone (profiling runs), one JSON line."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import softmax_covariance_correction_pass_b300 as px
+
+    px.load_library()
+    r = time_projection(args, dev, load_peaks(), lambda x: x, n_rep=args.steps)
+    print(json.dumps({"metric": "projection TFLOP/s", "value": r["achieved"], "unit": "TFLOP/s",
+                      "steps": args.steps, "warmup": args.warmup, "roofline": r}), flush=True)
+    return 0
+
 
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args):
@@ -276,20 +338,24 @@ def run_ours(args):
     po = torch.empty((PB, PH, PL, Pd), dtype=torch.float32, device=dev)
     kv_bytes, dec_bytes = decode_bytes(B, H, n, d)
     pre_flops = prefill_flops(PB, PH, PL, Pd)
+    if args.wr_zero:  # S and U only: two of the four contractions
+        pre_flops /= 2
     chunk = px.parallax_attn_decode_chunk_keys(B, H, n, d, 2)
     dec_launches = 2 if chunk < n else 1
 
     run_decode = args.only in (None, "decode")
     run_prefill = args.only in (None, "prefill")
 
+    drho = None if args.wr_zero else dinp.rho
+    prho = None if args.wr_zero else pinp.rho
+
     def decode():
         if run_decode:
-            px.parallax_attn_decode(dinp.q, dinp.rho, dinp.k_cache, dinp.v_cache, dinp.seqlens,
-                                    do)
+            px.parallax_attn_decode(dinp.q, drho, dinp.k_cache, dinp.v_cache, dinp.seqlens, do)
 
     def prefill():
         if run_prefill:
-            px.parallax_attn_prefill(pinp.q, pinp.rho, pinp.k, pinp.v, po, causal=True,
+            px.parallax_attn_prefill(pinp.q, prho, pinp.k, pinp.v, po, causal=True,
                                      scale=pinp.scale)
 
     for _ in range(max(args.warmup, 3)):
@@ -342,7 +408,7 @@ def run_ours(args):
                 "peak_source": peaks["source"]}
     roof_pre = {"bound": "tensor", "achieved": pre_tflops, "peak": peaks["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": pre_tflops / peaks["bf16_tflops_sustained"],
-                "traffic": TRAFFIC_BYTES["prefill"], "kernel": "prefill_tc_kernel",
+                "traffic": TRAFFIC_BYTES["prefill"], "kernel": "prefill_pair_kernel",
                 "algorithmic_flops_per_launch": pre_flops, "avg_launch_ms": pre_ms,
                 "peak_burst": peaks["bf16_tflops"],
                 "frac_burst": pre_tflops / peaks["bf16_tflops"],
@@ -370,6 +436,11 @@ def run_ours(args):
         b.record(stream)
         torch.cuda.synchronize()
         f0[name] = units / (a.elapsed_time(b) / 20 * 1e-3)
+
+    # ---- q/k/v/probe projection of the layer-shaped workload (one tcgen05 GEMM), timed alone
+    proj = None
+    if not args.only and not args.no_projection:
+        proj = time_projection(args, dev, peaks, max_over_ranks)
 
     # ---- end to end through the public call, host buffers (pinned), copies timed
     e2e = None
@@ -445,6 +516,7 @@ def run_ours(args):
                             "tokens_per_s": ws * PB * PL / (pre_ms * 1e-3)},
                 "l2": "inputs larger than L2 (4.3 GB KV cache; 1.07 GB of prefill tensors)",
                 "only": args.only,
+                "w_r_zero": bool(args.wr_zero),
                 "parallelism": f"replicas x{ws} (no collectives)"},
             "roofline": dominant,
             "roofline_decode": roof_dec,
@@ -456,6 +528,7 @@ def run_ours(args):
                 "metric": "decode KV-stream GB/s", "value": value, "unit": "GB/s",
                 "frac_of_peak": roof_dec["frac"], "ms_per_call": dec_ms},
             "w_r_zero_fast_path": f0,
+            "roofline_projection": proj,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks.summary(),
@@ -549,6 +622,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.only == "projection":
+        return run_projection_only(args)
     return run_ours(args)
 
 
