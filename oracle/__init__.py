@@ -205,3 +205,32 @@ def decode_paged(q, rho, k_pages, v_pages, block_table, seqlens, page_size: int,
     kc = gather_pages(k_pages, block_table, seqlens, page_size)
     vc = gather_pages(v_pages, block_table, seqlens, page_size)
     return decode_gqa(q, rho, kc, vc, seqlens, scale=scale, form=form)
+
+
+def prefill_chunk(q, rho, k_new, v_new, k_cache, v_cache, cache_lens, scale: float | None = None,
+                  form: str = "explicit") -> np.ndarray:
+    """Causal prefill of a chunk of new tokens that continues cached sequences.
+
+    q, rho, k_new, v_new : [B, H, Lq, d]   the chunk (Lq new tokens per sequence)
+    k_cache, v_cache     : [B, H, Lmax, d] sequence b holds cache_lens[b] earlier tokens
+    Token i of the chunk sits at position p = cache_lens[b] + i of its sequence; its
+    key set is the sequence's keys at positions 0..p: the cached rows 0..cache_lens[b]-1
+    followed by the chunk's rows 0..i.  Returns o [B, H, Lq, d].
+    """
+    q, rho, kn, vn = _f64(q), _f64(rho), _f64(k_new), _f64(v_new)
+    kc, vc = _f64(k_cache), _f64(v_cache)
+    if hasattr(cache_lens, "detach"):
+        cache_lens = cache_lens.detach().cpu().numpy()
+    B, H, Lq, d = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.empty_like(q)
+    for b in range(B):
+        off = int(cache_lens[b])
+        nkeys = off + 1 + np.arange(Lq)
+        for h in range(H):
+            K = np.concatenate([kc[b, h, :off], kn[b, h]])
+            V = np.concatenate([vc[b, h, :off], vn[b, h]])
+            o[b, h] = rows(q[b, h], None if rho is None else rho[b, h], K, V, nkeys, scale,
+                           form=form)
+    return o

@@ -169,3 +169,73 @@ def test_pins_reject_planted_mistake(name):
     except (IndexError, ValueError):
         return  # the mistake breaks the lookup outright
     assert not np.allclose(got, ref, rtol=0, atol=1e-9), f"mutant survived: {name}"
+
+
+# ----------------------------------------------------------------------------
+# chunked prefill that continues a cached sequence
+# ----------------------------------------------------------------------------
+def _brute_chunk(q, rho, kn, vn, kc, vc, cache_lens):
+    B, H, Lq, d = q.shape
+    o = np.zeros((B, H, Lq, d))
+    for b in range(B):
+        off = int(cache_lens[b])
+        for h in range(H):
+            for i in range(Lq):
+                K = [kc[b, h, t] for t in range(off)] + [kn[b, h, t] for t in range(i + 1)]
+                V = [vc[b, h, t] for t in range(off)] + [vn[b, h, t] for t in range(i + 1)]
+                o[b, h, i] = _brute_row(q[b, h, i], None if rho is None else rho[b, h, i], K, V,
+                                        1.0 / np.sqrt(d))
+    return o
+
+
+@pytest.mark.parametrize("with_rho", [True, False])
+def test_chunk_brute_force(with_rho):
+    rng = np.random.default_rng(12)
+    B, H, Lq, Lmax, d = 2, 2, 3, 6, 3
+    q = rng.standard_normal((B, H, Lq, d))
+    rho = 0.7 * rng.standard_normal((B, H, Lq, d)) if with_rho else None
+    kn, vn = 1.2 * rng.standard_normal((2, B, H, Lq, d))
+    kc, vc = 1.2 * rng.standard_normal((2, B, H, Lmax, d))
+    cl = np.array([3, 0])
+    ref = _brute_chunk(q, rho, kn, vn, kc, vc, cl)
+    got = oracle.prefill_chunk(q, rho, kn, vn, kc, vc, cl)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13 * max(1.0, np.abs(ref).max()))
+
+
+@pytest.mark.parametrize("off", [0, 1, 5, 9])
+def test_chunks_compose_to_one_prefill(off):
+    """Rows off..L-1 of one causal prefill of L tokens equal the chunk prefill of
+    those rows over a cache holding tokens 0..off-1 (whatever the cache holds
+    past off is never read)."""
+    rng = np.random.default_rng(off)
+    B, H, L, d = 2, 2, 10, 4
+    q, rho, k, v = (rng.standard_normal((B, H, L, d)) for _ in range(4))
+    full = oracle.prefill(q, rho, k, v, causal=True)
+    kc, vc = 99.0 * rng.standard_normal((2, B, H, L + 3, d))  # garbage past off
+    kc[:, :, :off], vc[:, :, :off] = k[:, :, :off], v[:, :, :off]
+    got = oracle.prefill_chunk(q[:, :, off:], rho[:, :, off:], k[:, :, off:], v[:, :, off:], kc,
+                               vc, np.array([off, off]))
+    np.testing.assert_allclose(got, full[:, :, off:], rtol=1e-13, atol=1e-13)
+
+
+CHUNK_MUTANTS = {
+    "diagonal excluded": ("nkeys = off + 1 + np.arange(Lq)", "nkeys = off + np.arange(Lq) + (off == 0)"),
+    "cache ignored": ("K = np.concatenate([kc[b, h, :off], kn[b, h]])",
+                      "K = np.concatenate([kn[b, h, :1].repeat(off, 0), kn[b, h]])"),
+    "cache one row short": ("V = np.concatenate([vc[b, h, :off], vn[b, h]])",
+                            "V = np.concatenate([vc[b, h, 1:off + 1], vn[b, h]])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CHUNK_MUTANTS))
+def test_chunk_pins_reject_planted_mistake(name):
+    old, new = CHUNK_MUTANTS[name]
+    ns = _mutant(oracle.prefill_chunk, old, new)
+    rng = np.random.default_rng(13)
+    B, H, Lq, Lmax, d = 2, 2, 3, 6, 3
+    q, rho, kn, vn = (rng.standard_normal((B, H, Lq, d)) for _ in range(4))
+    kc, vc = rng.standard_normal((2, B, H, Lmax, d))
+    cl = np.array([3, 2])
+    ref = _brute_chunk(q, rho, kn, vn, kc, vc, cl)
+    got = ns["prefill_chunk"](q, rho, kn, vn, kc, vc, cl)
+    assert not np.allclose(got, ref, rtol=0, atol=1e-9), f"mutant survived: {name}"
