@@ -234,3 +234,78 @@ def prefill_chunk(q, rho, k_new, v_new, k_cache, v_cache, cache_lens, scale: flo
             o[b, h] = rows(q[b, h], None if rho is None else rho[b, h], K, V, nkeys, scale,
                            form=form)
     return o
+
+
+def _head_terms(q, rho, k, v, causal: bool, scale: float):
+    """Per-head quantities of the forward pass (fp64, one head [L, d] at a time):
+    softmax weights P, probe scores R = rho k^T, rbar = sum_j p_j r_j, and the output
+    weights Wt = P (1 + rbar - R), so that o = Wt v (the output written as one
+    weighted sum: o_i = mu_v - sum_j p_j (r_j - rbar)(v_j - mu_v) = sum_j w_j v_j)."""
+    L = q.shape[0]
+    S = scale * (q @ k.T)
+    if causal:
+        S = np.where(np.tril(np.ones((L, k.shape[0]), dtype=bool)), S, -np.inf)
+    m = S.max(axis=1, keepdims=True)
+    E = np.exp(S - m)
+    Z = E.sum(axis=1, keepdims=True)
+    P = E / Z
+    lse = (m + np.log(Z))[:, 0]
+    R = np.zeros_like(S) if rho is None else rho @ k.T
+    rbar = (P * R).sum(axis=1)
+    Wt = P * (1.0 + rbar[:, None] - R)
+    return P, R, rbar, Wt, lse
+
+
+def prefill_stats(q, rho, k, v, causal: bool = True, scale: float | None = None):
+    """Per-row quantities a training forward keeps for the backward pass:
+    lse_i = log sum_j exp(s_ij) (natural log, s = scale q.k), rbar_i = sum_j p_ij r_ij
+    and mu_v,i = sum_j p_ij v_j.  Returns (lse [B,H,L], rbar [B,H,L], mu_v [B,H,L,d])."""
+    q, rho, k, v = _f64(q), _f64(rho), _f64(k), _f64(v)
+    B, H, L, d = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    lse = np.empty((B, H, L))
+    rbar = np.empty((B, H, L))
+    mu = np.empty((B, H, L, d))
+    for b in range(B):
+        for h in range(H):
+            P, _, rb, _, ls = _head_terms(q[b, h], None if rho is None else rho[b, h], k[b, h],
+                                          v[b, h], causal, scale)
+            lse[b, h], rbar[b, h], mu[b, h] = ls, rb, P @ v[b, h]
+    return lse, rbar, mu
+
+
+def prefill_backward(q, rho, k, v, do, causal: bool = True, scale: float | None = None):
+    """Gradients of sum(do * o) for the Parallax prefill o = prefill(q, rho, k, v).
+
+    With o_i = sum_j w_ij v_j, w_ij = p_ij (1 + rbar_i - r_ij) (see _head_terms),
+    D_ij = do_i . v_j, abar_i = sum_j p_ij D_ij (= do_i . mu_v,i), delta_i = do_i . o_i:
+      dv_j   = sum_i w_ij do_i
+      dr_ij  = p_ij (abar_i - D_ij)                      (r_ij = rho_i . k_j)
+      ds_ij  = p_ij ((D_ij - abar_i)(rbar_i - r_ij) + D_ij - delta_i)   (s_ij = scale q_i.k_j)
+      dq_i   = scale sum_j ds_ij k_j,     drho_i = sum_j dr_ij k_j
+      dk_j   = scale sum_i ds_ij q_i + sum_i dr_ij rho_i
+    Returns (dq, drho, dk, dv), each [B, H, L, d] in fp64 (drho is the gradient at the
+    given rho, zeros included: rho=None is treated as rho = 0)."""
+    q, rho, k, v, do = _f64(q), _f64(rho), _f64(k), _f64(v), _f64(do)
+    B, H, L, d = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    if rho is None:
+        rho = np.zeros_like(q)
+    dq, drho, dk, dv = (np.zeros_like(q) for _ in range(4))
+    for b in range(B):
+        for h in range(H):
+            qh, rh, kh, vh, doh = q[b, h], rho[b, h], k[b, h], v[b, h], do[b, h]
+            P, R, rbar, Wt, _ = _head_terms(qh, rh, kh, vh, causal, scale)
+            o = Wt @ vh
+            Dm = doh @ vh.T
+            abar = (P * Dm).sum(axis=1)
+            delta = (doh * o).sum(axis=1)
+            dR = P * (abar[:, None] - Dm)
+            dS = P * ((Dm - abar[:, None]) * (rbar[:, None] - R) + Dm - delta[:, None])
+            dv[b, h] = Wt.T @ doh
+            dq[b, h] = scale * (dS @ kh)
+            drho[b, h] = dR @ kh
+            dk[b, h] = scale * (dS.T @ qh) + dR.T @ rh
+    return dq, drho, dk, dv
