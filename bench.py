@@ -41,7 +41,9 @@ TRAFFIC_BYTES = {
     # B=2 capture of prefill_pair_kernel<128,1,1>: 135.49 MB read (x4 at B=8) + the 268.4 MB
     # fp32 output written
     "prefill": 4 * 135.49e6 + 268.4e6,
-    "projection": None,
+    # full-size capture: 177.38 MB read + 497.77 MB written (the rest of the 536.9 MB
+    # output was still in L2 when the kernel ended)
+    "projection": 177.38e6 + 497.77e6,
 }
 
 

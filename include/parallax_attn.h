@@ -31,7 +31,7 @@
  *     are detected on the host before anything is launched; the message is
  *     available from parallax_last_error() on the calling thread.
  *   - Head dimension d must be 64 or 128 (PARALLAX_ERR_UNSUPPORTED otherwise).
- *   - Output o is always fp32.
+ *   - Attention outputs o are always fp32 (the projection writes bf16).
  */
 #ifndef PARALLAX_ATTN_H
 #define PARALLAX_ATTN_H
@@ -55,6 +55,8 @@ typedef enum {
 /* Bits of the device error word returned by parallax_check_device_error(). */
 #define PARALLAX_DEVERR_SEQLEN_CLAMPED 0x1u /* a seqlens[b] lay outside [0, Lmax] */
 #define PARALLAX_DEVERR_WAIT_TIMEOUT 0x2u   /* a pipeline wait gave up (bug)      */
+#define PARALLAX_DEVERR_PAGE_OUT_OF_RANGE 0x4u /* a block-table entry lay outside
+                                                  [0, num_pages); page 0 was read */
 
 /*
  * Causal or full prefill, bf16 inputs, fp32 output.
@@ -68,6 +70,28 @@ typedef enum {
 int parallax_attn_prefill(const void* q, const void* rho, const void* k, const void* v, void* o,
                           int B, int H, int L, int d, int causal, float scale,
                           cudaStream_t stream);
+
+/*
+ * Chunked causal prefill that continues cached sequences (bf16 in, fp32 out):
+ * a serving engine prefills a long prompt, or appends a turn, a chunk at a time
+ * against the KV cache that the pages' decode setting keeps.
+ *   q, rho, k_new, v_new : bf16 [B, H, Lq, d]    the chunk (rho may be NULL)
+ *   k_cache, v_cache     : bf16 [B, H, Lmax, d]  sequence b holds cache_lens[b] tokens
+ *   cache_lens           : int32 [B] on the device (not modified)
+ *   o                    : fp32 [B, H, Lq, d]
+ * The call first writes the chunk's k_new / v_new rows into the caches at rows
+ * cache_lens[b] .. cache_lens[b] + Lq - 1, then chunk token i (position
+ * p = cache_lens[b] + i) attends causally to cache rows 0 .. p -- the earlier
+ * tokens and the chunk's own tokens up to itself.  Rows of o equal the rows
+ * p of one causal parallax_attn_prefill over the whole sequence.  A
+ * cache_lens[b] outside [0, Lmax - Lq] is clamped into it and raises
+ * PARALLAX_DEVERR_SEQLEN_CLAMPED.  The caller advances cache_lens by Lq.
+ * Lmax >= Lq >= 1.  No workspace.
+ */
+int parallax_attn_prefill_chunk(const void* q, const void* rho, const void* k_new,
+                                const void* v_new, void* k_cache, void* v_cache,
+                                const int32_t* cache_lens, void* o, int B, int H, int Lq,
+                                int Lmax, int d, float scale, cudaStream_t stream);
 
 /* Same as parallax_attn_prefill with fp32 q, rho, k, v (fp32 SIMT arithmetic). */
 int parallax_attn_prefill_f32(const void* q, const void* rho, const void* k, const void* v,
@@ -100,6 +124,43 @@ int parallax_attn_decode_f32(const void* q, const void* rho, const void* k_cache
                              int Lmax, int d, cudaStream_t stream);
 
 /*
+ * Decode with key/value heads shared by groups of query heads (grouped-query
+ * attention), bf16 inputs, fp32 output.
+ *   q, rho            : bf16 [B, H, d]            (rho may be NULL: W_R = 0)
+ *   k_cache, v_cache  : bf16 [B, H_kv, Lmax, d]   query head h reads head h / (H / H_kv)
+ *   seqlens, o        : as in parallax_attn_decode
+ * H / H_kv must be 1, 2, 4 or 8 (PARALLAX_ERR_UNSUPPORTED otherwise); each key
+ * and value row is read from HBM once for the whole group.  Workspace, split
+ * plan (keyed on B, H_kv, Lmax) and concurrency rules of parallax_attn_decode.
+ * The Parallax pages do not discuss head sharing; the result is, per query
+ * head, exactly parallax_attn_decode against that head's key/value head.
+ */
+int parallax_attn_decode_gqa(const void* q, const void* rho, const void* k_cache,
+                             const void* v_cache, const int32_t* seqlens, void* o, int B, int H,
+                             int H_kv, int Lmax, int d, cudaStream_t stream);
+
+/*
+ * Decode against a paged key/value cache (the pages' decode setting keeps a KV
+ * cache; a serving engine keeps it in fixed-size pages), bf16 inputs, fp32 out.
+ *   q, rho            : bf16 [B, H, d]            (rho may be NULL: W_R = 0)
+ *   k_pages, v_pages  : bf16 [num_pages, H_kv, page_size, d]  the page pool
+ *   block_table       : int32 [B, max_pages] on the device; key t of sequence b
+ *                       is row t % page_size of page block_table[b, t / page_size]
+ *   seqlens           : int32 [B] on the device, clamped to [0, max_pages * page_size]
+ *   o                 : fp32 [B, H, d]
+ * page_size must be a multiple of 16; H / H_kv must be 1, 2, 4 or 8.  Only the
+ * table entries of a sequence's first ceil(seqlens[b] / page_size) pages are
+ * read; an entry outside [0, num_pages) is replaced by page 0 and raises
+ * PARALLAX_DEVERR_PAGE_OUT_OF_RANGE (no read leaves the pool).  Workspace and
+ * concurrency rules of parallax_attn_decode.
+ */
+int parallax_attn_decode_paged(const void* q, const void* rho, const void* k_pages,
+                               const void* v_pages, const int32_t* block_table,
+                               const int32_t* seqlens, void* o, int B, int H, int H_kv,
+                               int page_size, int max_pages, int num_pages, int d,
+                               cudaStream_t stream);
+
+/*
  * parallax_attn_decode without any device allocation (bf16 inputs, fp32 o).
  * This entry point has no counterpart in the Parallax paper; it exists for
  * callers that cannot let a library call cudaMalloc -- serving engines that
@@ -121,8 +182,28 @@ int parallax_attn_decode_noalloc(const void* q, const void* rho, const void* k_c
                                  int H, int Lmax, int d, cudaStream_t stream);
 
 /*
+ * The layer's input projections in one tensor-core product: q, k, v and the
+ * probe rho_i = W_R x_i (the probe is a learned linear map of the layer input:
+ * "Parallax mantem softmax ...", zubnet.ai news page, paragraph 2).
+ *   x      : bf16 [B, L, width]                one row per token
+ *   w      : bf16 [n_out * H * d, width]       stacked weight W_q; W_k; W_v; W_R,
+ *                                              rows = output features (n_out = 4,
+ *                                              or 3 when rho == NULL: W_R = 0)
+ *   q, k, v, rho : bf16 [B, H, L, d]           written in full; rho may be NULL
+ *   out[t][b, h, l, c] = sum_a x[b, l, a] * w[t*H*d + h*d + c, a]
+ * fp32 accumulation on the tcgen05 tensor cores, rounded to bf16 (nearest even).
+ * The outputs are exactly the tensors parallax_attn_prefill reads.
+ * Requirements: B, L, H >= 1; d = 64 or 128; H*d a multiple of 128 and width a
+ * multiple of 8 (PARALLAX_ERR_UNSUPPORTED otherwise).  No workspace.
+ */
+int parallax_attn_qkvr_projection(const void* x, const void* w, void* q, void* k, void* v,
+                                  void* rho, int B, int L, int width, int H, int d,
+                                  cudaStream_t stream);
+
+/*
  * Keys per split-KV chunk that parallax_attn_decode{,_f32} would use for this
- * shape (elem_bytes = 2 for bf16, 4 for fp32).  Returns a negative
+ * shape (elem_bytes = 2 for bf16, 4 for fp32); with shared key/value heads
+ * pass H = H_kv.  Returns a negative
  * parallax_status for invalid arguments.  A result >= Lmax means no split.
  */
 int parallax_attn_decode_chunk_keys(int B, int H, int Lmax, int d, int elem_bytes);

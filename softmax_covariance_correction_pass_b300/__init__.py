@@ -26,6 +26,7 @@ PARALLAX_ERR_CUDA = -3
 PARALLAX_ERR_DEVICE = -4
 DEVERR_SEQLEN_CLAMPED = 0x1
 DEVERR_WAIT_TIMEOUT = 0x2
+DEVERR_PAGE_OUT_OF_RANGE = 0x4
 
 _lib = None
 
@@ -51,12 +52,21 @@ def load_library() -> ctypes.CDLL:
     lib.parallax_attn_prefill_f32.argtypes = lib.parallax_attn_prefill.argtypes
     lib.parallax_attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     lib.parallax_attn_decode_f32.argtypes = lib.parallax_attn_decode.argtypes
+    lib.parallax_attn_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                                i32, i32, f32, vp]
+    lib.parallax_attn_decode_gqa.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+    lib.parallax_attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                               i32, i32, i32, vp]
     lib.parallax_attn_decode_chunk_keys.argtypes = [i32, i32, i32, i32, i32]
+    lib.parallax_attn_qkvr_projection.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                  vp]
     lib.parallax_attn_set_decode_chunk_keys.argtypes = [i32]
     lib.parallax_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.parallax_last_error.restype = ctypes.c_char_p
     lib.parallax_check_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
     for name in ("parallax_attn_prefill", "parallax_attn_prefill_f32", "parallax_attn_decode",
+                 "parallax_attn_qkvr_projection", "parallax_attn_decode_gqa",
+                 "parallax_attn_decode_paged", "parallax_attn_prefill_chunk",
                  "parallax_attn_decode_f32", "parallax_attn_decode_chunk_keys",
                  "parallax_attn_set_decode_chunk_keys", "parallax_attn_release_workspace",
                  "parallax_check_device_error", "parallax_version"):
@@ -120,6 +130,34 @@ def parallax_attn_prefill(q, rho, k, v, o=None, causal: bool = True, scale: floa
     return o
 
 
+def parallax_attn_prefill_chunk(q, rho, k_new, v_new, k_cache, v_cache, cache_lens, o=None,
+                                scale: float | None = None, stream=None):
+    """Causal prefill of a chunk that continues cached sequences (bf16).
+
+    q, rho, k_new, v_new [B, H, Lq, d]; caches [B, H, Lmax, d] holding cache_lens[b]
+    tokens (int32 [B] on the device).  Writes the chunk's keys and values into the
+    caches, then returns o (fp32 [B, H, Lq, d]): chunk token i attends to the cached
+    tokens and to chunk tokens 0..i.  cache_lens is not advanced.
+    """
+    B, H, Lq, d = q.shape
+    Lmax = k_cache.shape[2]
+    for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new)) + \
+            ((("rho", rho),) if rho is not None else ()):
+        _need(t, name, torch.bfloat16, (B, H, Lq, d))
+    _need(k_cache, "k_cache", torch.bfloat16, (B, H, Lmax, d))
+    _need(v_cache, "v_cache", torch.bfloat16, (B, H, Lmax, d))
+    _need(cache_lens, "cache_lens", torch.int32, (B,))
+    if o is None:
+        o = torch.empty((B, H, Lq, d), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.float32, (B, H, Lq, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load_library().parallax_attn_prefill_chunk(
+        _ptr(q), _ptr(rho), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(cache_lens), _ptr(o), B, H, Lq, Lmax, d, float(scale), _stream(stream)))
+    return o
+
+
 def parallax_attn_decode(q, rho, k_cache, v_cache, seqlens, o=None, stream=None):
     """Single-token decode; q/rho [B, H, d], caches [B, H, Lmax, d], seqlens int32 [B].
 
@@ -145,6 +183,51 @@ def parallax_attn_decode(q, rho, k_cache, v_cache, seqlens, o=None, stream=None)
     return o
 
 
+def parallax_attn_decode_gqa(q, rho, k_cache, v_cache, seqlens, o=None, stream=None):
+    """Decode with shared key/value heads: q/rho bf16 [B, H, d], caches bf16
+    [B, H_kv, Lmax, d] (H / H_kv in {1, 2, 4, 8}), seqlens int32 [B].  Returns o fp32
+    [B, H, d]; query head h reads key/value head h // (H // H_kv)."""
+    B, Hkv, Lmax, d = k_cache.shape
+    H = q.shape[1]
+    _need(q, "q", torch.bfloat16, (B, H, d))
+    if rho is not None:
+        _need(rho, "rho", torch.bfloat16, (B, H, d))
+    _need(k_cache, "k_cache", torch.bfloat16, (B, Hkv, Lmax, d))
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Hkv, Lmax, d))
+    _need(seqlens, "seqlens", torch.int32, (B,))
+    if o is None:
+        o = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.float32, (B, H, d))
+    _check(load_library().parallax_attn_decode_gqa(
+        _ptr(q), _ptr(rho), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o), B, H, Hkv, Lmax,
+        d, _stream(stream)))
+    return o
+
+
+def parallax_attn_decode_paged(q, rho, k_pages, v_pages, block_table, seqlens, o=None,
+                               stream=None):
+    """Decode against a paged cache: pages bf16 [num_pages, H_kv, page_size, d], block_table
+    int32 [B, max_pages] (key t of sequence b is row t % page_size of page
+    block_table[b, t // page_size]), seqlens int32 [B].  Returns o fp32 [B, H, d]."""
+    num_pages, Hkv, P, d = k_pages.shape
+    B, H = q.shape[0], q.shape[1]
+    max_pages = block_table.shape[1]
+    _need(q, "q", torch.bfloat16, (B, H, d))
+    if rho is not None:
+        _need(rho, "rho", torch.bfloat16, (B, H, d))
+    _need(k_pages, "k_pages", torch.bfloat16, (num_pages, Hkv, P, d))
+    _need(v_pages, "v_pages", torch.bfloat16, (num_pages, Hkv, P, d))
+    _need(block_table, "block_table", torch.int32, (B, max_pages))
+    _need(seqlens, "seqlens", torch.int32, (B,))
+    if o is None:
+        o = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.float32, (B, H, d))
+    _check(load_library().parallax_attn_decode_paged(
+        _ptr(q), _ptr(rho), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens),
+        _ptr(o), B, H, Hkv, P, max_pages, num_pages, d, _stream(stream)))
+    return o
+
+
 def parallax_attn_decode_noalloc(q, rho, k_cache, v_cache, seqlens, o, stream=None):
     """parallax_attn_decode (bf16) with the split-KV partials in the library's fixed
     device array: the call allocates nothing (``o`` must be supplied)."""
@@ -163,6 +246,33 @@ def parallax_attn_decode_noalloc(q, rho, k_cache, v_cache, seqlens, o, stream=No
     _check(fn(_ptr(q), _ptr(rho), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o), B, H,
               Lmax, d, _stream(stream)))
     return o
+
+
+def parallax_attn_qkvr_projection(x, w, H: int, d: int, q=None, k=None, v=None, rho=None,
+                                  with_rho: bool = True, stream=None):
+    """q, k, v and the probe rho = W_R x of a layer in one tensor-core product.
+
+    ``x`` bf16 [B, L, width]; ``w`` bf16 [n_out*H*d, width], the stacked weight
+    W_q; W_k; W_v; W_R (rows = output features), n_out = 4, or 3 with
+    ``with_rho=False`` (W_R = 0: no probe is computed).  Returns
+    ``(q, k, v, rho)`` as bf16 [B, H, L, d] (``rho`` is None without the probe).
+    """
+    B, L, width = x.shape
+    n_out = 4 if with_rho else 3
+    _need(x, "x", torch.bfloat16, (B, L, width))
+    _need(w, "w", torch.bfloat16, (n_out * H * d, width))
+    outs = []
+    for name, t in (("q", q), ("k", k), ("v", v)) + ((("rho", rho),) if with_rho else ()):
+        if t is None:
+            t = torch.empty((B, H, L, d), dtype=torch.bfloat16, device=x.device)
+        _need(t, name, torch.bfloat16, (B, H, L, d))
+        outs.append(t)
+    if not with_rho:
+        outs.append(None)
+    lib = load_library()
+    _check(lib.parallax_attn_qkvr_projection(_ptr(x), _ptr(w), *[_ptr(t) for t in outs], B, L,
+                                             width, H, d, _stream(stream)))
+    return tuple(outs)
 
 
 def parallax_attn_decode_chunk_keys(B: int, H: int, Lmax: int, d: int, elem_bytes: int) -> int:
@@ -199,3 +309,7 @@ def parallax_version() -> int:
 
 prefill = parallax_attn_prefill
 decode = parallax_attn_decode
+qkvr_projection = parallax_attn_qkvr_projection
+decode_gqa = parallax_attn_decode_gqa
+prefill_chunk = parallax_attn_prefill_chunk
+decode_paged = parallax_attn_decode_paged

@@ -99,6 +99,71 @@ def decode_inputs(B, H, d, seqlens, Lmax, seed, rho_std=0.1, device="cpu",
     return DecodeInputs(q, k, v, rho, sl.to(device))
 
 
+def decode_gqa_inputs(B, H, Hkv, d, seqlens, Lmax, seed, rho_std=0.1, device="cpu"):
+    """q, rho [B, H, d]; caches [B, Hkv, Lmax, d] bf16 (draw order q, k, v, rho)."""
+    g = _gen(seed, device)
+    bf = torch.bfloat16
+    q = _randn((B, H, d), g, device, bf)
+    k = _randn((B, Hkv, Lmax, d), g, device, bf)
+    v = _randn((B, Hkv, Lmax, d), g, device, bf)
+    rho = (_randn((B, H, d), g, device, torch.float32) * rho_std).to(bf)
+    sl = torch.as_tensor(seqlens, dtype=torch.int32)
+    if sl.ndim == 0:
+        sl = sl.repeat(B)
+    return DecodeInputs(q, k, v, rho, sl.to(device))
+
+
+def page_cache(k_cache, v_cache, page_size, seed, spare_pages=3):
+    """Cut contiguous caches [B, Hkv, Lmax, d] (Lmax a multiple of page_size) into a shuffled
+    page pool [num_pages, Hkv, page_size, d] plus a block table [B, Lmax // page_size] that
+    maps every sequence's pages back; `spare_pages` unused pages are added to the pool.
+    Pure data movement (the permutation comes from a CPU generator)."""
+    B, Hkv, Lmax, d = k_cache.shape
+    assert Lmax % page_size == 0
+    mp = Lmax // page_size
+    n = B * mp + spare_pages
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(seed))
+    bt = perm[:B * mp].view(B, mp).to(torch.int32)
+
+    def pool(c):
+        pages = c.view(B, Hkv, mp, page_size, d).permute(0, 2, 1, 3, 4).reshape(B * mp, Hkv,
+                                                                                 page_size, d)
+        out = torch.zeros((n, Hkv, page_size, d), dtype=c.dtype, device=c.device)
+        out[perm[:B * mp].to(c.device)] = pages
+        return out
+
+    return pool(k_cache), pool(v_cache), bt.to(k_cache.device)
+
+
+def paged_decode_inputs(B, H, Hkv, d, seqlens, page_size, seed, rho_std=0.1, device="cpu",
+                        spare_pages=3):
+    """A paged cache drawn directly: q, rho [B, H, d]; a pool of exactly the pages the
+    sequences need (plus `spare_pages`) [num_pages, Hkv, page_size, d] ~ N(0,1) bf16; a
+    block table [B, max_pages] giving each sequence distinct pages in shuffled order
+    (entries past a sequence's last page are -1).  Draw order q, k pool, v pool, rho; the
+    shuffle comes from a CPU generator seeded with `seed`.
+    Returns (DecodeInputs with k_cache / v_cache holding the pools, block_table)."""
+    sl = torch.as_tensor(seqlens, dtype=torch.int32)
+    if sl.ndim == 0:
+        sl = sl.repeat(B)
+    npg = [(int(n) + page_size - 1) // page_size for n in sl]
+    max_pages = max(1, max(npg))
+    num_pages = sum(npg) + spare_pages
+    g = _gen(seed, device)
+    bf = torch.bfloat16
+    q = _randn((B, H, d), g, device, bf)
+    k = _randn((num_pages, Hkv, page_size, d), g, device, bf)
+    v = _randn((num_pages, Hkv, page_size, d), g, device, bf)
+    rho = (_randn((B, H, d), g, device, torch.float32) * rho_std).to(bf)
+    perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(seed))
+    bt = torch.full((B, max_pages), -1, dtype=torch.int32)
+    pos = 0
+    for b, n in enumerate(npg):
+        bt[b, :n] = perm[pos:pos + n].to(torch.int32)
+        pos += n
+    return DecodeInputs(q, k, v, rho, sl.to(device)), bt.to(device)
+
+
 def decode_uniform_inputs(device="cuda", B=None, ctx=None) -> DecodeInputs:
     c = DECODE_UNIFORM
     B = B or c["B"]
@@ -143,13 +208,10 @@ def decode_ragged_inputs(device="cuda", B=None, hi=None) -> DecodeInputs:
     return decode_inputs(B, c["H"], c["d"], sl, hi, c["seed"], c["rho_std"], device)
 
 
-def layer_prefill_inputs(device="cuda", B=None, L=None) -> PrefillInputs:
-    """Layer-shaped bf16 prefill: x ~ N(0,1) [B, L, width]; W_q, W_k, W_v ~ N(0, 1/width);
-    W_R ~ N(0, wr_std^2); q, k, v, rho = x W (bf16 matmuls on the device), viewed as
-    [B, L, H, d] and made [B, H, L, d].  Draw order: x, W_q, W_k, W_v, W_R."""
+def _layer_draws(device, B, L):
+    """x ~ N(0,1) [B, L, width]; W_q, W_k, W_v ~ N(0, 1/width), W_R ~ N(0, wr_std^2), each
+    [width, H*d] (bf16).  Draw order: x, W_q, W_k, W_v, W_R."""
     c = LAYER_PREFILL
-    B = B or c["B"]
-    L = L or c["L"]
     H, d, width = c["H"], c["d"], c["width"]
     g = _gen(c["seed"], device)
     bf = torch.bfloat16
@@ -157,9 +219,40 @@ def layer_prefill_inputs(device="cuda", B=None, L=None) -> PrefillInputs:
     ws = [(_randn((width, H * d), g, device, torch.float32) / math.sqrt(width)).to(bf)
           for _ in range(3)]
     wr = (_randn((width, H * d), g, device, torch.float32) * c["wr_std"]).to(bf)
+    return x, ws + [wr]
+
+
+def layer_prefill_inputs(device="cuda", B=None, L=None) -> PrefillInputs:
+    """Layer-shaped bf16 prefill: x ~ N(0,1) [B, L, width]; W_q, W_k, W_v ~ N(0, 1/width);
+    W_R ~ N(0, wr_std^2); q, k, v, rho = x W (bf16 matmuls on the device), viewed as
+    [B, L, H, d] and made [B, H, L, d].  Draw order: x, W_q, W_k, W_v, W_R."""
+    c = LAYER_PREFILL
+    B = B or c["B"]
+    L = L or c["L"]
+    H, d = c["H"], c["d"]
+    x, ws = _layer_draws(device, B, L)
 
     def proj(w):
         return (x @ w).view(B, L, H, d).permute(0, 2, 1, 3).contiguous()
 
-    q, k, v, rho = proj(ws[0]), proj(ws[1]), proj(ws[2]), proj(wr)
+    q, k, v, rho = (proj(w) for w in ws)
     return PrefillInputs(q, k, v, rho, 1.0 / math.sqrt(d))
+
+
+def layer_projection_inputs(device="cuda", B=None, L=None):
+    """The same draws as layer_prefill_inputs, as the projection's inputs: x [B, L, width]
+    and the stacked weight [W_q; W_k; W_v; W_R] of shape [4*H*d, width] (rows = output
+    features), both bf16."""
+    c = LAYER_PREFILL
+    x, ws = _layer_draws(device, B or c["B"], L or c["L"])
+    return x, torch.cat([w.t() for w in ws], dim=0).contiguous()
+
+
+def projection_inputs(B, L, width, H, d, n_out, seed, device="cpu"):
+    """x ~ N(0,1) [B, L, width] and a stacked weight ~ N(0, 1/width) [n_out*H*d, width],
+    bf16, for projection tests at arbitrary shapes (draw order x, w)."""
+    g = _gen(seed, device)
+    x = _randn((B, L, width), g, device, torch.bfloat16)
+    w = (_randn((n_out * H * d, width), g, device, torch.float32) / math.sqrt(width)).to(
+        torch.bfloat16)
+    return x, w

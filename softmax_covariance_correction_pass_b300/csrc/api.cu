@@ -117,27 +117,33 @@ int prefill_common(const void* q, const void* rho, const void* k, const void* v,
     return succeed();
 }
 
-int decode_common(const void* q, const void* rho, const void* kc, const void* vc,
-                  const int32_t* seqlens, void* o, int B, int H, int Lmax, int d,
-                  cudaStream_t stream, bool bf16) {
-    int rc = validate_common(q, kc, vc, o, rho, B, H, Lmax, d, "Lmax");
-    if (rc != PARALLAX_OK) return rc;
-    if (!seqlens) return fail(PARALLAX_ERR_INVALID, "null seqlens pointer");
-    int dev = 0;
-    DeviceState* ds = device_state(&dev);
-    if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
-
+// The split plan shared by every decode entry point.  Work items are (key/value
+// head, chunk); a paged cache caps the chunk so that an item's page ids fit the
+// kernel's per-item table.
+parallax::DecodePlan make_plan(int B, int H, int Hkv, int Lmax, int d, int num_sms,
+                               int page_size = 0, int max_pages = 0, int num_pages = 0) {
     parallax::DecodePlan plan;
     plan.B = B;
     plan.H = H;
+    plan.Hkv = Hkv;
     plan.Lmax = Lmax;
     plan.d = d;
+    plan.page_size = page_size;
+    plan.max_pages = max_pages;
+    plan.num_pages = num_pages;
     plan.scale = 1.0f / std::sqrt((float)d);
-    plan.chunk = plan_chunk(B, H, Lmax, ds->num_sms);
+    plan.chunk = plan_chunk(B, Hkv, Lmax, num_sms);
+    if (page_size > 0 && plan.chunk > parallax::decode_paged_max_chunk(page_size)) plan.chunk = 4096;
     plan.nsplit = (Lmax + plan.chunk - 1) / plan.chunk;
-    const long long items = (long long)B * H * plan.nsplit;
-    plan.grid = (int)std::min<long long>(items, (long long)ds->num_sms);
+    const long long items = (long long)B * Hkv * plan.nsplit;
+    plan.grid = (int)std::min<long long>(items, (long long)num_sms);
+    return plan;
+}
 
+int decode_run(const parallax::DecodePlan& plan, int dev, DeviceState* ds, const void* q,
+               const void* rho, const void* kc, const void* vc, const int32_t* seqlens, void* o,
+               cudaStream_t stream, bool bf16, const int32_t* block_table) {
+    (void)ds;
     const size_t need = parallax::decode_workspace_bytes(plan);
     void* ws = nullptr;
     if (need > 0) {
@@ -160,9 +166,36 @@ int decode_common(const void* q, const void* rho, const void* kc, const void* vc
         ws = s.ws;
     }
     cudaError_t e = parallax::decode_launch(plan, bf16, q, rho, kc, vc, seqlens,
-                                            static_cast<float*>(o), ws, stream);
+                                            static_cast<float*>(o), ws, stream, block_table);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return succeed();
+}
+
+int validate_groups(int H, int Hkv) {
+    if (Hkv <= 0 || H % Hkv != 0)
+        return fail(PARALLAX_ERR_INVALID, "H=%d must be a positive multiple of H_kv=%d", H, Hkv);
+    const int G = H / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(PARALLAX_ERR_UNSUPPORTED, "query heads per key/value head %d (supported: "
+                    "1, 2, 4, 8)", G);
+    return PARALLAX_OK;
+}
+
+int decode_common(const void* q, const void* rho, const void* kc, const void* vc,
+                  const int32_t* seqlens, void* o, int B, int H, int Hkv, int Lmax, int d,
+                  cudaStream_t stream, bool bf16) {
+    int rc = validate_common(q, kc, vc, o, rho, B, H, Lmax, d, "Lmax");
+    if (rc != PARALLAX_OK) return rc;
+    if (!seqlens) return fail(PARALLAX_ERR_INVALID, "null seqlens pointer");
+    rc = validate_groups(H, Hkv);
+    if (rc != PARALLAX_OK) return rc;
+    if (!bf16 && Hkv != H)
+        return fail(PARALLAX_ERR_UNSUPPORTED, "shared key/value heads need bf16 inputs");
+    int dev = 0;
+    DeviceState* ds = device_state(&dev);
+    if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
+    const parallax::DecodePlan plan = make_plan(B, H, Hkv, Lmax, d, ds->num_sms);
+    return decode_run(plan, dev, ds, q, rho, kc, vc, seqlens, o, stream, bf16, nullptr);
 }
 
 }  // namespace
@@ -184,13 +217,49 @@ int parallax_attn_prefill_f32(const void* q, const void* rho, const void* k, con
 int parallax_attn_decode(const void* q, const void* rho, const void* k_cache,
                          const void* v_cache, const int32_t* seqlens, void* o, int B, int H,
                          int Lmax, int d, cudaStream_t stream) {
-    return decode_common(q, rho, k_cache, v_cache, seqlens, o, B, H, Lmax, d, stream, true);
+    return decode_common(q, rho, k_cache, v_cache, seqlens, o, B, H, H, Lmax, d, stream, true);
 }
 
 int parallax_attn_decode_f32(const void* q, const void* rho, const void* k_cache,
                              const void* v_cache, const int32_t* seqlens, void* o, int B, int H,
                              int Lmax, int d, cudaStream_t stream) {
-    return decode_common(q, rho, k_cache, v_cache, seqlens, o, B, H, Lmax, d, stream, false);
+    return decode_common(q, rho, k_cache, v_cache, seqlens, o, B, H, H, Lmax, d, stream, false);
+}
+
+int parallax_attn_decode_gqa(const void* q, const void* rho, const void* k_cache,
+                             const void* v_cache, const int32_t* seqlens, void* o, int B, int H,
+                             int H_kv, int Lmax, int d, cudaStream_t stream) {
+    return decode_common(q, rho, k_cache, v_cache, seqlens, o, B, H, H_kv, Lmax, d, stream, true);
+}
+
+int parallax_attn_decode_paged(const void* q, const void* rho, const void* k_pages,
+                               const void* v_pages, const int32_t* block_table,
+                               const int32_t* seqlens, void* o, int B, int H, int H_kv,
+                               int page_size, int max_pages, int num_pages, int d,
+                               cudaStream_t stream) {
+    if (!block_table) return fail(PARALLAX_ERR_INVALID, "null block_table pointer");
+    if (page_size <= 0 || max_pages <= 0 || num_pages <= 0)
+        return fail(PARALLAX_ERR_INVALID, "page_size=%d, max_pages=%d, num_pages=%d must all be "
+                    ">= 1", page_size, max_pages, num_pages);
+    if (page_size % 16 != 0)
+        return fail(PARALLAX_ERR_UNSUPPORTED, "page_size=%d must be a multiple of 16", page_size);
+    if ((long long)page_size * max_pages > 2147483647LL)
+        return fail(PARALLAX_ERR_INVALID, "max_pages * page_size exceeds the int range");
+    const int Lmax = page_size * max_pages;
+    int rc = validate_common(q, k_pages, v_pages, o, rho, B, H, Lmax, d, "Lmax");
+    if (rc != PARALLAX_OK) return rc;
+    if (!seqlens) return fail(PARALLAX_ERR_INVALID, "null seqlens pointer");
+    rc = validate_groups(H, H_kv);
+    if (rc != PARALLAX_OK) return rc;
+    if ((double)num_pages * H_kv * page_size * d > 9.0e15)
+        return fail(PARALLAX_ERR_INVALID, "page pool too large");
+    int dev = 0;
+    DeviceState* ds = device_state(&dev);
+    if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
+    const parallax::DecodePlan plan =
+        make_plan(B, H, H_kv, Lmax, d, ds->num_sms, page_size, max_pages, num_pages);
+    return decode_run(plan, dev, ds, q, rho, k_pages, v_pages, seqlens, o, stream, true,
+                      block_table);
 }
 
 int parallax_attn_decode_noalloc(const void* q, const void* rho, const void* k_cache,
@@ -202,15 +271,7 @@ int parallax_attn_decode_noalloc(const void* q, const void* rho, const void* k_c
     DeviceState* ds = device_state(nullptr);
     if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
     // the same split plan as parallax_attn_decode, so both give the same result
-    parallax::DecodePlan plan;
-    plan.B = B;
-    plan.H = H;
-    plan.Lmax = Lmax;
-    plan.d = d;
-    plan.scale = 1.0f / std::sqrt((float)d);
-    plan.chunk = plan_chunk(B, H, Lmax, ds->num_sms);
-    plan.nsplit = (Lmax + plan.chunk - 1) / plan.chunk;
-    plan.grid = (int)std::min<long long>((long long)B * H * plan.nsplit, (long long)ds->num_sms);
+    const parallax::DecodePlan plan = make_plan(B, H, H, Lmax, d, ds->num_sms);
     const size_t need = parallax::decode_workspace_bytes(plan);
     const size_t cap = parallax::decode_noalloc_capacity();
     if (need > cap)
@@ -222,6 +283,62 @@ int parallax_attn_decode_noalloc(const void* q, const void* rho, const void* k_c
     cudaError_t e = parallax::decode_launch_noalloc(plan, true, q, rho, k_cache, v_cache,
                                                     seqlens, static_cast<float*>(o), stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode (no-allocation) launch");
+    return succeed();
+}
+
+int parallax_attn_prefill_chunk(const void* q, const void* rho, const void* k_new,
+                                const void* v_new, void* k_cache, void* v_cache,
+                                const int32_t* cache_lens, void* o, int B, int H, int Lq,
+                                int Lmax, int d, float scale, cudaStream_t stream) {
+    int rc = validate_common(q, k_new, v_new, o, rho, B, H, Lq, d, "Lq");
+    if (rc != PARALLAX_OK) return rc;
+    if (!k_cache || !v_cache || !cache_lens)
+        return fail(PARALLAX_ERR_INVALID, "null cache pointer (k_cache=%p v_cache=%p "
+                    "cache_lens=%p)", k_cache, v_cache, (const void*)cache_lens);
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PARALLAX_ERR_INVALID, "every tensor pointer must be 16-byte aligned");
+    if (Lmax < Lq) return fail(PARALLAX_ERR_INVALID, "Lmax=%d is smaller than the chunk Lq=%d",
+                               Lmax, Lq);
+    if ((double)B * H * Lmax * d > 9.0e15 || (double)Lmax * d > 2147483647.0)
+        return fail(PARALLAX_ERR_INVALID, "cache too large");
+    if (!std::isfinite(scale)) return fail(PARALLAX_ERR_INVALID, "scale must be finite");
+    DeviceState* ds = device_state(nullptr);
+    if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
+    parallax::PrefillShape s{B, H, Lq, d, 1, scale};
+    cudaError_t e = parallax::prefill_tc_chunk_launch(s, q, rho, k_new, v_new, k_cache, v_cache,
+                                                      cache_lens, Lmax, static_cast<float*>(o),
+                                                      ds->num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "chunked prefill launch");
+    return succeed();
+}
+
+int parallax_attn_qkvr_projection(const void* x, const void* w, void* q, void* k, void* v,
+                                  void* rho, int B, int L, int width, int H, int d,
+                                  cudaStream_t stream) {
+    if (!x || !w || !q || !k || !v)
+        return fail(PARALLAX_ERR_INVALID, "null tensor pointer (x=%p w=%p q=%p k=%p v=%p)", x, w,
+                    q, k, v);
+    if (B <= 0 || L <= 0 || width <= 0 || H <= 0)
+        return fail(PARALLAX_ERR_INVALID, "B=%d, L=%d, width=%d, H=%d must all be >= 1", B, L,
+                    width, H);
+    if (d != 64 && d != 128)
+        return fail(PARALLAX_ERR_UNSUPPORTED, "head dimension d=%d (supported: 64, 128)", d);
+    if ((H * d) % 128 != 0)
+        return fail(PARALLAX_ERR_UNSUPPORTED, "H*d=%d must be a multiple of 128", H * d);
+    if (width % 8 != 0)
+        return fail(PARALLAX_ERR_UNSUPPORTED, "width=%d must be a multiple of 8", width);
+    if (!aligned16(x) || !aligned16(w) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(rho))
+        return fail(PARALLAX_ERR_INVALID, "every tensor pointer must be 16-byte aligned");
+    if ((double)B * L * width > 9.0e15 || (double)B * H * L * d > 9.0e15 ||
+        (double)B * H > 2147483647.0 || (double)L * width > 9.0e15)
+        return fail(PARALLAX_ERR_INVALID, "tensor too large");
+    DeviceState* ds = device_state(nullptr);
+    if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
+    parallax::ProjShape s{B, L, width, H, d, rho ? 4 : 3};
+    void* const out[4] = {q, k, v, rho};
+    cudaError_t e = parallax::proj_tc_launch(s, x, w, out, ds->num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
     return succeed();
 }
 
@@ -272,7 +389,7 @@ int parallax_check_device_error(cudaStream_t stream, unsigned int* bits) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     const unsigned v = parallax::decode_take_error() | parallax::prefill_simt_take_error() |
-                       parallax::prefill_tc_take_error();
+                       parallax::prefill_tc_take_error() | parallax::proj_tc_take_error();
     if (bits) *bits = v;
     if (v) return fail(PARALLAX_ERR_DEVICE, "device error word 0x%x", v);
     return succeed();

@@ -1,16 +1,20 @@
 // Parallax split-KV decode (one query token per sequence and head).
 //
-// Kernel 1 (decode_kernel): a persistent CTA walks work items (head, key
-// chunk).  One producer warp streams the chunk's K and V rows -- contiguous
-// in the [B, H, Lmax, d] cache -- into a ring of shared-memory stages with
-// bulk asynchronous copies (cp.async.bulk, completion on mbarriers, L2
-// evict-first), eight consumer warps each take an eighth of every stage and
-// update the online state of BOTH Parallax branches from the same bytes
+// Kernel 1 (decode_kernel): a persistent CTA walks work items (key/value
+// head, key chunk).  One producer warp streams the chunk's K and V rows --
+// contiguous in the [B, H_kv, Lmax, d] cache, or looked up page by page
+// through a block table in a paged cache [num_pages, H_kv, page_size, d] --
+// into a ring of shared-memory stages with bulk asynchronous copies
+// (cp.async.bulk, completion on mbarriers, L2 evict-first).  Eight consumer
+// warps update the online state of BOTH Parallax branches from the same bytes
 // (Parallax, "Parallax mantem softmax ...", paragraph 2: one KV stream feeds
-// the softmax and the covariance branch).  At the end of an item the warps'
-// states are merged in shared memory; the result is either the finished
-// output (a single chunk per head) or a partial state (m, l, A, U, W) in the
-// workspace.
+// the softmax and the covariance branch).  With G query heads per key/value
+// head (grouped-query attention), the warps are split into G teams of 8/G
+// warps; team g serves query head g of the group and each of its warps takes
+// a 1/(8/G) share of every stage, so each K/V byte leaves HBM once for all G
+// heads.  At the end of an item each team's warps merge their states in
+// shared memory; the result is either the finished output (a single chunk per
+// head) or a partial state (m, l, A, U, W) in the workspace.
 // Kernel 2 (combine_kernel): per head, rescales the partial states to a common
 // maximum (log-sum-exp), sums them and finishes o = U/l - (W/l - (A/l)(U/l)).
 #include <mutex>
@@ -28,16 +32,21 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 4;
 constexpr int kStageRowBytes = 16384;  // bytes of K (and of V) per stage
 
-template <typename T, int D>
+constexpr int kMaxPageIds = 288;  // page ids of one work item held in shared memory
+
+template <typename T, int D, int G = 1>
 struct DecodeShape {
     using KL = KeyLayout<T, D>;
     static constexpr int STAGE_KEYS = kStageRowBytes / KL::ROW_BYTES;
-    static constexpr int KEYS_PER_WARP = STAGE_KEYS / kConsumerWarps;
+    static constexpr int WARPS_PER_HEAD = kConsumerWarps / G;
+    static constexpr int KEYS_PER_WARP = STAGE_KEYS / WARPS_PER_HEAD;
     static constexpr int BLOCKS_PER_WARP = KEYS_PER_WARP / KL::BLOCK_KEYS;
+    static_assert(kConsumerWarps % G == 0, "group size must divide the consumer warps");
     static_assert(BLOCKS_PER_WARP >= 1 && KEYS_PER_WARP % KL::BLOCK_KEYS == 0, "stage shape");
     static constexpr int MERGE_FLOATS = kConsumerWarps * (4 + 2 * D);
-    static constexpr size_t SMEM_BYTES =
-        (size_t)kStages * 2 * kStageRowBytes + MERGE_FLOATS * sizeof(float) + 2 * kStages * 8 + 16;
+    static constexpr size_t SMEM_BYTES = (size_t)kStages * 2 * kStageRowBytes +
+                                         MERGE_FLOATS * sizeof(float) + 2 * kStages * 8 + 16 +
+                                         kMaxPageIds * sizeof(int);
 };
 
 struct DecodeArgs {
@@ -49,7 +58,9 @@ struct DecodeArgs {
     float* o;
     float4* ws_stats;  // [B*H][nsplit]   (m, l, A, -)
     float* ws_uw;      // [B*H][nsplit][2][D]
-    int B, H, Lmax, chunk, nsplit;
+    const int32_t* block_table;  // paged cache: [B][max_pages] page ids
+    int B, H, Hkv, Lmax, chunk, nsplit;
+    int page_size, max_pages, num_pages;  // paged cache only
     float qscale;  // softmax scale * log2(e)
 };
 
@@ -62,23 +73,33 @@ __device__ __forceinline__ int clamp_seqlen(const int32_t* seqlens, int b, int L
     return n;
 }
 
-// Item (head bh, chunk ch) -> key range [start, end); returns false if the item is empty
-// and produces nothing.  Without split every head has exactly one item (it may be
-// empty: a zero-length sequence still writes o = 0).
+// Item (key/value head bh, chunk ch) -> key range [start, end); returns false if the item
+// is empty and produces nothing.  Without split every head has exactly one item (it may
+// be empty: a zero-length sequence still writes o = 0).
 __device__ __forceinline__ bool item_range(const DecodeArgs& a, int slot, int BH, int& bh,
                                            int& ch, int& start, int& end, bool split) {
     ch = slot / BH;
     bh = slot - ch * BH;
-    const int n = clamp_seqlen(a.seqlens, bh / a.H, a.Lmax);
+    const int n = clamp_seqlen(a.seqlens, bh / a.Hkv, a.Lmax);
     start = ch * a.chunk;
     end = min(start + a.chunk, n);
     return split ? start < n : true;
 }
 
-template <typename T, int D, bool RHO, bool SPLIT>
+// A page id from the block table; an id outside [0, num_pages) is replaced by
+// page 0 (so that no copy leaves the pool) and flagged.
+__device__ __forceinline__ int checked_page(const DecodeArgs& a, int id) {
+    if (id < 0 || id >= a.num_pages) {
+        raise_error(&g_decode_err, PARALLAX_DEVERR_PAGE_OUT_OF_RANGE);
+        return 0;
+    }
+    return id;
+}
+
+template <typename T, int D, bool RHO, bool SPLIT, int G, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
     using KL = KeyLayout<T, D>;
-    using SH = DecodeShape<T, D>;
+    using SH = DecodeShape<T, D, G>;
     constexpr int VEC = KL::VEC;
     extern __shared__ __align__(1024) unsigned char smem[];
     T* stage_k = reinterpret_cast<T*>(smem);                               // [kStages][STAGE_KEYS][D]
@@ -87,10 +108,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     uint64_t* full = reinterpret_cast<uint64_t*>(merge + SH::MERGE_FLOATS);
     uint64_t* empty = full + kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+    int* page_ids = const_cast<int*>(abort_flag) + 4;  // [kMaxPageIds], producer only
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int BH = a.B * a.H;
-    const int total = BH * a.nsplit;
+    const int BHkv = a.B * a.Hkv;
+    const int total = BHkv * a.nsplit;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -105,31 +127,64 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        if (lane != 0) return;
+        // Lane 0 issues every copy; with a paged cache the whole warp first
+        // loads the item's page ids into shared memory.
+        if (!PAGED && lane != 0) return;
         const uint64_t pol = l2_evict_first_policy();
         uint32_t it = 0;
         bool ok = true;
         for (int slot = blockIdx.x; slot < total && ok; slot += gridDim.x) {
             int bh, ch, start, end;
-            if (!item_range(a, slot, BH, bh, ch, start, end, SPLIT)) continue;
-            const size_t head = (size_t)bh * a.Lmax;
-            for (int t0 = start; t0 < end; t0 += SH::STAGE_KEYS, ++it) {
-                const int s = it % kStages;
-                if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, &g_decode_err)) {
-                    *abort_flag = 1;
-                    ok = false;
-                    break;
-                }
-                const int nk = min(SH::STAGE_KEYS, end - t0);
-                const uint32_t bytes = (uint32_t)nk * KL::ROW_BYTES;
-                mbar_arrive_expect_tx(&full[s], 2 * bytes);
-                bulk_copy_g2s(stage_k + (size_t)s * SH::STAGE_KEYS * D,
-                              static_cast<const T*>(a.kc) + (head + t0) * D, bytes, &full[s], pol);
-                bulk_copy_g2s(stage_v + (size_t)s * SH::STAGE_KEYS * D,
-                              static_cast<const T*>(a.vc) + (head + t0) * D, bytes, &full[s], pol);
+            if (!item_range(a, slot, BHkv, bh, ch, start, end, SPLIT)) continue;
+            int p0 = 0, b = 0, hk = 0;
+            if (PAGED) {
+                b = bh / a.Hkv;
+                hk = bh - b * a.Hkv;
+                p0 = start / a.page_size;
+                const int np = end > start ? (end - 1) / a.page_size - p0 + 1 : 0;
+                for (int i = lane; i < np; i += 32)
+                    page_ids[i] = checked_page(a, a.block_table[(size_t)b * a.max_pages + p0 + i]);
+                __syncwarp();
             }
+            if (lane == 0) {
+                const size_t head = (size_t)bh * a.Lmax;
+                for (int t0 = start; t0 < end; t0 += SH::STAGE_KEYS, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, &g_decode_err)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    const int nk = min(SH::STAGE_KEYS, end - t0);
+                    mbar_arrive_expect_tx(&full[s], 2u * (uint32_t)nk * KL::ROW_BYTES);
+                    T* dk = stage_k + (size_t)s * SH::STAGE_KEYS * D;
+                    T* dv = stage_v + (size_t)s * SH::STAGE_KEYS * D;
+                    if (!PAGED) {
+                        const uint32_t bytes = (uint32_t)nk * KL::ROW_BYTES;
+                        bulk_copy_g2s(dk, static_cast<const T*>(a.kc) + (head + t0) * D, bytes,
+                                      &full[s], pol);
+                        bulk_copy_g2s(dv, static_cast<const T*>(a.vc) + (head + t0) * D, bytes,
+                                      &full[s], pol);
+                    } else {
+                        // one copy per page the stage touches
+                        for (int t = t0; t < t0 + nk;) {
+                            const int pg = t / a.page_size, row = t - pg * a.page_size;
+                            const int seg = min(a.page_size - row, t0 + nk - t);
+                            const size_t src =
+                                (((size_t)page_ids[pg - p0] * a.Hkv + hk) * a.page_size + row) * D;
+                            const uint32_t bytes = (uint32_t)seg * KL::ROW_BYTES;
+                            bulk_copy_g2s(dk + (size_t)(t - t0) * D,
+                                          static_cast<const T*>(a.kc) + src, bytes, &full[s], pol);
+                            bulk_copy_g2s(dv + (size_t)(t - t0) * D,
+                                          static_cast<const T*>(a.vc) + src, bytes, &full[s], pol);
+                            t += seg;
+                        }
+                    }
+                }
+            }
+            if (PAGED) ok = __shfl_sync(kFullMask, ok, 0) != 0;  // also orders page_ids reuse
         }
-        if (!ok) {
+        if (!ok && lane == 0) {
             // drain the copies still in flight into this CTA's shared memory
             for (uint32_t k = (it >= kStages ? it - kStages : 0); k < it; ++k)
                 mbar_wait(&full[k % kStages], (k / kStages) & 1, &g_decode_err);
@@ -138,14 +193,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     }
 
     // ---------------------------------------------------------------- consumers
+    // warp -> (query head of the group, share of every stage)
+    const int hg = warp / SH::WARPS_PER_HEAD, share = warp - hg * SH::WARPS_PER_HEAD;
     const int g = lane / KL::LPK, e = lane % KL::LPK;
     uint32_t it = 0;
     for (int slot = blockIdx.x; slot < total; slot += gridDim.x) {
         int bh, ch, start, end;
-        if (!item_range(a, slot, BH, bh, ch, start, end, SPLIT)) continue;
+        if (!item_range(a, slot, BHkv, bh, ch, start, end, SPLIT)) continue;
+        const int bhq = bh * G + hg;  // this warp's query head
         float qf[VEC], rf[VEC];
-        load_row_slice<T, D>(static_cast<const T*>(a.q) + (size_t)bh * D, e, a.qscale, qf);
-        if (RHO) load_row_slice<T, D>(static_cast<const T*>(a.rho) + (size_t)bh * D, e, 1.f, rf);
+        load_row_slice<T, D>(static_cast<const T*>(a.q) + (size_t)bhq * D, e, a.qscale, qf);
+        if (RHO) load_row_slice<T, D>(static_cast<const T*>(a.rho) + (size_t)bhq * D, e, 1.f, rf);
         else
 #pragma unroll
             for (int x = 0; x < VEC; ++x) rf[x] = 0.f;
@@ -165,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             const T* sV = stage_v + (size_t)s * SH::STAGE_KEYS * D;
 #pragma unroll
             for (int blk = 0; blk < SH::BLOCKS_PER_WARP; ++blk) {
-                const int kb = warp * SH::KEYS_PER_WARP + blk * KL::BLOCK_KEYS;
+                const int kb = share * SH::KEYS_PER_WARP + blk * KL::BLOCK_KEYS;
                 if (kb < nk) warp_block<T, D, RHO>(st, qf, rf, sK, sV, kb, nk, lane);
             }
             __syncwarp();
@@ -176,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
         // is written.
         warp_merge_groups<T, D, RHO>(st);
 
-        // ---- merge the consumer warps' states
+        // ---- merge the states of each query head's warps
         float* mw = merge + warp * (4 + 2 * D);
         if (lane == 0) {
             mw[0] = st.m;
@@ -191,32 +249,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             }
         }
         named_bar_sync(1, kConsumerWarps * 32);
-        const int c = threadIdx.x;
-        if (c < D && ok && !*abort_flag) {
-            float M = -INFINITY;
+        if (ok && !*abort_flag) {
+            for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
+                const int h2 = idx / D, c = idx - h2 * D;
+                const float* m0 = merge + h2 * SH::WARPS_PER_HEAD * (4 + 2 * D);
+                float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge[w * (4 + 2 * D)]);
-            float l = 0.f, A = 0.f, U = 0.f, W = 0.f;
-            if (M > -INFINITY) {
+                for (int w = 0; w < SH::WARPS_PER_HEAD; ++w) M = fmaxf(M, m0[w * (4 + 2 * D)]);
+                float l = 0.f, A = 0.f, U = 0.f, W = 0.f;
+                if (M > -INFINITY) {
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float* m2 = merge + w * (4 + 2 * D);
-                    const float f = fast_exp2(m2[0] - M);
-                    l = fmaf(f, m2[1], l);
-                    A = fmaf(f, m2[2], A);
-                    U = fmaf(f, m2[4 + c], U);
-                    W = fmaf(f, m2[4 + D + c], W);
+                    for (int w = 0; w < SH::WARPS_PER_HEAD; ++w) {
+                        const float* m2 = m0 + w * (4 + 2 * D);
+                        const float f = fast_exp2(m2[0] - M);
+                        l = fmaf(f, m2[1], l);
+                        A = fmaf(f, m2[2], A);
+                        U = fmaf(f, m2[4 + c], U);
+                        W = fmaf(f, m2[4 + D + c], W);
+                    }
                 }
-            }
-            if (SPLIT) {
-                const size_t idx = (size_t)bh * a.nsplit + ch;
-                a.ws_uw[idx * 2 * D + c] = U;
-                a.ws_uw[idx * 2 * D + D + c] = W;
-                if (c == 0) a.ws_stats[idx] = make_float4(M, l, A, 0.f);
-            } else {
-                const float inv_l = l > 0.f ? 1.f / l : 0.f;
-                const float mu = U * inv_l;
-                a.o[(size_t)bh * D + c] = RHO ? mu - (W * inv_l - (A * inv_l) * mu) : mu;
+                const int bq = bh * G + h2;
+                if (SPLIT) {
+                    const size_t idx2 = (size_t)bq * a.nsplit + ch;
+                    a.ws_uw[idx2 * 2 * D + c] = U;
+                    a.ws_uw[idx2 * 2 * D + D + c] = W;
+                    if (c == 0) a.ws_stats[idx2] = make_float4(M, l, A, 0.f);
+                } else {
+                    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+                    const float mu = U * inv_l;
+                    a.o[(size_t)bq * D + c] = RHO ? mu - (W * inv_l - (A * inv_l) * mu) : mu;
+                }
             }
         }
         named_bar_sync(1, kConsumerWarps * 32);
@@ -246,10 +308,10 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a) {
     a.o[(size_t)bh * D + c] = RHO ? mu - (W * inv_l - (A * inv_l) * mu) : mu;
 }
 
-template <typename T, int D, bool RHO, bool SPLIT>
+template <typename T, int D, bool RHO, bool SPLIT, int G, bool PAGED>
 cudaError_t launch_decode_kernel(const DecodeArgs& a, int grid, cudaStream_t stream) {
-    using SH = DecodeShape<T, D>;
-    auto kern = decode_kernel<T, D, RHO, SPLIT>;
+    using SH = DecodeShape<T, D, G>;
+    auto kern = decode_kernel<T, D, RHO, SPLIT, G, PAGED>;
     static bool configured = false;  // per process; the attribute is per function
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -261,10 +323,10 @@ cudaError_t launch_decode_kernel(const DecodeArgs& a, int grid, cudaStream_t str
     return cudaGetLastError();
 }
 
-template <typename T, int D, bool RHO>
+template <typename T, int D, bool RHO, int G, bool PAGED>
 cudaError_t run_decode(const DecodePlan& plan, const void* q, const void* rho, const void* kc,
                        const void* vc, const int32_t* seqlens, float* o, void* ws,
-                       cudaStream_t stream) {
+                       const int32_t* block_table, cudaStream_t stream) {
     DecodeArgs a;
     a.q = q;
     a.rho = rho;
@@ -272,25 +334,57 @@ cudaError_t run_decode(const DecodePlan& plan, const void* q, const void* rho, c
     a.vc = vc;
     a.seqlens = seqlens;
     a.o = o;
+    a.block_table = block_table;
     a.B = plan.B;
     a.H = plan.H;
+    a.Hkv = plan.Hkv;
     a.Lmax = plan.Lmax;
     a.chunk = plan.chunk;
     a.nsplit = plan.nsplit;
+    a.page_size = plan.page_size;
+    a.max_pages = plan.max_pages;
+    a.num_pages = plan.num_pages;
     a.qscale = plan.scale * kLog2e;
     const size_t BH = (size_t)plan.B * plan.H;
     a.ws_stats = static_cast<float4*>(ws);
     a.ws_uw = reinterpret_cast<float*>(static_cast<char*>(ws) + BH * plan.nsplit * sizeof(float4));
     cudaError_t e;
     if (plan.nsplit > 1) {
-        e = launch_decode_kernel<T, D, RHO, true>(a, plan.grid, stream);
+        e = launch_decode_kernel<T, D, RHO, true, G, PAGED>(a, plan.grid, stream);
         if (e != cudaSuccess) return e;
         combine_kernel<D, RHO><<<(unsigned)BH, D, 0, stream>>>(a);
     } else {
-        e = launch_decode_kernel<T, D, RHO, false>(a, plan.grid, stream);
+        e = launch_decode_kernel<T, D, RHO, false, G, PAGED>(a, plan.grid, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
+}
+
+// bf16: every group size and both cache layouts; fp32: plain attention only.
+template <typename T, int D, bool RHO>
+cudaError_t run_decode_any(const DecodePlan& plan, const void* q, const void* rho, const void* kc,
+                           const void* vc, const int32_t* seqlens, float* o, void* ws,
+                           const int32_t* block_table, cudaStream_t stream) {
+    const int G = plan.H / plan.Hkv;
+    const bool paged = plan.page_size > 0;
+    if constexpr (sizeof(T) == 2) {
+#define PARALLAX_DECODE_G(GG)                                                                     \
+    if (G == GG)                                                                                  \
+        return paged ? run_decode<T, D, RHO, GG, true>(plan, q, rho, kc, vc, seqlens, o, ws,      \
+                                                       block_table, stream)                       \
+                     : run_decode<T, D, RHO, GG, false>(plan, q, rho, kc, vc, seqlens, o, ws,     \
+                                                        block_table, stream);
+        PARALLAX_DECODE_G(1)
+        PARALLAX_DECODE_G(2)
+        PARALLAX_DECODE_G(4)
+        PARALLAX_DECODE_G(8)
+#undef PARALLAX_DECODE_G
+        return cudaErrorInvalidValue;
+    } else {
+        if (G != 1 || paged) return cudaErrorInvalidValue;
+        return run_decode<T, D, RHO, 1, false>(plan, q, rho, kc, vc, seqlens, o, ws, block_table,
+                                               stream);
+    }
 }
 
 }  // namespace
@@ -305,14 +399,21 @@ int decode_stage_keys(int d, int elem_bytes) { return kStageRowBytes / (d * elem
 
 int decode_threads() { return kThreads; }
 
+int decode_paged_max_chunk(int page_size) { return (kMaxPageIds - 1) * page_size; }
+
 cudaError_t decode_launch(const DecodePlan& plan, bool bf16, const void* q, const void* rho,
                           const void* kc, const void* vc, const int32_t* seqlens, float* o,
-                          void* ws, cudaStream_t stream) {
+                          void* ws, cudaStream_t stream, const int32_t* block_table) {
     const bool r = rho != nullptr;
+    if (plan.Hkv <= 0 || plan.H % plan.Hkv != 0) return cudaErrorInvalidValue;
+    if (plan.page_size > 0 && (!block_table || plan.chunk > decode_paged_max_chunk(plan.page_size)))
+        return cudaErrorInvalidValue;
 #define PARALLAX_DECODE_CASE(T, DD)                                                              \
     if (plan.d == DD)                                                                            \
-        return r ? run_decode<T, DD, true>(plan, q, rho, kc, vc, seqlens, o, ws, stream)         \
-                 : run_decode<T, DD, false>(plan, q, rho, kc, vc, seqlens, o, ws, stream);
+        return r ? run_decode_any<T, DD, true>(plan, q, rho, kc, vc, seqlens, o, ws, block_table, \
+                                               stream)                                           \
+                 : run_decode_any<T, DD, false>(plan, q, rho, kc, vc, seqlens, o, ws,             \
+                                                block_table, stream);
     if (bf16) {
         PARALLAX_DECODE_CASE(__nv_bfloat16, 64)
         PARALLAX_DECODE_CASE(__nv_bfloat16, 128)
@@ -368,7 +469,7 @@ cudaError_t decode_launch_noalloc(const DecodePlan& plan, bool bf16, const void*
         }
         ptr = g_noalloc_addr[dev];
     }
-    return decode_launch(plan, bf16, q, rho, kc, vc, seqlens, o, ptr, stream);
+    return decode_launch(plan, bf16, q, rho, kc, vc, seqlens, o, ptr, stream, nullptr);
 }
 
 unsigned decode_take_error() {

@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -10,6 +11,10 @@ namespace parallax {
 // ---------------------------------------------------------------- decode
 struct DecodePlan {
     int B, H, Lmax, d;
+    int Hkv;  // key/value heads (H for plain attention; H / group size with shared heads)
+    // paged cache: page_size > 0; key t of sequence b is row t % page_size of page
+    // block_table[b * max_pages + t / page_size]; Lmax = max_pages * page_size
+    int page_size, max_pages, num_pages;
     int chunk;   // keys per split-KV chunk (a multiple of the stage size)
     int nsplit;  // ceil(Lmax / chunk); 1 = no split, no combine kernel
     int grid;    // persistent CTAs
@@ -21,7 +26,9 @@ int decode_stage_keys(int d, int elem_bytes);
 int decode_threads();
 cudaError_t decode_launch(const DecodePlan& plan, bool bf16, const void* q, const void* rho,
                           const void* kc, const void* vc, const int32_t* seqlens, float* o,
-                          void* ws, cudaStream_t stream);
+                          void* ws, cudaStream_t stream, const int32_t* block_table = nullptr);
+// Largest chunk (keys) whose page ids fit the per-item table of the paged decode.
+int decode_paged_max_chunk(int page_size);
 unsigned decode_take_error();
 // Same as decode_launch with the split-KV partials in a fixed device array
 // (no allocation).  Fails with cudaErrorInvalidValue if the plan needs more
@@ -48,5 +55,28 @@ cudaError_t prefill_tc_launch(const PrefillShape& s, const void* q, const void* 
                               const void* k, const void* v, float* o, int num_sms,
                               cudaStream_t stream);
 unsigned prefill_tc_take_error();
+// Chunked prefill: append k_new / v_new [B, H, L, d] to the caches [B, H, Lmax, d] at
+// rows cache_lens[b].., then causal attention of the chunk's queries over the cache.
+cudaError_t prefill_tc_chunk_launch(const PrefillShape& s, const void* q, const void* rho,
+                                    const void* k_new, const void* v_new, void* k_cache,
+                                    void* v_cache, const int32_t* cache_lens, int Lmax, float* o,
+                                    int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- tensor maps
+// bf16 tensor of `rank` dims (innermost first; strides in bytes of dims 1..rank-1),
+// box `box`, 128-byte swizzle, out-of-range elements read as zero.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
+
+// ---------------------------------------------------------------- q/k/v/probe projection
+struct ProjShape {
+    int B, L, width, H, d;
+    int n_out;  // 4 (q, k, v, rho) or 3 (no probe)
+};
+
+// out[t] = bf16 [B, H, L, d] slices of x [B, L, width] times w[t*H*d .. (t+1)*H*d - 1, :]^T
+cudaError_t proj_tc_launch(const ProjShape& s, const void* x, const void* w, void* const out[4],
+                           int num_sms, cudaStream_t stream);
+unsigned proj_tc_take_error();
 
 }  // namespace parallax

@@ -96,11 +96,28 @@ struct PairLayout {
 
 struct TcArgs {
     float* o;
-    int L;
+    // chunked prefill: keys already cached per sequence, or null (plain prefill).  Query
+    // row i of sequence b then sits at position cache_lens[b] + i and sees the keys at
+    // positions 0 .. cache_lens[b] + i of the K/V tensors.
+    const int32_t* cache_lens;
+    int L;         // query rows per head (also the key rows without a cache)
+    int Lcap;      // rows of the K/V tensors per head (L without a cache)
+    int H;
     int BH;
     int n_qb;      // query blocks per head
     float qscale;  // scale * log2(e)
 };
+
+// Keys already cached for the sequence of head bh, clamped so that the chunk fits.
+__device__ __forceinline__ int cached_keys(const TcArgs& a, int bh, unsigned* err, bool report) {
+    if (!a.cache_lens) return 0;
+    int off = __ldg(a.cache_lens + bh / a.H);
+    if (off < 0 || off > a.Lcap - a.L) {
+        if (report) raise_error(err, PARALLAX_DEVERR_SEQLEN_CLAMPED);
+        off = off < 0 ? 0 : a.Lcap - a.L;
+    }
+    return off;
+}
 
 // p = 2^(s*qs - m) for 32 consecutive values (in place), their sum into ls0/ls1,
 // and the bf16 pairs into pk; one pair in four through exp2_poly2, the rest on
@@ -161,12 +178,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qb = CAUSAL ? n_qb - 1 - r_in / gsize : r_in / gsize;
     const int bh = group * kHeadGroup + r_in % gsize;
     const int q0 = qb * LY::BLOCK;
+    // keys: `off` cached ones (chunked prefill) followed by the L rows of this call;
+    // query row i sits at key position off + i
+    // (a cached prefix only exists for causal attention)
+    const int off = CAUSAL ? cached_keys(a, bh, &g_tc_err, threadIdx.x == 0) : 0;
+    const int Lk = off + a.L;
     // key tiles of each sub-tile: causal rows q0 + QROWS*sub .. see keys up to
-    // their own index (the last tile is the diagonal one); sub-tile 0 may need
+    // their own position (the last tile is the diagonal one); sub-tile 0 may need
     // one tile fewer than sub-tile 1
-    const int n_all = (a.L + BN - 1) / BN;
-    const int n1 = CAUSAL ? min(n_all, (q0 + LY::BLOCK - 1) / BN + 1) : n_all;
-    const int n0 = CAUSAL ? min(n1, (q0 + LY::QROWS - 1) / BN + 1) : n_all;
+    const int n_all = (Lk + BN - 1) / BN;
+    const int n1 = CAUSAL ? min(n_all, (off + q0 + LY::BLOCK - 1) / BN + 1) : n_all;
+    const int n0 = CAUSAL ? min(n1, (off + q0 + LY::QROWS - 1) / BN + 1) : n_all;
     const bool precise = RHO && n1 == 1;
 
     if (threadIdx.x == 0) {
@@ -377,14 +399,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tmem_ld32_split<64>(tR + 32, rv[1]);
                 tc::tmem_ld_wait();
 
-                const bool need_mask = (it * BN + BN > a.L) || (CAUSAL && it * BN + BN - 1 > first_row);
+                // causal: keys past the row's position (for a real row that includes every
+                // key >= Lk; padding rows past L may see zero-filled keys); full: keys >= Lk
+                const bool need_mask = CAUSAL ? it * BN + BN - 1 > off + first_row : it * BN + BN > Lk;
                 if (need_mask) {
+                    const int lim = CAUSAL ? off + i : Lk - 1;
 #pragma unroll
                     for (int b = 0; b < 2; ++b)
 #pragma unroll
                         for (int x = 0; x < 32; ++x) {
                             const int key = k0 + 32 * b + x;
-                            if (!(key < a.L && (!CAUSAL || key <= i)))
+                            if (key > lim)
                                 sv[b][x] = __float_as_uint(-INFINITY);
                         }
                 }
@@ -553,14 +578,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int b = 0; b < 4; ++b) tc::tmem_ld32(tS + 32 * b, sv[b]);
                 tc::tmem_ld_wait();
-                const bool need_mask = (k0 + BN > a.L) || (CAUSAL && k0 + BN - 1 > first_row);
+                const bool need_mask = CAUSAL ? k0 + BN - 1 > off + first_row : k0 + BN > Lk;
                 if (need_mask) {
+                    const int lim = CAUSAL ? off + i : Lk - 1;
 #pragma unroll
                     for (int b = 0; b < 4; ++b)
 #pragma unroll
                         for (int x = 0; x < 32; ++x) {
                             const int key = k0 + 32 * b + x;
-                            if (!(key < a.L && (!CAUSAL || key <= i)))
+                            if (key > lim)
                                 sv[b][x] = __float_as_uint(-INFINITY);
                         }
                 }
@@ -640,36 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult qres;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &qres) == cudaSuccess &&
-            qres == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
 // [B*H, L, D] bf16 viewed as a 3-D tensor; box = 64 columns (128 bytes) x box_rows rows x 1 head,
 // 128-byte swizzle; rows past L read as zeros.
 bool make_map(CUtensorMap* m, const void* base, int BH, int L, int D, int box_rows = 128) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)BH};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * D * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)L, (uint64_t)BH};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)L * D * 2};
+    const uint32_t box[3] = {64, (uint32_t)box_rows, 1};
+    return make_tmap_bf16(m, base, 3, dims, strides, box);
 }
 
 template <int D, bool CAUSAL, bool RHO>
@@ -691,11 +694,73 @@ cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mr, const CUtensorM
 
 template <int D, bool RHO>
 cudaError_t launch_d(const PrefillShape& s, const CUtensorMap& mq, const CUtensorMap& mr,
-                     const CUtensorMap& mk, const CUtensorMap& mv, float* o, cudaStream_t stream) {
+                     const CUtensorMap& mk, const CUtensorMap& mv, float* o,
+                     const int32_t* cache_lens, int Lcap, cudaStream_t stream) {
     using LY = PairLayout<D, RHO>;
-    const TcArgs a{o, s.L, s.B * s.H, (s.L + LY::BLOCK - 1) / LY::BLOCK, s.scale * kLog2e};
+    const TcArgs a{o,   cache_lens, s.L, Lcap, s.H, s.B * s.H, (s.L + LY::BLOCK - 1) / LY::BLOCK,
+                   s.scale * kLog2e};
     return s.causal ? launch<D, true, RHO>(mq, mr, mk, mv, a, stream)
                     : launch<D, false, RHO>(mq, mr, mk, mv, a, stream);
+}
+
+// Query-side maps (q, rho: L rows per head) and key-side maps (k, v: Lcap rows per head).
+cudaError_t launch_any(const PrefillShape& s, const void* q, const void* rho, const void* k,
+                       const void* v, float* o, const int32_t* cache_lens, int Lcap,
+                       cudaStream_t stream) {
+    const int BH = s.B * s.H;
+    CUtensorMap mq, mr, mk, mv;
+    if (!make_map(&mk, k, BH, Lcap, s.d) || !make_map(&mv, v, BH, Lcap, s.d))
+        return cudaErrorInvalidValue;
+    if (rho) {
+        // correction path: query and probe maps use 16-row boxes (stacked operand)
+        if (!make_map(&mq, q, BH, s.L, s.d, 16) || !make_map(&mr, rho, BH, s.L, s.d, 16))
+            return cudaErrorInvalidValue;
+        if (s.d == 64) return launch_d<64, true>(s, mq, mr, mk, mv, o, cache_lens, Lcap, stream);
+        if (s.d == 128) return launch_d<128, true>(s, mq, mr, mk, mv, o, cache_lens, Lcap, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (!make_map(&mq, q, BH, s.L, s.d)) return cudaErrorInvalidValue;
+    mr = mq;  // unused
+    if (s.d == 64) return launch_d<64, false>(s, mq, mr, mk, mv, o, cache_lens, Lcap, stream);
+    if (s.d == 128) return launch_d<128, false>(s, mq, mr, mk, mv, o, cache_lens, Lcap, stream);
+    return cudaErrorInvalidValue;
+}
+
+// Copy the chunk's K and V rows [B, H, L, D] into the caches [B, H, Lcap, D] at rows
+// cache_lens[b] .. cache_lens[b] + L - 1 (16-byte vectors, grid-stride), and zero the
+// cache rows from there up to the end of that 128-key tile (at most Lcap): the
+// attention kernel multiplies those rows by zero weights, and they must not hold
+// NaN or Inf left over in unwritten memory.  A length that leaves no room for the
+// chunk is clamped exactly as the attention kernel does.
+constexpr int kPadRows = BN - 1;
+__global__ void __launch_bounds__(256) append_kernel(const uint4* __restrict__ k_new,
+                                                     const uint4* __restrict__ v_new,
+                                                     uint4* __restrict__ k_cache,
+                                                     uint4* __restrict__ v_cache,
+                                                     const int32_t* __restrict__ cache_lens, int H,
+                                                     int L, int Lcap, int vec_per_row,
+                                                     size_t total_vec) {
+    const int rows = L + kPadRows;  // per head: the chunk, then the padding of its last tile
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total_vec;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = idx / vec_per_row;  // (bh, i)
+        const int c = (int)(idx - row * vec_per_row);
+        const int bh = (int)(row / rows), i = (int)(row - (size_t)bh * rows);
+        int off = __ldg(cache_lens + bh / H);
+        off = off < 0 ? 0 : (off > Lcap - L ? Lcap - L : off);
+        const size_t dst = ((size_t)bh * Lcap + off + i) * vec_per_row + c;
+        if (i < L) {
+            const size_t src = ((size_t)bh * L + i) * vec_per_row + c;
+            k_cache[dst] = k_new[src];
+            v_cache[dst] = v_new[src];
+        } else {
+            const int end = off + L, tile_end = min(Lcap, (end + BN - 1) / BN * BN);
+            if (off + i < tile_end) {
+                k_cache[dst] = make_uint4(0, 0, 0, 0);
+                v_cache[dst] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
 }
 
 }  // namespace
@@ -703,23 +768,24 @@ cudaError_t launch_d(const PrefillShape& s, const CUtensorMap& mq, const CUtenso
 cudaError_t prefill_tc_launch(const PrefillShape& s, const void* q, const void* rho,
                               const void* k, const void* v, float* o, int /*num_sms*/,
                               cudaStream_t stream) {
-    const int BH = s.B * s.H;
-    CUtensorMap mq, mr, mk, mv;
-    if (!make_map(&mk, k, BH, s.L, s.d) || !make_map(&mv, v, BH, s.L, s.d))
-        return cudaErrorInvalidValue;
-    if (rho) {
-        // correction path: query and probe maps use 16-row boxes (stacked operand)
-        if (!make_map(&mq, q, BH, s.L, s.d, 16) || !make_map(&mr, rho, BH, s.L, s.d, 16))
-            return cudaErrorInvalidValue;
-        if (s.d == 64) return launch_d<64, true>(s, mq, mr, mk, mv, o, stream);
-        if (s.d == 128) return launch_d<128, true>(s, mq, mr, mk, mv, o, stream);
-        return cudaErrorInvalidValue;
-    }
-    if (!make_map(&mq, q, BH, s.L, s.d)) return cudaErrorInvalidValue;
-    mr = mq;  // unused
-    if (s.d == 64) return launch_d<64, false>(s, mq, mr, mk, mv, o, stream);
-    if (s.d == 128) return launch_d<128, false>(s, mq, mr, mk, mv, o, stream);
-    return cudaErrorInvalidValue;
+    return launch_any(s, q, rho, k, v, o, nullptr, s.L, stream);
+}
+
+cudaError_t prefill_tc_chunk_launch(const PrefillShape& s, const void* q, const void* rho,
+                                    const void* k_new, const void* v_new, void* k_cache,
+                                    void* v_cache, const int32_t* cache_lens, int Lmax, float* o,
+                                    int num_sms, cudaStream_t stream) {
+    const int vec_per_row = s.d * 2 / 16;
+    const size_t total_vec = (size_t)s.B * s.H * (s.L + kPadRows) * vec_per_row;
+    const size_t want = (total_vec + 255) / 256;
+    const unsigned grid = (unsigned)(want < (size_t)num_sms * 8 ? want : (size_t)num_sms * 8);
+    append_kernel<<<grid, 256, 0, stream>>>(
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), cache_lens, s.H, s.L, Lmax,
+        vec_per_row, total_vec);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_any(s, q, rho, k_cache, v_cache, o, cache_lens, Lmax, stream);
 }
 
 unsigned prefill_tc_take_error() {

@@ -130,3 +130,87 @@ def test_forced_chunk_validation(lib):
     assert px.parallax_attn_decode_chunk_keys(1, 1, 4096, 128, 2) == 512
     assert px.parallax_attn_decode_chunk_keys(1, 1, 300, 128, 2) == 300  # >= Lmax: no split
     px.parallax_attn_set_decode_chunk_keys(0)
+
+
+def _proj(lib, x=FAKE, w=FAKE, q=FAKE, k=FAKE, v=FAKE, rho=FAKE, B=1, L=8, width=64, H=2, d=64):
+    vp = ctypes.c_void_p
+    return lib.parallax_attn_qkvr_projection(vp(x), vp(w), vp(q), vp(k), vp(v), vp(rho), B, L,
+                                             width, H, d, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=0), px.PARALLAX_ERR_INVALID),
+    (dict(w=0), px.PARALLAX_ERR_INVALID),
+    (dict(v=0), px.PARALLAX_ERR_INVALID),
+    (dict(B=0), px.PARALLAX_ERR_INVALID),
+    (dict(L=-1), px.PARALLAX_ERR_INVALID),
+    (dict(width=0), px.PARALLAX_ERR_INVALID),
+    (dict(d=96), px.PARALLAX_ERR_UNSUPPORTED),
+    (dict(H=1, d=64), px.PARALLAX_ERR_UNSUPPORTED),   # H*d = 64 is not a multiple of 128
+    (dict(width=60), px.PARALLAX_ERR_UNSUPPORTED),
+    (dict(q=FAKE + 8), px.PARALLAX_ERR_INVALID),
+    (dict(rho=FAKE + 4), px.PARALLAX_ERR_INVALID),
+])
+def test_projection_validation(lib, kw, code):
+    assert _proj(lib, **kw) == code
+    assert px.last_error() != ""
+
+
+def _gqa(lib, q=FAKE, rho=None, k=FAKE, v=FAKE, sl=FAKE, o=FAKE, B=1, H=8, Hkv=2, Lmax=64,
+         d=128):
+    vp = ctypes.c_void_p
+    return lib.parallax_attn_decode_gqa(vp(q), vp(rho), vp(k), vp(v), vp(sl), vp(o), B, H, Hkv,
+                                        Lmax, d, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hkv=3), px.PARALLAX_ERR_INVALID),         # 8 is not a multiple of 3
+    (dict(Hkv=0), px.PARALLAX_ERR_INVALID),
+    (dict(H=16, Hkv=1), px.PARALLAX_ERR_UNSUPPORTED),  # 16 query heads per key/value head
+    (dict(H=6, Hkv=2), px.PARALLAX_ERR_UNSUPPORTED),   # group of 3
+    (dict(sl=0), px.PARALLAX_ERR_INVALID),
+    (dict(d=32), px.PARALLAX_ERR_UNSUPPORTED),
+])
+def test_gqa_validation(lib, kw, code):
+    assert _gqa(lib, **kw) == code
+
+
+def _paged(lib, q=FAKE, rho=None, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, o=FAKE, B=1, H=4, Hkv=4,
+           P=16, max_pages=4, num_pages=8, d=128):
+    vp = ctypes.c_void_p
+    return lib.parallax_attn_decode_paged(vp(q), vp(rho), vp(k), vp(v), vp(bt), vp(sl), vp(o), B,
+                                          H, Hkv, P, max_pages, num_pages, d, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bt=0), px.PARALLAX_ERR_INVALID),
+    (dict(P=0), px.PARALLAX_ERR_INVALID),
+    (dict(P=24), px.PARALLAX_ERR_UNSUPPORTED),      # not a multiple of 16
+    (dict(max_pages=0), px.PARALLAX_ERR_INVALID),
+    (dict(num_pages=0), px.PARALLAX_ERR_INVALID),
+    (dict(P=1 << 20, max_pages=1 << 12), px.PARALLAX_ERR_INVALID),  # Lmax beyond int
+    (dict(Hkv=3), px.PARALLAX_ERR_INVALID),
+    (dict(k=FAKE + 2), px.PARALLAX_ERR_INVALID),
+])
+def test_paged_validation(lib, kw, code):
+    assert _paged(lib, **kw) == code
+
+
+def _chunk(lib, q=FAKE, rho=None, k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, cl=FAKE, o=FAKE, B=1, H=1,
+           Lq=8, Lmax=16, d=64, scale=0.125):
+    vp = ctypes.c_void_p
+    return lib.parallax_attn_prefill_chunk(vp(q), vp(rho), vp(k), vp(v), vp(kc), vp(vc), vp(cl),
+                                           vp(o), B, H, Lq, Lmax, d, ctypes.c_float(scale), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kc=0), px.PARALLAX_ERR_INVALID),
+    (dict(cl=0), px.PARALLAX_ERR_INVALID),
+    (dict(Lmax=4), px.PARALLAX_ERR_INVALID),          # chunk longer than the cache
+    (dict(Lq=0), px.PARALLAX_ERR_INVALID),
+    (dict(d=80), px.PARALLAX_ERR_UNSUPPORTED),
+    (dict(vc=FAKE + 8), px.PARALLAX_ERR_INVALID),
+    (dict(scale=float("inf")), px.PARALLAX_ERR_INVALID),
+])
+def test_chunk_validation(lib, kw, code):
+    assert _chunk(lib, **kw) == code
