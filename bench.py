@@ -44,6 +44,7 @@ TRAFFIC_BYTES = {
     # full-size capture: 177.38 MB read + 497.77 MB written (the rest of the 536.9 MB
     # output was still in L2 when the kernel ended)
     "projection": 177.38e6 + 497.77e6,
+    "backward": None,
 }
 
 
@@ -58,7 +59,7 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["decode", "prefill", "projection"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "projection", "backward"], default=None,
                     help="time one kernel alone (profiling runs); the default times both")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="override the decode batch (profiling runs on smaller cases)")
@@ -66,9 +67,13 @@ def parse_args(argv=None):
                     help="override the prefill batch (profiling runs on smaller cases)")
     ap.add_argument("--no-projection", action="store_true",
                     help="skip the q/k/v/probe projection leg")
+    ap.add_argument("--no-backward", action="store_true", help="skip the prefill backward leg")
     ap.add_argument("--wr-zero", action="store_true",
                     help="time the W_R = 0 path (rho = NULL) in the step instead of the "
                          "correction path (profiling runs)")
+    ap.add_argument("--serving", action="store_true",
+                    help="instead of the step: time the serving variants (grouped-query decode, "
+                         "paged ragged decode, chunked prefill), one JSON line each")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the step: time the decode sweep cells and the ragged-batch "
                          "decode, one JSON line per case (plus a markdown table on stderr)")
@@ -287,6 +292,53 @@ def time_projection(args, dev, peaks, max_over_ranks, n_rep=20):
             "peak_source": peaks["source"] + f" (burst: timed alone, {n_rep} launches)"}
 
 
+def time_backward(args, dev, peaks, max_over_ranks, n_rep=10):
+    """Backward pass of the layer-shaped causal prefill (B=8, H=16, L=4096, d=128): the
+    training forward once (for lse, rbar, mu_v), then `n_rep` backward calls back to back
+    after warm-ups.  Algorithmic work: 8 causal contractions (S, R recomputed, D = dout V^T,
+    dV, the two dK terms, dQ, drho) = 16 d flop per (query, visible key)."""
+    import torch
+
+    import softmax_covariance_correction_pass_b300 as px
+    from softmax_covariance_correction_pass_b300 import configs
+
+    pc = configs.LAYER_PREFILL
+    PB = args.prefill_batch or pc["B"]
+    inp = configs.layer_prefill_inputs(dev, B=PB)
+    B, H, L, d = inp.q.shape
+    g = torch.Generator(device=dev).manual_seed(44)
+    dout = torch.randn(inp.q.shape, generator=g, device=dev).to(torch.bfloat16)
+    o, lse, rbar, mu = px.parallax_attn_prefill_train(inp.q, inp.rho, inp.k, inp.v, causal=True,
+                                                      scale=inp.scale)
+    stream = torch.cuda.current_stream()
+    flops = 16.0 * d * (L * (L + 1) / 2) * B * H
+
+    def backward():
+        return px.parallax_attn_prefill_backward(inp.q, inp.rho, inp.k, inp.v, o, mu, lse, rbar,
+                                                 dout, causal=True, scale=inp.scale)
+
+    for _ in range(max(args.warmup, 3)):
+        backward()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n_rep):
+        backward()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / n_rep)
+    if px.parallax_check_device_error() != 0:
+        raise RuntimeError("device error in the backward pass")
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": tf / peaks["bf16_tflops"], "traffic": TRAFFIC_BYTES.get("backward"),
+            "kernel": "bwd_pre_kernel + bwd_kv_kernel + bwd_q_kernel",
+            "algorithmic_flops_per_launch": flops, "avg_launch_ms": ms, "launches": n_rep,
+            "shape": f"causal prefill backward B={B} H={H} L={L} d={d}, bf16 in, fp32 grads",
+            "tokens_per_s": B * L / (ms * 1e-3),
+            "peak_source": peaks["source"] + f" (burst: timed alone, {n_rep} calls)"}
+
+
 def run_projection_only(args):
     """--only projection: the projection leg alone (profiling runs), one JSON line."""
     import torch
@@ -443,6 +495,10 @@ def run_ours(args):
     proj = None
     if not args.only and not args.no_projection:
         proj = time_projection(args, dev, peaks, max_over_ranks)
+    bwd = None
+    if not args.only and not args.no_backward:
+        bwd = time_backward(args, dev, peaks, max_over_ranks)
+        torch.cuda.empty_cache()
 
     # ---- end to end through the public call, host buffers (pinned), copies timed
     e2e = None
@@ -531,6 +587,7 @@ def run_ours(args):
                 "frac_of_peak": roof_dec["frac"], "ms_per_call": dec_ms},
             "w_r_zero_fast_path": f0,
             "roofline_projection": proj,
+            "roofline_backward": bwd,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks.summary(),
@@ -618,14 +675,102 @@ def run_sweep(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- serving variants
+def run_serving(args):
+    """Grouped-query decode (B=64, H=16 over H_kv in {8, 4, 2}, 8192 keys), paged decode of
+    the ragged batch (B=512, U[128,16384] keys, 256-key pages, H_kv in {16, 4}) and the
+    layer-shaped chunked prefill (3072 cached + 1024 new tokens).  Each case: 3 warm-ups,
+    then `reps` calls timed with CUDA events (inputs larger than L2, back to back)."""
+    import torch
+
+    import softmax_covariance_correction_pass_b300 as px
+    from softmax_covariance_correction_pass_b300 import configs
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    px.load_library()
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    def timed(call, reps):
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if px.parallax_check_device_error() != 0:
+            raise RuntimeError("device error")
+        return a.elapsed_time(b) / reps
+
+    rows = []
+    d = 128
+    for Hkv in (8, 4, 2):
+        B, H, n = 64, 16, 8192
+        inp = configs.decode_gqa_inputs(B, H, Hkv, d, n, n, seed=1, device=dev)
+        o = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+        ms = timed(lambda: px.parallax_attn_decode_gqa(inp.q, inp.rho, inp.k_cache, inp.v_cache,
+                                                        inp.seqlens, o), 20)
+        byts = 2 * B * Hkv * n * d * 2 + 2 * B * H * d * 2 + B * H * d * 4
+        rows.append({"case": f"gqa decode B={B} H={H} H_kv={Hkv} ctx={n}", "ms": ms,
+                     "GB/s": byts / ms / 1e6, "frac_of_hbm_peak": byts / ms / 1e6 / peaks["hbm_gbs"],
+                     "kv_bytes": 2 * B * Hkv * n * d * 2, "tokens_per_s": B / (ms * 1e-3)})
+        del inp, o
+    c = configs.DECODE_RAGGED
+    sl = configs.ragged_seqlens()
+    for Hkv in (16, 4):
+        B, H, P = c["B"], c["H"], 256
+        inp, bt = configs.paged_decode_inputs(B, H, Hkv, d, sl, P, seed=c["seed"], device=dev)
+        o = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+        ms = timed(lambda: px.parallax_attn_decode_paged(inp.q, inp.rho, inp.k_cache, inp.v_cache,
+                                                          bt, inp.seqlens, o), 10)
+        keys = int(sl.sum())
+        byts = 2 * keys * Hkv * d * 2 + 2 * B * H * d * 2 + B * H * d * 4
+        rows.append({"case": f"paged decode ragged B={B} H={H} H_kv={Hkv} page={P}", "ms": ms,
+                     "GB/s": byts / ms / 1e6, "frac_of_hbm_peak": byts / ms / 1e6 / peaks["hbm_gbs"],
+                     "kv_bytes": 2 * keys * Hkv * d * 2, "tokens_per_s": B / (ms * 1e-3)})
+        del inp, o, bt
+        torch.cuda.empty_cache()
+    full = configs.layer_prefill_inputs(dev)
+    B, H, L, _ = full.q.shape
+    off, Lq = 3072, 1024
+    kc, vc = full.k.clone(), full.v.clone()
+    cl = torch.full((B,), off, dtype=torch.int32, device=dev)
+    sl_ = slice(off, L)
+    qn, rn, kn, vn = (t[:, :, sl_].contiguous() for t in (full.q, full.rho, full.k, full.v))
+    o = torch.empty((B, H, Lq, d), dtype=torch.float32, device=dev)
+    ms = timed(lambda: px.parallax_attn_prefill_chunk(qn, rn, kn, vn, kc, vc, cl, o), 20)
+    pairs = B * H * sum(off + i + 1 for i in range(Lq))
+    flops = 8.0 * d * pairs
+    rows.append({"case": f"chunked prefill B={B} H={H} cached={off} chunk={Lq}", "ms": ms,
+                 "TFLOP/s": flops / ms / 1e9, "frac_of_tensor_peak_burst":
+                     flops / ms / 1e9 / peaks["bf16_tflops"], "tokens_per_s": B * Lq / (ms * 1e-3)})
+    for r in rows:
+        print(json.dumps(r), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.serving:
+        return run_serving(args)
     if args.only == "projection":
         return run_projection_only(args)
+    if args.only == "backward":
+        import torch
+
+        r = time_backward(args, torch.device("cuda", torch.cuda.current_device()), load_peaks(),
+                          lambda x: x, n_rep=args.steps)
+        print(json.dumps({"metric": "prefill backward TFLOP/s", "value": r["achieved"],
+                          "unit": "TFLOP/s", "steps": args.steps, "warmup": args.warmup,
+                          "roofline": r}), flush=True)
+        return 0
     return run_ours(args)
 
 

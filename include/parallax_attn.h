@@ -93,6 +93,42 @@ int parallax_attn_prefill_chunk(const void* q, const void* rho, const void* k_ne
                                 const int32_t* cache_lens, void* o, int B, int H, int Lq,
                                 int Lmax, int d, float scale, cudaStream_t stream);
 
+/*
+ * Training forward: parallax_attn_prefill (bf16, tensor cores) that also keeps
+ * the per-row quantities the backward pass needs.
+ *   lse   : fp32 [B, H, L]     log sum_j exp(scale q_i.k_j) over the row's keys
+ *   rbar  : fp32 [B, H, L]     sum_j p_ij r_ij (the p-weighted mean of rho_i.k_j; 0 if rho == NULL)
+ *   mu_v  : fp32 [B, H, L, d]  sum_j p_ij v_j (the softmax branch alone)
+ * Other arguments as parallax_attn_prefill.  No workspace.
+ */
+int parallax_attn_prefill_train(const void* q, const void* rho, const void* k, const void* v,
+                                void* o, float* lse, float* rbar, float* mu_v, int B, int H, int L,
+                                int d, int causal, float scale, cudaStream_t stream);
+
+/*
+ * Backward pass of the prefill (the pages' results all come from pretraining;
+ * this is the gradient of the forward above).  Writing o_i = sum_j w_ij v_j with
+ * w_ij = p_ij (1 + rbar_i - r_ij), r_ij = rho_i.k_j, and given dout = dL/do:
+ *   dv_j = sum_i w_ij dout_i
+ *   dq_i = scale sum_j ds_ij k_j,    drho_i = sum_j dr_ij k_j
+ *   dk_j = scale sum_i ds_ij q_i + sum_i dr_ij rho_i
+ *   dr_ij = p_ij (abar_i - D_ij),    ds_ij = p_ij ((D_ij - abar_i)(rbar_i - r_ij) + D_ij - delta_i)
+ * with D_ij = dout_i.v_j, abar_i = dout_i.mu_v,i, delta_i = dout_i.o_i.
+ *   q, rho, k, v      : bf16 [B, H, L, d] (the forward's inputs; rho may be NULL)
+ *   o, mu_v, lse, rbar: fp32, from parallax_attn_prefill_train on the same inputs
+ *   dout              : bf16 [B, H, L, d]
+ *   dq, drho, dk, dv  : fp32 [B, H, L, d], written in full (drho unused if rho == NULL)
+ * The contractions run on the tcgen05 tensor cores with bf16 operands (p-weighted
+ * terms rounded to bf16) and fp32 accumulation.  Uses a library-owned per-device
+ * workspace of 16 B per query row (grown on demand with cudaMalloc, which
+ * synchronises the device; same concurrency rules as the decode workspace).
+ */
+int parallax_attn_prefill_backward(const void* q, const void* rho, const void* k, const void* v,
+                                   const float* o, const float* mu_v, const float* lse,
+                                   const float* rbar, const void* dout, float* dq, float* drho,
+                                   float* dk, float* dv, int B, int H, int L, int d, int causal,
+                                   float scale, cudaStream_t stream);
+
 /* Same as parallax_attn_prefill with fp32 q, rho, k, v (fp32 SIMT arithmetic). */
 int parallax_attn_prefill_f32(const void* q, const void* rho, const void* k, const void* v,
                               void* o, int B, int H, int L, int d, int causal, float scale,
@@ -218,7 +254,7 @@ int parallax_attn_set_decode_chunk_keys(int keys);
 /* Bytes currently held by the calling device's decode workspace. */
 size_t parallax_attn_workspace_bytes(void);
 
-/* Free the calling device's decode workspace (synchronises the device). */
+/* Free the calling device's decode and backward workspaces (synchronises the device). */
 int parallax_attn_release_workspace(void);
 
 /*

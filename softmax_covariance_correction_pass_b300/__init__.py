@@ -52,6 +52,9 @@ def load_library() -> ctypes.CDLL:
     lib.parallax_attn_prefill_f32.argtypes = lib.parallax_attn_prefill.argtypes
     lib.parallax_attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     lib.parallax_attn_decode_f32.argtypes = lib.parallax_attn_decode.argtypes
+    lib.parallax_attn_prefill_train.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                i32, f32, vp]
+    lib.parallax_attn_prefill_backward.argtypes = [vp] * 13 + [i32] * 5 + [f32, vp]
     lib.parallax_attn_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                                 i32, i32, f32, vp]
     lib.parallax_attn_decode_gqa.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
@@ -67,6 +70,7 @@ def load_library() -> ctypes.CDLL:
     for name in ("parallax_attn_prefill", "parallax_attn_prefill_f32", "parallax_attn_decode",
                  "parallax_attn_qkvr_projection", "parallax_attn_decode_gqa",
                  "parallax_attn_decode_paged", "parallax_attn_prefill_chunk",
+                 "parallax_attn_prefill_train", "parallax_attn_prefill_backward",
                  "parallax_attn_decode_f32", "parallax_attn_decode_chunk_keys",
                  "parallax_attn_set_decode_chunk_keys", "parallax_attn_release_workspace",
                  "parallax_check_device_error", "parallax_version"):
@@ -128,6 +132,50 @@ def parallax_attn_prefill(q, rho, k, v, o=None, causal: bool = True, scale: floa
     _check(fn(_ptr(q), _ptr(rho), _ptr(k), _ptr(v), _ptr(o), B, H, L, d, 1 if causal else 0,
               float(scale), _stream(stream)))
     return o
+
+
+def parallax_attn_prefill_train(q, rho, k, v, causal: bool = True, scale: float | None = None,
+                                stream=None):
+    """Training forward (bf16 [B, H, L, d] inputs): returns (o, lse, rbar, mu_v), fp32;
+    lse/rbar [B, H, L] and mu_v [B, H, L, d] are what the backward pass needs."""
+    B, H, L, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)) + ((("rho", rho),) if rho is not None else ()):
+        _need(t, name, torch.bfloat16, (B, H, L, d))
+    o = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+    mu = torch.empty_like(o)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    rbar = torch.empty_like(lse)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load_library().parallax_attn_prefill_train(
+        _ptr(q), _ptr(rho), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(rbar), _ptr(mu), B, H, L,
+        d, 1 if causal else 0, float(scale), _stream(stream)))
+    return o, lse, rbar, mu
+
+
+def parallax_attn_prefill_backward(q, rho, k, v, o, mu_v, lse, rbar, dout, causal: bool = True,
+                                   scale: float | None = None, stream=None):
+    """Gradients (dq, drho, dk, dv), fp32 [B, H, L, d], of sum(dout * o) for the prefill;
+    o, mu_v, lse, rbar come from parallax_attn_prefill_train, dout is bf16.  drho is
+    None when rho is None."""
+    B, H, L, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)) + \
+            ((("rho", rho),) if rho is not None else ()):
+        _need(t, name, torch.bfloat16, (B, H, L, d))
+    _need(o, "o", torch.float32, (B, H, L, d))
+    _need(mu_v, "mu_v", torch.float32, (B, H, L, d))
+    _need(lse, "lse", torch.float32, (B, H, L))
+    _need(rbar, "rbar", torch.float32, (B, H, L))
+    dq, dk, dv = (torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+                  for _ in range(3))
+    drho = None if rho is None else torch.empty_like(dq)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load_library().parallax_attn_prefill_backward(
+        _ptr(q), _ptr(rho), _ptr(k), _ptr(v), _ptr(o), _ptr(mu_v), _ptr(lse), _ptr(rbar),
+        _ptr(dout), _ptr(dq), _ptr(drho), _ptr(dk), _ptr(dv), B, H, L, d, 1 if causal else 0,
+        float(scale), _stream(stream)))
+    return dq, drho, dk, dv
 
 
 def parallax_attn_prefill_chunk(q, rho, k_new, v_new, k_cache, v_cache, cache_lens, o=None,
@@ -312,4 +360,6 @@ decode = parallax_attn_decode
 qkvr_projection = parallax_attn_qkvr_projection
 decode_gqa = parallax_attn_decode_gqa
 prefill_chunk = parallax_attn_prefill_chunk
+prefill_train = parallax_attn_prefill_train
+prefill_backward = parallax_attn_prefill_backward
 decode_paged = parallax_attn_decode_paged

@@ -40,10 +40,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 std::atomic<int> g_chunk_override{0};
 
 struct DeviceState {
-    void* ws = nullptr;
+    void* ws = nullptr;  // decode split-KV partials
     size_t ws_bytes = 0;
+    void* bws = nullptr;  // prefill backward row statistics
+    size_t bws_bytes = 0;
     int num_sms = 0;
 };
+
+// Grow a per-device buffer to `need` bytes (cudaMalloc; growing synchronises the device).
+int grow(void*& buf, size_t& have, size_t need, const char* what);
 std::mutex g_mu;
 std::vector<DeviceState> g_dev;
 
@@ -78,6 +83,23 @@ int plan_chunk(int B, int H, int Lmax, int num_sms) {
         while (c < 4096 && (double)(2 * c) <= per_item) c *= 2;
     }
     return c >= Lmax ? Lmax : c;
+}
+
+int grow(void*& buf, size_t& have, size_t need, const char* what) {
+    if (have >= need) return PARALLAX_OK;
+    if (buf) {
+        cudaError_t e = cudaFree(buf);  // synchronises the device
+        buf = nullptr;
+        have = 0;
+        if (e != cudaSuccess) return cuda_fail(e, what);
+    }
+    cudaError_t e = cudaMalloc(&buf, need);
+    if (e != cudaSuccess) {
+        buf = nullptr;
+        return cuda_fail(e, what);
+    }
+    have = need;
+    return PARALLAX_OK;
 }
 
 int validate_common(const void* q, const void* k, const void* v, const void* o, const void* rho,
@@ -206,6 +228,67 @@ int parallax_attn_prefill(const void* q, const void* rho, const void* k, const v
                           int B, int H, int L, int d, int causal, float scale,
                           cudaStream_t stream) {
     return prefill_common(q, rho, k, v, o, B, H, L, d, causal, scale, stream, true);
+}
+
+int parallax_attn_prefill_train(const void* q, const void* rho, const void* k, const void* v,
+                                void* o, float* lse, float* rbar, float* mu_v, int B, int H, int L,
+                                int d, int causal, float scale, cudaStream_t stream) {
+    int rc = validate_common(q, k, v, o, rho, B, H, L, d, "L");
+    if (rc != PARALLAX_OK) return rc;
+    if (!lse || !rbar || !mu_v)
+        return fail(PARALLAX_ERR_INVALID, "null statistics pointer (lse=%p rbar=%p mu_v=%p)",
+                    (void*)lse, (void*)rbar, (void*)mu_v);
+    if (!aligned16(mu_v) || !aligned16(lse) || !aligned16(rbar))
+        return fail(PARALLAX_ERR_INVALID, "every tensor pointer must be 16-byte aligned");
+    if (causal != 0 && causal != 1)
+        return fail(PARALLAX_ERR_INVALID, "causal=%d must be 0 or 1", causal);
+    if (!std::isfinite(scale)) return fail(PARALLAX_ERR_INVALID, "scale must be finite");
+    DeviceState* ds = device_state(nullptr);
+    if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
+    parallax::PrefillShape s{B, H, L, d, causal, scale};
+    parallax::TrainStats ts;
+    ts.lse = lse;
+    ts.rbar = rbar;
+    ts.mu = mu_v;
+    cudaError_t e = parallax::prefill_tc_launch(s, q, rho, k, v, static_cast<float*>(o),
+                                                ds->num_sms, stream, ts);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return succeed();
+}
+
+int parallax_attn_prefill_backward(const void* q, const void* rho, const void* k, const void* v,
+                                   const float* o, const float* mu_v, const float* lse,
+                                   const float* rbar, const void* dout, float* dq, float* drho,
+                                   float* dk, float* dv, int B, int H, int L, int d, int causal,
+                                   float scale, cudaStream_t stream) {
+    int rc = validate_common(q, k, v, o, rho, B, H, L, d, "L");
+    if (rc != PARALLAX_OK) return rc;
+    if (!mu_v || !lse || !rbar || !dout || !dq || !dk || !dv || (rho && !drho))
+        return fail(PARALLAX_ERR_INVALID, "null pointer among mu_v, lse, rbar, dout, dq, drho, "
+                    "dk, dv (drho may be null only when rho is)");
+    if (!aligned16(mu_v) || !aligned16(lse) || !aligned16(rbar) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(drho) || !aligned16(dk) || !aligned16(dv))
+        return fail(PARALLAX_ERR_INVALID, "every tensor pointer must be 16-byte aligned");
+    if (causal != 0 && causal != 1)
+        return fail(PARALLAX_ERR_INVALID, "causal=%d must be 0 or 1", causal);
+    if (!std::isfinite(scale)) return fail(PARALLAX_ERR_INVALID, "scale must be finite");
+    int dev = 0;
+    DeviceState* ds = device_state(&dev);
+    if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState& st = g_dev[dev];
+        rc = grow(st.bws, st.bws_bytes, parallax::prefill_backward_workspace_bytes(B, H, L),
+                  "backward workspace");
+        if (rc != PARALLAX_OK) return rc;
+        ws = st.bws;
+    }
+    parallax::PrefillShape s{B, H, L, d, causal, scale};
+    cudaError_t e = parallax::prefill_backward_launch(s, q, rho, k, v, o, mu_v, lse, rbar, dout,
+                                                      dq, drho, dk, dv, ws, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return succeed();
 }
 
 int parallax_attn_prefill_f32(const void* q, const void* rho, const void* k, const void* v,
@@ -380,6 +463,12 @@ int parallax_attn_release_workspace(void) {
         g_dev[dev].ws_bytes = 0;
         if (e != cudaSuccess) return cuda_fail(e, "workspace free");
     }
+    if ((int)g_dev.size() > dev && g_dev[dev].bws) {
+        e = cudaFree(g_dev[dev].bws);
+        g_dev[dev].bws = nullptr;
+        g_dev[dev].bws_bytes = 0;
+        if (e != cudaSuccess) return cuda_fail(e, "workspace free");
+    }
     return succeed();
 }
 
@@ -389,7 +478,8 @@ int parallax_check_device_error(cudaStream_t stream, unsigned int* bits) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     const unsigned v = parallax::decode_take_error() | parallax::prefill_simt_take_error() |
-                       parallax::prefill_tc_take_error() | parallax::proj_tc_take_error();
+                       parallax::prefill_tc_take_error() | parallax::proj_tc_take_error() |
+                       parallax::prefill_backward_take_error();
     if (bits) *bits = v;
     if (v) return fail(PARALLAX_ERR_DEVICE, "device error word 0x%x", v);
     return succeed();

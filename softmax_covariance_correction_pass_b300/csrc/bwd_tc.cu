@@ -1,0 +1,717 @@
+// Backward pass of the Parallax prefill on the tcgen05 tensor cores (sm_103a).
+//
+// Forward, per query row i over its keys j: p_ij = softmax_j(scale q_i.k_j),
+// r_ij = rho_i.k_j, rbar_i = sum_j p_ij r_ij, and the output is one weighted sum
+//   o_i = sum_j w_ij v_j,   w_ij = p_ij (1 + rbar_i - r_ij)
+// (softmax attention minus the probe-projected key/value covariance, "Parallax
+// mantem softmax ...", paragraph 2, since sum_j p_ij (r_ij - rbar_i) mu_v = 0).
+// With dO the gradient of o, D_ij = dO_i.v_j, abar_i = dO_i.mu_v,i and
+// delta_i = dO_i.o_i, the gradients are
+//   dv_j  = sum_i w_ij dO_i
+//   dr_ij = p_ij (abar_i - D_ij),   ds_ij = p_ij ((D_ij - abar_i)(rbar_i - r_ij) + D_ij - delta_i)
+//   dq_i  = scale sum_j ds_ij k_j,  drho_i = sum_j dr_ij k_j
+//   dk_j  = scale sum_i ds_ij q_i + sum_i dr_ij rho_i.
+// p is recomputed from the forward's per-row log-sum-exp.
+//
+// Three kernels, in stream order:
+//   bwd_pre_kernel  per row: (lse2, rbar, abar, delta) into a row-stats buffer;
+//   bwd_kv_kernel   per 128-key tile: loops over 64-query tiles; MMAs
+//                   [S^T | R^T] = K [Q; rho]^T and D^T = V dO^T, the compute
+//                   warps form W, dS, dR (bf16, written back to TMEM), MMAs
+//                   dV += W dO and dK += dS Q + dR rho (A from TMEM);
+//   bwd_q_kernel    per 64-query tile, the forward's stacked layout (TMEM lane
+//                   32g+i: query 16g+i's S row, lane 32g+16+i: its R row): MMAs
+//                   [S; R] = [Q; rho] K^T and [D; D] = [dO; dO] V^T, the compute
+//                   warps form dS, dR, MMA [dQ; drho] += [dS; dR] K.
+// Every contraction is a tcgen05.mma with bf16 operands and fp32 TMEM
+// accumulators; K, V and the query-side tiles arrive by TMA (128-byte swizzle).
+#include "tcgen05.cuh"
+#include "kernels.h"
+
+namespace parallax {
+namespace {
+
+__device__ unsigned g_bwd_err = 0;
+
+constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-3 set-up, warps 4-7 compute
+constexpr int SUB = 128 * 128;  // [128 rows x 64 columns] bf16, 128-byte swizzled
+constexpr int SUB64 = 64 * 128; // [64 rows x 64 columns]
+
+struct BwdArgs {
+    const float* o;               // [BH, L, D] forward output
+    const float* mu;              // [BH, L, D] forward mu_v
+    const __nv_bfloat16* dout;    // [BH, L, D] gradient of o
+    const float* lse;             // [BH, L]
+    const float* rbar;            // [BH, L]
+    float4* rs;                   // [BH * L] (lse2, rbar, abar, delta)
+    float* dq;
+    float* drho;
+    float* dk;
+    float* dv;                    // [BH, L, D] fp32
+    int L, BH;
+    int n_kt, n_qt;               // 128-key tiles and 64-query tiles per head
+    float scale, qscale;          // softmax scale, scale * log2(e)
+};
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------ row statistics
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const size_t row = (size_t)blockIdx.x * 8 + warp;
+    if (row >= (size_t)a.BH * a.L) return;
+    constexpr int PER = D / 32;
+    float ab = 0.f, de = 0.f;
+#pragma unroll
+    for (int x = 0; x < PER; ++x) {
+        const size_t idx = row * D + lane + 32 * x;
+        const float g = __bfloat162float(a.dout[idx]);
+        ab = fmaf(g, a.mu[idx], ab);
+        de = fmaf(g, a.o[idx], de);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        ab += __shfl_xor_sync(kFullMask, ab, off);
+        de += __shfl_xor_sync(kFullMask, de, off);
+    }
+    if (lane == 0) a.rs[row] = make_float4(a.lse[row] * kLog2e, a.rbar[row], ab, de);
+}
+
+// ------------------------------------------------------------------------ dK, dV
+template <int D>
+struct KvLayout {
+    static constexpr int NCB = D / 64;
+    static constexpr int OPB = NCB * SUB;                // [128 x D] operand
+    static constexpr int K_OFF = 0, V_OFF = OPB;
+    static constexpr int QR_BYTES = OPB;                 // [Q; rho] rows 0..63 / 64..127
+    static constexpr int DO_BYTES = NCB * SUB64;         // dO [64 x D]
+    static constexpr int STAGE = QR_BYTES + DO_BYTES + 1024;  // + 64 row stats
+    static constexpr int ST_OFF = 2 * OPB;
+    static constexpr int BAR_OFF = ST_OFF + 2 * STAGE;
+    // kv_full, qr_full[2], qr_empty[2], s_full, p_full, o_full
+    static constexpr int NBARS = 8;
+    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    // TMEM columns
+    static constexpr uint32_t SR = 0, DT = 128, DV = 256, DK = 256 + D;
+};
+
+template <int D, bool CAUSAL, bool RHO>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmR,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmO, const BwdArgs a) {
+    using LY = KvLayout<D>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
+    uint64_t* kv_full = bars;
+    uint64_t* qr_full = bars + 1;
+    uint64_t* qr_empty = bars + 3;
+    uint64_t* s_full = bars + 5;
+    uint64_t* p_full = bars + 6;
+    uint64_t* o_full = bars + 7;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    const int kt = blockIdx.x / a.BH;  // causal: the first key tiles see the most queries
+    const int bh = blockIdx.x - kt * a.BH;
+    const int k0 = kt * 128;
+    const int qt0 = CAUSAL ? k0 / 64 : 0;
+    const int n_t = a.n_qt - qt0;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], b == 6 ? 128 : 1);
+        *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&tmQ);
+        if (RHO) tc::prefetch_tmap(&tmR);
+        tc::prefetch_tmap(&tmK);
+        tc::prefetch_tmap(&tmV);
+        tc::prefetch_tmap(&tmO);
+    }
+    if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort_flag != 0;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0 && !skip) {
+            mbar_arrive_expect_tx(kv_full, 2 * LY::OPB);
+            for (int cb = 0; cb < LY::NCB; ++cb) {
+                tc::tma_load_3d(smem + LY::K_OFF + cb * SUB, &tmK, cb * 64, k0, bh, kv_full);
+                tc::tma_load_3d(smem + LY::V_OFF + cb * SUB, &tmV, cb * 64, k0, bh, kv_full);
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int t = 0; t < n_t; ++t) {
+                const int st = t & 1;
+                if (t >= 2 && !mbar_wait(&qr_empty[st], ((t >> 1) - 1) & 1, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
+                const int q0 = (qt0 + t) * 64;
+                const int nrs = min(64, a.L - q0);
+                unsigned char* stage = smem + LY::ST_OFF + st * LY::STAGE;
+                mbar_arrive_expect_tx(&qr_full[st], (RHO ? 2 : 1) * LY::NCB * SUB64 + LY::DO_BYTES +
+                                                        nrs * 16);
+                for (int cb = 0; cb < LY::NCB; ++cb) {
+                    tc::tma_load_3d(stage + cb * SUB, &tmQ, cb * 64, q0, bh, &qr_full[st]);
+                    if (RHO)
+                        tc::tma_load_3d(stage + cb * SUB + SUB64, &tmR, cb * 64, q0, bh, &qr_full[st]);
+                    tc::tma_load_3d(stage + LY::QR_BYTES + cb * SUB64, &tmO, cb * 64, q0, bh,
+                                    &qr_full[st]);
+                }
+                bulk_g2s(stage + LY::QR_BYTES + LY::DO_BYTES, a.rs + (size_t)bh * a.L + q0,
+                         nrs * 16, &qr_full[st]);
+                issued = t + 1;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                mbar_wait(kv_full, 0, &g_bwd_err);
+                for (int t = issued >= 2 ? issued - 2 : 0; t < issued; ++t)
+                    mbar_wait(&qr_full[t & 1], (t >> 1) & 1, &g_bwd_err);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (!skip) {
+            constexpr uint32_t kIdescA = tc::idesc_bf16_f32(128, RHO ? 128 : 64, false);
+            constexpr uint32_t kIdescB = tc::idesc_bf16_f32(128, 64, false);
+            constexpr uint32_t kIdescMN = tc::idesc_bf16_f32(128, D, true);
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t dK = tc::smem_desc_sw128(sbase + LY::K_OFF, 16, 1024);
+            const uint64_t dV = tc::smem_desc_sw128(sbase + LY::V_OFF, 16, 1024);
+            constexpr uint32_t kStStep = LY::STAGE >> 4;
+            bool ok = mbar_wait_warp(kv_full, 0, &g_bwd_err);
+            for (int t = 0; t < n_t && ok; ++t) {
+                const int st = t & 1;
+                if (*abort_flag || !mbar_wait_warp(&qr_full[st], (t >> 1) & 1, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t stb = sbase + LY::ST_OFF;
+                const uint64_t dQR = tc::opaque(tc::smem_desc_sw128(stb, 16, 1024) + st * kStStep);
+                const uint64_t dDO =
+                    tc::opaque(tc::smem_desc_sw128(stb + LY::QR_BYTES, 16, 1024) + st * kStStep);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {  // [S^T | R^T] = K [Q; rho]^T
+                    const uint32_t off = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem + LY::SR, dK + off, dQR + off, kIdescA, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {  // D^T = V dO^T
+                    const uint32_t offA = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
+                    const uint32_t offB = ((kk / 4) * SUB64 + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem + LY::DT, dV + offA, dDO + offB, kIdescB, kk > 0);
+                }
+                tc::commit(s_full);
+                if (!mbar_wait_warp(p_full, t & 1, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                // MN-major views of the same tiles: rows = queries (the K dimension)
+                const uint64_t mQR = tc::opaque(tc::smem_desc_sw128(stb, SUB, 1024) + st * kStStep);
+                const uint64_t mDO =
+                    tc::opaque(tc::smem_desc_sw128(stb + LY::QR_BYTES, SUB64, 1024) + st * kStStep);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {  // dV += W dO
+                    const uint32_t acol = LY::SR + 32 * (kk >> 1) + 8 * (kk & 1);
+                    tc::mma_ts(tmem + LY::DV, tmem + acol, mDO + ((kk * 16 * 128) >> 4), kIdescMN,
+                               (t > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {  // dK += dS Q  (scale folded into dS)
+                    const uint32_t acol = LY::SR + 32 * (kk >> 1) + 16 + 8 * (kk & 1);
+                    tc::mma_ts(tmem + LY::DK, tmem + acol, mQR + ((kk * 16 * 128) >> 4), kIdescMN,
+                               (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (RHO) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {  // dK += dR rho
+                        const uint32_t acol = LY::SR + 64 + 32 * (kk >> 1) + 8 * (kk & 1);
+                        tc::mma_ts(tmem + LY::DK, tmem + acol, mQR + (((64 + kk * 16) * 128) >> 4),
+                                   kIdescMN, 1u);
+                    }
+                }
+                tc::commit(&qr_empty[st]);
+            }
+            tc::commit(o_full);
+            if (!ok) {
+                *abort_flag = 1;
+                mbar_wait_warp(o_full, 0, &g_bwd_err);
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- compute + epilogue
+        const int q4 = warp & 3;
+        const int j = k0 + 32 * q4 + lane;  // this thread's key
+        const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
+        const float qs = a.qscale, scale = a.scale;
+        bool ok = !skip;
+        for (int t = 0; t < n_t && ok; ++t) {
+            const int st = t & 1;
+            const bool got = !*abort_flag && mbar_wait(s_full, t & 1, &g_bwd_err);
+            if (!__all_sync(kFullMask, got)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            const int q0 = (qt0 + t) * 64;
+            const float4* rs = reinterpret_cast<const float4*>(smem + LY::ST_OFF + st * LY::STAGE +
+                                                               LY::QR_BYTES + LY::DO_BYTES);
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                uint32_t sv[32], rv[32], dv[32];
+                tc::tmem_ld32(trow + LY::SR + 32 * c, sv);
+                if (RHO) tc::tmem_ld32(trow + LY::SR + 64 + 32 * c, rv);
+                tc::tmem_ld32(trow + LY::DT + 32 * c, dv);
+                tc::tmem_ld_wait();
+                uint32_t wpk[16], spk[16], rpk[16];
+#pragma unroll
+                for (int y = 0; y < 16; ++y) {
+                    float w2[2], s2[2], r2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int x = 2 * y + e;
+                        const int qi = q0 + 32 * c + x;
+                        const bool valid = qi < a.L && (!CAUSAL || j <= qi);
+                        const float4 z = rs[32 * c + x];  // (lse2, rbar, abar, delta)
+                        const float dd = __uint_as_float(dv[x]);
+                        const float r = RHO ? __uint_as_float(rv[x]) : 0.f;
+                        const float p = fast_exp2(fmaf(__uint_as_float(sv[x]), qs, -z.x));
+                        const float w = p * (1.f + z.y - r);
+                        const float dr = p * (z.z - dd);
+                        const float ds = p * fmaf(dd - z.z, z.y - r, dd - z.w) * scale;
+                        w2[e] = valid ? w : 0.f;
+                        s2[e] = valid ? ds : 0.f;
+                        r2[e] = valid ? dr : 0.f;
+                    }
+                    wpk[y] = tc::pack_bf16(w2[0], w2[1]);
+                    spk[y] = tc::pack_bf16(s2[0], s2[1]);
+                    rpk[y] = tc::pack_bf16(r2[0], r2[1]);
+                }
+                // (columns already read above: W, dS over S^T, dR over R^T)
+                tc::tmem_st16(trow + LY::SR + 32 * c, wpk);
+                tc::tmem_st16(trow + LY::SR + 32 * c + 16, spk);
+                if (RHO) tc::tmem_st16(trow + LY::SR + 64 + 32 * c, rpk);
+            }
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            mbar_arrive(p_full);
+        }
+        const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
+        if (__all_sync(kFullMask, done)) {
+            tc::fence_after_sync();
+            float* dvrow = a.dv + ((size_t)bh * a.L + j) * D;
+            float* dkrow = a.dk + ((size_t)bh * a.L + j) * D;
+#pragma unroll 1
+            for (int b = 0; b < D / 32; ++b) {
+                uint32_t u[32], w[32];
+                tc::tmem_ld32(trow + LY::DV + 32 * b, u);
+                tc::tmem_ld32(trow + LY::DK + 32 * b, w);
+                tc::tmem_ld_wait();
+                if (j < a.L) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 4) {
+                        *reinterpret_cast<float4*>(dvrow + 32 * b + x) =
+                            make_float4(__uint_as_float(u[x]), __uint_as_float(u[x + 1]),
+                                        __uint_as_float(u[x + 2]), __uint_as_float(u[x + 3]));
+                        *reinterpret_cast<float4*>(dkrow + 32 * b + x) =
+                            make_float4(__uint_as_float(w[x]), __uint_as_float(w[x + 1]),
+                                        __uint_as_float(w[x + 2]), __uint_as_float(w[x + 3]));
+                    }
+                }
+            }
+        } else {
+            *abort_flag = 1;
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------------ dQ, drho
+template <int D>
+struct QLayout {
+    static constexpr int NCB = D / 64;
+    static constexpr int OPB = NCB * SUB;
+    static constexpr int QR_OFF = 0;           // stacked [Q; rho] (16-row groups)
+    static constexpr int DO_OFF = OPB;         // stacked [dO; dO]
+    static constexpr int K_OFF = 2 * OPB;      // K ring, 2 stages
+    static constexpr int V_OFF = 4 * OPB;      // V ring, 2 stages
+    static constexpr int BAR_OFF = 6 * OPB;
+    // q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full, p_full, o_full
+    static constexpr int NBARS = 12;
+    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    static constexpr uint32_t SR = 0, DD = 128, O = 256, PK = 384;  // TMEM columns
+};
+
+template <int D, bool CAUSAL, bool RHO>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmR,
+                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmO, const BwdArgs a) {
+    using LY = QLayout<D>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* v_full = bars + 3;
+    uint64_t* k_empty = bars + 5;
+    uint64_t* v_empty = bars + 7;
+    uint64_t* s_full = bars + 9;
+    uint64_t* p_full = bars + 10;
+    uint64_t* o_full = bars + 11;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    const int r_in = blockIdx.x / a.BH;
+    const int bh = blockIdx.x - r_in * a.BH;
+    const int qb = CAUSAL ? a.n_qt - 1 - r_in : r_in;  // causal: heaviest tiles first
+    const int q0 = qb * 64;
+    const int n_all = a.n_kt;
+    const int n_t = CAUSAL ? min(n_all, (q0 + 63) / 128 + 1) : n_all;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], b == 10 ? 128 : 1);
+        *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
+        fence_mbar_init();
+    }
+    if (!RHO && (warp == 2 || warp == 3)) {
+        // no probe: the rho rows of the stacked operand are zero (R = 0)
+        for (int i = threadIdx.x - 64; i < LY::NCB * 64 * 8; i += 64) {
+            const int cb = i / 512, rem = i % 512, g = rem / 128, w = rem % 128;
+            reinterpret_cast<uint4*>(smem + LY::QR_OFF + cb * SUB + (32 * g + 16) * 128)[w] =
+                make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&tmQ);
+        if (RHO) tc::prefetch_tmap(&tmR);
+        tc::prefetch_tmap(&tmK);
+        tc::prefetch_tmap(&tmV);
+        tc::prefetch_tmap(&tmO);
+    }
+    if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort_flag != 0;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0 && !skip) {
+            bool ok = true;
+            int kj = 0, vj = 0;
+            // Q (and rho) once, dO twice: 16-row boxes, NCB * SUB / 2 bytes per tensor copy
+            mbar_arrive_expect_tx(q_full, ((RHO ? 2 : 1) + 2) * LY::NCB * (SUB / 2));
+            for (int cb = 0; cb < LY::NCB; ++cb) {
+                unsigned char* qr = smem + LY::QR_OFF + cb * SUB;
+                unsigned char* d2 = smem + LY::DO_OFF + cb * SUB;
+                for (int g = 0; g < 4; ++g) {
+                    const int row = q0 + 16 * g;
+                    tc::tma_load_3d(qr + (32 * g) * 128, &tmQ, cb * 64, row, bh, q_full);
+                    if (RHO) tc::tma_load_3d(qr + (32 * g + 16) * 128, &tmR, cb * 64, row, bh, q_full);
+                    tc::tma_load_3d(d2 + (32 * g) * 128, &tmO, cb * 64, row, bh, q_full);
+                    tc::tma_load_3d(d2 + (32 * g + 16) * 128, &tmO, cb * 64, row, bh, q_full);
+                }
+            }
+            for (int j = 0; j < n_t && ok; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait(&k_empty[st], ((j >> 1) - 1) & 1, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&k_full[st], LY::OPB);
+                for (int cb = 0; cb < LY::NCB; ++cb)
+                    tc::tma_load_3d(smem + LY::K_OFF + st * LY::OPB + cb * SUB, &tmK, cb * 64, j * 128,
+                                    bh, &k_full[st]);
+                kj = j + 1;
+                if (j >= 2 && !mbar_wait(&v_empty[st], ((j >> 1) - 1) & 1, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&v_full[st], LY::OPB);
+                for (int cb = 0; cb < LY::NCB; ++cb)
+                    tc::tma_load_3d(smem + LY::V_OFF + st * LY::OPB + cb * SUB, &tmV, cb * 64, j * 128,
+                                    bh, &v_full[st]);
+                vj = j + 1;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                mbar_wait(q_full, 0, &g_bwd_err);
+                for (int k = (kj >= 2 ? kj - 2 : 0); k < kj; ++k)
+                    mbar_wait(&k_full[k & 1], (k >> 1) & 1, &g_bwd_err);
+                for (int k = (vj >= 2 ? vj - 2 : 0); k < vj; ++k)
+                    mbar_wait(&v_full[k & 1], (k >> 1) & 1, &g_bwd_err);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (!skip) {
+            constexpr uint32_t kIdesc1 = tc::idesc_bf16_f32(128, 128, false);
+            constexpr uint32_t kIdesc2 = tc::idesc_bf16_f32(128, D, true);
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t dQR = tc::smem_desc_sw128(sbase + LY::QR_OFF, 16, 1024);
+            const uint64_t dDO = tc::smem_desc_sw128(sbase + LY::DO_OFF, 16, 1024);
+            const uint64_t dK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, 16, 1024);
+            const uint64_t dV0 = tc::smem_desc_sw128(sbase + LY::V_OFF, 16, 1024);
+            const uint64_t mK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, SUB, 1024);
+            constexpr uint32_t kOpStep = LY::OPB >> 4;
+            bool ok = mbar_wait_warp(q_full, 0, &g_bwd_err);
+            for (int j = 0; j < n_t && ok; ++j) {
+                const int st = j & 1;
+                if (*abort_flag || !mbar_wait_warp(&k_full[st], (j >> 1) & 1, &g_bwd_err) ||
+                    !mbar_wait_warp(&v_full[st], (j >> 1) & 1, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint64_t dK = tc::opaque(dK0 + st * kOpStep);
+                const uint64_t dV = tc::opaque(dV0 + st * kOpStep);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {  // [S; R] = [Q; rho] K^T
+                    const uint32_t off = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem + LY::SR, dQR + off, dK + off, kIdesc1, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {  // [D; D] = [dO; dO] V^T
+                    const uint32_t off = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem + LY::DD, dDO + off, dV + off, kIdesc1, kk > 0);
+                }
+                tc::commit(s_full);
+                tc::commit(&v_empty[st]);
+                if (!mbar_wait_warp(p_full, j & 1, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint64_t mK = tc::opaque(mK0 + st * kOpStep);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // [dQ; drho] += [dS; dR] K
+                    tc::mma_ts(tmem + LY::O, tmem + LY::PK + 8 * kk, mK + ((kk * 16 * 128) >> 4),
+                               kIdesc2, (j > 0 || kk > 0) ? 1u : 0u);
+                tc::commit(&k_empty[st]);
+            }
+            tc::commit(o_full);
+            if (!ok) {
+                *abort_flag = 1;
+                mbar_wait_warp(o_full, 0, &g_bwd_err);
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- compute + epilogue
+        const int g = warp & 3;
+        const int h = lane >> 4;                       // which half of the keys / columns
+        const int i = q0 + 16 * g + (lane & 15);       // query row
+        const uint32_t rowS = tmem + ((uint32_t)(32 * g) << 16);
+        const uint32_t rowR = tmem + ((uint32_t)(32 * g + 16) << 16);
+        const float qs = a.qscale, scale = a.scale;
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < a.L) z = a.rs[(size_t)bh * a.L + i];
+        bool ok = !skip;
+        for (int j = 0; j < n_t && ok; ++j) {
+            const bool got = !*abort_flag && mbar_wait(s_full, j & 1, &g_bwd_err);
+            if (!__all_sync(kFullMask, got)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int b = 0; b < 2; ++b) {
+                uint32_t sv[32], rv[32], dv[32];
+                tc::tmem_ld32_split<64>(rowS + LY::SR + 32 * b, sv);
+                if (RHO) tc::tmem_ld32_split<64>(rowR + LY::SR + 32 * b, rv);
+                tc::tmem_ld32_split<64>(rowS + LY::DD + 32 * b, dv);
+                tc::tmem_ld_wait();
+                uint32_t spk[16], rpk[16];
+#pragma unroll
+                for (int y = 0; y < 16; ++y) {
+                    float s2[2], r2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int x = 2 * y + e;
+                        const int key = j * 128 + 64 * h + 32 * b + x;
+                        const bool valid = i < a.L && key < a.L && (!CAUSAL || key <= i);
+                        const float dd = __uint_as_float(dv[x]);
+                        const float r = RHO ? __uint_as_float(rv[x]) : 0.f;
+                        const float p = fast_exp2(fmaf(__uint_as_float(sv[x]), qs, -z.x));
+                        const float dr = p * (z.z - dd);
+                        const float ds = p * fmaf(dd - z.z, z.y - r, dd - z.w) * scale;
+                        s2[e] = valid ? ds : 0.f;
+                        r2[e] = valid ? dr : 0.f;
+                    }
+                    spk[y] = tc::pack_bf16(s2[0], s2[1]);
+                    rpk[y] = tc::pack_bf16(r2[0], r2[1]);
+                }
+                // packed operand columns PK..PK+63 (key 2c, 2c+1 at column PK + c); the
+                // dS rows sit in the query lanes, the dR rows in the probe lanes
+                tc::tmem_st16_split<32>(rowS + LY::PK + 16 * b, spk);
+                tc::tmem_st16_split<32>(rowR + LY::PK + 16 * b, rpk);
+            }
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            mbar_arrive(p_full);
+        }
+        const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
+        if (__all_sync(kFullMask, done)) {
+            tc::fence_after_sync();
+            float* qrow = a.dq + ((size_t)bh * a.L + i) * D + h * (D / 2);
+            float* rrow = RHO ? a.drho + ((size_t)bh * a.L + i) * D + h * (D / 2) : nullptr;
+#pragma unroll 1
+            for (int b = 0; b < D / 64; ++b) {
+                uint32_t u[32], w[32];
+                tc::tmem_ld32_split<D / 2>(rowS + LY::O + 32 * b, u);
+                tc::tmem_ld32_split<D / 2>(rowR + LY::O + 32 * b, w);
+                tc::tmem_ld_wait();
+                if (i < a.L) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 4) {
+                        *reinterpret_cast<float4*>(qrow + 32 * b + x) =
+                            make_float4(__uint_as_float(u[x]), __uint_as_float(u[x + 1]),
+                                        __uint_as_float(u[x + 2]), __uint_as_float(u[x + 3]));
+                        if (RHO)
+                            *reinterpret_cast<float4*>(rrow + 32 * b + x) =
+                                make_float4(__uint_as_float(w[x]), __uint_as_float(w[x + 1]),
+                                            __uint_as_float(w[x + 2]), __uint_as_float(w[x + 3]));
+                    }
+                }
+            }
+        } else {
+            *abort_flag = 1;
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------------ host side
+bool make_map(CUtensorMap* m, const void* base, int BH, int L, int D, int box_rows) {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)L, (uint64_t)BH};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)L * D * 2};
+    const uint32_t box[3] = {64, (uint32_t)box_rows, 1};
+    return make_tmap_bf16(m, base, 3, dims, strides, box);
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, int bytes) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D, bool CAUSAL, bool RHO>
+cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const void* k,
+                       const void* v, cudaStream_t stream) {
+    CUtensorMap q64, r64, k128, v128, o64, q16, r16, o16;
+    if (!make_map(&q64, q, a.BH, a.L, D, 64) || !make_map(&k128, k, a.BH, a.L, D, 128) ||
+        !make_map(&v128, v, a.BH, a.L, D, 128) || !make_map(&o64, a.dout, a.BH, a.L, D, 64) ||
+        !make_map(&q16, q, a.BH, a.L, D, 16) || !make_map(&o16, a.dout, a.BH, a.L, D, 16))
+        return cudaErrorInvalidValue;
+    if (RHO) {
+        if (!make_map(&r64, rho, a.BH, a.L, D, 64) || !make_map(&r16, rho, a.BH, a.L, D, 16))
+            return cudaErrorInvalidValue;
+    } else {
+        r64 = q64;
+        r16 = q16;
+    }
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = set_smem(bwd_kv_kernel<D, CAUSAL, RHO>, KvLayout<D>::SMEM_BYTES);
+        if (e == cudaSuccess) e = set_smem(bwd_q_kernel<D, CAUSAL, RHO>, QLayout<D>::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const size_t rows = (size_t)a.BH * a.L;
+    bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
+    bwd_kv_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_kt * a.BH), kThreads,
+                                    KvLayout<D>::SMEM_BYTES, stream>>>(q64, r64, k128, v128, o64, a);
+    bwd_q_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_qt * a.BH), kThreads,
+                                   QLayout<D>::SMEM_BYTES, stream>>>(q16, r16, k128, v128, o16, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t prefill_backward_workspace_bytes(int B, int H, int L) {
+    return (size_t)B * H * L * sizeof(float4);
+}
+
+cudaError_t prefill_backward_launch(const PrefillShape& s, const void* q, const void* rho,
+                                    const void* k, const void* v, const float* o,
+                                    const float* mu, const float* lse, const float* rbar,
+                                    const void* dout, float* dq, float* drho, float* dk,
+                                    float* dv, void* ws, cudaStream_t stream) {
+    BwdArgs a;
+    a.o = o;
+    a.mu = mu;
+    a.dout = static_cast<const __nv_bfloat16*>(dout);
+    a.lse = lse;
+    a.rbar = rbar;
+    a.rs = static_cast<float4*>(ws);
+    a.dq = dq;
+    a.drho = drho;
+    a.dk = dk;
+    a.dv = dv;
+    a.L = s.L;
+    a.BH = s.B * s.H;
+    a.n_kt = (s.L + 127) / 128;
+    a.n_qt = (s.L + 63) / 64;
+    a.scale = s.scale;
+    a.qscale = s.scale * kLog2e;
+    const bool r = rho != nullptr;
+#define PARALLAX_BWD_CASE(DD)                                                                   \
+    if (s.d == DD) {                                                                            \
+        if (s.causal)                                                                           \
+            return r ? launch_all<DD, true, true>(a, q, rho, k, v, stream)                      \
+                     : launch_all<DD, true, false>(a, q, rho, k, v, stream);                    \
+        return r ? launch_all<DD, false, true>(a, q, rho, k, v, stream)                         \
+                 : launch_all<DD, false, false>(a, q, rho, k, v, stream);                       \
+    }
+    PARALLAX_BWD_CASE(64)
+    PARALLAX_BWD_CASE(128)
+#undef PARALLAX_BWD_CASE
+    return cudaErrorInvalidValue;
+}
+
+unsigned prefill_backward_take_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_bwd_err, sizeof(v)) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_bwd_err, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace parallax

@@ -17,6 +17,7 @@ namespace parallax {
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // ----------------------------------------------------------------------------
 // error word: one per translation unit, read and cleared by the host

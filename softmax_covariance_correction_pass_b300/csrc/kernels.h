@@ -50,10 +50,17 @@ cudaError_t prefill_simt_launch(const PrefillShape& s, bool bf16, const void* q,
                                 const void* k, const void* v, float* o, cudaStream_t stream);
 unsigned prefill_simt_take_error();
 
+// Per-row quantities a training forward keeps for the backward pass (all null: none).
+struct TrainStats {
+    float* lse = nullptr;   // [B, H, L] log-sum-exp of the scaled scores (natural log)
+    float* rbar = nullptr;  // [B, H, L] sum_j p_j r_j (0 without the probe)
+    float* mu = nullptr;    // [B, H, L, d] mu_v = sum_j p_j v_j
+};
+
 // bf16 tcgen05 / TMEM / TMA prefill
 cudaError_t prefill_tc_launch(const PrefillShape& s, const void* q, const void* rho,
                               const void* k, const void* v, float* o, int num_sms,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const TrainStats& ts = TrainStats{});
 unsigned prefill_tc_take_error();
 // Chunked prefill: append k_new / v_new [B, H, L, d] to the caches [B, H, Lmax, d] at
 // rows cache_lens[b].., then causal attention of the chunk's queries over the cache.
@@ -61,6 +68,16 @@ cudaError_t prefill_tc_chunk_launch(const PrefillShape& s, const void* q, const 
                                     const void* k_new, const void* v_new, void* k_cache,
                                     void* v_cache, const int32_t* cache_lens, int Lmax, float* o,
                                     int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- prefill backward
+// Row-stats workspace (float4 per query row) the backward needs.
+size_t prefill_backward_workspace_bytes(int B, int H, int L);
+cudaError_t prefill_backward_launch(const PrefillShape& s, const void* q, const void* rho,
+                                    const void* k, const void* v, const float* o,
+                                    const float* mu, const float* lse, const float* rbar,
+                                    const void* dout, float* dq, float* drho, float* dk,
+                                    float* dv, void* ws, cudaStream_t stream);
+unsigned prefill_backward_take_error();
 
 // ---------------------------------------------------------------- tensor maps
 // bf16 tensor of `rank` dims (innermost first; strides in bytes of dims 1..rank-1),

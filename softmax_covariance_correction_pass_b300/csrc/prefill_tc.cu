@@ -106,6 +106,11 @@ struct TcArgs {
     int BH;
     int n_qb;      // query blocks per head
     float qscale;  // scale * log2(e)
+    // training forward (all three set or all null): per-row log-sum-exp of the scaled
+    // scores (natural log) and rbar = sum_j p_j r_j, [B*H, L]; mu_v = sum_j p_j v_j [B*H, L, D]
+    float* lse;
+    float* rbar;
+    float* mu;
 };
 
 // Keys already cached for the sequence of head bh, clamped so that the chunk fits.
@@ -556,7 +561,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<float4*>(orow + 32 * b + x) =
                                 make_float4(out[0], out[1], out[2], out[3]);
                         }
+                        if (a.mu) {
+                            float* mrow = a.mu + ((size_t)bh * a.L + i) * D + h * (D / 2);
+#pragma unroll
+                            for (int x = 0; x < 32; x += 4)
+                                *reinterpret_cast<float4*>(mrow + 32 * b + x) = make_float4(
+                                    __uint_as_float(u[x]) * inv_l, __uint_as_float(u[x + 1]) * inv_l,
+                                    __uint_as_float(u[x + 2]) * inv_l, __uint_as_float(u[x + 3]) * inv_l);
+                        }
                     }
+                }
+                if (a.lse && h == 0 && i < a.L) {
+                    a.lse[(size_t)bh * a.L + i] = (m + __log2f(lt)) * kLn2;
+                    a.rbar[(size_t)bh * a.L + i] = At * inv_l + c;
                 }
             } else {
                 *abort_flag = 1;
@@ -645,11 +662,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::tmem_ld_wait();
                     if (i < a.L) {
 #pragma unroll
-                        for (int x = 0; x < 32; x += 4)
-                            *reinterpret_cast<float4*>(orow + 32 * b + x) = make_float4(
+                        for (int x = 0; x < 32; x += 4) {
+                            const float4 v4 = make_float4(
                                 __uint_as_float(u[x]) * inv_l, __uint_as_float(u[x + 1]) * inv_l,
                                 __uint_as_float(u[x + 2]) * inv_l, __uint_as_float(u[x + 3]) * inv_l);
+                            *reinterpret_cast<float4*>(orow + 32 * b + x) = v4;
+                            if (a.mu)
+                                *reinterpret_cast<float4*>(a.mu + ((size_t)bh * a.L + i) * D + 32 * b + x) = v4;
+                        }
                     }
+                }
+                if (a.lse && i < a.L) {
+                    a.lse[(size_t)bh * a.L + i] = (m + __log2f(l)) * kLn2;
+                    a.rbar[(size_t)bh * a.L + i] = 0.f;
                 }
             } else {
                 *abort_flag = 1;
@@ -695,10 +720,11 @@ cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mr, const CUtensorM
 template <int D, bool RHO>
 cudaError_t launch_d(const PrefillShape& s, const CUtensorMap& mq, const CUtensorMap& mr,
                      const CUtensorMap& mk, const CUtensorMap& mv, float* o,
-                     const int32_t* cache_lens, int Lcap, cudaStream_t stream) {
+                     const int32_t* cache_lens, int Lcap, const TrainStats& ts,
+                     cudaStream_t stream) {
     using LY = PairLayout<D, RHO>;
-    const TcArgs a{o,   cache_lens, s.L, Lcap, s.H, s.B * s.H, (s.L + LY::BLOCK - 1) / LY::BLOCK,
-                   s.scale * kLog2e};
+    const TcArgs a{o,      cache_lens, s.L,    Lcap,  s.H,  s.B * s.H, (s.L + LY::BLOCK - 1) / LY::BLOCK,
+                   s.scale * kLog2e, ts.lse, ts.rbar, ts.mu};
     return s.causal ? launch<D, true, RHO>(mq, mr, mk, mv, a, stream)
                     : launch<D, false, RHO>(mq, mr, mk, mv, a, stream);
 }
@@ -706,7 +732,7 @@ cudaError_t launch_d(const PrefillShape& s, const CUtensorMap& mq, const CUtenso
 // Query-side maps (q, rho: L rows per head) and key-side maps (k, v: Lcap rows per head).
 cudaError_t launch_any(const PrefillShape& s, const void* q, const void* rho, const void* k,
                        const void* v, float* o, const int32_t* cache_lens, int Lcap,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const TrainStats& ts = TrainStats{}) {
     const int BH = s.B * s.H;
     CUtensorMap mq, mr, mk, mv;
     if (!make_map(&mk, k, BH, Lcap, s.d) || !make_map(&mv, v, BH, Lcap, s.d))
@@ -715,14 +741,14 @@ cudaError_t launch_any(const PrefillShape& s, const void* q, const void* rho, co
         // correction path: query and probe maps use 16-row boxes (stacked operand)
         if (!make_map(&mq, q, BH, s.L, s.d, 16) || !make_map(&mr, rho, BH, s.L, s.d, 16))
             return cudaErrorInvalidValue;
-        if (s.d == 64) return launch_d<64, true>(s, mq, mr, mk, mv, o, cache_lens, Lcap, stream);
-        if (s.d == 128) return launch_d<128, true>(s, mq, mr, mk, mv, o, cache_lens, Lcap, stream);
+        if (s.d == 64) return launch_d<64, true>(s, mq, mr, mk, mv, o, cache_lens, Lcap, ts, stream);
+        if (s.d == 128) return launch_d<128, true>(s, mq, mr, mk, mv, o, cache_lens, Lcap, ts, stream);
         return cudaErrorInvalidValue;
     }
     if (!make_map(&mq, q, BH, s.L, s.d)) return cudaErrorInvalidValue;
     mr = mq;  // unused
-    if (s.d == 64) return launch_d<64, false>(s, mq, mr, mk, mv, o, cache_lens, Lcap, stream);
-    if (s.d == 128) return launch_d<128, false>(s, mq, mr, mk, mv, o, cache_lens, Lcap, stream);
+    if (s.d == 64) return launch_d<64, false>(s, mq, mr, mk, mv, o, cache_lens, Lcap, ts, stream);
+    if (s.d == 128) return launch_d<128, false>(s, mq, mr, mk, mv, o, cache_lens, Lcap, ts, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -767,8 +793,8 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4* __restrict__ k
 
 cudaError_t prefill_tc_launch(const PrefillShape& s, const void* q, const void* rho,
                               const void* k, const void* v, float* o, int /*num_sms*/,
-                              cudaStream_t stream) {
-    return launch_any(s, q, rho, k, v, o, nullptr, s.L, stream);
+                              cudaStream_t stream, const TrainStats& ts) {
+    return launch_any(s, q, rho, k, v, o, nullptr, s.L, stream, ts);
 }
 
 cudaError_t prefill_tc_chunk_launch(const PrefillShape& s, const void* q, const void* rho,
