@@ -309,3 +309,63 @@ def prefill_backward(q, rho, k, v, do, causal: bool = True, scale: float | None 
             drho[b, h] = dR @ kh
             dk[b, h] = scale * (dS.T @ qh) + dR.T @ rh
     return dq, drho, dk, dv
+
+
+def conjugate_gradient(A, b, iters: int, tol: float = 0.0):
+    """Plain conjugate gradient for a symmetric positive (semi)definite A, from x = 0:
+    r = b, p = r; each step a = (r.r)/(p.A p), x += a p, r -= a A p, p = r + (r'.r')/(r.r) p.
+    Stops after `iters` steps or once |r| <= tol |b|."""
+    x = np.zeros_like(b)
+    r = b.copy()
+    p = r.copy()
+    rs = float(r @ r)
+    stop = (tol * float(np.sqrt(b @ b))) ** 2
+    for _ in range(iters):
+        if rs <= stop or rs == 0.0:
+            break
+        Ap = A @ p
+        alpha = rs / float(p @ Ap)
+        x += alpha * p
+        r -= alpha * Ap
+        rs_new = float(r @ r)
+        p = r + (rs_new / rs) * p
+        rs = rs_new
+    return x
+
+
+def lla_decode(q, k_cache, v_cache, seqlens, scale: float | None = None, iters: int | None = None,
+               tol: float = 0.0):
+    """Exact local linear attention for one query token per (b, h), the method the Parallax
+    probe replaces (the pages: Parallax keeps LLA's covariance correction but swaps its
+    per-query solve for the learned probe W_R x).
+
+    With softmax weights p_j over the sequence's keys, mu_k = sum p k, mu_v = sum p v and
+    Sigma_kk = sum_j p_j (k_j - mu_k)(k_j - mu_k)^T, the probe is the solution of
+    Sigma_kk rho = mu_k - q, found by conjugate gradient (conjugate_gradient, `iters`
+    steps, default d: exact in exact arithmetic); the output is the Parallax output with
+    that probe, o = mu_v - C^T rho.  Returns (o [B, H, d], rho [B, H, d]).  A sequence
+    with no keys gives o = 0 and rho = 0."""
+    q, kc, vc = _f64(q), _f64(k_cache), _f64(v_cache)
+    if hasattr(seqlens, "detach"):
+        seqlens = seqlens.detach().cpu().numpy()
+    B, H, Lmax, d = kc.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    if iters is None:
+        iters = d
+    rho = np.zeros((B, H, d))
+    for b in range(B):
+        n = int(seqlens[b])
+        if n == 0:
+            continue
+        for h in range(H):
+            K = kc[b, h, :n]
+            s = scale * (K @ q[b, h])
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            mu_k = p @ K
+            Kc = K - mu_k
+            sigma = (Kc * p[:, None]).T @ Kc
+            rho[b, h] = conjugate_gradient(sigma, mu_k - q[b, h], iters, tol)
+    o = decode(q, rho, kc, vc, seqlens, scale=scale)
+    return o, rho
