@@ -747,6 +747,21 @@ def run_serving(args):
     rows.append({"case": f"chunked prefill B={B} H={H} cached={off} chunk={Lq}", "ms": ms,
                  "TFLOP/s": flops / ms / 1e9, "frac_of_tensor_peak_burst":
                      flops / ms / 1e9 / peaks["bf16_tflops"], "tokens_per_s": B * Lq / (ms * 1e-3)})
+    del full, kc, vc, qn, rn, kn, vn, o
+    torch.cuda.empty_cache()
+    # exact local linear attention decode (comparison workload) at the uniform decode shape
+    dc = configs.DECODE_UNIFORM
+    inp = configs.decode_uniform_inputs(dev)
+    B, H, n = dc["B"], dc["H"], dc["ctx"]
+    ms = timed(lambda: px.parallax_lla_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens), 5)
+    gram = 2.0 * d * d * n * B * H        # p-weighted second moment of the keys
+    flops = gram + 2.0 * d * n * B * H + 8.0 * d * n * B * H  # + scores + the Parallax decode pass
+    fp32_peak = 148 * 128 * 2 * 2.032e9 / 1e12  # FMA lanes x 2 flop x max SM clock
+    rows.append({"case": f"exact LLA decode B={B} H={H} ctx={n} (CG probe + Parallax decode)",
+                 "ms": ms, "TFLOP/s": flops / ms / 1e9, "bound": "alu",
+                 "frac_of_fp32_fma_peak": flops / ms / 1e9 / fp32_peak,
+                 "fp32_fma_peak_tflops": fp32_peak, "tokens_per_s": B / (ms * 1e-3),
+                 "vs_parallax_decode": "see the decode line of the step"})
     for r in rows:
         print(json.dumps(r), flush=True)
     return 0

@@ -197,6 +197,26 @@ int parallax_attn_decode_paged(const void* q, const void* rho, const void* k_pag
                                cudaStream_t stream);
 
 /*
+ * Exact local linear attention (LLA) decode, the method whose per-query solve the
+ * Parallax probe replaces (the pages: Parallax keeps LLA's covariance correction
+ * and swaps the solve for rho = W_R x).  For one query token per (b, h):
+ *   p_j = softmax_j(q.k_j / sqrt(d)),  mu_k = sum p k,
+ *   Sigma_kk = sum_j p_j (k_j - mu_k)(k_j - mu_k)^T,
+ *   rho = Sigma_kk^-1 (mu_k - q)  by conjugate gradient from rho = 0 (cg_iters
+ *         steps, 0 = d; it also stops at a relative residual of 1e-6),
+ *   o   = mu_v - C^T rho  (parallax_attn_decode with that probe, rounded to bf16).
+ *   q                 : bf16 [B, H, d]
+ *   k_cache, v_cache  : bf16 [B, H, Lmax, d];  seqlens: int32 [B] on the device
+ *   o                 : fp32 [B, H, d];  rho: fp32 [B, H, d] (the solved probes)
+ * One CTA per (b, h) forms Sigma_kk in fp32 (compute-bound: d^2 multiply-adds
+ * per key) and runs the CG in shared memory.  Uses a library-owned workspace of
+ * B*H*d*2 bytes plus the decode workspace (same rules as parallax_attn_decode).
+ */
+int parallax_lla_decode(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* seqlens, void* o, float* rho, int B, int H, int Lmax,
+                        int d, int cg_iters, cudaStream_t stream);
+
+/*
  * parallax_attn_decode without any device allocation (bf16 inputs, fp32 o).
  * This entry point has no counterpart in the Parallax paper; it exists for
  * callers that cannot let a library call cudaMalloc -- serving engines that

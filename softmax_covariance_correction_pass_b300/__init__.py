@@ -55,6 +55,7 @@ def load_library() -> ctypes.CDLL:
     lib.parallax_attn_prefill_train.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                 i32, f32, vp]
     lib.parallax_attn_prefill_backward.argtypes = [vp] * 13 + [i32] * 5 + [f32, vp]
+    lib.parallax_lla_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
     lib.parallax_attn_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                                 i32, i32, f32, vp]
     lib.parallax_attn_decode_gqa.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
@@ -71,6 +72,7 @@ def load_library() -> ctypes.CDLL:
                  "parallax_attn_qkvr_projection", "parallax_attn_decode_gqa",
                  "parallax_attn_decode_paged", "parallax_attn_prefill_chunk",
                  "parallax_attn_prefill_train", "parallax_attn_prefill_backward",
+                 "parallax_lla_decode",
                  "parallax_attn_decode_f32", "parallax_attn_decode_chunk_keys",
                  "parallax_attn_set_decode_chunk_keys", "parallax_attn_release_workspace",
                  "parallax_check_device_error", "parallax_version"):
@@ -276,6 +278,29 @@ def parallax_attn_decode_paged(q, rho, k_pages, v_pages, block_table, seqlens, o
     return o
 
 
+def parallax_lla_decode(q, k_cache, v_cache, seqlens, o=None, rho=None, cg_iters: int = 0,
+                        stream=None):
+    """Exact local linear attention decode (the per-query solve the Parallax probe replaces):
+    q bf16 [B, H, d], caches bf16 [B, H, Lmax, d], seqlens int32 [B].  Returns (o, rho),
+    fp32 [B, H, d]: rho = Sigma_kk^-1 (mu_k - q) by conjugate gradient (cg_iters steps,
+    0 = d), o = the Parallax decode with that probe."""
+    B, H, Lmax, d = k_cache.shape
+    _need(q, "q", torch.bfloat16, (B, H, d))
+    _need(k_cache, "k_cache", torch.bfloat16, (B, H, Lmax, d))
+    _need(v_cache, "v_cache", torch.bfloat16, (B, H, Lmax, d))
+    _need(seqlens, "seqlens", torch.int32, (B,))
+    if o is None:
+        o = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    if rho is None:
+        rho = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.float32, (B, H, d))
+    _need(rho, "rho", torch.float32, (B, H, d))
+    _check(load_library().parallax_lla_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o), _ptr(rho), B, H, Lmax, d,
+        int(cg_iters), _stream(stream)))
+    return o, rho
+
+
 def parallax_attn_decode_noalloc(q, rho, k_cache, v_cache, seqlens, o, stream=None):
     """parallax_attn_decode (bf16) with the split-KV partials in the library's fixed
     device array: the call allocates nothing (``o`` must be supplied)."""
@@ -362,4 +387,5 @@ decode_gqa = parallax_attn_decode_gqa
 prefill_chunk = parallax_attn_prefill_chunk
 prefill_train = parallax_attn_prefill_train
 prefill_backward = parallax_attn_prefill_backward
+lla_decode = parallax_lla_decode
 decode_paged = parallax_attn_decode_paged

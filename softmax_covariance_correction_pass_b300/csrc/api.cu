@@ -44,6 +44,8 @@ struct DeviceState {
     size_t ws_bytes = 0;
     void* bws = nullptr;  // prefill backward row statistics
     size_t bws_bytes = 0;
+    void* lws = nullptr;  // exact-LLA probes in bf16
+    size_t lws_bytes = 0;
     int num_sms = 0;
 };
 
@@ -425,6 +427,32 @@ int parallax_attn_qkvr_projection(const void* x, const void* w, void* q, void* k
     return succeed();
 }
 
+int parallax_lla_decode(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* seqlens, void* o, float* rho, int B, int H, int Lmax,
+                        int d, int cg_iters, cudaStream_t stream) {
+    int rc = validate_common(q, k_cache, v_cache, o, rho, B, H, Lmax, d, "Lmax");
+    if (rc != PARALLAX_OK) return rc;
+    if (!seqlens || !rho) return fail(PARALLAX_ERR_INVALID, "null seqlens or rho pointer");
+    if (cg_iters < 0) return fail(PARALLAX_ERR_INVALID, "cg_iters=%d must be >= 0", cg_iters);
+    int dev = 0;
+    DeviceState* ds = device_state(&dev);
+    if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
+    void* rb = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState& st = g_dev[dev];
+        rc = grow(st.lws, st.lws_bytes, (size_t)B * H * d * 2, "LLA workspace");
+        if (rc != PARALLAX_OK) return rc;
+        rb = st.lws;
+    }
+    cudaError_t e = parallax::lla_probe_launch(q, k_cache, seqlens, rho, rb, B, H, Lmax, d,
+                                               cg_iters > 0 ? cg_iters : d, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "LLA probe launch");
+    // the output: the Parallax decode with the solved probe
+    const parallax::DecodePlan plan = make_plan(B, H, H, Lmax, d, ds->num_sms);
+    return decode_run(plan, dev, ds, q, rb, k_cache, v_cache, seqlens, o, stream, true, nullptr);
+}
+
 int parallax_attn_decode_chunk_keys(int B, int H, int Lmax, int d, int elem_bytes) {
     if (B <= 0 || H <= 0 || Lmax <= 0)
         return fail(PARALLAX_ERR_INVALID, "B, H, Lmax must be >= 1");
@@ -469,6 +497,12 @@ int parallax_attn_release_workspace(void) {
         g_dev[dev].bws_bytes = 0;
         if (e != cudaSuccess) return cuda_fail(e, "workspace free");
     }
+    if ((int)g_dev.size() > dev && g_dev[dev].lws) {
+        e = cudaFree(g_dev[dev].lws);
+        g_dev[dev].lws = nullptr;
+        g_dev[dev].lws_bytes = 0;
+        if (e != cudaSuccess) return cuda_fail(e, "workspace free");
+    }
     return succeed();
 }
 
@@ -479,7 +513,7 @@ int parallax_check_device_error(cudaStream_t stream, unsigned int* bits) {
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     const unsigned v = parallax::decode_take_error() | parallax::prefill_simt_take_error() |
                        parallax::prefill_tc_take_error() | parallax::proj_tc_take_error() |
-                       parallax::prefill_backward_take_error();
+                       parallax::prefill_backward_take_error() | parallax::lla_take_error();
     if (bits) *bits = v;
     if (v) return fail(PARALLAX_ERR_DEVICE, "device error word 0x%x", v);
     return succeed();

@@ -79,6 +79,13 @@ cudaError_t prefill_backward_launch(const PrefillShape& s, const void* q, const 
                                     float* dv, void* ws, cudaStream_t stream);
 unsigned prefill_backward_take_error();
 
+// ---------------------------------------------------------------- exact LLA decode
+// Probe rho = Sigma_kk^-1 (mu_k - q) per (b, h) by conjugate gradient (fp32 and bf16 copies).
+cudaError_t lla_probe_launch(const void* q, const void* kc, const int32_t* seqlens, float* rho,
+                             void* rho_bf16, int B, int H, int Lmax, int d, int iters,
+                             cudaStream_t stream);
+unsigned lla_take_error();
+
 // ---------------------------------------------------------------- tensor maps
 // bf16 tensor of `rank` dims (innermost first; strides in bytes of dims 1..rank-1),
 // box `box`, 128-byte swizzle, out-of-range elements read as zero.

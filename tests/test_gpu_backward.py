@@ -25,8 +25,9 @@ def assert_grad(got, ref, what):
     rel, mx = errors(got, ref)
     scale = float(np.abs(ref).max())
     if scale == 0.0:
-        # an exactly-zero gradient (one key per row: dq = 0); fp32 rounding only
-        assert mx <= 1e-5, f"{what}: zero gradient expected, max-abs {mx:.3e}"
+        # an exactly-zero gradient (one key per row: dq = drho = 0): only rounding, of
+        # a p (abar - D) difference of O(1) terms times O(1) keys
+        assert mx <= 1e-4, f"{what}: zero gradient expected, max-abs {mx:.3e}"
         return rel, mx
     assert rel <= 1e-2 and mx <= 2e-2 * scale, \
         f"{what}: rel-L2 {rel:.3e} (<= 1e-2), max-abs {mx:.3e} (<= {2e-2 * scale:.3e})"

@@ -1,0 +1,56 @@
+"""GPU parity of the exact local linear attention (LLA) decode against the fp64
+oracle (conjugate gradient run to convergence: d steps).
+
+The GPU forms Sigma_kk in fp32, runs CG in fp32 to a relative residual of 1e-6
+(or d steps), rounds the probe to bf16 for the Parallax decode pass.  The
+probe is compared at rel-L2 <= 1e-3 (CG residual 1e-6 times the condition
+number of Sigma_kk, which is below 25 for these draws, plus fp32 rounding of
+the d x d moments), the output at the bf16 criterion (rel-L2 <= 1e-2,
+max-abs <= 2e-2).  Sequences are long enough that Sigma_kk has full rank
+(LLA is undefined otherwise).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import softmax_covariance_correction_pass_b300 as px
+from softmax_covariance_correction_pass_b300 import configs
+from parity_util import assert_bf16, errors
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("d,sl", [(128, [1000, 600, 0]), (64, [300, 1000, 517])])
+def test_lla_matches_oracle(d, sl):
+    inp = configs.decode_inputs(3, 4, d, sl, 1000, seed=d, device=DEV)
+    o, rho = px.parallax_lla_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens)
+    torch.cuda.synchronize()
+    assert px.parallax_check_device_error() == 0
+    ro, rr = oracle.lla_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens)
+    rel, _ = errors(rho, rr)
+    assert rel <= 1e-3, f"probe rel-L2 {rel:.3e}"
+    assert_bf16(o, ro, f"lla o d={d}")
+    for b, n in enumerate(sl):
+        if n == 0:
+            assert torch.all(o[b] == 0) and torch.all(rho[b] == 0)
+
+
+def test_lla_decode_layer_size_sampled():
+    """The uniform decode workload's shape (B=64, H=16, d=128, 8192 keys): 32
+    sampled heads against the oracle."""
+    inp = configs.decode_uniform_inputs(DEV)
+    o, rho = px.parallax_lla_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens)
+    torch.cuda.synchronize()
+    assert px.parallax_check_device_error() == 0
+    rng = np.random.default_rng(1)
+    bs = rng.choice(64, 8, replace=False)
+    for b in bs:
+        for h in rng.choice(16, 4, replace=False):
+            sl = (slice(int(b), int(b) + 1), slice(int(h), int(h) + 1))
+            ro, rr = oracle.lla_decode(inp.q[sl], inp.k_cache[sl], inp.v_cache[sl],
+                                       inp.seqlens[int(b):int(b) + 1])
+            rel, _ = errors(rho[sl], rr)
+            assert rel <= 1e-3, f"probe b={b} h={h} rel-L2 {rel:.3e}"
+            assert_bf16(o[sl], ro, f"lla o b={b} h={h}")
