@@ -33,7 +33,10 @@ namespace {
 
 __device__ unsigned g_bwd_err = 0;
 
-constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-3 set-up, warps 4-7 compute
+// warp 0 TMA, warp 1 MMA, warps 2-3 set-up, warps 4-11 compute: two warps per TMEM
+// lane quarter, each taking half of the columns of every tile
+constexpr int kThreads = 384;
+constexpr int kComputeThreads = 256;
 constexpr int SUB = 128 * 128;  // [128 rows x 64 columns] bf16, 128-byte swizzled
 constexpr int SUB64 = 64 * 128; // [64 rows x 64 columns]
 
@@ -59,6 +62,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Shared-memory load the compiler may not hoist or merge (keeps the per-query
+// statistics out of registers until the moment they are used).
+__device__ __forceinline__ float lds(const float* p) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(p)));
+    return v;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -133,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_t = a.n_qt - qt0;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], b == 6 ? 128 : 1);
+        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], b == 6 ? kComputeThreads : 1);
         *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
         fence_mbar_init();
     }
@@ -264,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- compute + epilogue
         const int q4 = warp & 3;
+        const int c = (warp - 4) >> 2;      // which 32 queries of every 64-query tile
         const int j = k0 + 32 * q4 + lane;  // this thread's key
         const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
         const float qs = a.qscale, scale = a.scale;
@@ -276,44 +288,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc::fence_after_sync();
-            const int q0 = (qt0 + t) * 64;
-            const float4* rs = reinterpret_cast<const float4*>(smem + LY::ST_OFF + st * LY::STAGE +
-                                                               LY::QR_BYTES + LY::DO_BYTES);
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                uint32_t sv[32], rv[32], dv[32];
-                tc::tmem_ld32(trow + LY::SR + 32 * c, sv);
-                if (RHO) tc::tmem_ld32(trow + LY::SR + 64 + 32 * c, rv);
-                tc::tmem_ld32(trow + LY::DT + 32 * c, dv);
-                tc::tmem_ld_wait();
-                uint32_t wpk[16], spk[16], rpk[16];
+            const int q0 = (qt0 + t) * 64 + 32 * c;
+            // row statistics of this warp's 32 queries: (lse2, rbar, abar, delta) each
+            const float* rs = reinterpret_cast<const float*>(
+                                  smem + LY::ST_OFF + st * LY::STAGE + LY::QR_BYTES + LY::DO_BYTES) +
+                              4 * 32 * c;
+            uint32_t sv[32], rv[32], dv[32];
+            tc::tmem_ld32(trow + LY::SR + 32 * c, sv);
+            if (RHO) tc::tmem_ld32(trow + LY::SR + 64 + 32 * c, rv);
+            tc::tmem_ld32(trow + LY::DT + 32 * c, dv);
+            tc::tmem_ld_wait();
+            // p in place of s; queries past L or (causal) before this key get no weight.
+            // The row statistics of queries past L were not loaded: they are never read.
+            const int nvalid = min(32, a.L - q0);
+            uint32_t vmask = nvalid >= 32 ? 0xffffffffu : ((1u << nvalid) - 1u);
+            if (CAUSAL && j > q0) vmask &= j - q0 >= 32 ? 0u : ~((1u << (j - q0)) - 1u);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                const bool valid = (vmask >> x) & 1u;
+                const float p = fast_exp2(fmaf(__uint_as_float(sv[x]), qs, valid ? -lds(rs + 4 * x) : 0.f));
+                sv[x] = __float_as_uint(valid ? p : 0.f);
+            }
+            uint32_t pk[16];
+            // W = p (1 + rbar - r)  -> over the S^T columns just read
+#pragma unroll
+            for (int y = 0; y < 16; ++y) {
+                float w2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int x = 2 * y + e;
+                    const float r = RHO ? __uint_as_float(rv[x]) : 0.f;
+                    const float rb = (vmask >> x) & 1u ? lds(rs + 4 * x + 1) : 0.f;
+                    w2[e] = __uint_as_float(sv[x]) * (1.f + rb - r);
+                }
+                pk[y] = tc::pack_bf16(w2[0], w2[1]);
+            }
+            tc::tmem_st16(trow + LY::SR + 32 * c, pk);
+            // dS = scale p ((D - abar)(rbar - r) + D - delta)
+#pragma unroll
+            for (int y = 0; y < 16; ++y) {
+                float s2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int x = 2 * y + e;
+                    const bool v = (vmask >> x) & 1u;
+                    const float zy = v ? lds(rs + 4 * x + 1) : 0.f;
+                    const float zz = v ? lds(rs + 4 * x + 2) : 0.f;
+                    const float zw = v ? lds(rs + 4 * x + 3) : 0.f;
+                    const float dd = __uint_as_float(dv[x]);
+                    const float r = RHO ? __uint_as_float(rv[x]) : 0.f;
+                    s2[e] = __uint_as_float(sv[x]) * fmaf(dd - zz, zy - r, dd - zw) * scale;
+                }
+                pk[y] = tc::pack_bf16(s2[0], s2[1]);
+            }
+            tc::tmem_st16(trow + LY::SR + 32 * c + 16, pk);
+            if (RHO) {
+                // dR = p (abar - D)  -> over the R^T columns just read
 #pragma unroll
                 for (int y = 0; y < 16; ++y) {
-                    float w2[2], s2[2], r2[2];
+                    float r2[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int x = 2 * y + e;
-                        const int qi = q0 + 32 * c + x;
-                        const bool valid = qi < a.L && (!CAUSAL || j <= qi);
-                        const float4 z = rs[32 * c + x];  // (lse2, rbar, abar, delta)
-                        const float dd = __uint_as_float(dv[x]);
-                        const float r = RHO ? __uint_as_float(rv[x]) : 0.f;
-                        const float p = fast_exp2(fmaf(__uint_as_float(sv[x]), qs, -z.x));
-                        const float w = p * (1.f + z.y - r);
-                        const float dr = p * (z.z - dd);
-                        const float ds = p * fmaf(dd - z.z, z.y - r, dd - z.w) * scale;
-                        w2[e] = valid ? w : 0.f;
-                        s2[e] = valid ? ds : 0.f;
-                        r2[e] = valid ? dr : 0.f;
+                        const float ab = (vmask >> x) & 1u ? lds(rs + 4 * x + 2) : 0.f;
+                        r2[e] = __uint_as_float(sv[x]) * (ab - __uint_as_float(dv[x]));
                     }
-                    wpk[y] = tc::pack_bf16(w2[0], w2[1]);
-                    spk[y] = tc::pack_bf16(s2[0], s2[1]);
-                    rpk[y] = tc::pack_bf16(r2[0], r2[1]);
+                    pk[y] = tc::pack_bf16(r2[0], r2[1]);
                 }
-                // (columns already read above: W, dS over S^T, dR over R^T)
-                tc::tmem_st16(trow + LY::SR + 32 * c, wpk);
-                tc::tmem_st16(trow + LY::SR + 32 * c + 16, spk);
-                if (RHO) tc::tmem_st16(trow + LY::SR + 64 + 32 * c, rpk);
+                tc::tmem_st16(trow + LY::SR + 64 + 32 * c, pk);
             }
             tc::tmem_st_wait();
             tc::fence_before_sync();
@@ -322,24 +364,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
         if (__all_sync(kFullMask, done)) {
             tc::fence_after_sync();
-            float* dvrow = a.dv + ((size_t)bh * a.L + j) * D;
-            float* dkrow = a.dk + ((size_t)bh * a.L + j) * D;
+            // warps 4-7 store dV, warps 8-11 dK
+            float* orow = (c == 0 ? a.dv : a.dk) + ((size_t)bh * a.L + j) * D;
+            const uint32_t col = c == 0 ? LY::DV : LY::DK;
 #pragma unroll 1
             for (int b = 0; b < D / 32; ++b) {
-                uint32_t u[32], w[32];
-                tc::tmem_ld32(trow + LY::DV + 32 * b, u);
-                tc::tmem_ld32(trow + LY::DK + 32 * b, w);
+                uint32_t u[32];
+                tc::tmem_ld32(trow + col + 32 * b, u);
                 tc::tmem_ld_wait();
                 if (j < a.L) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 4) {
-                        *reinterpret_cast<float4*>(dvrow + 32 * b + x) =
+                    for (int x = 0; x < 32; x += 4)
+                        *reinterpret_cast<float4*>(orow + 32 * b + x) =
                             make_float4(__uint_as_float(u[x]), __uint_as_float(u[x + 1]),
                                         __uint_as_float(u[x + 2]), __uint_as_float(u[x + 3]));
-                        *reinterpret_cast<float4*>(dkrow + 32 * b + x) =
-                            make_float4(__uint_as_float(w[x]), __uint_as_float(w[x + 1]),
-                                        __uint_as_float(w[x + 2]), __uint_as_float(w[x + 3]));
-                    }
                 }
             }
         } else {
@@ -401,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_t = CAUSAL ? min(n_all, (q0 + 63) / 128 + 1) : n_all;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], b == 10 ? 128 : 1);
+        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], b == 10 ? kComputeThreads : 1);
         *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
         fence_mbar_init();
     }
@@ -532,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- compute + epilogue
         const int g = warp & 3;
+        const int bb = (warp - 4) >> 2;               // which 32-key block of each half
         const int h = lane >> 4;                       // which half of the keys / columns
         const int i = q0 + 16 * g + (lane & 15);       // query row
         const uint32_t rowS = tmem + ((uint32_t)(32 * g) << 16);
@@ -547,38 +586,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc::fence_after_sync();
-#pragma unroll 1
-            for (int b = 0; b < 2; ++b) {
-                uint32_t sv[32], rv[32], dv[32];
-                tc::tmem_ld32_split<64>(rowS + LY::SR + 32 * b, sv);
-                if (RHO) tc::tmem_ld32_split<64>(rowR + LY::SR + 32 * b, rv);
-                tc::tmem_ld32_split<64>(rowS + LY::DD + 32 * b, dv);
-                tc::tmem_ld_wait();
-                uint32_t spk[16], rpk[16];
+            uint32_t sv[32], rv[32], dv[32];
+            tc::tmem_ld32_split<64>(rowS + LY::SR + 32 * bb, sv);
+            if (RHO) tc::tmem_ld32_split<64>(rowR + LY::SR + 32 * bb, rv);
+            tc::tmem_ld32_split<64>(rowS + LY::DD + 32 * bb, dv);
+            tc::tmem_ld_wait();
+            const int k0 = j * 128 + 64 * h + 32 * bb;
+            uint32_t spk[16], rpk[16];
 #pragma unroll
-                for (int y = 0; y < 16; ++y) {
-                    float s2[2], r2[2];
+            for (int y = 0; y < 16; ++y) {
+                float s2[2], r2[2];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int x = 2 * y + e;
-                        const int key = j * 128 + 64 * h + 32 * b + x;
-                        const bool valid = i < a.L && key < a.L && (!CAUSAL || key <= i);
-                        const float dd = __uint_as_float(dv[x]);
-                        const float r = RHO ? __uint_as_float(rv[x]) : 0.f;
-                        const float p = fast_exp2(fmaf(__uint_as_float(sv[x]), qs, -z.x));
-                        const float dr = p * (z.z - dd);
-                        const float ds = p * fmaf(dd - z.z, z.y - r, dd - z.w) * scale;
-                        s2[e] = valid ? ds : 0.f;
-                        r2[e] = valid ? dr : 0.f;
-                    }
-                    spk[y] = tc::pack_bf16(s2[0], s2[1]);
-                    rpk[y] = tc::pack_bf16(r2[0], r2[1]);
+                for (int e = 0; e < 2; ++e) {
+                    const int x = 2 * y + e;
+                    const int key = k0 + x;
+                    const bool valid = i < a.L && key < a.L && (!CAUSAL || key <= i);
+                    const float dd = __uint_as_float(dv[x]);
+                    const float r = RHO ? __uint_as_float(rv[x]) : 0.f;
+                    const float p = fast_exp2(fmaf(__uint_as_float(sv[x]), qs, -z.x));
+                    const float dr = p * (z.z - dd);
+                    const float ds = p * fmaf(dd - z.z, z.y - r, dd - z.w) * scale;
+                    s2[e] = valid ? ds : 0.f;
+                    r2[e] = valid ? dr : 0.f;
                 }
-                // packed operand columns PK..PK+63 (key 2c, 2c+1 at column PK + c); the
-                // dS rows sit in the query lanes, the dR rows in the probe lanes
-                tc::tmem_st16_split<32>(rowS + LY::PK + 16 * b, spk);
-                tc::tmem_st16_split<32>(rowR + LY::PK + 16 * b, rpk);
+                spk[y] = tc::pack_bf16(s2[0], s2[1]);
+                rpk[y] = tc::pack_bf16(r2[0], r2[1]);
             }
+            // packed operand columns PK..PK+63 (keys 2c, 2c+1 at column PK + c); the
+            // dS rows sit in the query lanes, the dR rows in the probe lanes
+            tc::tmem_st16_split<32>(rowS + LY::PK + 16 * bb, spk);
+            tc::tmem_st16_split<32>(rowR + LY::PK + 16 * bb, rpk);
             tc::tmem_st_wait();
             tc::fence_before_sync();
             mbar_arrive(p_full);
@@ -586,24 +623,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
         if (__all_sync(kFullMask, done)) {
             tc::fence_after_sync();
-            float* qrow = a.dq + ((size_t)bh * a.L + i) * D + h * (D / 2);
-            float* rrow = RHO ? a.drho + ((size_t)bh * a.L + i) * D + h * (D / 2) : nullptr;
+            // warps 4-7 store dQ (query lanes), warps 8-11 drho (probe lanes)
+            if (bb == 0 || RHO) {
+                float* orow = (bb == 0 ? a.dq : a.drho) + ((size_t)bh * a.L + i) * D + h * (D / 2);
+                const uint32_t base = (bb == 0 ? rowS : rowR) + LY::O;
 #pragma unroll 1
-            for (int b = 0; b < D / 64; ++b) {
-                uint32_t u[32], w[32];
-                tc::tmem_ld32_split<D / 2>(rowS + LY::O + 32 * b, u);
-                tc::tmem_ld32_split<D / 2>(rowR + LY::O + 32 * b, w);
-                tc::tmem_ld_wait();
-                if (i < a.L) {
+                for (int b = 0; b < D / 64; ++b) {
+                    uint32_t u[32];
+                    tc::tmem_ld32_split<D / 2>(base + 32 * b, u);
+                    tc::tmem_ld_wait();
+                    if (i < a.L) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 4) {
-                        *reinterpret_cast<float4*>(qrow + 32 * b + x) =
-                            make_float4(__uint_as_float(u[x]), __uint_as_float(u[x + 1]),
-                                        __uint_as_float(u[x + 2]), __uint_as_float(u[x + 3]));
-                        if (RHO)
-                            *reinterpret_cast<float4*>(rrow + 32 * b + x) =
-                                make_float4(__uint_as_float(w[x]), __uint_as_float(w[x + 1]),
-                                            __uint_as_float(w[x + 2]), __uint_as_float(w[x + 3]));
+                        for (int x = 0; x < 32; x += 4)
+                            *reinterpret_cast<float4*>(orow + 32 * b + x) =
+                                make_float4(__uint_as_float(u[x]), __uint_as_float(u[x + 1]),
+                                            __uint_as_float(u[x + 2]), __uint_as_float(u[x + 3]));
                     }
                 }
             }
