@@ -160,7 +160,7 @@ parallax::DecodePlan make_plan(int B, int H, int Hkv, int Lmax, int d, int num_s
     if (page_size > 0 && plan.chunk > parallax::decode_paged_max_chunk(page_size)) plan.chunk = 4096;
     plan.nsplit = (Lmax + plan.chunk - 1) / plan.chunk;
     const long long items = (long long)B * Hkv * plan.nsplit;
-    plan.grid = (int)std::min<long long>(items, (long long)num_sms);
+    plan.grid = (int)std::min<long long>(items, (long long)num_sms * parallax::decode_ctas_per_sm());
     return plan;
 }
 

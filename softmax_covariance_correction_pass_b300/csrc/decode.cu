@@ -29,7 +29,10 @@ __device__ unsigned g_decode_err = 0;
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 4;
+// Two CTAs per SM (18 warps) with 3 stages each: 192 KB of K/V in flight per SM and
+// twice the warps of one CTA to hide the latency of the per-key dependency chains.
+constexpr int kStages = 3;
+constexpr int kCtasPerSm = 2;
 constexpr int kStageRowBytes = 16384;  // bytes of K (and of V) per stage
 
 constexpr int kMaxPageIds = 288;  // page ids of one work item held in shared memory
@@ -97,7 +100,7 @@ __device__ __forceinline__ int checked_page(const DecodeArgs& a, int id) {
 }
 
 template <typename T, int D, bool RHO, bool SPLIT, int G, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeArgs a) {
     using KL = KeyLayout<T, D>;
     using SH = DecodeShape<T, D, G>;
     constexpr int VEC = KL::VEC;
@@ -398,6 +401,8 @@ size_t decode_workspace_bytes(const DecodePlan& plan) {
 int decode_stage_keys(int d, int elem_bytes) { return kStageRowBytes / (d * elem_bytes); }
 
 int decode_threads() { return kThreads; }
+
+int decode_ctas_per_sm() { return kCtasPerSm; }
 
 int decode_paged_max_chunk(int page_size) { return (kMaxPageIds - 1) * page_size; }
 

@@ -24,6 +24,7 @@ struct DecodePlan {
 size_t decode_workspace_bytes(const DecodePlan& plan);
 int decode_stage_keys(int d, int elem_bytes);
 int decode_threads();
+int decode_ctas_per_sm();  // resident decode CTAs per SM the kernel is built for
 cudaError_t decode_launch(const DecodePlan& plan, bool bf16, const void* q, const void* rho,
                           const void* kc, const void* vc, const int32_t* seqlens, float* o,
                           void* ws, cudaStream_t stream, const int32_t* block_table = nullptr);
