@@ -36,11 +36,9 @@ METRIC = "decode KV-stream GB/s (% B300 HBM peak); causal prefill TFLOP/s (% TC 
 # smaller cases and scaled by the units processed; see those files).  None when
 # the kernel has changed since its counters were taken.
 TRAFFIC_BYTES = {
-    # B=8 capture: 536.98 MB read (x8 heads' worth at B=64) + ~5.9 MB partials and o
-    "decode": 8 * 536.98e6 + 5.9e6,
-    # B=2 capture of prefill_pair_kernel<128,1,1>: 135.49 MB read (x4 at B=8) + the 268.4 MB
-    # fp32 output written
-    "prefill": 4 * 135.49e6 + 268.4e6,
+    # the decode and prefill kernels changed after their captures; re-measure before quoting
+    "decode": None,
+    "prefill": None,
     # full-size capture: 177.38 MB read + 497.77 MB written (the rest of the 536.9 MB
     # output was still in L2 when the kernel ended)
     "projection": 177.38e6 + 497.77e6,
@@ -59,7 +57,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["decode", "prefill", "projection", "backward"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "projection", "backward", "gqa", "lla"],
+                    default=None,
                     help="time one kernel alone (profiling runs); the default times both")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="override the decode batch (profiling runs on smaller cases)")
@@ -676,6 +675,42 @@ def run_sweep(args):
 
 
 # ----------------------------------------------------------------------------- serving variants
+def run_serving_one(args):
+    """--only gqa / --only lla (profiling runs): the grouped-query decode at B=64, H=16 over
+    H_kv=2, 8192 keys, or the exact LLA decode at the uniform decode shape; `--steps` timed
+    calls after `--warmup` warm-ups, one JSON line."""
+    import torch
+
+    import softmax_covariance_correction_pass_b300 as px
+    from softmax_covariance_correction_pass_b300 import configs
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    px.load_library()
+    B = args.decode_batch or 64
+    if args.only == "gqa":
+        inp = configs.decode_gqa_inputs(B, 16, 2, 128, 8192, 8192, seed=1, device=dev)
+        call = lambda: px.parallax_attn_decode_gqa(inp.q, inp.rho, inp.k_cache, inp.v_cache,
+                                                   inp.seqlens)
+    else:
+        inp = configs.decode_uniform_inputs(dev, B=B)
+        call = lambda: px.parallax_lla_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if px.parallax_check_device_error() != 0:
+        raise RuntimeError("device error")
+    print(json.dumps({"case": args.only, "B": B, "ms": a.elapsed_time(b) / args.steps}),
+          flush=True)
+    return 0
+
+
 def run_serving(args):
     """Grouped-query decode (B=64, H=16 over H_kv in {8, 4, 2}, 8192 keys), paged decode of
     the ragged batch (B=512, U[128,16384] keys, 256-key pages, H_kv in {16, 4}) and the
@@ -777,6 +812,8 @@ def main(argv=None):
         return run_serving(args)
     if args.only == "projection":
         return run_projection_only(args)
+    if args.only in ("gqa", "lla"):
+        return run_serving_one(args)
     if args.only == "backward":
         import torch
 

@@ -46,12 +46,13 @@ struct BwdArgs {
     const __nv_bfloat16* dout;    // [BH, L, D] gradient of o
     const float* lse;             // [BH, L]
     const float* rbar;            // [BH, L]
-    float4* rs;                   // [BH * L] (lse2, rbar, abar, delta)
+    float* rs;                    // [BH][4][Lp]: lse2, rbar, abar, delta of each row (0 past L)
     float* dq;
     float* drho;
     float* dk;
     float* dv;                    // [BH, L, D] fp32
     int L, BH;
+    int Lp;                       // L rounded up to 64 (row-statistics stride)
     int n_kt, n_qt;               // 128-key tiles and 64-query tiles per head
     float scale, qscale;          // softmax scale, scale * log2(e)
 };
@@ -80,8 +81,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const size_t row = (size_t)blockIdx.x * 8 + warp;
-    if (row >= (size_t)a.BH * a.L) return;
+    const size_t prow = (size_t)blockIdx.x * 8 + warp;  // padded row: (bh, i < Lp)
+    if (prow >= (size_t)a.BH * a.Lp) return;
+    const int bh = (int)(prow / a.Lp), i = (int)(prow - (size_t)bh * a.Lp);
+    float* out = a.rs + (size_t)bh * 4 * a.Lp + i;
+    if (i >= a.L) {  // padding rows: zeros, so that tiles past L read finite values
+        if (lane < 4) out[(size_t)lane * a.Lp] = 0.f;
+        return;
+    }
+    const size_t row = (size_t)bh * a.L + i;
     constexpr int PER = D / 32;
     float ab = 0.f, de = 0.f;
 #pragma unroll
@@ -96,10 +104,20 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
         ab += __shfl_xor_sync(kFullMask, ab, off);
         de += __shfl_xor_sync(kFullMask, de, off);
     }
-    if (lane == 0) a.rs[row] = make_float4(a.lse[row] * kLog2e, a.rbar[row], ab, de);
+    if (lane == 0) {
+        out[0] = a.lse[row] * kLog2e;
+        out[a.Lp] = a.rbar[row];
+        out[2 * (size_t)a.Lp] = ab;
+        out[3 * (size_t)a.Lp] = de;
+    }
 }
 
+__device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
+
 // ------------------------------------------------------------------------ dK, dV
+// One 128-key tile per CTA, 64-query tiles in a 2-deep TMA ring; warp 0 TMA,
+// warp 1 MMA, warps 4-7 compute (one key per TMEM lane, all 64 queries of a tile).
+constexpr int kKvThreads = 256;
 template <int D>
 struct KvLayout {
     static constexpr int NCB = D / 64;
@@ -118,7 +136,7 @@ struct KvLayout {
 };
 
 template <int D, bool CAUSAL, bool RHO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmR,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmO, const BwdArgs a) {
@@ -144,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_t = a.n_qt - qt0;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], b == 6 ? kComputeThreads : 1);
+        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], b == 6 ? 128 : 1);
         *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
         fence_mbar_init();
     }
@@ -179,10 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int q0 = (qt0 + t) * 64;
-                const int nrs = min(64, a.L - q0);
                 unsigned char* stage = smem + LY::ST_OFF + st * LY::STAGE;
                 mbar_arrive_expect_tx(&qr_full[st], (RHO ? 2 : 1) * LY::NCB * SUB64 + LY::DO_BYTES +
-                                                        nrs * 16);
+                                                        4 * 64 * 4);
                 for (int cb = 0; cb < LY::NCB; ++cb) {
                     tc::tma_load_3d(stage + cb * SUB, &tmQ, cb * 64, q0, bh, &qr_full[st]);
                     if (RHO)
@@ -190,8 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::tma_load_3d(stage + LY::QR_BYTES + cb * SUB64, &tmO, cb * 64, q0, bh,
                                     &qr_full[st]);
                 }
-                bulk_g2s(stage + LY::QR_BYTES + LY::DO_BYTES, a.rs + (size_t)bh * a.L + q0,
-                         nrs * 16, &qr_full[st]);
+                for (int c = 0; c < 4; ++c)  // the 64 rows' statistics, one array each
+                    bulk_g2s(stage + LY::QR_BYTES + LY::DO_BYTES + c * 256,
+                             a.rs + ((size_t)bh * 4 + c) * a.Lp + q0, 256, &qr_full[st]);
                 issued = t + 1;
             }
             if (!ok) {
@@ -275,7 +293,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- compute + epilogue
         const int q4 = warp & 3;
-        const int c = (warp - 4) >> 2;      // which 32 queries of every 64-query tile
         const int j = k0 + 32 * q4 + lane;  // this thread's key
         const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
         const float qs = a.qscale, scale = a.scale;
@@ -288,74 +305,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc::fence_after_sync();
-            const int q0 = (qt0 + t) * 64 + 32 * c;
-            // row statistics of this warp's 32 queries: (lse2, rbar, abar, delta) each
-            const float* rs = reinterpret_cast<const float*>(
-                                  smem + LY::ST_OFF + st * LY::STAGE + LY::QR_BYTES + LY::DO_BYTES) +
-                              4 * 32 * c;
-            uint32_t sv[32], rv[32], dv[32];
-            tc::tmem_ld32(trow + LY::SR + 32 * c, sv);
-            if (RHO) tc::tmem_ld32(trow + LY::SR + 64 + 32 * c, rv);
-            tc::tmem_ld32(trow + LY::DT + 32 * c, dv);
-            tc::tmem_ld_wait();
-            // p in place of s; queries past L or (causal) before this key get no weight.
-            // The row statistics of queries past L were not loaded: they are never read.
-            const int nvalid = min(32, a.L - q0);
-            uint32_t vmask = nvalid >= 32 ? 0xffffffffu : ((1u << nvalid) - 1u);
-            if (CAUSAL && j > q0) vmask &= j - q0 >= 32 ? 0u : ~((1u << (j - q0)) - 1u);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                const bool valid = (vmask >> x) & 1u;
-                const float p = fast_exp2(fmaf(__uint_as_float(sv[x]), qs, valid ? -lds(rs + 4 * x) : 0.f));
-                sv[x] = __float_as_uint(valid ? p : 0.f);
-            }
-            uint32_t pk[16];
-            // W = p (1 + rbar - r)  -> over the S^T columns just read
-#pragma unroll
-            for (int y = 0; y < 16; ++y) {
-                float w2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int x = 2 * y + e;
-                    const float r = RHO ? __uint_as_float(rv[x]) : 0.f;
-                    const float rb = (vmask >> x) & 1u ? lds(rs + 4 * x + 1) : 0.f;
-                    w2[e] = __uint_as_float(sv[x]) * (1.f + rb - r);
-                }
-                pk[y] = tc::pack_bf16(w2[0], w2[1]);
-            }
-            tc::tmem_st16(trow + LY::SR + 32 * c, pk);
-            // dS = scale p ((D - abar)(rbar - r) + D - delta)
-#pragma unroll
-            for (int y = 0; y < 16; ++y) {
-                float s2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int x = 2 * y + e;
-                    const bool v = (vmask >> x) & 1u;
-                    const float zy = v ? lds(rs + 4 * x + 1) : 0.f;
-                    const float zz = v ? lds(rs + 4 * x + 2) : 0.f;
-                    const float zw = v ? lds(rs + 4 * x + 3) : 0.f;
-                    const float dd = __uint_as_float(dv[x]);
-                    const float r = RHO ? __uint_as_float(rv[x]) : 0.f;
-                    s2[e] = __uint_as_float(sv[x]) * fmaf(dd - zz, zy - r, dd - zw) * scale;
-                }
-                pk[y] = tc::pack_bf16(s2[0], s2[1]);
-            }
-            tc::tmem_st16(trow + LY::SR + 32 * c + 16, pk);
-            if (RHO) {
-                // dR = p (abar - D)  -> over the R^T columns just read
+            const int q0 = (qt0 + t) * 64;
+            // row statistics of the tile: lse2[64], rbar[64], abar[64], delta[64]
+            const float* rst = reinterpret_cast<const float*>(smem + LY::ST_OFF + st * LY::STAGE +
+                                                              LY::QR_BYTES + LY::DO_BYTES);
+            const float2 qs2 = make_float2(qs, qs), sc2 = make_float2(scale, scale);
+            const float2 one2 = make_float2(1.f, 1.f);
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                uint32_t sv[32], rv[32], dv[32];
+                tc::tmem_ld32(trow + LY::SR + 32 * c, sv);
+                if (RHO) tc::tmem_ld32(trow + LY::SR + 64 + 32 * c, rv);
+                tc::tmem_ld32(trow + LY::DT + 32 * c, dv);
+                tc::tmem_ld_wait();
+                // queries past L or (causal) before this key get no weight
+                const int qc = q0 + 32 * c;
+                const int nvalid = min(32, a.L - qc);
+                uint32_t vmask = nvalid >= 32 ? 0xffffffffu : ((1u << nvalid) - 1u);
+                if (CAUSAL && j > qc) vmask &= j - qc >= 32 ? 0u : ~((1u << (j - qc)) - 1u);
+                const float* st0 = rst + 32 * c;
+                uint32_t wpk[16], spk[16], rpk[16];
 #pragma unroll
                 for (int y = 0; y < 16; ++y) {
-                    float r2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int x = 2 * y + e;
-                        const float ab = (vmask >> x) & 1u ? lds(rs + 4 * x + 2) : 0.f;
-                        r2[e] = __uint_as_float(sv[x]) * (ab - __uint_as_float(dv[x]));
-                    }
-                    pk[y] = tc::pack_bf16(r2[0], r2[1]);
+                    const int x = 2 * y;
+                    const float2 lse = *reinterpret_cast<const float2*>(st0 + x);
+                    const float2 rb = *reinterpret_cast<const float2*>(st0 + 64 + x);
+                    const float2 ab = *reinterpret_cast<const float2*>(st0 + 128 + x);
+                    const float2 de = *reinterpret_cast<const float2*>(st0 + 192 + x);
+                    const float2 s2 = make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]));
+                    const float2 r2 = RHO ? make_float2(__uint_as_float(rv[x]), __uint_as_float(rv[x + 1]))
+                                          : make_float2(0.f, 0.f);
+                    const float2 d2 = make_float2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1]));
+                    const float2 t = __ffma2_rn(s2, qs2, neg2(lse));
+                    float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+                    p.x = (vmask >> x) & 1u ? p.x : 0.f;
+                    p.y = (vmask >> (x + 1)) & 1u ? p.y : 0.f;
+                    const float2 rr = __fadd2_rn(rb, neg2(r2));  // rbar - r
+                    const float2 w = __fmul2_rn(p, __fadd2_rn(one2, rr));
+                    const float2 f = __ffma2_rn(__fadd2_rn(d2, neg2(ab)), rr, __fadd2_rn(d2, neg2(de)));
+                    const float2 ds = __fmul2_rn(__fmul2_rn(p, f), sc2);
+                    const float2 dr = __fmul2_rn(p, __fadd2_rn(ab, neg2(d2)));
+                    wpk[y] = tc::pack_bf16(w.x, w.y);
+                    spk[y] = tc::pack_bf16(ds.x, ds.y);
+                    rpk[y] = tc::pack_bf16(dr.x, dr.y);
                 }
-                tc::tmem_st16(trow + LY::SR + 64 + 32 * c, pk);
+                // (columns already read above: W, dS over S^T, dR over R^T)
+                tc::tmem_st16(trow + LY::SR + 32 * c, wpk);
+                tc::tmem_st16(trow + LY::SR + 32 * c + 16, spk);
+                if (RHO) tc::tmem_st16(trow + LY::SR + 64 + 32 * c, rpk);
             }
             tc::tmem_st_wait();
             tc::fence_before_sync();
@@ -364,20 +361,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
         if (__all_sync(kFullMask, done)) {
             tc::fence_after_sync();
-            // warps 4-7 store dV, warps 8-11 dK
-            float* orow = (c == 0 ? a.dv : a.dk) + ((size_t)bh * a.L + j) * D;
-            const uint32_t col = c == 0 ? LY::DV : LY::DK;
+            float* dvrow = a.dv + ((size_t)bh * a.L + j) * D;
+            float* dkrow = a.dk + ((size_t)bh * a.L + j) * D;
 #pragma unroll 1
             for (int b = 0; b < D / 32; ++b) {
-                uint32_t u[32];
-                tc::tmem_ld32(trow + col + 32 * b, u);
+                uint32_t u[32], w[32];
+                tc::tmem_ld32(trow + LY::DV + 32 * b, u);
+                tc::tmem_ld32(trow + LY::DK + 32 * b, w);
                 tc::tmem_ld_wait();
                 if (j < a.L) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 4)
-                        *reinterpret_cast<float4*>(orow + 32 * b + x) =
+                    for (int x = 0; x < 32; x += 4) {
+                        *reinterpret_cast<float4*>(dvrow + 32 * b + x) =
                             make_float4(__uint_as_float(u[x]), __uint_as_float(u[x + 1]),
                                         __uint_as_float(u[x + 2]), __uint_as_float(u[x + 3]));
+                        *reinterpret_cast<float4*>(dkrow + 32 * b + x) =
+                            make_float4(__uint_as_float(w[x]), __uint_as_float(w[x + 1]),
+                                        __uint_as_float(w[x + 2]), __uint_as_float(w[x + 3]));
+                    }
                 }
             }
         } else {
@@ -394,19 +395,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------ dQ, drho
+// One 64-query tile per CTA (the forward's stacked lane layout), 64-key tiles in
+// a 4-deep TMA ring.  Two TMEM buffers Y0, Y1 of [S|R 64 | D 64] columns and two
+// packed operand slots let the key tiles ping-pong between compute group
+// g (warps 4+4g .. 7+4g, key tiles j = g mod 2) and the tensor core.
+constexpr int Q_KT = 64;       // keys per tile
+constexpr int Q_STAGES = 4;
+
 template <int D>
 struct QLayout {
     static constexpr int NCB = D / 64;
-    static constexpr int OPB = NCB * SUB;
-    static constexpr int QR_OFF = 0;           // stacked [Q; rho] (16-row groups)
-    static constexpr int DO_OFF = OPB;         // stacked [dO; dO]
-    static constexpr int K_OFF = 2 * OPB;      // K ring, 2 stages
-    static constexpr int V_OFF = 4 * OPB;      // V ring, 2 stages
-    static constexpr int BAR_OFF = 6 * OPB;
-    // q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full, p_full, o_full
-    static constexpr int NBARS = 12;
+    static constexpr int OPB = NCB * SUB;             // [128 x D] operand
+    static constexpr int KSUB = Q_KT * 128;           // [64 keys x 64 columns]
+    static constexpr int KT_BYTES = NCB * KSUB;       // one 64-key tile of K (or V)
+    static constexpr int QR_OFF = 0;                  // stacked [Q; rho] (16-row groups)
+    static constexpr int DO_OFF = OPB;                // stacked [dO; dO]
+    static constexpr int K_OFF = 2 * OPB;             // K ring
+    static constexpr int V_OFF = K_OFF + Q_STAGES * KT_BYTES;  // V ring
+    static constexpr int BAR_OFF = V_OFF + Q_STAGES * KT_BYTES;
+    // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_full
+    static constexpr int NBARS = 4 * Q_STAGES + 6;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
-    static constexpr uint32_t SR = 0, DD = 128, O = 256, PK = 384;  // TMEM columns
+    // TMEM columns: Y_g = 128 g: [S|R] (64), [D|D] (64); accumulator; packed dS/dR slots
+    static constexpr uint32_t YW = 128, O = 256, PK = 384;
 };
 
 template <int D, bool CAUSAL, bool RHO>
@@ -415,18 +426,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmO, const BwdArgs a) {
     using LY = QLayout<D>;
+    constexpr int S = Q_STAGES;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
     uint64_t* q_full = bars;
     uint64_t* k_full = bars + 1;
-    uint64_t* v_full = bars + 3;
-    uint64_t* k_empty = bars + 5;
-    uint64_t* v_empty = bars + 7;
-    uint64_t* s_full = bars + 9;
-    uint64_t* p_full = bars + 10;
-    uint64_t* o_full = bars + 11;
+    uint64_t* v_full = bars + 1 + S;
+    uint64_t* k_empty = bars + 1 + 2 * S;
+    uint64_t* v_empty = bars + 1 + 3 * S;
+    uint64_t* s_full = bars + 1 + 4 * S;
+    uint64_t* p_full = bars + 3 + 4 * S;
+    uint64_t* o_full = bars + 5 + 4 * S;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -435,11 +447,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = blockIdx.x - r_in * a.BH;
     const int qb = CAUSAL ? a.n_qt - 1 - r_in : r_in;  // causal: heaviest tiles first
     const int q0 = qb * 64;
-    const int n_all = a.n_kt;
-    const int n_t = CAUSAL ? min(n_all, (q0 + 63) / 128 + 1) : n_all;
+    const int n_all = (a.L + Q_KT - 1) / Q_KT;
+    const int n_t = CAUSAL ? min(n_all, qb + 1) : n_all;  // 64-key tiles up to the diagonal
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], b == 10 ? kComputeThreads : 1);
+        for (int b = 0; b < LY::NBARS; ++b)
+            mbar_init(&bars[b], (b == 3 + 4 * S || b == 4 + 4 * S) ? 128 : 1);
         *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
         fence_mbar_init();
     }
@@ -485,81 +498,90 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             for (int j = 0; j < n_t && ok; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait(&k_empty[st], ((j >> 1) - 1) & 1, &g_bwd_err)) {
+                const int st = j % S;
+                if (j >= S && !mbar_wait(&k_empty[st], ((j / S) - 1) & 1, &g_bwd_err)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&k_full[st], LY::OPB);
+                mbar_arrive_expect_tx(&k_full[st], LY::KT_BYTES);
                 for (int cb = 0; cb < LY::NCB; ++cb)
-                    tc::tma_load_3d(smem + LY::K_OFF + st * LY::OPB + cb * SUB, &tmK, cb * 64, j * 128,
-                                    bh, &k_full[st]);
+                    tc::tma_load_3d(smem + LY::K_OFF + st * LY::KT_BYTES + cb * LY::KSUB, &tmK,
+                                    cb * 64, j * Q_KT, bh, &k_full[st]);
                 kj = j + 1;
-                if (j >= 2 && !mbar_wait(&v_empty[st], ((j >> 1) - 1) & 1, &g_bwd_err)) {
+                if (j >= S && !mbar_wait(&v_empty[st], ((j / S) - 1) & 1, &g_bwd_err)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&v_full[st], LY::OPB);
+                mbar_arrive_expect_tx(&v_full[st], LY::KT_BYTES);
                 for (int cb = 0; cb < LY::NCB; ++cb)
-                    tc::tma_load_3d(smem + LY::V_OFF + st * LY::OPB + cb * SUB, &tmV, cb * 64, j * 128,
-                                    bh, &v_full[st]);
+                    tc::tma_load_3d(smem + LY::V_OFF + st * LY::KT_BYTES + cb * LY::KSUB, &tmV,
+                                    cb * 64, j * Q_KT, bh, &v_full[st]);
                 vj = j + 1;
             }
             if (!ok) {
                 *abort_flag = 1;
                 mbar_wait(q_full, 0, &g_bwd_err);
-                for (int k = (kj >= 2 ? kj - 2 : 0); k < kj; ++k)
-                    mbar_wait(&k_full[k & 1], (k >> 1) & 1, &g_bwd_err);
-                for (int k = (vj >= 2 ? vj - 2 : 0); k < vj; ++k)
-                    mbar_wait(&v_full[k & 1], (k >> 1) & 1, &g_bwd_err);
+                for (int k = (kj >= S ? kj - S : 0); k < kj; ++k)
+                    mbar_wait(&k_full[k % S], (k / S) & 1, &g_bwd_err);
+                for (int k = (vj >= S ? vj - S : 0); k < vj; ++k)
+                    mbar_wait(&v_full[k % S], (k / S) & 1, &g_bwd_err);
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (!skip) {
-            constexpr uint32_t kIdesc1 = tc::idesc_bf16_f32(128, 128, false);
+            constexpr uint32_t kIdesc1 = tc::idesc_bf16_f32(128, Q_KT, false);
             constexpr uint32_t kIdesc2 = tc::idesc_bf16_f32(128, D, true);
             const uint32_t sbase = smem_u32(smem);
             const uint64_t dQR = tc::smem_desc_sw128(sbase + LY::QR_OFF, 16, 1024);
             const uint64_t dDO = tc::smem_desc_sw128(sbase + LY::DO_OFF, 16, 1024);
             const uint64_t dK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, 16, 1024);
             const uint64_t dV0 = tc::smem_desc_sw128(sbase + LY::V_OFF, 16, 1024);
-            const uint64_t mK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, SUB, 1024);
-            constexpr uint32_t kOpStep = LY::OPB >> 4;
-            bool ok = mbar_wait_warp(q_full, 0, &g_bwd_err);
-            for (int j = 0; j < n_t && ok; ++j) {
-                const int st = j & 1;
-                if (*abort_flag || !mbar_wait_warp(&k_full[st], (j >> 1) & 1, &g_bwd_err) ||
-                    !mbar_wait_warp(&v_full[st], (j >> 1) & 1, &g_bwd_err)) {
-                    ok = false;
-                    break;
-                }
+            const uint64_t mK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, LY::KSUB, 1024);
+            constexpr uint32_t kKtStep = LY::KT_BYTES >> 4;
+            auto issue_ab = [&](int j) -> bool {  // [S; R] and [D; D] of key tile j into Y_(j&1)
+                const int st = j % S;
+                if (*abort_flag || !mbar_wait_warp(&k_full[st], (j / S) & 1, &g_bwd_err) ||
+                    !mbar_wait_warp(&v_full[st], (j / S) & 1, &g_bwd_err))
+                    return false;
                 tc::fence_after_sync();
-                const uint64_t dK = tc::opaque(dK0 + st * kOpStep);
-                const uint64_t dV = tc::opaque(dV0 + st * kOpStep);
+                const uint32_t Y = LY::YW * (j & 1);
+                const uint64_t dK = tc::opaque(dK0 + st * kKtStep);
+                const uint64_t dV = tc::opaque(dV0 + st * kKtStep);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {  // [S; R] = [Q; rho] K^T
-                    const uint32_t off = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
-                    tc::mma_ss(tmem + LY::SR, dQR + off, dK + off, kIdesc1, kk > 0);
+                    const uint32_t offA = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
+                    const uint32_t offB = ((kk / 4) * LY::KSUB + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem + Y, dQR + offA, dK + offB, kIdesc1, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {  // [D; D] = [dO; dO] V^T
-                    const uint32_t off = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
-                    tc::mma_ss(tmem + LY::DD, dDO + off, dV + off, kIdesc1, kk > 0);
+                    const uint32_t offA = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
+                    const uint32_t offB = ((kk / 4) * LY::KSUB + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem + Y + Q_KT, dDO + offA, dV + offB, kIdesc1, kk > 0);
                 }
-                tc::commit(s_full);
+                tc::commit(&s_full[j & 1]);
                 tc::commit(&v_empty[st]);
-                if (!mbar_wait_warp(p_full, j & 1, &g_bwd_err)) {
+                return true;
+            };
+            bool ok = mbar_wait_warp(q_full, 0, &g_bwd_err);
+            if (ok) ok = issue_ab(0);
+            if (ok && n_t > 1) ok = issue_ab(1);
+            for (int j = 0; j < n_t && ok; ++j) {
+                if (!mbar_wait_warp(&p_full[j & 1], (j >> 1) & 1, &g_bwd_err)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
-                const uint64_t mK = tc::opaque(mK0 + st * kOpStep);
+                const int st = j % S;
+                const uint64_t mK = tc::opaque(mK0 + st * kKtStep);
+                const uint32_t pk = LY::PK + 32 * (j & 1);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // [dQ; drho] += [dS; dR] K
-                    tc::mma_ts(tmem + LY::O, tmem + LY::PK + 8 * kk, mK + ((kk * 16 * 128) >> 4),
+                for (int kk = 0; kk < Q_KT / 16; ++kk)  // [dQ; drho] += [dS; dR] K
+                    tc::mma_ts(tmem + LY::O, tmem + pk + 8 * kk, mK + ((kk * 16 * 128) >> 4),
                                kIdesc2, (j > 0 || kk > 0) ? 1u : 0u);
                 tc::commit(&k_empty[st]);
+                if (j + 2 < n_t) ok = issue_ab(j + 2);
             }
             tc::commit(o_full);
             if (!ok) {
@@ -570,63 +592,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- compute + epilogue
         const int g = warp & 3;
-        const int bb = (warp - 4) >> 2;               // which 32-key block of each half
+        const int grp = (warp - 4) >> 2;               // key tiles j = grp mod 2
         const int h = lane >> 4;                       // which half of the keys / columns
         const int i = q0 + 16 * g + (lane & 15);       // query row
         const uint32_t rowS = tmem + ((uint32_t)(32 * g) << 16);
         const uint32_t rowR = tmem + ((uint32_t)(32 * g + 16) << 16);
+        const uint32_t Y = LY::YW * grp, pk = LY::PK + 32 * grp;
         const float qs = a.qscale, scale = a.scale;
-        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < a.L) z = a.rs[(size_t)bh * a.L + i];
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);  // (lse2, rbar, abar, delta)
+        if (i < a.L) {
+            const float* zr = a.rs + (size_t)bh * 4 * a.Lp + i;
+            z = make_float4(zr[0], zr[a.Lp], zr[2 * (size_t)a.Lp], zr[3 * (size_t)a.Lp]);
+        }
         bool ok = !skip;
-        for (int j = 0; j < n_t && ok; ++j) {
-            const bool got = !*abort_flag && mbar_wait(s_full, j & 1, &g_bwd_err);
+        for (int j = grp; j < n_t && ok; j += 2) {
+            const bool got = !*abort_flag && mbar_wait(&s_full[grp], (j >> 1) & 1, &g_bwd_err);
             if (!__all_sync(kFullMask, got)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
             uint32_t sv[32], rv[32], dv[32];
-            tc::tmem_ld32_split<64>(rowS + LY::SR + 32 * bb, sv);
-            if (RHO) tc::tmem_ld32_split<64>(rowR + LY::SR + 32 * bb, rv);
-            tc::tmem_ld32_split<64>(rowS + LY::DD + 32 * bb, dv);
+            tc::tmem_ld32_split<32>(rowS + Y, sv);
+            if (RHO) tc::tmem_ld32_split<32>(rowR + Y, rv);
+            tc::tmem_ld32_split<32>(rowS + Y + Q_KT, dv);
             tc::tmem_ld_wait();
-            const int k0 = j * 128 + 64 * h + 32 * bb;
+            const int k0 = j * Q_KT + 32 * h;
+            // keys past L or (causal) past this query get no weight
+            const int lim = min(a.L - 1, CAUSAL ? i : a.L - 1) - k0;  // last valid x
+            const uint32_t vmask = i >= a.L || lim < 0 ? 0u
+                                   : lim >= 31     ? 0xffffffffu
+                                                   : ((2u << lim) - 1u);
+            const float2 qs2 = make_float2(qs, qs), sc2 = make_float2(scale, scale);
+            const float2 nl2 = make_float2(-z.x, -z.x), rb2 = make_float2(z.y, z.y);
+            const float2 ab2 = make_float2(z.z, z.z), de2 = make_float2(z.w, z.w);
             uint32_t spk[16], rpk[16];
 #pragma unroll
             for (int y = 0; y < 16; ++y) {
-                float s2[2], r2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int x = 2 * y + e;
-                    const int key = k0 + x;
-                    const bool valid = i < a.L && key < a.L && (!CAUSAL || key <= i);
-                    const float dd = __uint_as_float(dv[x]);
-                    const float r = RHO ? __uint_as_float(rv[x]) : 0.f;
-                    const float p = fast_exp2(fmaf(__uint_as_float(sv[x]), qs, -z.x));
-                    const float dr = p * (z.z - dd);
-                    const float ds = p * fmaf(dd - z.z, z.y - r, dd - z.w) * scale;
-                    s2[e] = valid ? ds : 0.f;
-                    r2[e] = valid ? dr : 0.f;
-                }
-                spk[y] = tc::pack_bf16(s2[0], s2[1]);
-                rpk[y] = tc::pack_bf16(r2[0], r2[1]);
+                const int x = 2 * y;
+                const float2 s2 = make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]));
+                const float2 r2 = RHO ? make_float2(__uint_as_float(rv[x]), __uint_as_float(rv[x + 1]))
+                                      : make_float2(0.f, 0.f);
+                const float2 d2 = make_float2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1]));
+                const float2 t = __ffma2_rn(s2, qs2, nl2);
+                float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+                p.x = (vmask >> x) & 1u ? p.x : 0.f;
+                p.y = (vmask >> (x + 1)) & 1u ? p.y : 0.f;
+                const float2 dr = __fmul2_rn(p, __fadd2_rn(ab2, neg2(d2)));
+                const float2 f = __ffma2_rn(__fadd2_rn(d2, neg2(ab2)), __fadd2_rn(rb2, neg2(r2)),
+                                            __fadd2_rn(d2, neg2(de2)));
+                const float2 ds = __fmul2_rn(__fmul2_rn(p, f), sc2);
+                spk[y] = tc::pack_bf16(ds.x, ds.y);
+                rpk[y] = tc::pack_bf16(dr.x, dr.y);
             }
-            // packed operand columns PK..PK+63 (keys 2c, 2c+1 at column PK + c); the
-            // dS rows sit in the query lanes, the dR rows in the probe lanes
-            tc::tmem_st16_split<32>(rowS + LY::PK + 16 * bb, spk);
-            tc::tmem_st16_split<32>(rowR + LY::PK + 16 * bb, rpk);
+            // packed operand slot (key 2c, 2c+1 at column pk + c): dS in the query lanes,
+            // dR in the probe lanes
+            tc::tmem_st16_split<16>(rowS + pk, spk);
+            tc::tmem_st16_split<16>(rowR + pk, rpk);
             tc::tmem_st_wait();
             tc::fence_before_sync();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[grp]);
         }
         const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
         if (__all_sync(kFullMask, done)) {
             tc::fence_after_sync();
-            // warps 4-7 store dQ (query lanes), warps 8-11 drho (probe lanes)
-            if (bb == 0 || RHO) {
-                float* orow = (bb == 0 ? a.dq : a.drho) + ((size_t)bh * a.L + i) * D + h * (D / 2);
-                const uint32_t base = (bb == 0 ? rowS : rowR) + LY::O;
+            // group 0 stores dQ (query lanes), group 1 drho (probe lanes)
+            if (grp == 0 || RHO) {
+                float* orow = (grp == 0 ? a.dq : a.drho) + ((size_t)bh * a.L + i) * D + h * (D / 2);
+                const uint32_t base = (grp == 0 ? rowS : rowR) + LY::O;
 #pragma unroll 1
                 for (int b = 0; b < D / 64; ++b) {
                     uint32_t u[32];
@@ -670,16 +703,17 @@ cudaError_t set_smem(K kern, int bytes) {
 template <int D, bool CAUSAL, bool RHO>
 cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const void* k,
                        const void* v, cudaStream_t stream) {
-    CUtensorMap q64, r64, k128, v128, o64, q16, r16, o16;
-    if (!make_map(&q64, q, a.BH, a.L, D, 64) || !make_map(&k128, k, a.BH, a.L, D, 128) ||
-        !make_map(&v128, v, a.BH, a.L, D, 128) || !make_map(&o64, a.dout, a.BH, a.L, D, 64) ||
-        !make_map(&q16, q, a.BH, a.L, D, 16) || !make_map(&o16, a.dout, a.BH, a.L, D, 16))
+    CUtensorMap q32, r32, k128, v128, o32, q16, r16, o16, k64, v64;
+    if (!make_map(&q32, q, a.BH, a.L, D, 64) || !make_map(&k128, k, a.BH, a.L, D, 128) ||
+        !make_map(&v128, v, a.BH, a.L, D, 128) || !make_map(&o32, a.dout, a.BH, a.L, D, 64) ||
+        !make_map(&q16, q, a.BH, a.L, D, 16) || !make_map(&o16, a.dout, a.BH, a.L, D, 16) ||
+        !make_map(&k64, k, a.BH, a.L, D, Q_KT) || !make_map(&v64, v, a.BH, a.L, D, Q_KT))
         return cudaErrorInvalidValue;
     if (RHO) {
-        if (!make_map(&r64, rho, a.BH, a.L, D, 64) || !make_map(&r16, rho, a.BH, a.L, D, 16))
+        if (!make_map(&r32, rho, a.BH, a.L, D, 64) || !make_map(&r16, rho, a.BH, a.L, D, 16))
             return cudaErrorInvalidValue;
     } else {
-        r64 = q64;
+        r32 = q32;
         r16 = q16;
     }
     static bool configured = false;
@@ -689,19 +723,19 @@ cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const v
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const size_t rows = (size_t)a.BH * a.L;
+    const size_t rows = (size_t)a.BH * a.Lp;
     bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
-    bwd_kv_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_kt * a.BH), kThreads,
-                                    KvLayout<D>::SMEM_BYTES, stream>>>(q64, r64, k128, v128, o64, a);
+    bwd_kv_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_kt * a.BH), kKvThreads,
+                                    KvLayout<D>::SMEM_BYTES, stream>>>(q32, r32, k128, v128, o32, a);
     bwd_q_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_qt * a.BH), kThreads,
-                                   QLayout<D>::SMEM_BYTES, stream>>>(q16, r16, k128, v128, o16, a);
+                                   QLayout<D>::SMEM_BYTES, stream>>>(q16, r16, k64, v64, o16, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t prefill_backward_workspace_bytes(int B, int H, int L) {
-    return (size_t)B * H * L * sizeof(float4);
+    return (size_t)B * H * 4 * ((L + 63) / 64 * 64) * sizeof(float);
 }
 
 cudaError_t prefill_backward_launch(const PrefillShape& s, const void* q, const void* rho,
@@ -715,13 +749,14 @@ cudaError_t prefill_backward_launch(const PrefillShape& s, const void* q, const 
     a.dout = static_cast<const __nv_bfloat16*>(dout);
     a.lse = lse;
     a.rbar = rbar;
-    a.rs = static_cast<float4*>(ws);
+    a.rs = static_cast<float*>(ws);
     a.dq = dq;
     a.drho = drho;
     a.dk = dk;
     a.dv = dv;
     a.L = s.L;
     a.BH = s.B * s.H;
+    a.Lp = (s.L + 63) / 64 * 64;
     a.n_kt = (s.L + 127) / 128;
     a.n_qt = (s.L + 63) / 64;
     a.scale = s.scale;
