@@ -36,9 +36,10 @@ METRIC = "decode KV-stream GB/s (% B300 HBM peak); causal prefill TFLOP/s (% TC 
 # smaller cases and scaled by the units processed; see those files).  None when
 # the kernel has changed since its counters were taken.
 TRAFFIC_BYTES = {
-    # the decode and prefill kernels changed after their captures; re-measure before quoting
-    "decode": None,
-    "prefill": None,
+    # B=8 capture: 536.97 MB read (x8 at B=64) + 4.8 MB of partials and o at B=64
+    "decode": 8 * 536.97e6 + 4.8e6,
+    # B=2 capture: 135.47 MB read (x4 at B=8) + the 268.4 MB fp32 output written
+    "prefill": 4 * 135.47e6 + 268.4e6,
     # full-size capture: 177.38 MB read + 497.77 MB written (the rest of the 536.9 MB
     # output was still in L2 when the kernel ended)
     "projection": 177.38e6 + 497.77e6,
