@@ -19,6 +19,7 @@
 // maximum (log-sum-exp), sums them and finishes o = U/l - (W/l - (A/l)(U/l)).
 #include <mutex>
 
+#include "tcgen05.cuh"
 #include "warp_stream.cuh"
 #include "kernels.h"
 
@@ -311,6 +312,353 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a) {
     a.o[(size_t)bh * D + c] = RHO ? mu - (W * inv_l - (A * inv_l) * mu) : mu;
 }
 
+// ---------------------------------------------------------------------------
+// Grouped-query decode on the tensor cores (bf16, G = 2, 4 or 8 query heads per
+// key/value head).  The G query rows and their G probe rows form one 16-row
+// operand [q; rho] (rows g and 8 + g: head g), so that per 16-key block one
+// warp computes
+//     [S; R] = [q; rho] K^T            (16 x 16, fp32, warp-level mma m16n8k16)
+// takes the online-softmax step on the scores it holds in registers, and
+//     [U; W] += [P; P o R] V           (16 x D, fp32)
+// with the MMA outputs of the first product reused in registers as the A
+// operand of the second.  Per key and head this replaces the SIMT decode's two
+// dot products and two axpys on the FMA pipes by a share of two tensor-core
+// products; the SIMT decode is issue-bound at G >= 2.  The operand has only 2G
+// real rows, below the 64-row minimum of tcgen05.mma, so the warp-level form
+// is the one that fits.
+//
+// The producer lane loads each stage of keys and values with TMA tile copies
+// (boxes of 64 columns x STAGE_KEYS rows, 128-byte swizzle), so that the
+// ldmatrix fragment loads of eight consecutive rows hit eight different bank
+// groups.  A paged cache is loaded the same way when its pages hold whole
+// stages (page_size a multiple of STAGE_KEYS); other page sizes use the SIMT
+// decode.  Four consumer warps take 16 keys (D = 128) or 32 keys (D = 64) of
+// every stage; at the end of an item their states are merged in shared memory
+// into the same partial-state / output format as decode_kernel (same plan,
+// workspace and combine kernel).
+constexpr int kMmaWarps = 4;
+constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
+constexpr int kMmaStages = 2;
+
+template <int D>
+struct MmaShape {
+    static constexpr int STAGE_KEYS = kStageRowBytes / (D * 2);
+    static constexpr int NCB = D / 64;                  // 64-column (128-byte) blocks per row
+    static constexpr int CB_BYTES = STAGE_KEYS * 128;   // one swizzled column block of a stage
+    static constexpr int KPW = STAGE_KEYS / kMmaWarps;  // keys per warp per stage
+    static_assert(KPW % 16 == 0, "16-key blocks");
+    static constexpr int STAGE_BYTES = NCB * CB_BYTES;
+    static constexpr int SLOT_FLOATS = 8 * (2 * D + 4);  // per warp: 8 heads x (U, W, m, l, A)
+    static constexpr int MERGE_OFF = 2 * kMmaStages * STAGE_BYTES;
+    static constexpr int BAR_OFF = MERGE_OFF + kMmaWarps * SLOT_FLOATS * 4;
+    static constexpr size_t SMEM_BYTES = BAR_OFF + 2 * kMmaStages * 8 + 16 + 1024;
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Byte offset in a stage of (row, 16-byte chunk c16 of the row): 128-byte swizzle
+// within each 64-column block.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int c16) {
+    using MS = MmaShape<D>;
+    return (uint32_t)((c16 >> 3) * MS::CB_BYTES + row * 128 + (((c16 & 7) ^ (row & 7)) << 4));
+}
+
+template <int D, bool RHO, bool SPLIT, int G, bool PAGED>
+__global__ void __launch_bounds__(kMmaThreads, 2)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const DecodeArgs a) {
+    using MS = MmaShape<D>;
+    using T = __nv_bfloat16;
+    constexpr int ROW_BYTES = D * 2;
+    extern __shared__ unsigned char smem_raw[];
+    // 128-byte swizzled TMA tiles need 1024-byte aligned destinations
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* stage_k = smem;
+    unsigned char* stage_v = smem + kMmaStages * MS::STAGE_BYTES;
+    float* merge = reinterpret_cast<float*>(smem + MS::MERGE_OFF);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + MS::BAR_OFF);
+    uint64_t* empty = full + kMmaStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMmaStages);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int BHkv = a.B * a.Hkv;
+    const int total = BHkv * a.nsplit;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMmaStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kMmaWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (*(volatile unsigned*)&g_decode_err & PARALLAX_DEVERR_WAIT_TIMEOUT) return;
+
+    if (warp == kMmaWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int slot = blockIdx.x; slot < total && ok; slot += gridDim.x) {
+            int bh, ch, start, end;
+            if (!item_range(a, slot, BHkv, bh, ch, start, end, SPLIT)) continue;
+            const int b = bh / a.Hkv, hk = bh - b * a.Hkv;
+            for (int t0 = start; t0 < end; t0 += MS::STAGE_KEYS, ++it) {
+                const int s = it % kMmaStages;
+                if (!mbar_wait(&empty[s], ((it / kMmaStages) & 1) ^ 1, &g_decode_err)) {
+                    ok = false;
+                    break;
+                }
+                // row of the first key of the stage in the [rows, D] view of the cache
+                int row0;
+                if (PAGED) {
+                    const int pg = t0 / a.page_size;  // a stage never crosses a page
+                    row0 = (checked_page(a, a.block_table[(size_t)b * a.max_pages + pg]) * a.Hkv + hk) *
+                               a.page_size + (t0 - pg * a.page_size);
+                } else {
+                    row0 = bh * a.Lmax + t0;
+                }
+                mbar_arrive_expect_tx(&full[s], 2u * MS::STAGE_BYTES);
+                for (int cb = 0; cb < MS::NCB; ++cb) {
+                    tc::tma_load_2d(stage_k + s * MS::STAGE_BYTES + cb * MS::CB_BYTES, &tmK, cb * 64,
+                                    row0, &full[s]);
+                    tc::tma_load_2d(stage_v + s * MS::STAGE_BYTES + cb * MS::CB_BYTES, &tmV, cb * 64,
+                                    row0, &full[s]);
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            // drain the copies still in flight into this CTA's shared memory
+            for (uint32_t k = (it >= kMmaStages ? it - kMmaStages : 0); k < it; ++k)
+                mbar_wait(&full[k % kMmaStages], (k / kMmaStages) & 1, &g_decode_err);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates: row g (and g + 8)
+    const float qs = a.qscale;
+    const uint32_t sk = smem_u32(stage_k), sv = smem_u32(stage_v);
+    float* slot = merge + warp * MS::SLOT_FLOATS;
+    uint32_t it = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+        int bh, ch, start, end;
+        if (!item_range(a, item, BHkv, bh, ch, start, end, SPLIT)) continue;
+        // A fragments of [q; rho]: row g = query head g of the group, row 8 + g its probe
+        uint32_t aq[D / 16][4];
+        {
+            const bool real = g < G;
+            const T* qr = static_cast<const T*>(a.q) + (size_t)(bh * G + (real ? g : 0)) * D;
+            const T* rr = RHO ? static_cast<const T*>(a.rho) + (size_t)(bh * G + (real ? g : 0)) * D
+                              : qr;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int c = 16 * kk + 2 * t;
+                aq[kk][0] = real ? __ldg(reinterpret_cast<const uint32_t*>(qr + c)) : 0u;
+                aq[kk][1] = real && RHO ? __ldg(reinterpret_cast<const uint32_t*>(rr + c)) : 0u;
+                aq[kk][2] = real ? __ldg(reinterpret_cast<const uint32_t*>(qr + c + 8)) : 0u;
+                aq[kk][3] = real && RHO ? __ldg(reinterpret_cast<const uint32_t*>(rr + c + 8)) : 0u;
+            }
+        }
+        float acc[D / 8][4];
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        float m = -INFINITY, l = 0.f, A = 0.f;
+        bool ok = true;
+        for (int t0 = start; t0 < end; t0 += MS::STAGE_KEYS, ++it) {
+            const int s = it % kMmaStages;
+            if (*abort_flag || !mbar_wait(&full[s], (it / kMmaStages) & 1, &g_decode_err)) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            const int nk = min(MS::STAGE_KEYS, end - t0);
+            const uint32_t kbase = sk + s * MS::STAGE_BYTES, vbase = sv + s * MS::STAGE_BYTES;
+#pragma unroll
+            for (int blk = 0; blk < MS::KPW / 16; ++blk) {
+                const int key0 = warp * MS::KPW + 16 * blk;
+                if (key0 >= nk) break;  // warp-uniform
+                // ---- [S; R] for keys key0 .. key0 + 15 (two n-tiles of 8 keys)
+                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                {
+                    const int mi = lane >> 3, r = lane & 7;
+                    const int row = key0 + (mi >> 1) * 8 + r;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kbase + swz<D>(row, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+                        mma_bf16_16816(c0, aq[kk], b0, b1);
+                        mma_bf16_16816(c1, aq[kk], b2, b3);
+                    }
+                }
+                // keys of this thread: key0 + 2t, +1 (c0) and key0 + 8 + 2t, +1 (c1)
+                const int kx = key0 + 2 * t;
+                const bool v0 = kx < nk, v1 = kx + 1 < nk, v2 = kx + 8 < nk, v3 = kx + 9 < nk;
+                const float s0 = v0 ? c0[0] * qs : -INFINITY, s1 = v1 ? c0[1] * qs : -INFINITY;
+                const float s2 = v2 ? c1[0] * qs : -INFINITY, s3 = v3 ? c1[1] * qs : -INFINITY;
+                float bm = fmaxf(fmaxf(s0, s1), fmaxf(s2, s3));
+                bm = fmaxf(bm, __shfl_xor_sync(kFullMask, bm, 1));
+                bm = fmaxf(bm, __shfl_xor_sync(kFullMask, bm, 2));
+                if (bm > m) {  // uniform over the 4 lanes of head g
+                    const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - bm);
+                    l *= alpha;
+                    A *= alpha;
+#pragma unroll
+                    for (int nt = 0; nt < D / 8; ++nt) {
+                        acc[nt][0] *= alpha;
+                        acc[nt][1] *= alpha;
+                        acc[nt][2] *= alpha;
+                        acc[nt][3] *= alpha;
+                    }
+                    m = bm;
+                }
+                const float p0 = fast_exp2(s0 - m), p1 = fast_exp2(s1 - m);
+                const float p2 = fast_exp2(s2 - m), p3 = fast_exp2(s3 - m);
+                const float q0 = v0 ? p0 * c0[2] : 0.f, q1 = v1 ? p1 * c0[3] : 0.f;
+                const float q2 = v2 ? p2 * c1[2] : 0.f, q3 = v3 ? p3 * c1[3] : 0.f;
+                l += (p0 + p1) + (p2 + p3);
+                A += (q0 + q1) + (q2 + q3);
+                const uint32_t pa[4] = {pack2_bf16(p0, p1), pack2_bf16(q0, q1), pack2_bf16(p2, p3),
+                                        pack2_bf16(q2, q3)};
+                if (key0 + 16 > nk) {
+                    // value rows past the chunk hold stale shared memory: zero them, since a
+                    // zero weight times a NaN would still be NaN in the product
+                    const int nz = key0 + 16 - nk;
+                    for (int e = lane; e < nz * (ROW_BYTES / 16); e += 32) {
+                        const int row = nk + e / (ROW_BYTES / 16), c16 = e % (ROW_BYTES / 16);
+                        *reinterpret_cast<uint4*>(stage_v + s * MS::STAGE_BYTES + swz<D>(row, c16)) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                }
+                // ---- [U; W] += [P; P o R] V
+                {
+                    const int mi = lane >> 3, r = lane & 7;
+                    const int row = key0 + (mi & 1) * 8 + r;
+#pragma unroll
+                    for (int np = 0; np < D / 16; ++np) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_trans(vbase + swz<D>(row, 2 * np + (mi >> 1)), b0, b1, b2, b3);
+                        mma_bf16_16816(acc[2 * np], pa, b0, b1);
+                        mma_bf16_16816(acc[2 * np + 1], pa, b2, b3);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        // ---- this warp's state -> its merge slot (rows of head g)
+        l += __shfl_xor_sync(kFullMask, l, 1);
+        l += __shfl_xor_sync(kFullMask, l, 2);
+        A += __shfl_xor_sync(kFullMask, A, 1);
+        A += __shfl_xor_sync(kFullMask, A, 2);
+        float* hs = slot + g * (2 * D + 4);
+        if (t == 0) {
+            hs[0] = m;
+            hs[1] = l;
+            hs[2] = A;
+        }
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+            *reinterpret_cast<float2*>(hs + 4 + 8 * nt + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2*>(hs + 4 + D + 8 * nt + 2 * t) =
+                make_float2(acc[nt][2], acc[nt][3]);
+        }
+        named_bar_sync(1, kMmaWarps * 32);
+        if (ok && !*abort_flag) {
+            for (int idx = threadIdx.x; idx < G * D; idx += kMmaWarps * 32) {
+                const int h2 = idx / D, c = idx - h2 * D;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kMmaWarps; ++w)
+                    M = fmaxf(M, merge[w * MS::SLOT_FLOATS + h2 * (2 * D + 4)]);
+                float ls = 0.f, As = 0.f, U = 0.f, W = 0.f;
+                if (M > -INFINITY) {
+#pragma unroll
+                    for (int w = 0; w < kMmaWarps; ++w) {
+                        const float* x = merge + w * MS::SLOT_FLOATS + h2 * (2 * D + 4);
+                        const float f = fast_exp2(x[0] - M);
+                        ls = fmaf(f, x[1], ls);
+                        As = fmaf(f, x[2], As);
+                        U = fmaf(f, x[4 + c], U);
+                        W = fmaf(f, x[4 + D + c], W);
+                    }
+                }
+                const int bq = bh * G + h2;
+                if (SPLIT) {
+                    const size_t idx2 = (size_t)bq * a.nsplit + ch;
+                    a.ws_uw[idx2 * 2 * D + c] = U;
+                    a.ws_uw[idx2 * 2 * D + D + c] = W;
+                    if (c == 0) a.ws_stats[idx2] = make_float4(M, ls, As, 0.f);
+                } else {
+                    const float inv_l = ls > 0.f ? 1.f / ls : 0.f;
+                    const float mu = U * inv_l;
+                    a.o[(size_t)bq * D + c] = RHO ? mu - (W * inv_l - (As * inv_l) * mu) : mu;
+                }
+            }
+        }
+        named_bar_sync(1, kMmaWarps * 32);
+    }
+}
+
+template <int D, bool RHO, bool SPLIT, int G, bool PAGED>
+cudaError_t launch_decode_mma_kernel(const DecodeArgs& a, int grid, cudaStream_t stream) {
+    using MS = MmaShape<D>;
+    auto kern = decode_mma_kernel<D, RHO, SPLIT, G, PAGED>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)MS::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    // the caches as [rows, D] bf16 tensors: (b, h_kv, key) -> row (b*H_kv + h_kv)*Lmax + key,
+    // or, paged, (page, h_kv, row) -> (page*H_kv + h_kv)*page_size + row
+    const uint64_t rows = PAGED ? (uint64_t)a.num_pages * a.Hkv * a.page_size
+                                : (uint64_t)a.B * a.Hkv * a.Lmax;
+    const uint64_t dims[2] = {(uint64_t)D, rows};
+    const uint64_t strides[1] = {(uint64_t)D * 2};
+    const uint32_t box[2] = {64, (uint32_t)MS::STAGE_KEYS};
+    CUtensorMap mk, mv;
+    if (!make_tmap_bf16(&mk, a.kc, 2, dims, strides, box) ||
+        !make_tmap_bf16(&mv, a.vc, 2, dims, strides, box))
+        return cudaErrorInvalidValue;
+    kern<<<grid, kMmaThreads, MS::SMEM_BYTES, stream>>>(mk, mv, a);
+    return cudaGetLastError();
+}
+
 template <typename T, int D, bool RHO, bool SPLIT, int G, bool PAGED>
 cudaError_t launch_decode_kernel(const DecodeArgs& a, int grid, cudaStream_t stream) {
     using SH = DecodeShape<T, D, G>;
@@ -351,13 +699,27 @@ cudaError_t run_decode(const DecodePlan& plan, const void* q, const void* rho, c
     const size_t BH = (size_t)plan.B * plan.H;
     a.ws_stats = static_cast<float4*>(ws);
     a.ws_uw = reinterpret_cast<float*>(static_cast<char*>(ws) + BH * plan.nsplit * sizeof(float4));
-    cudaError_t e;
+    cudaError_t e = cudaSuccess;
+    // grouped heads: the tensor-core decode (a paged cache only when every stage lies in one page)
+    constexpr bool kMmaOk = sizeof(T) == 2 && G >= 2;
+    const bool mma = kMmaOk && (!PAGED || (plan.page_size % MmaShape<D>::STAGE_KEYS == 0 &&
+                                           plan.chunk % MmaShape<D>::STAGE_KEYS == 0));
     if (plan.nsplit > 1) {
-        e = launch_decode_kernel<T, D, RHO, true, G, PAGED>(a, plan.grid, stream);
+        if constexpr (kMmaOk) {
+            if (mma) e = launch_decode_mma_kernel<D, RHO, true, G, PAGED>(a, plan.grid, stream);
+            else e = launch_decode_kernel<T, D, RHO, true, G, PAGED>(a, plan.grid, stream);
+        } else {
+            e = launch_decode_kernel<T, D, RHO, true, G, PAGED>(a, plan.grid, stream);
+        }
         if (e != cudaSuccess) return e;
         combine_kernel<D, RHO><<<(unsigned)BH, D, 0, stream>>>(a);
     } else {
-        e = launch_decode_kernel<T, D, RHO, false, G, PAGED>(a, plan.grid, stream);
+        if constexpr (kMmaOk) {
+            if (mma) e = launch_decode_mma_kernel<D, RHO, false, G, PAGED>(a, plan.grid, stream);
+            else e = launch_decode_kernel<T, D, RHO, false, G, PAGED>(a, plan.grid, stream);
+        } else {
+            e = launch_decode_kernel<T, D, RHO, false, G, PAGED>(a, plan.grid, stream);
+        }
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
