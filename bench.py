@@ -105,6 +105,24 @@ def prefill_flops(B, H, L, d):
     return 8.0 * d * (L * (L + 1) / 2) * B * H
 
 
+def reduce_max(x: float, dev, ws: int) -> float:
+    """The largest of the ranks' values (each rank passes its own); ws == 1: x itself."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(ws: int, units_per_rank: float, max_ms: float) -> float:
+    """Units per second of the whole job: every replica processes units_per_rank, the job
+    takes as long as its slowest rank (weak scaling, no exchange between replicas)."""
+    return ws * units_per_rank / (max_ms * 1e-3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -375,11 +393,7 @@ def run_ours(args):
             dist.barrier()
 
     def max_over_ranks(x: float) -> float:
-        if ws == 1:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dev, ws)
 
     # ---- inputs resident in HBM
     dc = configs.DECODE_UNIFORM
@@ -453,7 +467,7 @@ def run_ours(args):
     pre_ms = max(pre_ms, 1e-9)
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
     pre_tflops = pre_flops / (pre_ms * 1e-3) / 1e12
-    value = ws * dec_bytes / (dec_ms * 1e-3) / 1e9  # whole job: all replicas' bytes / max time
+    value = whole_job_rate(ws, dec_bytes, dec_ms) / 1e9  # all replicas' bytes / slowest time
 
     roof_dec = {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": dec_gbs / peaks["hbm_gbs"], "traffic": TRAFFIC_BYTES["decode"],
