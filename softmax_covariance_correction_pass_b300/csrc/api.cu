@@ -74,13 +74,13 @@ DeviceState* device_state(int* dev_out) {
 // persistent CTAs balance well (also for ragged lengths), with chunks of
 // 256..4096 keys: long enough that the 1 KB partial state per chunk is noise
 // next to the chunk's K/V bytes.
-int plan_chunk(int B, int H, int Lmax, int num_sms) {
+int plan_chunk(int B, int H, int Lmax, int num_sms, double items_per_sm = 16.0) {
     const int forced = g_chunk_override.load();
     int c;
     if (forced > 0) {
         c = forced;
     } else {
-        const double per_item = (double)B * H * Lmax / (16.0 * num_sms);
+        const double per_item = (double)B * H * Lmax / (items_per_sm * num_sms);
         c = 256;
         while (c < 4096 && (double)(2 * c) <= per_item) c *= 2;
     }
@@ -156,7 +156,9 @@ parallax::DecodePlan make_plan(int B, int H, int Hkv, int Lmax, int d, int num_s
     plan.max_pages = max_pages;
     plan.num_pages = num_pages;
     plan.scale = 1.0f / std::sqrt((float)d);
-    plan.chunk = plan_chunk(B, Hkv, Lmax, num_sms);
+    // grouped heads run the tensor-core decode, whose per-key cost is lower and whose
+    // per-item merge costs more: half as many items, twice the keys each
+    plan.chunk = plan_chunk(B, Hkv, Lmax, num_sms, H > Hkv ? 8.0 : 16.0);
     if (page_size > 0 && plan.chunk > parallax::decode_paged_max_chunk(page_size)) plan.chunk = 4096;
     plan.nsplit = (Lmax + plan.chunk - 1) / plan.chunk;
     const long long items = (long long)B * Hkv * plan.nsplit;

@@ -128,8 +128,8 @@ struct KvLayout {
     static constexpr int STAGE = QR_BYTES + DO_BYTES + 1024;  // + 64 row stats
     static constexpr int ST_OFF = 2 * OPB;
     static constexpr int BAR_OFF = ST_OFF + 2 * STAGE;
-    // kv_full, qr_full[2], qr_empty[2], s_full, p_full, o_full
-    static constexpr int NBARS = 8;
+    // kv_full, qr_full[2], qr_empty[2], s_full, p_part[2], o_full
+    static constexpr int NBARS = 9;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
     // TMEM columns
     static constexpr uint32_t SR = 0, DT = 128, DV = 256, DK = 256 + D;
@@ -149,8 +149,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     uint64_t* qr_full = bars + 1;
     uint64_t* qr_empty = bars + 3;
     uint64_t* s_full = bars + 5;
-    uint64_t* p_full = bars + 6;
-    uint64_t* o_full = bars + 7;
+    uint64_t* p_part = bars + 6;  // W, dS, dR of queries 32c .. 32c + 31 are in TMEM
+    uint64_t* o_full = bars + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const int n_t = a.n_qt - qt0;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], b == 6 ? 128 : 1);
+        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], (b == 6 || b == 7) ? 128 : 1);
         *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
         fence_mbar_init();
     }
@@ -253,35 +253,34 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     tc::mma_ss(tmem + LY::DT, dV + offA, dDO + offB, kIdescB, kk > 0);
                 }
                 tc::commit(s_full);
-                if (!mbar_wait_warp(p_full, t & 1, &g_bwd_err)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
                 // MN-major views of the same tiles: rows = queries (the K dimension)
                 const uint64_t mQR = tc::opaque(tc::smem_desc_sw128(stb, SUB, 1024) + st * kStStep);
                 const uint64_t mDO =
                     tc::opaque(tc::smem_desc_sw128(stb + LY::QR_BYTES, SUB64, 1024) + st * kStStep);
+                // the gradient MMAs of each 32-query half start as soon as the compute
+                // warps have handed that half over, overlapping the other half's compute
+                for (int c = 0; c < 2 && ok; ++c) {
+                    if (!mbar_wait_warp(&p_part[c], t & 1, &g_bwd_err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {  // dV += W dO
-                    const uint32_t acol = LY::SR + 32 * (kk >> 1) + 8 * (kk & 1);
-                    tc::mma_ts(tmem + LY::DV, tmem + acol, mDO + ((kk * 16 * 128) >> 4), kIdescMN,
-                               (t > 0 || kk > 0) ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {  // dK += dS Q  (scale folded into dS)
-                    const uint32_t acol = LY::SR + 32 * (kk >> 1) + 16 + 8 * (kk & 1);
-                    tc::mma_ts(tmem + LY::DK, tmem + acol, mQR + ((kk * 16 * 128) >> 4), kIdescMN,
-                               (t > 0 || kk > 0) ? 1u : 0u);
-                }
-                if (RHO) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {  // dK += dR rho
-                        const uint32_t acol = LY::SR + 64 + 32 * (kk >> 1) + 8 * (kk & 1);
-                        tc::mma_ts(tmem + LY::DK, tmem + acol, mQR + (((64 + kk * 16) * 128) >> 4),
-                                   kIdescMN, 1u);
+                    for (int h = 0; h < 2; ++h) {
+                        const int kk = 2 * c + h;  // queries 16kk .. 16kk + 15
+                        const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                        // dV += W dO
+                        tc::mma_ts(tmem + LY::DV, tmem + LY::SR + 32 * c + 8 * h,
+                                   mDO + ((kk * 16 * 128) >> 4), kIdescMN, acc);
+                        // dK += dS Q  (scale folded into dS)
+                        tc::mma_ts(tmem + LY::DK, tmem + LY::SR + 32 * c + 16 + 8 * h,
+                                   mQR + ((kk * 16 * 128) >> 4), kIdescMN, acc);
+                        if (RHO)  // dK += dR rho
+                            tc::mma_ts(tmem + LY::DK, tmem + LY::SR + 64 + 32 * c + 8 * h,
+                                       mQR + (((64 + kk * 16) * 128) >> 4), kIdescMN, 1u);
                     }
                 }
+                if (!ok) break;
                 tc::commit(&qr_empty[st]);
             }
             tc::commit(o_full);
@@ -353,10 +352,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 tc::tmem_st16(trow + LY::SR + 32 * c, wpk);
                 tc::tmem_st16(trow + LY::SR + 32 * c + 16, spk);
                 if (RHO) tc::tmem_st16(trow + LY::SR + 64 + 32 * c, rpk);
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+                mbar_arrive(&p_part[c]);  // this half's gradient MMAs may start
             }
-            tc::tmem_st_wait();
-            tc::fence_before_sync();
-            mbar_arrive(p_full);
         }
         const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
         if (__all_sync(kFullMask, done)) {
