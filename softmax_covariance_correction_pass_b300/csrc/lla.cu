@@ -8,11 +8,14 @@
 //   rho = Sigma_kk^-1 (mu_k - q)    by conjugate gradient from rho = 0
 //   o   = mu_v - C^T rho            (the Parallax decode with that rho)
 //
-// lla_probe_kernel: one CTA per (b, h).  Pass 1 streams the head's keys through
-// shared memory in tiles of 32 (bf16 -> fp32), keeps an online-softmax max,
-// and accumulates l = sum p, sum p k and the p-weighted second moment
-// sum p k k^T (each of the 256 threads owns a (D/16) x (D/16) block of it, in
-// registers).  The centred covariance then goes to shared memory and the CG
+// lla_probe_kernel: one CTA per (b, h), 8 warps.  Pass 1 streams the head's keys
+// through shared memory in tiles of 32, keeps an online-softmax max, and
+// accumulates l = sum p and sum p k on the FMA pipes and the p-weighted second
+// moment G = sum_j k_j (p_j k_j)^T on the tensor cores: warp w owns rows
+// 16w .. 16w + 15 of G as warp-level mma.sync m16n8k16 accumulators (fp32), with
+// A = the keys (exact bf16) and B = p_j k_j split into a bf16 high part and a
+// bf16 residual (two MMAs, so the product keeps ~16 bits).  The centred
+// covariance then goes to shared memory (over the dead key tiles) and the CG
 // iterations run there (matrix-vector products split over 256 threads, dot
 // products by block reduction), stopping after `iters` steps or at a relative
 // residual of 1e-6.  The probe is written in fp32 (returned) and bf16 (for the
@@ -39,6 +42,18 @@ struct LlaArgs {
 
 __device__ unsigned g_lla_err = 0;
 
+__device__ __forceinline__ uint32_t smem_u32_lla(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint32_t smem_u32_lla(uint32_t a) { return a; }
+
+// Two fp32 -> packed bf16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16_lla(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Sum over the block; every thread gets the result.  `red` holds 8 floats.
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -52,22 +67,58 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return s;
 }
 
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32_lla(addr)));
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) lla_probe_kernel(const LlaArgs a) {
-    constexpr int BS = D / 16;          // this thread's block of the second moment: BS x BS
+struct LlaLayout {
+    static constexpr int PITCH = D * 2 + 16;  // bytes per bf16 key row: conflict-free ldmatrix
+    static constexpr int KT_F32 = 0;                                 // [kTile][D] fp32 keys
+    static constexpr int KT_B16 = KT_F32 + kTile * D * 4;            // [kTile][PITCH] bf16 keys
+    static constexpr int PK_HI = KT_B16 + kTile * PITCH;             // bf16(p k)
+    static constexpr int PK_LO = PK_HI + kTile * PITCH;              // bf16(p k - hi)
+    static constexpr int TILES_END = PK_LO + kTile * PITCH;
+    static constexpr int SIG_BYTES = D * (D + 1) * 4;                // covariance (aliases tiles)
+    static constexpr int VEC_OFF = (TILES_END > SIG_BYTES ? TILES_END : SIG_BYTES);
+    static constexpr size_t SMEM_BYTES = VEC_OFF + sizeof(float) * (6 * D + 2 * kTile + 8);
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2) lla_probe_kernel(const LlaArgs a) {
+    using LY = LlaLayout<D>;
     constexpr int TPR = kThreads / D;   // threads per matrix row in the CG products
     constexpr int LD = D + 1;           // padded row stride of the covariance (bank spread)
-    extern __shared__ __align__(16) float sm[];
-    float* kt = sm;                     // [kTile][D] key tile (fp32)
-    float* sig = kt + kTile * D;        // [D][LD] covariance
-    float* qv = sig + D * LD;           // [D] query
+    // warp -> a 16-row stripe and a column group of the Gram matrix
+    constexpr int STRIPES = D / 16, CGS = (kThreads / 32) / STRIPES, COLS = D / CGS, NT = COLS / 8;
+    static_assert(STRIPES * CGS == kThreads / 32 && NT % 2 == 0, "Gram matrix tiling");
+    extern __shared__ __align__(16) unsigned char smb[];
+    float* kt = reinterpret_cast<float*>(smb + LY::KT_F32);   // [kTile][D] key tile (fp32)
+    unsigned char* kb16 = smb + LY::KT_B16;
+    unsigned char* pkh = smb + LY::PK_HI;
+    unsigned char* pkl = smb + LY::PK_LO;
+    float* sig = reinterpret_cast<float*>(smb);               // [D][LD], after pass 1
+    float* qv = reinterpret_cast<float*>(smb + LY::VEC_OFF);  // [D] query
     float* mu = qv + D;                 // [D] mu_k
     float* xv = mu + D;                 // [D] CG iterate
     float* rv = xv + D;                 // [D] residual
     float* pv = rv + D;                 // [D] search direction
     float* ap = pv + D;                 // [D] Sigma p
     float* s2 = ap + D;                 // [kTile] scaled scores of the tile
-    float* red = s2 + kTile;            // [8] reduction scratch
+    float* pw = s2 + kTile;             // [kTile] their weights p = 2^(s - m)
+    float* red = pw + kTile;            // [8] reduction scratch
 
     const int t = threadIdx.x, warp = t / 32, lane = t % 32;
     const int bh = blockIdx.x, b = bh / a.H;
@@ -80,27 +131,24 @@ __global__ void __launch_bounds__(kThreads, 1) lla_probe_kernel(const LlaArgs a)
     __syncthreads();
 
     // ---------------------------------------------------------------- pass 1
-    const int ra = BS * (t >> 4), cb = BS * (t & 15);
-    float acc[BS][BS];
+    const int stripe = warp % STRIPES, col0 = (warp / STRIPES) * COLS;
+    float acc[NT][4];  // rows 16 stripe + g (and + 8) of G, columns col0 + 8 nt + 2 (lane & 3) (+1)
 #pragma unroll
-    for (int x = 0; x < BS; ++x)
-#pragma unroll
-        for (int y = 0; y < BS; ++y) acc[x][y] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     float muacc = 0.f, l = 0.f, m = -INFINITY;
     const __nv_bfloat16* kh = a.kc + (size_t)bh * a.Lmax * D;
     constexpr int VPR = D / 8;  // 16-byte vectors per key row
+    const int mi = lane >> 3, r8 = lane & 7;
     for (int j0 = 0; j0 < n; j0 += kTile) {
         const int nk = min(kTile, n - j0);
         __syncthreads();  // the previous tile is consumed
         for (int vi = t; vi < kTile * VPR; vi += kThreads) {
             const int row = vi / VPR, c8 = (vi - row * VPR) * 8;
+            uint4 raw = make_uint4(0, 0, 0, 0);
+            if (row < nk) raw = ld_global_16(kh + (size_t)(j0 + row) * D + c8);
+            *reinterpret_cast<uint4*>(kb16 + row * LY::PITCH + c8 * 2) = raw;
             float f[8];
-            if (row < nk) {
-                Vec16<__nv_bfloat16>::unpack(ld_global_16(kh + (size_t)(j0 + row) * D + c8), f);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = 0.f;
-            }
+            Vec16<__nv_bfloat16>::unpack(raw, f);
 #pragma unroll
             for (int e = 0; e < 8; ++e) kt[row * D + c8 + e] = f[e];
         }
@@ -126,37 +174,71 @@ __global__ void __launch_bounds__(kThreads, 1) lla_probe_kernel(const LlaArgs a)
             l *= alpha;
             muacc *= alpha;
 #pragma unroll
-            for (int x = 0; x < BS; ++x)
-#pragma unroll
-                for (int y = 0; y < BS; ++y) acc[x][y] *= alpha;
+            for (int nt = 0; nt < NT; ++nt) {
+                acc[nt][0] *= alpha;
+                acc[nt][1] *= alpha;
+                acc[nt][2] *= alpha;
+                acc[nt][3] *= alpha;
+            }
             m = m_new;
         }
+        if (t < kTile) pw[t] = fast_exp2(s2[t] - m);  // 0 for keys past the sequence
+        __syncthreads();
+        // p_j k_j as a bf16 pair (high part, residual): the B operand of the Gram MMAs
+        for (int e = t; e < kTile * D / 2; e += kThreads) {
+            const int row = e / (D / 2), c2 = 2 * (e - row * (D / 2));
+            const float p = pw[row];
+            const float v0 = p * kt[row * D + c2], v1 = p * kt[row * D + c2 + 1];
+            const uint32_t hi = pack_bf16_lla(v0, v1);
+            const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+            *reinterpret_cast<uint32_t*>(pkh + row * LY::PITCH + c2 * 2) = hi;
+            *reinterpret_cast<uint32_t*>(pkl + row * LY::PITCH + c2 * 2) = pack_bf16_lla(v0 - h0, v1 - h1);
+        }
         for (int j = 0; j < nk; ++j) {
-            const float p = fast_exp2(s2[j] - m);
+            const float p = pw[j];
             l += p;
-            float ka[BS], kb[BS];
-#pragma unroll
-            for (int x = 0; x < BS; ++x) {
-                ka[x] = p * kt[j * D + ra + x];
-                kb[x] = kt[j * D + cb + x];
-            }
-#pragma unroll
-            for (int x = 0; x < BS; ++x)
-#pragma unroll
-                for (int y = 0; y < BS; ++y) acc[x][y] = fmaf(ka[x], kb[y], acc[x][y]);
             if (t < D) muacc = fmaf(p, kt[j * D + t], muacc);
+        }
+        __syncthreads();
+        // G[stripe rows][column group] += K[:, stripe]^T (p K)[:, group] over the tile's keys
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks) {
+            const int j0k = 16 * ks;
+            uint32_t af[4];
+            ldsm_x4_t(smem_u32_lla(kb16) + (j0k + (mi >> 1) * 8 + r8) * LY::PITCH +
+                          (16 * stripe + (mi & 1) * 8) * 2,
+                      af[0], af[1], af[2], af[3]);
+            // ldmatrix.trans hands out A fragments in the order (rows g, g+8) x (keys lo, hi)
+            const uint32_t a4[4] = {af[0], af[1], af[2], af[3]};
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                const uint32_t off =
+                    (j0k + (mi & 1) * 8 + r8) * LY::PITCH + (col0 + 16 * np + (mi >> 1) * 8) * 2;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(smem_u32_lla(pkh) + off, b0, b1, b2, b3);
+                mma_16816(acc[2 * np], a4, b0, b1);
+                mma_16816(acc[2 * np + 1], a4, b2, b3);
+                ldsm_x4_t(smem_u32_lla(pkl) + off, b0, b1, b2, b3);
+                mma_16816(acc[2 * np], a4, b0, b1);
+                mma_16816(acc[2 * np + 1], a4, b2, b3);
+            }
         }
     }
 
     // ---------------------------------------------------------------- covariance
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     if (t < D) mu[t] = muacc * inv_l;
-    __syncthreads();
+    __syncthreads();  // the key tiles are dead: sig takes their place
+    {
+        const int g = lane >> 2, c = 2 * (lane & 3);
 #pragma unroll
-    for (int x = 0; x < BS; ++x)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int y = 0; y < BS; ++y)
-            sig[(ra + x) * LD + cb + y] = acc[x][y] * inv_l - mu[ra + x] * mu[cb + y];
+            for (int e = 0; e < 4; ++e) {
+                const int row = 16 * stripe + g + 8 * (e >> 1), col = col0 + 8 * nt + c + (e & 1);
+                sig[row * LD + col] = acc[nt][e] * inv_l - mu[row] * mu[col];
+            }
+    }
     if (t < D) {
         const float bt = n > 0 ? mu[t] - qv[t] : 0.f;
         xv[t] = 0.f;
@@ -200,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) lla_probe_kernel(const LlaArgs a)
 
 template <int D>
 size_t smem_bytes() {
-    return sizeof(float) * ((size_t)kTile * D + (size_t)D * (D + 1) + 6 * D + kTile + 8);
+    return LlaLayout<D>::SMEM_BYTES;
 }
 
 template <int D>
