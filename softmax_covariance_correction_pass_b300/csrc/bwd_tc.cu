@@ -14,7 +14,7 @@
 // p is recomputed from the forward's per-row log-sum-exp.
 //
 // Three kernels, in stream order:
-//   bwd_pre_kernel  per row: (lse2, rbar, abar, delta) into a row-stats buffer;
+//   bwd_pre_kernel  per row: (-lse2, 1 + rbar, abar, delta - abar) into a row-stats buffer;
 //   bwd_kv_kernel   per 128-key tile: loops over 64-query tiles; MMAs
 //                   [S^T | R^T] = K [Q; rho]^T and D^T = V dO^T, the compute
 //                   warps form W, dS, dR (bf16, written back to TMEM), MMAs
@@ -25,6 +25,8 @@
 //                   warps form dS, dR, MMA [dQ; drho] += [dS; dR] K.
 // Every contraction is a tcgen05.mma with bf16 operands and fp32 TMEM
 // accumulators; K, V and the query-side tiles arrive by TMA (128-byte swizzle).
+#include <type_traits>
+
 #include "tcgen05.cuh"
 #include "kernels.h"
 
@@ -46,7 +48,9 @@ struct BwdArgs {
     const __nv_bfloat16* dout;    // [BH, L, D] gradient of o
     const float* lse;             // [BH, L]
     const float* rbar;            // [BH, L]
-    float* rs;                    // [BH][4][Lp]: lse2, rbar, abar, delta of each row (0 past L)
+    // [BH][4][Lp] per row (0 past L): -lse log2(e), 1 + rbar, abar, delta - abar -- the
+    // forms the per-pair arithmetic uses directly
+    float* rs;
     float* dq;
     float* drho;
     float* dk;
@@ -105,14 +109,43 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
         de += __shfl_xor_sync(kFullMask, de, off);
     }
     if (lane == 0) {
-        out[0] = a.lse[row] * kLog2e;
-        out[a.Lp] = a.rbar[row];
+        out[0] = -a.lse[row] * kLog2e;
+        out[a.Lp] = 1.f + a.rbar[row];
         out[2 * (size_t)a.Lp] = ab;
-        out[3 * (size_t)a.Lp] = de;
+        out[3 * (size_t)a.Lp] = de - ab;
     }
 }
 
 __device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
+
+// The per-(query, key) gradient terms for two pairs at once (packed fp32x2).  In:
+// the scores s, probe scores r and D = dO.v of the pairs; the rows' statistics
+// nl = -lse log2(e), rb1 = 1 + rbar, ab = abar, ne = delta - abar; keep = which
+// of the two pairs are visible.  With g = 1 + rbar - r and u = abar - D:
+//   w = p g,   dr = p u,   ds scale = p (u g + ne) (-scale)
+// (u g + ne = -((D - abar)(rbar - r) + D - delta)).
+struct PairTerms {
+    float2 w, ds, dr;
+};
+template <bool MASKED, bool WANT_W>
+__device__ __forceinline__ PairTerms pair_terms(float2 s, float2 r, float2 d, float2 qs2, float2 nl,
+                                                float2 rb1, float2 ab, float2 ne, float2 nsc2,
+                                                bool keep0, bool keep1) {
+    const float2 m1 = make_float2(-1.f, -1.f);
+    const float2 t = __ffma2_rn(s, qs2, nl);
+    float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+    if (MASKED) {
+        p.x = keep0 ? p.x : 0.f;
+        p.y = keep1 ? p.y : 0.f;
+    }
+    const float2 g = __ffma2_rn(r, m1, rb1);
+    const float2 u = __ffma2_rn(d, m1, ab);
+    PairTerms o;
+    if (WANT_W) o.w = __fmul2_rn(p, g);
+    o.dr = __fmul2_rn(p, u);
+    o.ds = __fmul2_rn(__fmul2_rn(p, __ffma2_rn(u, g, ne)), nsc2);
+    return o;
+}
 
 // ------------------------------------------------------------------------ dK, dV
 // One 128-key tile per CTA, 64-query tiles in a 2-deep TMA ring; warp 0 TMA,
@@ -305,11 +338,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             }
             tc::fence_after_sync();
             const int q0 = (qt0 + t) * 64;
-            // row statistics of the tile: lse2[64], rbar[64], abar[64], delta[64]
+            // row statistics of the tile: -lse2[64], 1 + rbar[64], abar[64], delta - abar[64]
             const float* rst = reinterpret_cast<const float*>(smem + LY::ST_OFF + st * LY::STAGE +
                                                               LY::QR_BYTES + LY::DO_BYTES);
-            const float2 qs2 = make_float2(qs, qs), sc2 = make_float2(scale, scale);
-            const float2 one2 = make_float2(1.f, 1.f);
+            const float2 qs2 = make_float2(qs, qs), nsc2 = make_float2(-scale, -scale);
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 uint32_t sv[32], rv[32], dv[32];
@@ -324,30 +356,40 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 if (CAUSAL && j > qc) vmask &= j - qc >= 32 ? 0u : ~((1u << (j - qc)) - 1u);
                 const float* st0 = rst + 32 * c;
                 uint32_t wpk[16], spk[16], rpk[16];
+                auto run = [&](auto masked) {
+                    constexpr bool M = decltype(masked)::value;
 #pragma unroll
-                for (int y = 0; y < 16; ++y) {
-                    const int x = 2 * y;
-                    const float2 lse = *reinterpret_cast<const float2*>(st0 + x);
-                    const float2 rb = *reinterpret_cast<const float2*>(st0 + 64 + x);
-                    const float2 ab = *reinterpret_cast<const float2*>(st0 + 128 + x);
-                    const float2 de = *reinterpret_cast<const float2*>(st0 + 192 + x);
-                    const float2 s2 = make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]));
-                    const float2 r2 = RHO ? make_float2(__uint_as_float(rv[x]), __uint_as_float(rv[x + 1]))
-                                          : make_float2(0.f, 0.f);
-                    const float2 d2 = make_float2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1]));
-                    const float2 t = __ffma2_rn(s2, qs2, neg2(lse));
-                    float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-                    p.x = (vmask >> x) & 1u ? p.x : 0.f;
-                    p.y = (vmask >> (x + 1)) & 1u ? p.y : 0.f;
-                    const float2 rr = __fadd2_rn(rb, neg2(r2));  // rbar - r
-                    const float2 w = __fmul2_rn(p, __fadd2_rn(one2, rr));
-                    const float2 f = __ffma2_rn(__fadd2_rn(d2, neg2(ab)), rr, __fadd2_rn(d2, neg2(de)));
-                    const float2 ds = __fmul2_rn(__fmul2_rn(p, f), sc2);
-                    const float2 dr = __fmul2_rn(p, __fadd2_rn(ab, neg2(d2)));
-                    wpk[y] = tc::pack_bf16(w.x, w.y);
-                    spk[y] = tc::pack_bf16(ds.x, ds.y);
-                    rpk[y] = tc::pack_bf16(dr.x, dr.y);
-                }
+                    for (int y4 = 0; y4 < 8; ++y4) {  // four queries per step: 128-bit stat loads
+                        const int x4 = 4 * y4;
+                        const float4 nl = *reinterpret_cast<const float4*>(st0 + x4);
+                        const float4 rb = *reinterpret_cast<const float4*>(st0 + 64 + x4);
+                        const float4 ab = *reinterpret_cast<const float4*>(st0 + 128 + x4);
+                        const float4 ne = *reinterpret_cast<const float4*>(st0 + 192 + x4);
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int x = x4 + 2 * hh, y = x / 2;
+                            const float2 s2 = make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]));
+                            const float2 r2 = RHO ? make_float2(__uint_as_float(rv[x]),
+                                                                __uint_as_float(rv[x + 1]))
+                                                  : make_float2(0.f, 0.f);
+                            const float2 d2 = make_float2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1]));
+                            const PairTerms pt = pair_terms<M, true>(
+                                s2, r2, d2, qs2, hh ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y),
+                                hh ? make_float2(rb.z, rb.w) : make_float2(rb.x, rb.y),
+                                hh ? make_float2(ab.z, ab.w) : make_float2(ab.x, ab.y),
+                                hh ? make_float2(ne.z, ne.w) : make_float2(ne.x, ne.y), nsc2,
+                                (vmask >> x) & 1u, (vmask >> (x + 1)) & 1u);
+                            wpk[y] = tc::pack_bf16(pt.w.x, pt.w.y);
+                            spk[y] = tc::pack_bf16(pt.ds.x, pt.ds.y);
+                            rpk[y] = tc::pack_bf16(pt.dr.x, pt.dr.y);
+                        }
+                    }
+                };
+                // warp-uniform: every (key, query) pair of the warp's half tile is visible
+                if (__all_sync(kFullMask, vmask == 0xffffffffu))
+                    run(std::false_type{});
+                else
+                    run(std::true_type{});
                 // (columns already read above: W, dS over S^T, dR over R^T)
                 tc::tmem_st16(trow + LY::SR + 32 * c, wpk);
                 tc::tmem_st16(trow + LY::SR + 32 * c + 16, spk);
@@ -598,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t rowR = tmem + ((uint32_t)(32 * g + 16) << 16);
         const uint32_t Y = LY::YW * grp, pk = LY::PK + 32 * grp;
         const float qs = a.qscale, scale = a.scale;
-        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);  // (lse2, rbar, abar, delta)
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);  // (-lse2, 1 + rbar, abar, delta - abar)
         if (i < a.L) {
             const float* zr = a.rs + (size_t)bh * 4 * a.Lp + i;
             z = make_float4(zr[0], zr[a.Lp], zr[2 * (size_t)a.Lp], zr[3 * (size_t)a.Lp]);
@@ -622,28 +664,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t vmask = i >= a.L || lim < 0 ? 0u
                                    : lim >= 31     ? 0xffffffffu
                                                    : ((2u << lim) - 1u);
-            const float2 qs2 = make_float2(qs, qs), sc2 = make_float2(scale, scale);
-            const float2 nl2 = make_float2(-z.x, -z.x), rb2 = make_float2(z.y, z.y);
-            const float2 ab2 = make_float2(z.z, z.z), de2 = make_float2(z.w, z.w);
+            const float2 qs2 = make_float2(qs, qs), nsc2 = make_float2(-scale, -scale);
+            const float2 nl2 = make_float2(z.x, z.x), rb2 = make_float2(z.y, z.y);
+            const float2 ab2 = make_float2(z.z, z.z), ne2 = make_float2(z.w, z.w);
             uint32_t spk[16], rpk[16];
+            auto run = [&](auto masked) {
+                constexpr bool M = decltype(masked)::value;
 #pragma unroll
-            for (int y = 0; y < 16; ++y) {
-                const int x = 2 * y;
-                const float2 s2 = make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]));
-                const float2 r2 = RHO ? make_float2(__uint_as_float(rv[x]), __uint_as_float(rv[x + 1]))
-                                      : make_float2(0.f, 0.f);
-                const float2 d2 = make_float2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1]));
-                const float2 t = __ffma2_rn(s2, qs2, nl2);
-                float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-                p.x = (vmask >> x) & 1u ? p.x : 0.f;
-                p.y = (vmask >> (x + 1)) & 1u ? p.y : 0.f;
-                const float2 dr = __fmul2_rn(p, __fadd2_rn(ab2, neg2(d2)));
-                const float2 f = __ffma2_rn(__fadd2_rn(d2, neg2(ab2)), __fadd2_rn(rb2, neg2(r2)),
-                                            __fadd2_rn(d2, neg2(de2)));
-                const float2 ds = __fmul2_rn(__fmul2_rn(p, f), sc2);
-                spk[y] = tc::pack_bf16(ds.x, ds.y);
-                rpk[y] = tc::pack_bf16(dr.x, dr.y);
-            }
+                for (int y = 0; y < 16; ++y) {
+                    const int x = 2 * y;
+                    const float2 s2 = make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]));
+                    const float2 r2 = RHO ? make_float2(__uint_as_float(rv[x]), __uint_as_float(rv[x + 1]))
+                                          : make_float2(0.f, 0.f);
+                    const float2 d2 = make_float2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1]));
+                    const PairTerms pt = pair_terms<M, false>(s2, r2, d2, qs2, nl2, rb2, ab2, ne2, nsc2,
+                                                              (vmask >> x) & 1u, (vmask >> (x + 1)) & 1u);
+                    spk[y] = tc::pack_bf16(pt.ds.x, pt.ds.y);
+                    rpk[y] = tc::pack_bf16(pt.dr.x, pt.dr.y);
+                }
+            };
+            // warp-uniform: every (query, key) pair of the warp's tile is visible
+            if (__all_sync(kFullMask, vmask == 0xffffffffu))
+                run(std::false_type{});
+            else
+                run(std::true_type{});
             // packed operand slot (key 2c, 2c+1 at column pk + c): dS in the query lanes,
             // dR in the probe lanes
             tc::tmem_st16_split<16>(rowS + pk, spk);
