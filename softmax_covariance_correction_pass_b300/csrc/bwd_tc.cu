@@ -436,29 +436,34 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 }
 
 // ------------------------------------------------------------------------ dQ, drho
-// One 64-query tile per CTA (the forward's stacked lane layout), 64-key tiles in
-// a 4-deep TMA ring.  Two TMEM buffers Y0, Y1 of [S|R 64 | D 64] columns and two
-// packed operand slots let the key tiles ping-pong between compute group
-// g (warps 4+4g .. 7+4g, key tiles j = g mod 2) and the tensor core.
-constexpr int Q_KT = 64;       // keys per tile
-constexpr int Q_STAGES = 4;
+// One 64-query tile per CTA (the forward's stacked lane layout), 128-key tiles
+// (K in a 3-deep TMA ring, V in a 2-deep one).  TMEM: Y = [S; R] (128 columns)
+// and [D; D] (128 columns) of the current key tile, the [dQ; drho] accumulator,
+// and two packed dS/dR operand slots.  The compute warps release Y as soon as
+// they have loaded it, so the MMAs of key tile t + 1 run while they work on
+// tile t; [dQ; drho] += [dS; dR] K of tile t follows.  Every MMA has N = 128
+// (the tensor core's full rate; N = 64 runs at ~60% of it).  Eight compute
+// warps: two per TMEM lane quarter, each taking 64 of the 128 key columns.
+constexpr int Q_KT = 128;     // keys per tile
+constexpr int Q_KSTAGES = 3;  // K is read by two MMA groups (S|R of its tile, then dQ)
+constexpr int Q_VSTAGES = 2;
 
 template <int D>
 struct QLayout {
     static constexpr int NCB = D / 64;
-    static constexpr int OPB = NCB * SUB;             // [128 x D] operand
-    static constexpr int KSUB = Q_KT * 128;           // [64 keys x 64 columns]
-    static constexpr int KT_BYTES = NCB * KSUB;       // one 64-key tile of K (or V)
+    static constexpr int OPB = NCB * SUB;             // [128 x D] operand, also one K or V tile
     static constexpr int QR_OFF = 0;                  // stacked [Q; rho] (16-row groups)
     static constexpr int DO_OFF = OPB;                // stacked [dO; dO]
     static constexpr int K_OFF = 2 * OPB;             // K ring
-    static constexpr int V_OFF = K_OFF + Q_STAGES * KT_BYTES;  // V ring
-    static constexpr int BAR_OFF = V_OFF + Q_STAGES * KT_BYTES;
-    // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_full
-    static constexpr int NBARS = 4 * Q_STAGES + 6;
+    static constexpr int V_OFF = K_OFF + Q_KSTAGES * OPB;  // V ring
+    static constexpr int BAR_OFF = V_OFF + Q_VSTAGES * OPB;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full, y_free, p_full[2],
+    // pk_empty[2], o_full
+    static constexpr int B_S = 1 + 2 * Q_KSTAGES + 2 * Q_VSTAGES;
+    static constexpr int NBARS = B_S + 7;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
-    // TMEM columns: Y_g = 128 g: [S|R] (64), [D|D] (64); accumulator; packed dS/dR slots
-    static constexpr uint32_t YW = 128, O = 256, PK = 384;
+    // TMEM columns: [S; R] at 0, [D; D] at YD, the accumulator at O, packed slots at PK
+    static constexpr uint32_t YD = 128, O = 256, PK = 256 + D;
 };
 
 template <int D, bool CAUSAL, bool RHO>
@@ -467,19 +472,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmO, const BwdArgs a) {
     using LY = QLayout<D>;
-    constexpr int S = Q_STAGES;
+    constexpr int KS = Q_KSTAGES, VS = Q_VSTAGES;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
     uint64_t* q_full = bars;
     uint64_t* k_full = bars + 1;
-    uint64_t* v_full = bars + 1 + S;
-    uint64_t* k_empty = bars + 1 + 2 * S;
-    uint64_t* v_empty = bars + 1 + 3 * S;
-    uint64_t* s_full = bars + 1 + 4 * S;
-    uint64_t* p_full = bars + 3 + 4 * S;
-    uint64_t* o_full = bars + 5 + 4 * S;
+    uint64_t* k_empty = bars + 1 + KS;
+    uint64_t* v_full = bars + 1 + 2 * KS;
+    uint64_t* v_empty = bars + 1 + 2 * KS + VS;
+    uint64_t* s_full = bars + LY::B_S;
+    uint64_t* y_free = bars + LY::B_S + 1;    // the compute warps have loaded Y
+    uint64_t* p_full = bars + LY::B_S + 2;    // [2] packed slot written
+    uint64_t* pk_empty = bars + LY::B_S + 4;  // [2] packed slot read by its dQ MMAs
+    uint64_t* o_full = bars + LY::B_S + 6;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -489,11 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qb = CAUSAL ? a.n_qt - 1 - r_in : r_in;  // causal: heaviest tiles first
     const int q0 = qb * 64;
     const int n_all = (a.L + Q_KT - 1) / Q_KT;
-    const int n_t = CAUSAL ? min(n_all, qb + 1) : n_all;  // 64-key tiles up to the diagonal
+    const int n_t = CAUSAL ? min(n_all, (q0 + 63) / Q_KT + 1) : n_all;  // key tiles up to the diagonal
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < LY::NBARS; ++b)
-            mbar_init(&bars[b], (b == 3 + 4 * S || b == 4 + 4 * S) ? 128 : 1);
+        for (int b = 0; b < LY::NBARS; ++b) {
+            const bool many = b == LY::B_S + 1 || b == LY::B_S + 2 || b == LY::B_S + 3;
+            mbar_init(&bars[b], many ? kComputeThreads : 1);
+        }
         *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
         fence_mbar_init();
     }
@@ -539,33 +548,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             for (int j = 0; j < n_t && ok; ++j) {
-                const int st = j % S;
-                if (j >= S && !mbar_wait(&k_empty[st], ((j / S) - 1) & 1, &g_bwd_err)) {
+                // V first: its slot frees (S|R MMAs of tile j - VS) before K's (dQ of tile j - KS)
+                const int vs = j % VS, ks = j % KS;
+                if (j >= VS && !mbar_wait(&v_empty[vs], ((j / VS) - 1) & 1, &g_bwd_err)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&k_full[st], LY::KT_BYTES);
+                mbar_arrive_expect_tx(&v_full[vs], LY::OPB);
                 for (int cb = 0; cb < LY::NCB; ++cb)
-                    tc::tma_load_3d(smem + LY::K_OFF + st * LY::KT_BYTES + cb * LY::KSUB, &tmK,
-                                    cb * 64, j * Q_KT, bh, &k_full[st]);
-                kj = j + 1;
-                if (j >= S && !mbar_wait(&v_empty[st], ((j / S) - 1) & 1, &g_bwd_err)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&v_full[st], LY::KT_BYTES);
-                for (int cb = 0; cb < LY::NCB; ++cb)
-                    tc::tma_load_3d(smem + LY::V_OFF + st * LY::KT_BYTES + cb * LY::KSUB, &tmV,
-                                    cb * 64, j * Q_KT, bh, &v_full[st]);
+                    tc::tma_load_3d(smem + LY::V_OFF + vs * LY::OPB + cb * SUB, &tmV, cb * 64,
+                                    j * Q_KT, bh, &v_full[vs]);
                 vj = j + 1;
+                if (j >= KS && !mbar_wait(&k_empty[ks], ((j / KS) - 1) & 1, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&k_full[ks], LY::OPB);
+                for (int cb = 0; cb < LY::NCB; ++cb)
+                    tc::tma_load_3d(smem + LY::K_OFF + ks * LY::OPB + cb * SUB, &tmK, cb * 64,
+                                    j * Q_KT, bh, &k_full[ks]);
+                kj = j + 1;
             }
             if (!ok) {
                 *abort_flag = 1;
                 mbar_wait(q_full, 0, &g_bwd_err);
-                for (int k = (kj >= S ? kj - S : 0); k < kj; ++k)
-                    mbar_wait(&k_full[k % S], (k / S) & 1, &g_bwd_err);
-                for (int k = (vj >= S ? vj - S : 0); k < vj; ++k)
-                    mbar_wait(&v_full[k % S], (k / S) & 1, &g_bwd_err);
+                for (int k = (kj >= KS ? kj - KS : 0); k < kj; ++k)
+                    mbar_wait(&k_full[k % KS], (k / KS) & 1, &g_bwd_err);
+                for (int k = (vj >= VS ? vj - VS : 0); k < vj; ++k)
+                    mbar_wait(&v_full[k % VS], (k / VS) & 1, &g_bwd_err);
             }
         }
     } else if (warp == 1) {
@@ -578,51 +588,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dDO = tc::smem_desc_sw128(sbase + LY::DO_OFF, 16, 1024);
             const uint64_t dK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, 16, 1024);
             const uint64_t dV0 = tc::smem_desc_sw128(sbase + LY::V_OFF, 16, 1024);
-            const uint64_t mK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, LY::KSUB, 1024);
-            constexpr uint32_t kKtStep = LY::KT_BYTES >> 4;
-            auto issue_ab = [&](int j) -> bool {  // [S; R] and [D; D] of key tile j into Y_(j&1)
-                const int st = j % S;
-                if (*abort_flag || !mbar_wait_warp(&k_full[st], (j / S) & 1, &g_bwd_err) ||
-                    !mbar_wait_warp(&v_full[st], (j / S) & 1, &g_bwd_err))
+            // MN-major view of a K tile: rows = keys (the K dimension of dQ += dS K)
+            const uint64_t mK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, SUB, 1024);
+            constexpr uint32_t kStep = LY::OPB >> 4;
+            auto issue_ab = [&](int j) -> bool {  // [S; R] and [D; D] of key tile j into Y
+                const int ks = j % KS, vs = j % VS;
+                if (*abort_flag || !mbar_wait_warp(&k_full[ks], (j / KS) & 1, &g_bwd_err) ||
+                    !mbar_wait_warp(&v_full[vs], (j / VS) & 1, &g_bwd_err))
                     return false;
                 tc::fence_after_sync();
-                const uint32_t Y = LY::YW * (j & 1);
-                const uint64_t dK = tc::opaque(dK0 + st * kKtStep);
-                const uint64_t dV = tc::opaque(dV0 + st * kKtStep);
+                const uint64_t dK = tc::opaque(dK0 + ks * kStep);
+                const uint64_t dV = tc::opaque(dV0 + vs * kStep);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {  // [S; R] = [Q; rho] K^T
-                    const uint32_t offA = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
-                    const uint32_t offB = ((kk / 4) * LY::KSUB + (kk % 4) * 32) >> 4;
-                    tc::mma_ss(tmem + Y, dQR + offA, dK + offB, kIdesc1, kk > 0);
+                    const uint32_t off = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem, dQR + off, dK + off, kIdesc1, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {  // [D; D] = [dO; dO] V^T
-                    const uint32_t offA = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
-                    const uint32_t offB = ((kk / 4) * LY::KSUB + (kk % 4) * 32) >> 4;
-                    tc::mma_ss(tmem + Y + Q_KT, dDO + offA, dV + offB, kIdesc1, kk > 0);
+                    const uint32_t off = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem + LY::YD, dDO + off, dV + off, kIdesc1, kk > 0);
                 }
-                tc::commit(&s_full[j & 1]);
-                tc::commit(&v_empty[st]);
+                tc::commit(s_full);
+                tc::commit(&v_empty[vs]);
                 return true;
             };
             bool ok = mbar_wait_warp(q_full, 0, &g_bwd_err);
             if (ok) ok = issue_ab(0);
-            if (ok && n_t > 1) ok = issue_ab(1);
-            for (int j = 0; j < n_t && ok; ++j) {
-                if (!mbar_wait_warp(&p_full[j & 1], (j >> 1) & 1, &g_bwd_err)) {
+            for (int t = 0; t < n_t && ok; ++t) {
+                if (t + 1 < n_t) {  // the next tile's S|R and D as soon as Y is free
+                    if (!mbar_wait_warp(y_free, t & 1, &g_bwd_err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!(ok = issue_ab(t + 1))) break;
+                }
+                if (!mbar_wait_warp(&p_full[t & 1], (t >> 1) & 1, &g_bwd_err)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
-                const int st = j % S;
-                const uint64_t mK = tc::opaque(mK0 + st * kKtStep);
-                const uint32_t pk = LY::PK + 32 * (j & 1);
+                const uint64_t mK = tc::opaque(mK0 + (t % KS) * kStep);
+                const uint32_t pk = LY::PK + 64 * (t & 1);
 #pragma unroll
                 for (int kk = 0; kk < Q_KT / 16; ++kk)  // [dQ; drho] += [dS; dR] K
                     tc::mma_ts(tmem + LY::O, tmem + pk + 8 * kk, mK + ((kk * 16 * 128) >> 4),
-                               kIdesc2, (j > 0 || kk > 0) ? 1u : 0u);
-                tc::commit(&k_empty[st]);
-                if (j + 2 < n_t) ok = issue_ab(j + 2);
+                               kIdesc2, (t > 0 || kk > 0) ? 1u : 0u);
+                tc::commit(&k_empty[t % KS]);
+                tc::commit(&pk_empty[t & 1]);
             }
             tc::commit(o_full);
             if (!ok) {
@@ -633,12 +646,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- compute + epilogue
         const int g = warp & 3;
-        const int grp = (warp - 4) >> 2;               // key tiles j = grp mod 2
-        const int h = lane >> 4;                       // which half of the keys / columns
+        const int set = (warp - 4) >> 2;               // key columns 64 set .. 64 set + 63
+        const int h = lane >> 4;                       // which half of those
         const int i = q0 + 16 * g + (lane & 15);       // query row
         const uint32_t rowS = tmem + ((uint32_t)(32 * g) << 16);
         const uint32_t rowR = tmem + ((uint32_t)(32 * g + 16) << 16);
-        const uint32_t Y = LY::YW * grp, pk = LY::PK + 32 * grp;
         const float qs = a.qscale, scale = a.scale;
         float4 z = make_float4(0.f, 0.f, 0.f, 0.f);  // (-lse2, 1 + rbar, abar, delta - abar)
         if (i < a.L) {
@@ -646,19 +658,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             z = make_float4(zr[0], zr[a.Lp], zr[2 * (size_t)a.Lp], zr[3 * (size_t)a.Lp]);
         }
         bool ok = !skip;
-        for (int j = grp; j < n_t && ok; j += 2) {
-            const bool got = !*abort_flag && mbar_wait(&s_full[grp], (j >> 1) & 1, &g_bwd_err);
+        for (int t = 0; t < n_t && ok; ++t) {
+            const bool got = !*abort_flag && mbar_wait(s_full, t & 1, &g_bwd_err);
             if (!__all_sync(kFullMask, got)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
             uint32_t sv[32], rv[32], dv[32];
-            tc::tmem_ld32_split<32>(rowS + Y, sv);
-            if (RHO) tc::tmem_ld32_split<32>(rowR + Y, rv);
-            tc::tmem_ld32_split<32>(rowS + Y + Q_KT, dv);
+            tc::tmem_ld32_split<32>(rowS + 64 * set, sv);
+            if (RHO) tc::tmem_ld32_split<32>(rowR + 64 * set, rv);
+            tc::tmem_ld32_split<32>(rowS + LY::YD + 64 * set, dv);
             tc::tmem_ld_wait();
-            const int k0 = j * Q_KT + 32 * h;
+            tc::fence_before_sync();
+            mbar_arrive(y_free);  // the next tile's MMAs may overwrite Y
+            const int k0 = t * Q_KT + 64 * set + 32 * h;
             // keys past L or (causal) past this query get no weight
             const int lim = min(a.L - 1, CAUSAL ? i : a.L - 1) - k0;  // last valid x
             const uint32_t vmask = i >= a.L || lim < 0 ? 0u
@@ -683,26 +697,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rpk[y] = tc::pack_bf16(pt.dr.x, pt.dr.y);
                 }
             };
-            // warp-uniform: every (query, key) pair of the warp's tile is visible
+            // warp-uniform: every (query, key) pair of the warp's columns is visible
             if (__all_sync(kFullMask, vmask == 0xffffffffu))
                 run(std::false_type{});
             else
                 run(std::true_type{});
-            // packed operand slot (key 2c, 2c+1 at column pk + c): dS in the query lanes,
-            // dR in the probe lanes
+            // the packed slot of this tile was read by the dQ MMAs of tile t - 2
+            const bool slot_free = t < 2 || (!*abort_flag &&
+                                        mbar_wait(&pk_empty[t & 1], ((t >> 1) - 1) & 1, &g_bwd_err));
+            if (!__all_sync(kFullMask, slot_free)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            // packed slot (keys 2c, 2c+1 at column c): dS in the query lanes, dR in the probe lanes
+            const uint32_t pk = LY::PK + 64 * (t & 1) + 32 * set;
             tc::tmem_st16_split<16>(rowS + pk, spk);
             tc::tmem_st16_split<16>(rowR + pk, rpk);
             tc::tmem_st_wait();
             tc::fence_before_sync();
-            mbar_arrive(&p_full[grp]);
+            mbar_arrive(&p_full[t & 1]);
         }
         const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
         if (__all_sync(kFullMask, done)) {
             tc::fence_after_sync();
-            // group 0 stores dQ (query lanes), group 1 drho (probe lanes)
-            if (grp == 0 || RHO) {
-                float* orow = (grp == 0 ? a.dq : a.drho) + ((size_t)bh * a.L + i) * D + h * (D / 2);
-                const uint32_t base = (grp == 0 ? rowS : rowR) + LY::O;
+            // set 0 stores dQ (query lanes), set 1 drho (probe lanes)
+            if (set == 0 || RHO) {
+                float* orow = (set == 0 ? a.dq : a.drho) + ((size_t)bh * a.L + i) * D + h * (D / 2);
+                const uint32_t base = (set == 0 ? rowS : rowR) + LY::O;
 #pragma unroll 1
                 for (int b = 0; b < D / 64; ++b) {
                     uint32_t u[32];
@@ -746,11 +768,10 @@ cudaError_t set_smem(K kern, int bytes) {
 template <int D, bool CAUSAL, bool RHO>
 cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const void* k,
                        const void* v, cudaStream_t stream) {
-    CUtensorMap q32, r32, k128, v128, o32, q16, r16, o16, k64, v64;
+    CUtensorMap q32, r32, k128, v128, o32, q16, r16, o16;
     if (!make_map(&q32, q, a.BH, a.L, D, 64) || !make_map(&k128, k, a.BH, a.L, D, 128) ||
         !make_map(&v128, v, a.BH, a.L, D, 128) || !make_map(&o32, a.dout, a.BH, a.L, D, 64) ||
-        !make_map(&q16, q, a.BH, a.L, D, 16) || !make_map(&o16, a.dout, a.BH, a.L, D, 16) ||
-        !make_map(&k64, k, a.BH, a.L, D, Q_KT) || !make_map(&v64, v, a.BH, a.L, D, Q_KT))
+        !make_map(&q16, q, a.BH, a.L, D, 16) || !make_map(&o16, a.dout, a.BH, a.L, D, 16))
         return cudaErrorInvalidValue;
     if (RHO) {
         if (!make_map(&r32, rho, a.BH, a.L, D, 64) || !make_map(&r16, rho, a.BH, a.L, D, 16))
@@ -771,7 +792,7 @@ cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const v
     bwd_kv_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_kt * a.BH), kKvThreads,
                                     KvLayout<D>::SMEM_BYTES, stream>>>(q32, r32, k128, v128, o32, a);
     bwd_q_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_qt * a.BH), kThreads,
-                                   QLayout<D>::SMEM_BYTES, stream>>>(q16, r16, k64, v64, o16, a);
+                                   QLayout<D>::SMEM_BYTES, stream>>>(q16, r16, k128, v128, o16, a);
     return cudaGetLastError();
 }
 
