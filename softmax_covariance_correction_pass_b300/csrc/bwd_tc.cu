@@ -41,6 +41,7 @@ constexpr int kThreads = 384;
 constexpr int kComputeThreads = 256;
 constexpr int SUB = 128 * 128;  // [128 rows x 64 columns] bf16, 128-byte swizzled
 constexpr int SUB64 = 64 * 128; // [64 rows x 64 columns]
+constexpr int kBwdHeadGroup = 16;  // heads per CTA-scheduling group
 
 struct BwdArgs {
     const float* o;               // [BH, L, D] forward output
@@ -188,8 +189,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    const int kt = blockIdx.x / a.BH;  // causal: the first key tiles see the most queries
-    const int bh = blockIdx.x - kt * a.BH;
+    // CTA -> (head, key tile): heads in groups of kBwdHeadGroup, the key tiles that
+    // see the most queries first within a group, so that the CTAs resident at any
+    // time share the query-side tiles of a few heads in L2
+    const int group = blockIdx.x / (kBwdHeadGroup * a.n_kt);
+    const int gsize = min(kBwdHeadGroup, a.BH - group * kBwdHeadGroup);
+    const int r_in = blockIdx.x - group * kBwdHeadGroup * a.n_kt;
+    const int kt = r_in / gsize;
+    const int bh = group * kBwdHeadGroup + r_in % gsize;
     const int k0 = kt * 128;
     const int qt0 = CAUSAL ? k0 / 64 : 0;
     const int n_t = a.n_qt - qt0;
@@ -491,9 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    const int r_in = blockIdx.x / a.BH;
-    const int bh = blockIdx.x - r_in * a.BH;
-    const int qb = CAUSAL ? a.n_qt - 1 - r_in : r_in;  // causal: heaviest tiles first
+    // CTA -> (head, query tile): heads in groups of kBwdHeadGroup, heaviest query
+    // tile first within a group (their K/V tiles stay in L2 while the group runs)
+    const int group = blockIdx.x / (kBwdHeadGroup * a.n_qt);
+    const int gsize = min(kBwdHeadGroup, a.BH - group * kBwdHeadGroup);
+    const int r_in = (blockIdx.x - group * kBwdHeadGroup * a.n_qt) / gsize;
+    const int bh = group * kBwdHeadGroup + (blockIdx.x - group * kBwdHeadGroup * a.n_qt) % gsize;
+    const int qb = CAUSAL ? a.n_qt - 1 - r_in : r_in;
     const int q0 = qb * 64;
     const int n_all = (a.L + Q_KT - 1) / Q_KT;
     const int n_t = CAUSAL ? min(n_all, (q0 + 63) / Q_KT + 1) : n_all;  // key tiles up to the diagonal
