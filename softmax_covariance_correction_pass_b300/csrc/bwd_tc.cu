@@ -82,6 +82,23 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 16-byte read-only global load kept where it is written (not hoisted across the
+// other inline-asm statements, so the statistics do not pile up in registers).
+__device__ __forceinline__ float4 ldg_stream4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
+                 "r"(w)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------------ row statistics
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
@@ -149,24 +166,38 @@ __device__ __forceinline__ PairTerms pair_terms(float2 s, float2 r, float2 d, fl
 }
 
 // ------------------------------------------------------------------------ dK, dV
-// One 128-key tile per CTA, 64-query tiles in a 2-deep TMA ring; warp 0 TMA,
-// warp 1 MMA, warps 4-7 compute (one key per TMEM lane, all 64 queries of a tile).
-constexpr int kKvThreads = 256;
+// One 128-key tile per CTA (one key per TMEM lane), 64-query tiles of Q, rho and
+// dO in a 3-deep TMA ring.  V sits in TMEM as the A operand of D^T = V dO^T, so
+// shared memory holds K, the ring and the gradient operands W, dS, dR (bf16,
+// [128 keys x 64 queries], written by the compute warps).  The compute warps
+// release TMEM as soon as they have loaded S, R and D of a tile: the MMAs of
+// the next tile then run while they work, and dV += W dO, dK += dS Q + dR rho
+// (A from shared memory) follow once the operands are written.
+// Warps: 0 TMA, 1 MMA (+ TMEM owner), 2-9 compute: warp w serves TMEM lane
+// quarter w % 4, warps 2-5 queries 0-31 and warps 6-9 queries 32-63 of a tile.
+// Ten warps leave each thread 200 registers.
+constexpr int kKvThreads = 320;
+constexpr int kKvStages = 3;
+
 template <int D>
 struct KvLayout {
     static constexpr int NCB = D / 64;
     static constexpr int OPB = NCB * SUB;                // [128 x D] operand
-    static constexpr int K_OFF = 0, V_OFF = OPB;
+    static constexpr int K_OFF = 0;
     static constexpr int QR_BYTES = OPB;                 // [Q; rho] rows 0..63 / 64..127
     static constexpr int DO_BYTES = NCB * SUB64;         // dO [64 x D]
-    static constexpr int STAGE = QR_BYTES + DO_BYTES + 1024;  // + 64 row stats
-    static constexpr int ST_OFF = 2 * OPB;
-    static constexpr int BAR_OFF = ST_OFF + 2 * STAGE;
-    // kv_full, qr_full[2], qr_empty[2], s_full, p_part[2], o_full
-    static constexpr int NBARS = 9;
+    static constexpr int STAGE = QR_BYTES + DO_BYTES;
+    static constexpr int ST_OFF = OPB;
+    // W, dS, dR: [128 keys x 64 queries] bf16 each, 128-byte swizzled (K-major A operands).
+    // The V tile lands here first, on its way to TMEM.
+    static constexpr int G_OFF = ST_OFF + kKvStages * STAGE;
+    static constexpr int BAR_OFF = G_OFF + 3 * SUB;
+    // kv_full, v_ready, qr_full[S], qr_empty[S], s_full, y_free, p_full, g_done, o_full
+    static constexpr int NBARS = 2 + 2 * kKvStages + 5;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    static_assert(OPB <= 3 * SUB, "the V tile must fit in the gradient-operand area");
     // TMEM columns
-    static constexpr uint32_t SR = 0, DT = 128, DV = 256, DK = 256 + D;
+    static constexpr uint32_t SR = 0, DT = 128, VA = 192, DV = 256, DK = 256 + D;
 };
 
 template <int D, bool CAUSAL, bool RHO>
@@ -175,16 +206,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmO, const BwdArgs a) {
     using LY = KvLayout<D>;
+    constexpr int S = kKvStages;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
     uint64_t* kv_full = bars;
-    uint64_t* qr_full = bars + 1;
-    uint64_t* qr_empty = bars + 3;
-    uint64_t* s_full = bars + 5;
-    uint64_t* p_part = bars + 6;  // W, dS, dR of queries 32c .. 32c + 31 are in TMEM
-    uint64_t* o_full = bars + 8;
+    uint64_t* v_ready = bars + 1;        // V is in TMEM (128 arrivals)
+    uint64_t* qr_full = bars + 2;
+    uint64_t* qr_empty = bars + 2 + S;
+    uint64_t* s_full = bars + 2 + 2 * S;
+    uint64_t* y_free = bars + 3 + 2 * S;  // S, R, D of the tile loaded (256 arrivals)
+    uint64_t* p_full = bars + 4 + 2 * S;  // W, dS, dR of the tile written (256 arrivals)
+    uint64_t* g_done = bars + 5 + 2 * S;  // the gradient MMAs of the tile have read them
+    uint64_t* o_full = bars + 6 + 2 * S;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -202,7 +237,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const int n_t = a.n_qt - qt0;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], (b == 6 || b == 7) ? 128 : 1);
+        for (int b = 0; b < LY::NBARS; ++b) {
+            uint32_t count = 1;
+            if (b == 1) count = 128;
+            if (b == 3 + 2 * S || b == 4 + 2 * S) count = kComputeThreads;
+            mbar_init(&bars[b], count);
+        }
         *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
         fence_mbar_init();
     }
@@ -226,20 +266,19 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mbar_arrive_expect_tx(kv_full, 2 * LY::OPB);
             for (int cb = 0; cb < LY::NCB; ++cb) {
                 tc::tma_load_3d(smem + LY::K_OFF + cb * SUB, &tmK, cb * 64, k0, bh, kv_full);
-                tc::tma_load_3d(smem + LY::V_OFF + cb * SUB, &tmV, cb * 64, k0, bh, kv_full);
+                tc::tma_load_3d(smem + LY::G_OFF + cb * SUB, &tmV, cb * 64, k0, bh, kv_full);
             }
             int issued = 0;
             bool ok = true;
             for (int t = 0; t < n_t; ++t) {
-                const int st = t & 1;
-                if (t >= 2 && !mbar_wait(&qr_empty[st], ((t >> 1) - 1) & 1, &g_bwd_err)) {
+                const int st = t % S;
+                if (t >= S && !mbar_wait(&qr_empty[st], ((t / S) - 1) & 1, &g_bwd_err)) {
                     ok = false;
                     break;
                 }
                 const int q0 = (qt0 + t) * 64;
                 unsigned char* stage = smem + LY::ST_OFF + st * LY::STAGE;
-                mbar_arrive_expect_tx(&qr_full[st], (RHO ? 2 : 1) * LY::NCB * SUB64 + LY::DO_BYTES +
-                                                        4 * 64 * 4);
+                mbar_arrive_expect_tx(&qr_full[st], (RHO ? 2 : 1) * LY::NCB * SUB64 + LY::DO_BYTES);
                 for (int cb = 0; cb < LY::NCB; ++cb) {
                     tc::tma_load_3d(stage + cb * SUB, &tmQ, cb * 64, q0, bh, &qr_full[st]);
                     if (RHO)
@@ -247,16 +286,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     tc::tma_load_3d(stage + LY::QR_BYTES + cb * SUB64, &tmO, cb * 64, q0, bh,
                                     &qr_full[st]);
                 }
-                for (int c = 0; c < 4; ++c)  // the 64 rows' statistics, one array each
-                    bulk_g2s(stage + LY::QR_BYTES + LY::DO_BYTES + c * 256,
-                             a.rs + ((size_t)bh * 4 + c) * a.Lp + q0, 256, &qr_full[st]);
                 issued = t + 1;
             }
             if (!ok) {
                 *abort_flag = 1;
                 mbar_wait(kv_full, 0, &g_bwd_err);
-                for (int t = issued >= 2 ? issued - 2 : 0; t < issued; ++t)
-                    mbar_wait(&qr_full[t & 1], (t >> 1) & 1, &g_bwd_err);
+                for (int t = issued >= S ? issued - S : 0; t < issued; ++t)
+                    mbar_wait(&qr_full[t % S], (t / S) & 1, &g_bwd_err);
             }
         }
     } else if (warp == 1) {
@@ -267,60 +303,66 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             constexpr uint32_t kIdescMN = tc::idesc_bf16_f32(128, D, true);
             const uint32_t sbase = smem_u32(smem);
             const uint64_t dK = tc::smem_desc_sw128(sbase + LY::K_OFF, 16, 1024);
-            const uint64_t dV = tc::smem_desc_sw128(sbase + LY::V_OFF, 16, 1024);
+            const uint64_t dG = tc::smem_desc_sw128(sbase + LY::G_OFF, 16, 1024);
+            const uint32_t stb = sbase + LY::ST_OFF;
             constexpr uint32_t kStStep = LY::STAGE >> 4;
-            bool ok = mbar_wait_warp(kv_full, 0, &g_bwd_err);
-            for (int t = 0; t < n_t && ok; ++t) {
-                const int st = t & 1;
-                if (*abort_flag || !mbar_wait_warp(&qr_full[st], (t >> 1) & 1, &g_bwd_err)) {
-                    ok = false;
-                    break;
-                }
+            // [S^T | R^T] = K [Q; rho]^T (A and B from shared memory) and D^T = V dO^T
+            // (A = V from TMEM) of query tile t
+            auto issue_srd = [&](int t) -> bool {
+                const int st = t % S;
+                if (*abort_flag || !mbar_wait_warp(&qr_full[st], (t / S) & 1, &g_bwd_err))
+                    return false;
                 tc::fence_after_sync();
-                const uint32_t stb = sbase + LY::ST_OFF;
                 const uint64_t dQR = tc::opaque(tc::smem_desc_sw128(stb, 16, 1024) + st * kStStep);
                 const uint64_t dDO =
                     tc::opaque(tc::smem_desc_sw128(stb + LY::QR_BYTES, 16, 1024) + st * kStStep);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // [S^T | R^T] = K [Q; rho]^T
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
                     tc::mma_ss(tmem + LY::SR, dK + off, dQR + off, kIdescA, kk > 0);
                 }
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // D^T = V dO^T
-                    const uint32_t offA = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t offB = ((kk / 4) * SUB64 + (kk % 4) * 32) >> 4;
-                    tc::mma_ss(tmem + LY::DT, dV + offA, dDO + offB, kIdescB, kk > 0);
+                    tc::mma_ts(tmem + LY::DT, tmem + LY::VA + 8 * kk, dDO + offB, kIdescB, kk > 0);
                 }
                 tc::commit(s_full);
-                // MN-major views of the same tiles: rows = queries (the K dimension)
-                const uint64_t mQR = tc::opaque(tc::smem_desc_sw128(stb, SUB, 1024) + st * kStStep);
-                const uint64_t mDO =
-                    tc::opaque(tc::smem_desc_sw128(stb + LY::QR_BYTES, SUB64, 1024) + st * kStStep);
-                // the gradient MMAs of each 32-query half start as soon as the compute
-                // warps have handed that half over, overlapping the other half's compute
-                for (int c = 0; c < 2 && ok; ++c) {
-                    if (!mbar_wait_warp(&p_part[c], t & 1, &g_bwd_err)) {
+                return true;
+            };
+            bool ok = mbar_wait_warp(kv_full, 0, &g_bwd_err) && mbar_wait_warp(v_ready, 0, &g_bwd_err);
+            if (ok) ok = issue_srd(0);
+            for (int t = 0; t < n_t && ok; ++t) {
+                if (t + 1 < n_t) {  // the next tile's S|R and D as soon as TMEM is free
+                    if (!mbar_wait_warp(y_free, t & 1, &g_bwd_err)) {
                         ok = false;
                         break;
                     }
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int kk = 2 * c + h;  // queries 16kk .. 16kk + 15
-                        const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                        // dV += W dO
-                        tc::mma_ts(tmem + LY::DV, tmem + LY::SR + 32 * c + 8 * h,
-                                   mDO + ((kk * 16 * 128) >> 4), kIdescMN, acc);
-                        // dK += dS Q  (scale folded into dS)
-                        tc::mma_ts(tmem + LY::DK, tmem + LY::SR + 32 * c + 16 + 8 * h,
-                                   mQR + ((kk * 16 * 128) >> 4), kIdescMN, acc);
-                        if (RHO)  // dK += dR rho
-                            tc::mma_ts(tmem + LY::DK, tmem + LY::SR + 64 + 32 * c + 8 * h,
-                                       mQR + (((64 + kk * 16) * 128) >> 4), kIdescMN, 1u);
-                    }
+                    if (!(ok = issue_srd(t + 1))) break;
                 }
-                if (!ok) break;
+                if (*abort_flag || !mbar_wait_warp(p_full, t & 1, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const int st = t % S;
+                // MN-major views of the query-side tiles: rows = queries (the K dimension)
+                const uint64_t mQR = tc::opaque(tc::smem_desc_sw128(stb, SUB, 1024) + st * kStStep);
+                const uint64_t mDO =
+                    tc::opaque(tc::smem_desc_sw128(stb + LY::QR_BYTES, SUB64, 1024) + st * kStStep);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {  // queries 16kk .. 16kk + 15
+                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                    const uint32_t ka = (kk * 32) >> 4;
+                    // dV += W dO
+                    tc::mma_ss(tmem + LY::DV, dG + ka, mDO + ((kk * 16 * 128) >> 4), kIdescMN, acc);
+                    // dK += dS Q  (scale folded into dS)
+                    tc::mma_ss(tmem + LY::DK, dG + (SUB >> 4) + ka, mQR + ((kk * 16 * 128) >> 4),
+                               kIdescMN, acc);
+                    if (RHO)  // dK += dR rho
+                        tc::mma_ss(tmem + LY::DK, dG + ((2 * SUB) >> 4) + ka,
+                                   mQR + (((64 + kk * 16) * 128) >> 4), kIdescMN, 1u);
+                }
+                tc::commit(g_done);
                 tc::commit(&qr_empty[st]);
             }
             tc::commit(o_full);
@@ -329,52 +371,83 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 mbar_wait_warp(o_full, 0, &g_bwd_err);
             }
         }
-    } else if (warp >= 4) {
+    } else {
         // ---------------------------------------------------------------- compute + epilogue
-        const int q4 = warp & 3;
-        const int j = k0 + 32 * q4 + lane;  // this thread's key
+        const int q4 = warp & 3;                // TMEM lane quarter
+        const int c = (warp - 2) >> 2;          // queries 32c .. 32c + 31 of every tile
+        const int row = 32 * q4 + lane;         // this thread's key within the tile
+        const int j = k0 + row;
         const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
         const float qs = a.qscale, scale = a.scale;
         bool ok = !skip;
+        if (c == 0) {
+            // V -> TMEM: lane = key, column x holds elements 2x, 2x + 1 (the A-operand layout)
+            const bool got = ok && mbar_wait(kv_full, 0, &g_bwd_err);
+            if (__all_sync(kFullMask, got)) {
+#pragma unroll 1
+                for (int cb = 0; cb < LY::NCB; ++cb) {
+                    uint32_t u[32];
+                    const unsigned char* vrow = smem + LY::G_OFF + cb * SUB + row * 128;
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        const uint4 q = *reinterpret_cast<const uint4*>(vrow + ((x ^ (row & 7)) * 16));
+                        u[4 * x] = q.x;
+                        u[4 * x + 1] = q.y;
+                        u[4 * x + 2] = q.z;
+                        u[4 * x + 3] = q.w;
+                    }
+                    tc::tmem_st32(trow + LY::VA + 32 * cb, u);
+                }
+                tc::tmem_st_wait();
+            } else {
+                ok = false;
+                *abort_flag = 1;
+            }
+            tc::fence_before_sync();
+            mbar_arrive(v_ready);
+        }
+        const uint32_t gbase = smem_u32(smem + LY::G_OFF) + row * 128;
         for (int t = 0; t < n_t && ok; ++t) {
-            const int st = t & 1;
             const bool got = !*abort_flag && mbar_wait(s_full, t & 1, &g_bwd_err);
             if (!__all_sync(kFullMask, got)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            const int q0 = (qt0 + t) * 64;
-            // row statistics of the tile: -lse2[64], 1 + rbar[64], abar[64], delta - abar[64]
-            const float* rst = reinterpret_cast<const float*>(smem + LY::ST_OFF + st * LY::STAGE +
-                                                              LY::QR_BYTES + LY::DO_BYTES);
+            const int qc = (qt0 + t) * 64 + 32 * c;
+            // row statistics of the 32 queries (rows past L hold zeros)
+            const float* st0 = a.rs + (size_t)bh * 4 * a.Lp + qc;
             const float2 qs2 = make_float2(qs, qs), nsc2 = make_float2(-scale, -scale);
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                uint32_t sv[32], rv[32], dv[32];
-                tc::tmem_ld32(trow + LY::SR + 32 * c, sv);
-                if (RHO) tc::tmem_ld32(trow + LY::SR + 64 + 32 * c, rv);
-                tc::tmem_ld32(trow + LY::DT + 32 * c, dv);
+            uint32_t wpk[16], spk[16], rpk[16];
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {  // 16 queries at a time
+                uint32_t sv[16], rv[16], dv[16];
+                tc::tmem_ld16(trow + LY::SR + 32 * c + 16 * qq, sv);
+                if (RHO) tc::tmem_ld16(trow + LY::SR + 64 + 32 * c + 16 * qq, rv);
+                tc::tmem_ld16(trow + LY::DT + 32 * c + 16 * qq, dv);
                 tc::tmem_ld_wait();
+                if (qq == 1) {
+                    tc::fence_before_sync();
+                    mbar_arrive(y_free);  // the next tile's MMAs may overwrite S, R, D
+                }
                 // queries past L or (causal) before this key get no weight
-                const int qc = q0 + 32 * c;
-                const int nvalid = min(32, a.L - qc);
-                uint32_t vmask = nvalid >= 32 ? 0xffffffffu : ((1u << nvalid) - 1u);
-                if (CAUSAL && j > qc) vmask &= j - qc >= 32 ? 0u : ~((1u << (j - qc)) - 1u);
-                const float* st0 = rst + 32 * c;
-                uint32_t wpk[16], spk[16], rpk[16];
+                const int qb16 = qc + 16 * qq;
+                const int nvalid = min(16, a.L - qb16);
+                uint32_t vmask = nvalid >= 16 ? 0xffffu : nvalid <= 0 ? 0u : ((1u << nvalid) - 1u);
+                if (CAUSAL && j > qb16) vmask &= j - qb16 >= 16 ? 0u : ~((1u << (j - qb16)) - 1u);
+                const float* sq = st0 + 16 * qq;
                 auto run = [&](auto masked) {
                     constexpr bool M = decltype(masked)::value;
 #pragma unroll
-                    for (int y4 = 0; y4 < 8; ++y4) {  // four queries per step: 128-bit stat loads
+                    for (int y4 = 0; y4 < 4; ++y4) {  // four queries per step: 128-bit stat loads
                         const int x4 = 4 * y4;
-                        const float4 nl = *reinterpret_cast<const float4*>(st0 + x4);
-                        const float4 rb = *reinterpret_cast<const float4*>(st0 + 64 + x4);
-                        const float4 ab = *reinterpret_cast<const float4*>(st0 + 128 + x4);
-                        const float4 ne = *reinterpret_cast<const float4*>(st0 + 192 + x4);
+                        const float4 nl = ldg_stream4(sq + x4);
+                        const float4 rb = ldg_stream4(sq + a.Lp + x4);
+                        const float4 ab = ldg_stream4(sq + 2 * (size_t)a.Lp + x4);
+                        const float4 ne = ldg_stream4(sq + 3 * (size_t)a.Lp + x4);
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
-                            const int x = x4 + 2 * hh, y = x / 2;
+                            const int x = x4 + 2 * hh, y = 8 * qq + x / 2;
                             const float2 s2 = make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]));
                             const float2 r2 = RHO ? make_float2(__uint_as_float(rv[x]),
                                                                 __uint_as_float(rv[x + 1]))
@@ -392,41 +465,49 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                         }
                     }
                 };
-                // warp-uniform: every (key, query) pair of the warp's half tile is visible
-                if (__all_sync(kFullMask, vmask == 0xffffffffu))
+                // warp-uniform: every (key, query) pair of the warp's 16 queries is visible
+                if (__all_sync(kFullMask, vmask == 0xffffu))
                     run(std::false_type{});
                 else
                     run(std::true_type{});
-                // (columns already read above: W, dS over S^T, dR over R^T)
-                tc::tmem_st16(trow + LY::SR + 32 * c, wpk);
-                tc::tmem_st16(trow + LY::SR + 32 * c + 16, spk);
-                if (RHO) tc::tmem_st16(trow + LY::SR + 64 + 32 * c, rpk);
-                tc::tmem_st_wait();
-                tc::fence_before_sync();
-                mbar_arrive(&p_part[c]);  // this half's gradient MMAs may start
             }
+            // the previous tile's gradient MMAs must have read the operand area
+            const bool free_g = t == 0 || (!*abort_flag && mbar_wait(g_done, (t - 1) & 1, &g_bwd_err));
+            if (!__all_sync(kFullMask, free_g)) {
+                ok = false;
+                break;
+            }
+            // row `row` of W, dS, dR: queries 32c .. 32c + 31 = 16-byte chunks 4c .. 4c + 3,
+            // stored at chunk (index ^ row % 8) of the 128-byte row (128-byte swizzle)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const uint32_t off = (uint32_t)(((4 * c + x) ^ (row & 7)) * 16);
+                st_shared_v4(gbase + off, wpk[4 * x], wpk[4 * x + 1], wpk[4 * x + 2], wpk[4 * x + 3]);
+                st_shared_v4(gbase + SUB + off, spk[4 * x], spk[4 * x + 1], spk[4 * x + 2], spk[4 * x + 3]);
+                if (RHO)
+                    st_shared_v4(gbase + 2 * SUB + off, rpk[4 * x], rpk[4 * x + 1], rpk[4 * x + 2],
+                                 rpk[4 * x + 3]);
+            }
+            fence_proxy_async_smem();  // visible to the tensor core's reads
+            mbar_arrive(p_full);
         }
         const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
         if (__all_sync(kFullMask, done)) {
             tc::fence_after_sync();
-            float* dvrow = a.dv + ((size_t)bh * a.L + j) * D;
-            float* dkrow = a.dk + ((size_t)bh * a.L + j) * D;
+            // half 0 stores dV, half 1 dK
+            float* orow = (c == 0 ? a.dv : a.dk) + ((size_t)bh * a.L + j) * D;
+            const uint32_t base = trow + (c == 0 ? LY::DV : LY::DK);
 #pragma unroll 1
             for (int b = 0; b < D / 32; ++b) {
-                uint32_t u[32], w[32];
-                tc::tmem_ld32(trow + LY::DV + 32 * b, u);
-                tc::tmem_ld32(trow + LY::DK + 32 * b, w);
+                uint32_t u[32];
+                tc::tmem_ld32(base + 32 * b, u);
                 tc::tmem_ld_wait();
                 if (j < a.L) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 4) {
-                        *reinterpret_cast<float4*>(dvrow + 32 * b + x) =
+                    for (int x = 0; x < 32; x += 4)
+                        *reinterpret_cast<float4*>(orow + 32 * b + x) =
                             make_float4(__uint_as_float(u[x]), __uint_as_float(u[x + 1]),
                                         __uint_as_float(u[x + 2]), __uint_as_float(u[x + 3]));
-                        *reinterpret_cast<float4*>(dkrow + 32 * b + x) =
-                            make_float4(__uint_as_float(w[x]), __uint_as_float(w[x + 1]),
-                                        __uint_as_float(w[x + 2]), __uint_as_float(w[x + 3]));
-                    }
                 }
             }
         } else {
