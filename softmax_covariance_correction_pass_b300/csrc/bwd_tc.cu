@@ -92,6 +92,10 @@ __device__ __forceinline__ float4 ldg_stream4(const float* p) {
     return v;
 }
 
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
                                              uint32_t w) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
@@ -407,6 +411,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mbar_arrive(v_ready);
         }
         const uint32_t gbase = smem_u32(smem + LY::G_OFF) + row * 128;
+        // the statistics of a tile's 32 queries: four 128-byte lines, fetched into L1 one
+        // tile ahead (lanes 0-3, one line each)
+        const float* rs_h = a.rs + (size_t)bh * 4 * a.Lp + 32 * c;
+        if (lane < 4) prefetch_l1(rs_h + (size_t)lane * a.Lp + qt0 * 64);
         for (int t = 0; t < n_t && ok; ++t) {
             const bool got = !*abort_flag && mbar_wait(s_full, t & 1, &g_bwd_err);
             if (!__all_sync(kFullMask, got)) {
@@ -414,6 +422,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 break;
             }
             tc::fence_after_sync();
+            if (lane < 4 && t + 1 < n_t) prefetch_l1(rs_h + (size_t)lane * a.Lp + (qt0 + t + 1) * 64);
             const int qc = (qt0 + t) * 64 + 32 * c;
             // row statistics of the 32 queries (rows past L hold zeros)
             const float* st0 = a.rs + (size_t)bh * 4 * a.Lp + qc;
