@@ -57,6 +57,8 @@ typedef enum {
 #define PARALLAX_DEVERR_WAIT_TIMEOUT 0x2u   /* a pipeline wait gave up (bug)      */
 #define PARALLAX_DEVERR_PAGE_OUT_OF_RANGE 0x4u /* a block-table entry lay outside
                                                   [0, num_pages); page 0 was read */
+#define PARALLAX_DEVERR_SMEM_MISALIGNED 0x8u /* a kernel's dynamic shared memory was not
+                                                1024-byte aligned; it did no work (bug) */
 
 /*
  * Causal or full prefill, bf16 inputs, fp32 output.

@@ -27,6 +27,7 @@ PARALLAX_ERR_DEVICE = -4
 DEVERR_SEQLEN_CLAMPED = 0x1
 DEVERR_WAIT_TIMEOUT = 0x2
 DEVERR_PAGE_OUT_OF_RANGE = 0x4
+DEVERR_SMEM_MISALIGNED = 0x8
 
 _lib = None
 

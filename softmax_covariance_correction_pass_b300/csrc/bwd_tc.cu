@@ -82,20 +82,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// 16-byte read-only global load kept where it is written (not hoisted across the
-// other inline-asm statements, so the statistics do not pile up in registers).
-__device__ __forceinline__ float4 ldg_stream4(const float* p) {
-    float4 v;
-    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
                                              uint32_t w) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
@@ -195,10 +181,14 @@ struct KvLayout {
     // W, dS, dR: [128 keys x 64 queries] bf16 each, 128-byte swizzled (K-major A operands).
     // The V tile lands here first, on its way to TMEM.
     static constexpr int G_OFF = ST_OFF + kKvStages * STAGE;
-    static constexpr int BAR_OFF = G_OFF + 3 * SUB;
-    // kv_full, v_ready, qr_full[S], qr_empty[S], s_full, y_free, p_full, g_done, o_full
-    static constexpr int NBARS = 2 + 2 * kKvStages + 5;
-    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    // row statistics of a query tile, [4][64] fp32, in two slots
+    static constexpr int RS_OFF = G_OFF + 3 * SUB;
+    static constexpr int BAR_OFF = RS_OFF + 2 * 1024;
+    // kv_full, v_ready, qr_full[S], qr_empty[S], s_full, y_free, p_full, g_done, o_full,
+    // rs_full[2], rs_free[2]
+    static constexpr int NBARS = 2 + 2 * kKvStages + 9;
+    // the buffers start at the (1024-byte aligned) base of dynamic shared memory
+    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16;
     static_assert(OPB <= 3 * SUB, "the V tile must fit in the gradient-operand area");
     // TMEM columns
     static constexpr uint32_t SR = 0, DT = 128, VA = 192, DV = 256, DK = 256 + D;
@@ -211,9 +201,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                   const __grid_constant__ CUtensorMap tmO, const BwdArgs a) {
     using LY = KvLayout<D>;
     constexpr int S = kKvStages;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) unsigned char smem[];
+    // the 128-byte-swizzled tiles need 1024-byte alignment; the layout leaves no room to
+    // realign, so a misaligned base is reported instead of used
+    if (smem_u32(smem) & 1023u) {
+        if (threadIdx.x == 0) raise_error(&g_bwd_err, PARALLAX_DEVERR_SMEM_MISALIGNED);
+        return;
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
     uint64_t* kv_full = bars;
     uint64_t* v_ready = bars + 1;        // V is in TMEM (128 arrivals)
@@ -224,6 +218,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     uint64_t* p_full = bars + 4 + 2 * S;  // W, dS, dR of the tile written (256 arrivals)
     uint64_t* g_done = bars + 5 + 2 * S;  // the gradient MMAs of the tile have read them
     uint64_t* o_full = bars + 6 + 2 * S;
+    uint64_t* rs_full = bars + 7 + 2 * S;  // [2] statistics slot loaded
+    uint64_t* rs_free = bars + 9 + 2 * S;  // [2] statistics slot read (256 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -244,7 +240,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         for (int b = 0; b < LY::NBARS; ++b) {
             uint32_t count = 1;
             if (b == 1) count = 128;
-            if (b == 3 + 2 * S || b == 4 + 2 * S) count = kComputeThreads;
+            if (b == 3 + 2 * S || b == 4 + 2 * S || b == 9 + 2 * S || b == 10 + 2 * S)
+                count = kComputeThreads;
             mbar_init(&bars[b], count);
         }
         *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
@@ -272,7 +269,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 tc::tma_load_3d(smem + LY::K_OFF + cb * SUB, &tmK, cb * 64, k0, bh, kv_full);
                 tc::tma_load_3d(smem + LY::G_OFF + cb * SUB, &tmV, cb * 64, k0, bh, kv_full);
             }
-            int issued = 0;
+            int issued = 0, rs_issued = 0;
             bool ok = true;
             for (int t = 0; t < n_t; ++t) {
                 const int st = t % S;
@@ -291,12 +288,26 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                                     &qr_full[st]);
                 }
                 issued = t + 1;
+                // the 64 rows' statistics (one 256-byte copy per array) into slot t % 2, once
+                // the compute warps are done with tile t - 2
+                const int rsl = t & 1;
+                if (t >= 2 && !mbar_wait(&rs_free[rsl], ((t >> 1) - 1) & 1, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&rs_full[rsl], 4 * 64 * 4);
+                for (int k = 0; k < 4; ++k)
+                    bulk_g2s(smem + LY::RS_OFF + rsl * 1024 + k * 256,
+                             a.rs + ((size_t)bh * 4 + k) * a.Lp + q0, 256, &rs_full[rsl]);
+                rs_issued = t + 1;
             }
             if (!ok) {
                 *abort_flag = 1;
                 mbar_wait(kv_full, 0, &g_bwd_err);
                 for (int t = issued >= S ? issued - S : 0; t < issued; ++t)
                     mbar_wait(&qr_full[t % S], (t / S) & 1, &g_bwd_err);
+                for (int t = rs_issued >= 2 ? rs_issued - 2 : 0; t < rs_issued; ++t)
+                    mbar_wait(&rs_full[t & 1], (t >> 1) & 1, &g_bwd_err);
             }
         }
     } else if (warp == 1) {
@@ -411,10 +422,6 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mbar_arrive(v_ready);
         }
         const uint32_t gbase = smem_u32(smem + LY::G_OFF) + row * 128;
-        // the statistics of a tile's 32 queries: four 128-byte lines, fetched into L1 one
-        // tile ahead (lanes 0-3, one line each)
-        const float* rs_h = a.rs + (size_t)bh * 4 * a.Lp + 32 * c;
-        if (lane < 4) prefetch_l1(rs_h + (size_t)lane * a.Lp + qt0 * 64);
         for (int t = 0; t < n_t && ok; ++t) {
             const bool got = !*abort_flag && mbar_wait(s_full, t & 1, &g_bwd_err);
             if (!__all_sync(kFullMask, got)) {
@@ -422,10 +429,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 break;
             }
             tc::fence_after_sync();
-            if (lane < 4 && t + 1 < n_t) prefetch_l1(rs_h + (size_t)lane * a.Lp + (qt0 + t + 1) * 64);
             const int qc = (qt0 + t) * 64 + 32 * c;
-            // row statistics of the 32 queries (rows past L hold zeros)
-            const float* st0 = a.rs + (size_t)bh * 4 * a.Lp + qc;
+            // row statistics of the 32 queries (rows past L hold zeros): slot t % 2 holds
+            // [4][64] for the tile
+            const bool have = !*abort_flag && mbar_wait(&rs_full[t & 1], (t >> 1) & 1, &g_bwd_err);
+            if (!__all_sync(kFullMask, have)) {
+                ok = false;
+                break;
+            }
+            const float* st0 = reinterpret_cast<const float*>(smem + LY::RS_OFF + (t & 1) * 1024) + 32 * c;
             const float2 qs2 = make_float2(qs, qs), nsc2 = make_float2(-scale, -scale);
             uint32_t wpk[16], spk[16], rpk[16];
 #pragma unroll
@@ -450,10 +462,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
                     for (int y4 = 0; y4 < 4; ++y4) {  // four queries per step: 128-bit stat loads
                         const int x4 = 4 * y4;
-                        const float4 nl = ldg_stream4(sq + x4);
-                        const float4 rb = ldg_stream4(sq + a.Lp + x4);
-                        const float4 ab = ldg_stream4(sq + 2 * (size_t)a.Lp + x4);
-                        const float4 ne = ldg_stream4(sq + 3 * (size_t)a.Lp + x4);
+                        const float4 nl = *reinterpret_cast<const float4*>(sq + x4);
+                        const float4 rb = *reinterpret_cast<const float4*>(sq + 64 + x4);
+                        const float4 ab = *reinterpret_cast<const float4*>(sq + 128 + x4);
+                        const float4 ne = *reinterpret_cast<const float4*>(sq + 192 + x4);
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
                             const int x = x4 + 2 * hh, y = 8 * qq + x / 2;
@@ -480,6 +492,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 else
                     run(std::true_type{});
             }
+            mbar_arrive(&rs_free[t & 1]);  // this thread is done with the slot
             // the previous tile's gradient MMAs must have read the operand area
             const bool free_g = t == 0 || (!*abort_flag && mbar_wait(g_done, (t - 1) & 1, &g_bwd_err));
             if (!__all_sync(kFullMask, free_g)) {
