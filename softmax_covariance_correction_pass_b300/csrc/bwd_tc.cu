@@ -440,17 +440,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const float* st0 = reinterpret_cast<const float*>(smem + LY::RS_OFF + (t & 1) * 1024) + 32 * c;
             const float2 qs2 = make_float2(qs, qs), nsc2 = make_float2(-scale, -scale);
             uint32_t wpk[16], spk[16], rpk[16];
+            // S, R, D of the thread's 32 queries, all loaded before TMEM is released
+            uint32_t sv[32], rv[32], dv[32];
+            tc::tmem_ld32(trow + LY::SR + 32 * c, sv);
+            if (RHO) tc::tmem_ld32(trow + LY::SR + 64 + 32 * c, rv);
+            tc::tmem_ld32(trow + LY::DT + 32 * c, dv);
+            tc::tmem_ld_wait();
+            tc::fence_before_sync();
+            mbar_arrive(y_free);  // the next tile's MMAs may overwrite S, R, D
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq) {  // 16 queries at a time
-                uint32_t sv[16], rv[16], dv[16];
-                tc::tmem_ld16(trow + LY::SR + 32 * c + 16 * qq, sv);
-                if (RHO) tc::tmem_ld16(trow + LY::SR + 64 + 32 * c + 16 * qq, rv);
-                tc::tmem_ld16(trow + LY::DT + 32 * c + 16 * qq, dv);
-                tc::tmem_ld_wait();
-                if (qq == 1) {
-                    tc::fence_before_sync();
-                    mbar_arrive(y_free);  // the next tile's MMAs may overwrite S, R, D
-                }
                 // queries past L or (causal) before this key get no weight
                 const int qb16 = qc + 16 * qq;
                 const int nvalid = min(16, a.L - qb16);
@@ -468,7 +467,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                         const float4 ne = *reinterpret_cast<const float4*>(sq + 192 + x4);
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
-                            const int x = x4 + 2 * hh, y = 8 * qq + x / 2;
+                            const int xl = x4 + 2 * hh, x = 16 * qq + xl, y = x / 2;
                             const float2 s2 = make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]));
                             const float2 r2 = RHO ? make_float2(__uint_as_float(rv[x]),
                                                                 __uint_as_float(rv[x + 1]))
@@ -479,7 +478,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                                 hh ? make_float2(rb.z, rb.w) : make_float2(rb.x, rb.y),
                                 hh ? make_float2(ab.z, ab.w) : make_float2(ab.x, ab.y),
                                 hh ? make_float2(ne.z, ne.w) : make_float2(ne.x, ne.y), nsc2,
-                                (vmask >> x) & 1u, (vmask >> (x + 1)) & 1u);
+                                (vmask >> xl) & 1u, (vmask >> (xl + 1)) & 1u);
                             wpk[y] = tc::pack_bf16(pt.w.x, pt.w.y);
                             spk[y] = tc::pack_bf16(pt.ds.x, pt.ds.y);
                             rpk[y] = tc::pack_bf16(pt.dr.x, pt.dr.y);
