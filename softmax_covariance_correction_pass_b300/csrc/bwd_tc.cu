@@ -546,33 +546,37 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
 // ------------------------------------------------------------------------ dQ, drho
 // One 64-query tile per CTA (the forward's stacked lane layout), 128-key tiles
-// (K in a 3-deep TMA ring, V in a 2-deep one).  TMEM: Y = [S; R] (128 columns)
+// (K in a 4-deep TMA ring, V in a 2-deep one).  TMEM: Y = [S; R] (128 columns)
 // and [D; D] (128 columns) of the current key tile, the [dQ; drho] accumulator,
-// and two packed dS/dR operand slots.  The compute warps release Y as soon as
-// they have loaded it, so the MMAs of key tile t + 1 run while they work on
-// tile t; [dQ; drho] += [dS; dR] K of tile t follows.  Every MMA has N = 128
-// (the tensor core's full rate; N = 64 runs at ~60% of it).  Eight compute
-// warps: two per TMEM lane quarter, each taking 64 of the 128 key columns.
+// the packed dS/dR operand slot, and the stacked [Q; rho] tile itself (the A
+// operand of [S; R], copied in once, which leaves shared memory to the K ring).
+// The compute warps release Y as soon as they have loaded it, so the MMAs of
+// key tile t + 1 run while they work on tile t; [dQ; drho] += [dS; dR] K of
+// tile t follows.  Every MMA has N = 128 (the tensor core's full rate; N = 64
+// runs at ~60% of it).  Eight compute warps: two per TMEM lane quarter, each
+// taking 64 of the 128 key columns.
 constexpr int Q_KT = 128;     // keys per tile
-constexpr int Q_KSTAGES = 3;  // K is read by two MMA groups (S|R of its tile, then dQ)
+constexpr int Q_KSTAGES = 4;  // K is read by two MMA groups (S|R of its tile, then dQ)
 constexpr int Q_VSTAGES = 2;
 
 template <int D>
 struct QLayout {
     static constexpr int NCB = D / 64;
     static constexpr int OPB = NCB * SUB;             // [128 x D] operand, also one K or V tile
-    static constexpr int QR_OFF = 0;                  // stacked [Q; rho] (16-row groups)
-    static constexpr int DO_OFF = OPB;                // stacked [dO; dO]
-    static constexpr int K_OFF = 2 * OPB;             // K ring
+    static constexpr int DO_OFF = 0;                  // stacked [dO; dO] (16-row groups)
+    static constexpr int K_OFF = OPB;                 // K ring
     static constexpr int V_OFF = K_OFF + Q_KSTAGES * OPB;  // V ring
+    // the stacked [Q; rho] tile lands in the last K stage, on its way to TMEM
+    static constexpr int QR_OFF = K_OFF + (Q_KSTAGES - 1) * OPB;
     static constexpr int BAR_OFF = V_OFF + Q_VSTAGES * OPB;
-    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full, y_free, p_full[2],
-    // pk_empty[2], o_full
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full, y_free, p_full,
+    // pk_empty, o_full, qr_in
     static constexpr int B_S = 1 + 2 * Q_KSTAGES + 2 * Q_VSTAGES;
-    static constexpr int NBARS = B_S + 7;
+    static constexpr int NBARS = B_S + 6;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
-    // TMEM columns: [S; R] at 0, [D; D] at YD, the accumulator at O, packed slots at PK
-    static constexpr uint32_t YD = 128, O = 256, PK = 256 + D;
+    // TMEM columns: [S; R] at 0, [D; D] at YD, the accumulator at O, the packed slot at PK,
+    // [Q; rho] (bf16 pairs) at QA
+    static constexpr uint32_t YD = 128, O = 256, PK = 256 + D, QA = 256 + D + 64;
 };
 
 template <int D, bool CAUSAL, bool RHO>
@@ -593,9 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* v_empty = bars + 1 + 2 * KS + VS;
     uint64_t* s_full = bars + LY::B_S;
     uint64_t* y_free = bars + LY::B_S + 1;    // the compute warps have loaded Y
-    uint64_t* p_full = bars + LY::B_S + 2;    // [2] packed slot written
-    uint64_t* pk_empty = bars + LY::B_S + 4;  // [2] packed slot read by its dQ MMAs
-    uint64_t* o_full = bars + LY::B_S + 6;
+    uint64_t* p_full = bars + LY::B_S + 2;    // packed slot written
+    uint64_t* pk_empty = bars + LY::B_S + 3;  // packed slot read by its dQ MMAs
+    uint64_t* o_full = bars + LY::B_S + 4;
+    uint64_t* qr_in = bars + LY::B_S + 5;     // [Q; rho] copied to TMEM (128 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -613,8 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < LY::NBARS; ++b) {
-            const bool many = b == LY::B_S + 1 || b == LY::B_S + 2 || b == LY::B_S + 3;
-            mbar_init(&bars[b], many ? kComputeThreads : 1);
+            uint32_t count = 1;
+            if (b == LY::B_S + 1 || b == LY::B_S + 2) count = kComputeThreads;
+            if (b == LY::B_S + 5) count = 128;
+            mbar_init(&bars[b], count);
         }
         *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
         fence_mbar_init();
@@ -676,6 +683,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                // the last stage first holds [Q; rho] until it is in TMEM
+                if (j == KS - 1 && !mbar_wait(qr_in, 0, &g_bwd_err)) {
+                    ok = false;
+                    break;
+                }
                 mbar_arrive_expect_tx(&k_full[ks], LY::OPB);
                 for (int cb = 0; cb < LY::NCB; ++cb)
                     tc::tma_load_3d(smem + LY::K_OFF + ks * LY::OPB + cb * SUB, &tmK, cb * 64,
@@ -697,7 +709,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdesc1 = tc::idesc_bf16_f32(128, Q_KT, false);
             constexpr uint32_t kIdesc2 = tc::idesc_bf16_f32(128, D, true);
             const uint32_t sbase = smem_u32(smem);
-            const uint64_t dQR = tc::smem_desc_sw128(sbase + LY::QR_OFF, 16, 1024);
             const uint64_t dDO = tc::smem_desc_sw128(sbase + LY::DO_OFF, 16, 1024);
             const uint64_t dK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, 16, 1024);
             const uint64_t dV0 = tc::smem_desc_sw128(sbase + LY::V_OFF, 16, 1024);
@@ -713,9 +724,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dK = tc::opaque(dK0 + ks * kStep);
                 const uint64_t dV = tc::opaque(dV0 + vs * kStep);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // [S; R] = [Q; rho] K^T
+                for (int kk = 0; kk < D / 16; ++kk) {  // [S; R] = [Q; rho] K^T, A from TMEM
                     const uint32_t off = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
-                    tc::mma_ss(tmem, dQR + off, dK + off, kIdesc1, kk > 0);
+                    tc::mma_ts(tmem, tmem + LY::QA + 8 * kk, dK + off, kIdesc1, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {  // [D; D] = [dO; dO] V^T
@@ -726,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::commit(&v_empty[vs]);
                 return true;
             };
-            bool ok = mbar_wait_warp(q_full, 0, &g_bwd_err);
+            bool ok = mbar_wait_warp(q_full, 0, &g_bwd_err) && mbar_wait_warp(qr_in, 0, &g_bwd_err);
             if (ok) ok = issue_ab(0);
             for (int t = 0; t < n_t && ok; ++t) {
                 if (t + 1 < n_t) {  // the next tile's S|R and D as soon as Y is free
@@ -736,19 +747,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!(ok = issue_ab(t + 1))) break;
                 }
-                if (!mbar_wait_warp(&p_full[t & 1], (t >> 1) & 1, &g_bwd_err)) {
+                if (!mbar_wait_warp(p_full, t & 1, &g_bwd_err)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
                 const uint64_t mK = tc::opaque(mK0 + (t % KS) * kStep);
-                const uint32_t pk = LY::PK + 64 * (t & 1);
+                const uint32_t pk = LY::PK;
 #pragma unroll
                 for (int kk = 0; kk < Q_KT / 16; ++kk)  // [dQ; drho] += [dS; dR] K
                     tc::mma_ts(tmem + LY::O, tmem + pk + 8 * kk, mK + ((kk * 16 * 128) >> 4),
                                kIdesc2, (t > 0 || kk > 0) ? 1u : 0u);
                 tc::commit(&k_empty[t % KS]);
-                tc::commit(&pk_empty[t & 1]);
+                tc::commit(pk_empty);
             }
             tc::commit(o_full);
             if (!ok) {
@@ -771,6 +782,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             z = make_float4(zr[0], zr[a.Lp], zr[2 * (size_t)a.Lp], zr[3 * (size_t)a.Lp]);
         }
         bool ok = !skip;
+        if (set == 0) {
+            // [Q; rho] -> TMEM: lane = operand row, column x holds elements 2x, 2x + 1
+            const int orow = 32 * g + lane;
+            const bool got = ok && mbar_wait(q_full, 0, &g_bwd_err);
+            if (__all_sync(kFullMask, got)) {
+#pragma unroll 1
+                for (int cb = 0; cb < LY::NCB; ++cb) {
+                    uint32_t u[32];
+                    const unsigned char* src = smem + LY::QR_OFF + cb * SUB + orow * 128;
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        const uint4 q = *reinterpret_cast<const uint4*>(src + ((x ^ (orow & 7)) * 16));
+                        u[4 * x] = q.x;
+                        u[4 * x + 1] = q.y;
+                        u[4 * x + 2] = q.z;
+                        u[4 * x + 3] = q.w;
+                    }
+                    tc::tmem_st32(rowS + LY::QA + 32 * cb, u);
+                }
+                tc::tmem_st_wait();
+            } else {
+                ok = false;
+                *abort_flag = 1;
+            }
+            tc::fence_before_sync();
+            mbar_arrive(qr_in);
+        }
         for (int t = 0; t < n_t && ok; ++t) {
             const bool got = !*abort_flag && mbar_wait(s_full, t & 1, &g_bwd_err);
             if (!__all_sync(kFullMask, got)) {
@@ -815,21 +853,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 run(std::false_type{});
             else
                 run(std::true_type{});
-            // the packed slot of this tile was read by the dQ MMAs of tile t - 2
-            const bool slot_free = t < 2 || (!*abort_flag &&
-                                        mbar_wait(&pk_empty[t & 1], ((t >> 1) - 1) & 1, &g_bwd_err));
+            // the packed slot was read by the dQ MMAs of tile t - 1
+            const bool slot_free = t < 1 || (!*abort_flag && mbar_wait(pk_empty, (t - 1) & 1, &g_bwd_err));
             if (!__all_sync(kFullMask, slot_free)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
             // packed slot (keys 2c, 2c+1 at column c): dS in the query lanes, dR in the probe lanes
-            const uint32_t pk = LY::PK + 64 * (t & 1) + 32 * set;
+            const uint32_t pk = LY::PK + 32 * set;
             tc::tmem_st16_split<16>(rowS + pk, spk);
             tc::tmem_st16_split<16>(rowR + pk, rpk);
             tc::tmem_st_wait();
             tc::fence_before_sync();
-            mbar_arrive(&p_full[t & 1]);
+            mbar_arrive(p_full);
         }
         const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
         if (__all_sync(kFullMask, done)) {
