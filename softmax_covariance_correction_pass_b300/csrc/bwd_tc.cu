@@ -556,8 +556,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 // runs at ~60% of it).  Eight compute warps: two per TMEM lane quarter, each
 // taking 64 of the 128 key columns.
 constexpr int Q_KT = 128;     // keys per tile
-constexpr int Q_KSTAGES = 4;  // K is read by two MMA groups (S|R of its tile, then dQ)
-constexpr int Q_VSTAGES = 2;
+constexpr int Q_KSTAGES = 3;  // K is read by two MMA groups (S|R of its tile, then dQ)
+constexpr int Q_VSTAGES = 3;
 
 template <int D>
 struct QLayout {
