@@ -206,13 +206,15 @@ int parallax_attn_decode_paged(const void* q, const void* rho, const void* k_pag
  *   Sigma_kk = sum_j p_j (k_j - mu_k)(k_j - mu_k)^T,
  *   rho = Sigma_kk^-1 (mu_k - q)  by conjugate gradient from rho = 0 (cg_iters
  *         steps, 0 = d; it also stops at a relative residual of 1e-6),
- *   o   = mu_v - C^T rho  (parallax_attn_decode with that probe, rounded to bf16).
+ *   o   = mu_v - C^T rho,  mu_v = sum p v,  C = sum_j p_j (k_j - mu_k)(v_j - mu_v)^T
+ *         (the Parallax output with that probe, in fp32).
  *   q                 : bf16 [B, H, d]
  *   k_cache, v_cache  : bf16 [B, H, Lmax, d];  seqlens: int32 [B] on the device
  *   o                 : fp32 [B, H, d];  rho: fp32 [B, H, d] (the solved probes)
- * One CTA per (b, h) forms Sigma_kk in fp32 (compute-bound: d^2 multiply-adds
- * per key) and runs the CG in shared memory.  Uses a library-owned workspace of
- * B*H*d*2 bytes plus the decode workspace (same rules as parallax_attn_decode).
+ * One CTA per (b, h) reads K and V once, accumulates the p-weighted key/key and
+ * key/value second moments on the tensor cores (bf16 keys times p k and p v split
+ * into a bf16 high part and residual, fp32 accumulators), and runs the CG in shared
+ * memory.  A sequence with no keys gives o = 0 and rho = 0.  Allocates nothing.
  */
 int parallax_lla_decode(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* seqlens, void* o, float* rho, int B, int H, int Lmax,

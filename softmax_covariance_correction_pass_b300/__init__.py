@@ -284,7 +284,7 @@ def parallax_lla_decode(q, k_cache, v_cache, seqlens, o=None, rho=None, cg_iters
     """Exact local linear attention decode (the per-query solve the Parallax probe replaces):
     q bf16 [B, H, d], caches bf16 [B, H, Lmax, d], seqlens int32 [B].  Returns (o, rho),
     fp32 [B, H, d]: rho = Sigma_kk^-1 (mu_k - q) by conjugate gradient (cg_iters steps,
-    0 = d), o = the Parallax decode with that probe."""
+    0 = d), o = mu_v - C^T rho (the Parallax output with that probe), one pass over K and V."""
     B, H, Lmax, d = k_cache.shape
     _need(q, "q", torch.bfloat16, (B, H, d))
     _need(k_cache, "k_cache", torch.bfloat16, (B, H, Lmax, d))

@@ -44,8 +44,6 @@ struct DeviceState {
     size_t ws_bytes = 0;
     void* bws = nullptr;  // prefill backward row statistics
     size_t bws_bytes = 0;
-    void* lws = nullptr;  // exact-LLA probes in bf16
-    size_t lws_bytes = 0;
     int num_sms = 0;
 };
 
@@ -439,20 +437,10 @@ int parallax_lla_decode(const void* q, const void* k_cache, const void* v_cache,
     int dev = 0;
     DeviceState* ds = device_state(&dev);
     if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
-    void* rb = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        DeviceState& st = g_dev[dev];
-        rc = grow(st.lws, st.lws_bytes, (size_t)B * H * d * 2, "LLA workspace");
-        if (rc != PARALLAX_OK) return rc;
-        rb = st.lws;
-    }
-    cudaError_t e = parallax::lla_probe_launch(q, k_cache, seqlens, rho, rb, B, H, Lmax, d,
-                                               cg_iters > 0 ? cg_iters : d, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "LLA probe launch");
-    // the output: the Parallax decode with the solved probe
-    const parallax::DecodePlan plan = make_plan(B, H, H, Lmax, d, ds->num_sms);
-    return decode_run(plan, dev, ds, q, rb, k_cache, v_cache, seqlens, o, stream, true, nullptr);
+    cudaError_t e = parallax::lla_launch(q, k_cache, v_cache, seqlens, rho, static_cast<float*>(o),
+                                         B, H, Lmax, d, cg_iters > 0 ? cg_iters : d, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "LLA launch");
+    return succeed();
 }
 
 int parallax_attn_decode_chunk_keys(int B, int H, int Lmax, int d, int elem_bytes) {
@@ -497,12 +485,6 @@ int parallax_attn_release_workspace(void) {
         e = cudaFree(g_dev[dev].bws);
         g_dev[dev].bws = nullptr;
         g_dev[dev].bws_bytes = 0;
-        if (e != cudaSuccess) return cuda_fail(e, "workspace free");
-    }
-    if ((int)g_dev.size() > dev && g_dev[dev].lws) {
-        e = cudaFree(g_dev[dev].lws);
-        g_dev[dev].lws = nullptr;
-        g_dev[dev].lws_bytes = 0;
         if (e != cudaSuccess) return cuda_fail(e, "workspace free");
     }
     return succeed();

@@ -81,10 +81,11 @@ cudaError_t prefill_backward_launch(const PrefillShape& s, const void* q, const 
 unsigned prefill_backward_take_error();
 
 // ---------------------------------------------------------------- exact LLA decode
-// Probe rho = Sigma_kk^-1 (mu_k - q) per (b, h) by conjugate gradient (fp32 and bf16 copies).
-cudaError_t lla_probe_launch(const void* q, const void* kc, const int32_t* seqlens, float* rho,
-                             void* rho_bf16, int B, int H, int Lmax, int d, int iters,
-                             cudaStream_t stream);
+// Per (b, h), one pass over K and V: rho = Sigma_kk^-1 (mu_k - q) by conjugate gradient and
+// o = mu_v - C^T rho (both fp32 [B*H, d]).
+cudaError_t lla_launch(const void* q, const void* kc, const void* vc, const int32_t* seqlens,
+                       float* rho, float* o, int B, int H, int Lmax, int d, int iters,
+                       cudaStream_t stream);
 unsigned lla_take_error();
 
 // ---------------------------------------------------------------- tensor maps

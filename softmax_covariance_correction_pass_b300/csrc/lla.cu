@@ -4,44 +4,45 @@
 // for the learned rho = W_R x ("Parallax mantem softmax ...", paragraphs 1-2);
 // this computes the original, for comparison, for one query token per head:
 //
-//   p_j = softmax_j(scale q.k_j),  mu_k = sum p k,  Sigma_kk = sum_j p_j (k_j - mu_k)(k_j - mu_k)^T
+//   p_j = softmax_j(scale q.k_j),  mu_k = sum p k,  mu_v = sum p v
+//   Sigma_kk = sum_j p_j (k_j - mu_k)(k_j - mu_k)^T,  C = sum_j p_j (k_j - mu_k)(v_j - mu_v)^T
 //   rho = Sigma_kk^-1 (mu_k - q)    by conjugate gradient from rho = 0
-//   o   = mu_v - C^T rho            (the Parallax decode with that rho)
+//   o   = mu_v - C^T rho            (the Parallax output with that probe)
 //
-// lla_probe_kernel: one CTA per (b, h), 8 warps.  Pass 1 streams the head's keys
-// through shared memory in tiles of 64 (cp.async, double-buffered, so the next
-// tile loads while this one is used).  Per tile: the scores (each warp 8 keys,
-// the query held in registers), the online-softmax max, then p_j k_j written as
-// a bf16 pair (high part, residual) with p_j itself in the row's spare columns.
-// The p-weighted second moment G = sum_j k_j (p_j k_j)^T and the weighted mean
-// l mu_k = sum_j p_j k_j run on the tensor cores: warp w owns a 16-row stripe of
-// G (and of l mu_k) as warp-level mma.sync m16n8k16 accumulators (fp32), with
-// A = the keys (exact bf16) and B = the high part and the residual (two MMAs, so
-// the product keeps ~16 bits).  The centred covariance then goes to shared
-// memory (over the dead key tiles) and the CG iterations run there
-// (matrix-vector products split over 256 threads, dot products by block
-// reduction), stopping after `iters` steps or at a relative residual of 1e-6.
-// The probe is written in fp32 (returned) and bf16 (for the decode pass); o
-// comes from the Parallax decode kernel with that probe.
+// lla_kernel: one CTA per (b, h), one pass over the head's keys and values.
+// Warp 0 streams 64-key tiles of K and V by TMA (3-deep ring, 128-byte
+// swizzle); warps 2-9 compute the scores, the online-softmax max (moved only
+// when a tile's max exceeds it by more than 2^8; the accumulators are then
+// rescaled), the weights p~_j, the weighted sums l = sum p~, l mu_k, l mu_v
+// (fp32), and write p~_j k_j and p~_j v_j as bf16 pairs (high part, residual)
+// into shared memory; warp 1 issues the tcgen05 MMAs
+//   G_kk += K^T (p~ K),   G_kv += K^T (p~ V)      (fp32 accumulators in TMEM)
+// with the key tile itself as the (MN-major) A operand and the two parts of
+// each product as B (so the products keep ~16 significant bits).  After the
+// stream: Sigma_kk = G_kk / l - mu_k mu_k^T and C = G_kv / l - mu_k mu_v^T go
+// to shared memory, conjugate gradient runs there (matrix-vector products over
+// 256 threads, dot products by group reduction), stopping after `iters` steps or
+// at a relative residual of 1e-6, and o = mu_v - C^T rho is formed in fp32.
+#include "tcgen05.cuh"
 #include "kernels.h"
-#include "common.cuh"
 
 namespace parallax {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kTile = 64;  // keys per tile
+constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 compute
+constexpr int kCompute = 256;
+constexpr int kTile = 64;       // keys per tile
+constexpr int kStages = 3;
 constexpr float kCgTol = 1e-6f;
+constexpr float kRescale = 8.f;  // log2 units
 
 struct LlaArgs {
     const __nv_bfloat16* q;
-    const __nv_bfloat16* kc;
     const int32_t* seqlens;
-    float* rho;                 // [B*H, D]
-    __nv_bfloat16* rho_bf16;    // [B*H, D]
+    float* rho;  // [B*H, D]
+    float* o;    // [B*H, D]
     int H, Lmax, iters;
-    float qscale;               // scale * log2(e)
+    float qscale;  // scale * log2(e)
 };
 
 __device__ unsigned g_lla_err = 0;
@@ -53,341 +54,507 @@ __device__ __forceinline__ uint32_t pack_bf16_lla(float lo, float hi) {
     return r;
 }
 
-// Sum over the block; every thread gets the result.  `red` holds 8 floats.
-__device__ __forceinline__ float block_sum(float v, float* red) {
+__device__ __forceinline__ void st_shared_16(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
+                 "r"(w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_16u(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Named barrier 1 over the compute threads, returning the AND of `p` over all of them
+// (so that a failed wait takes every compute warp down the same path).
+__device__ __forceinline__ bool named_bar_and(int nthreads, bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, 1, %2, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// Sum over the 256 compute threads (named barrier 1); every one gets the result.
+__device__ __forceinline__ float grp_sum(float v, float* red, int cw, int lane) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
-    __syncthreads();  // red is free
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
+    named_bar_sync(1, kCompute);  // red is free
+    if (lane == 0) red[cw] = v;
+    named_bar_sync(1, kCompute);
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) s += red[w];
+    for (int w = 0; w < kCompute / 32; ++w) s += red[w];
     return s;
 }
 
-__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
-                 : "=r"(r0), "=r"(r1)
-                 : "r"(addr));
-}
-
-// 16-byte global -> shared copy; src_bytes = 0 fills the destination with zeros.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// kind::f16 instruction descriptor with both operands MN-major (A: M contiguous,
+// B: N contiguous), bf16 in, fp32 accumulate.
+constexpr uint32_t idesc_mn_mn(int M, int N) { return tc::idesc_bf16_f32(M, N, true) | (1u << 15); }
 
 template <int D>
 struct LlaLayout {
-    // bytes per key row: the D bf16 values, then 8 spare bf16 columns.  The
-    // 16-byte pad also spreads 8 consecutive rows over the 8 bank groups, so the
-    // transposing ldmatrix loads are conflict-free.
-    static constexpr int PITCH = D * 2 + 16;
-    static constexpr int TILE_BYTES = kTile * PITCH;
-    static constexpr int KB = 0;                          // 2 x [kTile][PITCH] keys (double buffer)
-    static constexpr int PK_HI = 2 * TILE_BYTES;          // bf16(p k); spare column 0 = bf16(p)
-    static constexpr int PK_LO = 3 * TILE_BYTES;          // the residuals p k - hi, p - hi
-    static constexpr int TILES_END = 4 * TILE_BYTES;
-    static constexpr int SIG_BYTES = D * (D + 1) * 4;     // covariance (aliases the tiles)
-    static constexpr int VEC_OFF = (TILES_END > SIG_BYTES ? TILES_END : SIG_BYTES);
-    static constexpr size_t SMEM_BYTES = VEC_OFF + sizeof(float) * (6 * D + kTile + 2 * kWarps);
+    static constexpr int NCB = D / 64;                 // 64-feature column blocks
+    static constexpr int SUBT = kTile * 128;           // [64 keys x 64 features] bf16, swizzled
+    static constexpr int TILE = NCB * SUBT;            // a 64-key tile of K or V
+    static constexpr int STAGE = 2 * TILE;             // K, then V
+    static constexpr int B_OFF = kStages * STAGE;      // 2 buffers of {p~K hi, lo, p~V hi, lo}
+    static constexpr int BBUF = 4 * TILE;
+    // d = 64: a zero block stands in for features 64..127 of the M = 128 A operand
+    static constexpr int ZERO_OFF = B_OFF + 2 * BBUF;
+    static constexpr int STREAM_END = ZERO_OFF + (D == 64 ? SUBT : 0);
+    // after the stream the same bytes hold Sigma_kk, C^T (rows padded to LD), the
+    // per-thread partial means and the CG vectors
+    static constexpr int LD = D + 1;
+    static constexpr int SIG_OFF = 0;
+    static constexpr int CT_OFF = D * LD * 4;
+    static constexpr int CPR = D / 8;                  // 16-byte chunks per key row
+    static constexpr int RGRP = kCompute / CPR;        // rows handled in parallel
+    static constexpr int MUP_OFF = 2 * D * LD * 4;     // [RGRP][2][D] partial sums
+    static constexpr int CGV_OFF = MUP_OFF + RGRP * 2 * D * 4;  // 6 x [D]
+    static constexpr int POST_END = CGV_OFF + 6 * D * 4;
+    static constexpr int VEC_OFF = (STREAM_END > POST_END ? STREAM_END : POST_END);
+    // sc[kTile] scaled scores, wmax[8], red[8]
+    static constexpr int BAR_OFF = VEC_OFF + (kTile + 16) * 4;
+    // kv_full[S], kv_empty[S], b_full[2], b_empty[2], acc_full
+    static constexpr int NBARS = 2 * kStages + 5;
+    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    static constexpr uint32_t TMEM_COLS = 2 * D;       // G_kk at 0, G_kv at D
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) lla_probe_kernel(const LlaArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    lla_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const LlaArgs a) {
     using LY = LlaLayout<D>;
-    constexpr int TPR = kThreads / D;   // threads per matrix row in the CG products
-    constexpr int LD = D + 1;           // padded row stride of the covariance (bank spread)
-    // warp -> a 16-row stripe and a column group of the Gram matrix
-    constexpr int STRIPES = D / 16, CGS = kWarps / STRIPES, COLS = D / CGS, NT = COLS / 8;
-    static_assert(STRIPES * CGS == kWarps && NT % 2 == 0, "Gram matrix tiling");
-    constexpr int QPL = D / 32;          // query elements per lane in the score dot products
-    constexpr int VPR = D / 8;           // 16-byte vectors per key row
-    constexpr int KPW = kTile / kWarps;  // keys per warp in the score pass
-    constexpr int RPP = kThreads / 8;    // rows per pass of the p k pass (8 threads per row)
-    static_assert(KPW <= 32 && kTile % RPP == 0 && VPR % 8 == 0, "tile shape");
-    extern __shared__ __align__(16) unsigned char smb[];
-    unsigned char* pkh = smb + LY::PK_HI;
-    unsigned char* pkl = smb + LY::PK_LO;
-    float* sig = reinterpret_cast<float*>(smb);               // [D][LD], after pass 1
-    float* qv = reinterpret_cast<float*>(smb + LY::VEC_OFF);  // [D] query
-    float* mu = qv + D;                 // [D] mu_k
-    float* xv = mu + D;                 // [D] CG iterate
-    float* rv = xv + D;                 // [D] residual
-    float* pv = rv + D;                 // [D] search direction
-    float* ap = pv + D;                 // [D] Sigma p
-    float* s2 = ap + D;                 // [kTile] scaled scores of the tile
-    float* wmax = s2 + kTile;           // [kWarps] per-warp maxima of the tile
-    float* red = wmax + kWarps;         // [kWarps] reduction scratch
+    constexpr int S = kStages;
+    constexpr int QPL = D / 32;  // query features per lane in the score dot products
+    constexpr int ROWS_PER_T = kTile * LY::CPR / kCompute;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* sc = reinterpret_cast<float*>(smem + LY::VEC_OFF);
+    float* wmax = sc + kTile;
+    float* red = wmax + 8;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
+    uint64_t* kv_full = bars;
+    uint64_t* kv_empty = bars + S;
+    uint64_t* b_full = bars + 2 * S;   // [2] 256 arrivals
+    uint64_t* b_empty = bars + 2 * S + 2;
+    uint64_t* acc_full = bars + 2 * S + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    const int t = threadIdx.x, warp = t / 32, lane = t % 32;
     const int bh = blockIdx.x, b = bh / a.H;
     int n = a.seqlens[b];
     if (n < 0 || n > a.Lmax) {
-        if (t == 0) raise_error(&g_lla_err, PARALLAX_DEVERR_SEQLEN_CLAMPED);
+        if (threadIdx.x == 0) raise_error(&g_lla_err, PARALLAX_DEVERR_SEQLEN_CLAMPED);
         n = n < 0 ? 0 : a.Lmax;
     }
-    const __nv_bfloat16* qh = a.q + (size_t)bh * D;
-    if (t < D) qv[t] = __bfloat162float(qh[t]);
-    __syncthreads();
-
-    // ---------------------------------------------------------------- pass 1
-    const int stripe = warp % STRIPES, col0 = (warp / STRIPES) * COLS;
-    const bool mean_warp = col0 + COLS == D;  // also accumulates l mu_k for its stripe
-    float acc[NT][4];  // rows 16 stripe + g (and + 8) of G, columns col0 + 8 nt + 2 (lane & 3) (+1)
-    float accx[4] = {0.f, 0.f, 0.f, 0.f};  // column 0: l mu_k for the same rows
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    float lpart = 0.f, m = -INFINITY;
-    const __nv_bfloat16* kh = a.kc + (size_t)bh * a.Lmax * D;
-    const uint32_t kb_s = smem_u32(smb + LY::KB);
-    const uint32_t pkh_s = smem_u32(pkh), pkl_s = smem_u32(pkl);
-    const int mi = lane >> 3, r8 = lane & 7;
     const int ntiles = (n + kTile - 1) / kTile;
-    auto issue = [&](int tile, int buf) {
-        const int j0 = tile * kTile;
-#pragma unroll
-        for (int vi = t; vi < kTile * VPR; vi += kThreads) {
-            const int row = vi / VPR, c8 = (vi - row * VPR) * 8;
-            const bool in = j0 + row < n;  // rows past the sequence are zero-filled
-            cp_async_16(kb_s + buf * LY::TILE_BYTES + row * LY::PITCH + c8 * 2,
-                        kh + (size_t)(in ? j0 + row : 0) * D + c8, in ? 16u : 0u);
-        }
-        cp_async_commit();
-    };
-    if (ntiles > 0) issue(0, 0);
-    for (int it = 0; it < ntiles; ++it) {
-        const int buf = it & 1, nk = min(kTile, n - it * kTile);
-        cp_async_wait_all();
-        __syncthreads();  // tile `it` is in for every thread; tile it - 1 is consumed
-        if (it + 1 < ntiles) issue(it + 1, buf ^ 1);
-        const unsigned char* kb = smb + LY::KB + buf * LY::TILE_BYTES;
-        // scores: warp w takes keys KPW w .. KPW w + KPW - 1
-        float mine = -INFINITY, wm = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < KPW; ++e) {
-            const int j = warp * KPW + e;
-            float dot = 0.f;
-            if constexpr (QPL == 4) {
-                const uint2 raw = *reinterpret_cast<const uint2*>(kb + j * LY::PITCH + lane * 8);
-                const float4 qq = *reinterpret_cast<const float4*>(qv + 4 * lane);
-                dot = qq.x * __uint_as_float(raw.x << 16);
-                dot = fmaf(qq.y, __uint_as_float(raw.x & 0xffff0000u), dot);
-                dot = fmaf(qq.z, __uint_as_float(raw.y << 16), dot);
-                dot = fmaf(qq.w, __uint_as_float(raw.y & 0xffff0000u), dot);
-            } else {
-                const uint32_t raw = *reinterpret_cast<const uint32_t*>(kb + j * LY::PITCH + lane * 4);
-                const float2 qq = *reinterpret_cast<const float2*>(qv + 2 * lane);
-                dot = qq.x * __uint_as_float(raw << 16);
-                dot = fmaf(qq.y, __uint_as_float(raw & 0xffff0000u), dot);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < LY::NBARS; ++i)
+            mbar_init(&bars[i], (i == 2 * S || i == 2 * S + 1) ? kCompute : 1);
+        *abort_flag = (*(volatile unsigned*)&g_lla_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
+        fence_mbar_init();
+    }
+    if (D == 64 && warp >= 2) {  // the zero block of the padded A operand
+        for (int i = threadIdx.x - 64; i < LY::SUBT / 16; i += kCompute)
+            reinterpret_cast<uint4*>(smem + LY::ZERO_OFF)[i] = make_uint4(0, 0, 0, 0);
+        fence_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&tmK);
+        tc::prefetch_tmap(&tmV);
+    }
+    if (warp == 1) tc::tmem_alloc(tmem_slot, LY::TMEM_COLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort_flag != 0;
+    const uint32_t sbase = smem_u32(smem);
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0 && !skip) {
+            int issued = 0;
+            bool ok = true;
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % S;
+                if (t >= S && !mbar_wait(&kv_empty[s], ((t / S) - 1) & 1, &g_lla_err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&kv_full[s], LY::STAGE);
+                unsigned char* st = smem + s * LY::STAGE;
+                for (int cb = 0; cb < LY::NCB; ++cb) {
+                    tc::tma_load_3d(st + cb * LY::SUBT, &tmK, cb * 64, t * kTile, bh, &kv_full[s]);
+                    tc::tma_load_3d(st + LY::TILE + cb * LY::SUBT, &tmV, cb * 64, t * kTile, bh,
+                                    &kv_full[s]);
+                }
+                issued = t + 1;
             }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(kFullMask, dot, off);
-            const float s = j < nk ? dot * a.qscale : -INFINITY;
-            wm = fmaxf(wm, s);
-            if (lane == e) mine = s;
-        }
-        if (lane < KPW) s2[warp * KPW + lane] = mine;
-        if (lane == 0) wmax[warp] = wm;
-        __syncthreads();
-        float bm = wmax[0];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) bm = fmaxf(bm, wmax[w]);
-        const float m_new = fmaxf(m, bm);
-        if (m_new > m) {  // uniform: every thread sees the same maxima
-            const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - m_new);
-            lpart *= alpha;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) accx[e] *= alpha;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                acc[nt][0] *= alpha;
-                acc[nt][1] *= alpha;
-                acc[nt][2] *= alpha;
-                acc[nt][3] *= alpha;
+            if (!ok) {
+                *abort_flag = 1;
+                for (int t = issued >= S ? issued - S : 0; t < issued; ++t)
+                    mbar_wait(&kv_full[t % S], (t / S) & 1, &g_lla_err);
             }
-            m = m_new;
         }
-        // p_j k_j (and p_j) as a bf16 pair (high part, residual): the B operand of the MMAs.
-        // 8 threads per key row, each taking 16-byte vectors e8, e8 + 8, ...
-        {
-            const int e8 = t & 7;
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (!skip) {
+            constexpr uint32_t kIdesc = idesc_mn_mn(128, D);
+            bool ok = true;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int s = t % S, buf = t & 1;
+                if (*abort_flag || !mbar_wait_warp(&b_full[buf], (t >> 1) & 1, &g_lla_err)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                // A = the key tile, M = features (MN-major: 64-feature atoms LBO apart; for
+                // d = 64 the second atom is the zero block), K = keys
+                const uint32_t abase = sbase + s * LY::STAGE;
+                const uint32_t lbo = D == 64 ? (uint32_t)(LY::ZERO_OFF - s * LY::STAGE) : LY::SUBT;
+                const uint64_t dA = tc::opaque(tc::smem_desc_sw128(abase, lbo, 1024));
+                const uint64_t dB =
+                    tc::opaque(tc::smem_desc_sw128(sbase + LY::B_OFF + buf * LY::BBUF, LY::SUBT, 1024));
+                constexpr uint32_t kTileStep = LY::TILE >> 4;
 #pragma unroll
-            for (int pass = 0; pass < kTile / RPP; ++pass) {
-                const int row = (t >> 3) + pass * RPP;
-                const float p = fast_exp2(s2[row] - m);  // 0 past the sequence
-                if (e8 == 0) {
-                    lpart += p;
-                    const uint32_t ph = pack_bf16_lla(p, 0.f);
-                    const uint32_t pl = pack_bf16_lla(p - __uint_as_float(ph << 16), 0.f);
-                    *reinterpret_cast<uint4*>(pkh + row * LY::PITCH + D * 2) = make_uint4(ph, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(pkl + row * LY::PITCH + D * 2) = make_uint4(pl, 0, 0, 0);
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    const uint32_t off = (kk * 16 * 128) >> 4;
+                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                    tc::mma_ss(tmem, dA + off, dB + off, kIdesc, acc);                       // p~K hi
+                    tc::mma_ss(tmem, dA + off, dB + kTileStep + off, kIdesc, 1u);            // p~K lo
+                    tc::mma_ss(tmem + D, dA + off, dB + 2 * kTileStep + off, kIdesc, acc);  // p~V hi
+                    tc::mma_ss(tmem + D, dA + off, dB + 3 * kTileStep + off, kIdesc, 1u);   // p~V lo
+                }
+                tc::commit(&b_empty[buf]);
+                tc::commit(&kv_empty[s]);
+            }
+            tc::commit(acc_full);
+            if (!ok) {
+                *abort_flag = 1;
+                mbar_wait_warp(acc_full, 0, &g_lla_err);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- compute
+        const int t = threadIdx.x - 64;  // 0 .. 255
+        const int cw = warp - 2;          // compute warp 0 .. 7
+        const int q4 = warp & 3;          // TMEM lane quarter
+        const int half = cw >> 2;         // TMEM: G_kk (0) or G_kv (1)
+        bool ok = !skip;
+        // the query, pre-scaled: lane l holds features QPL l .. QPL l + QPL - 1
+        float qr[QPL];
+#pragma unroll
+        for (int e = 0; e < QPL; ++e)
+            qr[e] = __bfloat162float(a.q[(size_t)bh * D + QPL * lane + e]) * a.qscale;
+        const int f0 = QPL * lane;
+        const uint32_t qoff = (uint32_t)((f0 / 64) * LY::SUBT);
+        const int qchunk = (f0 % 64) / 8, qbyte = (f0 % 8) * 2;
+        // the B-operand chunk of this thread: 8 features, ROWS_PER_T rows per tile
+        const int c = t % LY::CPR, rg = t / LY::CPR;
+        const uint32_t coff = (uint32_t)((c / 8) * LY::SUBT);
+        const int cc = c % 8;
+        float mk[8], mv[8];  // partial sums of p~ k and p~ v over this thread's rows
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mk[e] = mv[e] = 0.f;
+        float lpart = 0.f, m = -INFINITY;
+
+        for (int it = 0; it < ntiles; ++it) {
+            const int s = it % S, buf = it & 1;
+            const int nk = min(kTile, n - it * kTile);
+            const bool got = ok && !*abort_flag && mbar_wait(&kv_full[s], (it / S) & 1, &g_lla_err);
+            // every compute thread leaves the loop at the same tile (the barriers below are
+            // counted); this barrier also orders the previous tile's reads of sc and wmax
+            // before this tile's writes
+            ok = named_bar_and(kCompute, __all_sync(kFullMask, got));
+            if (!ok) break;
+            const uint32_t kst = sbase + s * LY::STAGE;
+            // scores: compute warp cw takes keys 8 cw .. 8 cw + 7
+            float wm = -INFINITY, mine = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = 8 * cw + e;
+                const uint32_t addr = kst + qoff + j * 128 + ((qchunk ^ (j & 7)) * 16) + qbyte;
+                float dot;
+                if constexpr (QPL == 4) {
+                    uint32_t x0, x1;
+                    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(x0), "=r"(x1) : "r"(addr));
+                    dot = qr[0] * __uint_as_float(x0 << 16);
+                    dot = fmaf(qr[1], __uint_as_float(x0 & 0xffff0000u), dot);
+                    dot = fmaf(qr[2], __uint_as_float(x1 << 16), dot);
+                    dot = fmaf(qr[3], __uint_as_float(x1 & 0xffff0000u), dot);
+                } else {
+                    uint32_t x0;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x0) : "r"(addr));
+                    dot = qr[0] * __uint_as_float(x0 << 16);
+                    dot = fmaf(qr[1], __uint_as_float(x0 & 0xffff0000u), dot);
                 }
 #pragma unroll
-                for (int cc = 0; cc < VPR / 8; ++cc) {
-                    const int off = row * LY::PITCH + (e8 + 8 * cc) * 16;
+                for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(kFullMask, dot, off);
+                const float sj = j < nk ? dot : -INFINITY;
+                wm = fmaxf(wm, sj);
+                if (lane == e) mine = sj;
+            }
+            if (lane < 8) sc[8 * cw + lane] = mine;
+            if (lane == 0) wmax[cw] = wm;
+            named_bar_sync(1, kCompute);
+            float tmax = wmax[0];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) tmax = fmaxf(tmax, wmax[w]);
+            if (m == -INFINITY) {
+                m = tmax;  // nothing accumulated yet
+            } else if (tmax > m + kRescale) {
+                // uniform: move the max and rescale everything accumulated so far, after
+                // the MMAs of the previous tile have finished
+                const float alpha = fast_exp2(m - tmax);
+                m = tmax;
+                lpart *= alpha;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    mk[e] *= alpha;
+                    mv[e] *= alpha;
+                }
+                const bool done = !*abort_flag &&
+                                  mbar_wait(&b_empty[(it - 1) & 1], ((it - 1) >> 1) & 1, &g_lla_err);
+                if (!__all_sync(kFullMask, done)) {
+                    ok = false;  // this warp stops here; the others stop at the next tile
+                    *abort_flag = 1;
+                    continue;
+                }
+                tc::fence_after_sync();
+                const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * D;
+#pragma unroll 1
+                for (int x = 0; x < D / 32; ++x) {
+                    uint32_t u[32];
+                    tc::tmem_ld32(trow + 32 * x, u);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int y = 0; y < 32; ++y) u[y] = __float_as_uint(__uint_as_float(u[y]) * alpha);
+                    tc::tmem_st32(trow + 32 * x, u);
+                }
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+            }
+            // the B operands of this tile go into buffer `buf`, last read by the MMAs of it - 2
+            if (it >= 2) {
+                const bool freed = !*abort_flag &&
+                                   mbar_wait(&b_empty[buf], ((it >> 1) - 1) & 1, &g_lla_err);
+                if (!__all_sync(kFullMask, freed)) {
+                    ok = false;
+                    *abort_flag = 1;
+                    continue;
+                }
+            }
+            const uint32_t bb = sbase + LY::B_OFF + buf * LY::BBUF;
+#pragma unroll
+            for (int r = 0; r < ROWS_PER_T; ++r) {
+                const int j = rg + r * LY::RGRP;
+                const bool live = j < nk;
+                const float p = live ? fast_exp2(sc[j] - m) : 0.f;
+                if (c == 0) lpart += p;
+                const uint32_t off = coff + j * 128 + ((cc ^ (j & 7)) * 16);
+#pragma unroll
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint4 raw = ld_shared_16u(kst + kv * LY::TILE + off);
                     float f[8];
-                    Vec16<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(kb + off), f);
+                    Vec16<__nv_bfloat16>::unpack(raw, f);
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
-                        const float v0 = p * f[2 * h], v1 = p * f[2 * h + 1];
+                        // rows past the sequence may hold anything: select, do not multiply
+                        const float v0 = live ? p * f[2 * h] : 0.f;
+                        const float v1 = live ? p * f[2 * h + 1] : 0.f;
+                        if (kv == 0) {
+                            mk[2 * h] += v0;
+                            mk[2 * h + 1] += v1;
+                        } else {
+                            mv[2 * h] += v0;
+                            mv[2 * h + 1] += v1;
+                        }
                         hi[h] = pack_bf16_lla(v0, v1);
                         lo[h] = pack_bf16_lla(v0 - __uint_as_float(hi[h] << 16),
                                               v1 - __uint_as_float(hi[h] & 0xffff0000u));
                     }
-                    *reinterpret_cast<uint4*>(pkh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(pkl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    st_shared_16(bb + (2 * kv) * LY::TILE + off, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_16(bb + (2 * kv + 1) * LY::TILE + off, lo[0], lo[1], lo[2], lo[3]);
+                    // the key tile is the A operand: rows past the sequence become zeros
+                    if (kv == 0 && !live) st_shared_16(kst + off, 0u, 0u, 0u, 0u);
+                }
+            }
+            fence_async_smem();  // visible to the tensor core's reads
+            mbar_arrive(&b_full[buf]);
+        }
+
+        // ---------------------------------------------------------------- covariances
+        const bool acc = ok && !*abort_flag && mbar_wait(acc_full, 0, &g_lla_err);
+        if (!__all_sync(kFullMask, acc)) ok = false;
+        // every compute warp is past the stream before its buffers are reused
+        named_bar_sync(1, kCompute);
+        tc::fence_after_sync();
+        const float l = grp_sum(lpart, red, cw, lane);
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        float* sig = reinterpret_cast<float*>(smem + LY::SIG_OFF);
+        float* ct = reinterpret_cast<float*>(smem + LY::CT_OFF);
+        float* mup = reinterpret_cast<float*>(smem + LY::MUP_OFF);
+        float* cgv = reinterpret_cast<float*>(smem + LY::CGV_OFF);
+        float* muk = cgv;           // [D] mu_k
+        float* muv = cgv + D;       // [D] mu_v
+        float* xv = cgv + 2 * D;    // CG iterate
+        float* rv = cgv + 3 * D;    // residual
+        float* pv = cgv + 4 * D;    // search direction
+        float* ap = cgv + 5 * D;    // Sigma p
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            mup[(rg * 2 + 0) * D + 8 * c + e] = mk[e];
+            mup[(rg * 2 + 1) * D + 8 * c + e] = mv[e];
+        }
+        named_bar_sync(1, kCompute);
+        if (t < 2 * D) {
+            const int f = t % D, kind = t / D;
+            float sum = 0.f;
+            for (int r = 0; r < LY::RGRP; ++r) sum += mup[(r * 2 + kind) * D + f];
+            (kind ? muv : muk)[f] = sum * inv_l;
+        }
+        named_bar_sync(1, kCompute);
+        {
+            // Sigma_kk (half 0) or C^T (half 1) from TMEM: lane = feature of k
+            const int f1 = 32 * q4 + lane;
+            const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * D;
+            const bool have = ntiles > 0 && ok;
+            if (f1 < D) {
+                const float mk1 = muk[f1];
+#pragma unroll 1
+                for (int x = 0; x < D / 32; ++x) {
+                    uint32_t u[32];
+                    if (have) {
+                        tc::tmem_ld32(trow + 32 * x, u);
+                        tc::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int y = 0; y < 32; ++y) u[y] = 0u;
+                    }
+#pragma unroll
+                    for (int y = 0; y < 32; ++y) {
+                        const int f2 = 32 * x + y;
+                        const float g = __uint_as_float(u[y]) * inv_l;
+                        if (half == 0)
+                            sig[f1 * LY::LD + f2] = g - mk1 * muk[f2];
+                        else
+                            ct[f2 * LY::LD + f1] = g - mk1 * muv[f2];
+                    }
                 }
             }
         }
-        __syncthreads();
-        // G[stripe rows][column group] += K[:, stripe]^T (p K)[:, group] over the tile's keys
-        const uint32_t kb_a = kb_s + buf * LY::TILE_BYTES;
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks) {
-            const int j0k = 16 * ks;
-            uint32_t af[4];
-            // ldmatrix.trans hands out A fragments in the order (rows g, g+8) x (keys lo, hi)
-            ldsm_x4_t(kb_a + (j0k + (mi >> 1) * 8 + r8) * LY::PITCH + (16 * stripe + (mi & 1) * 8) * 2,
-                      af[0], af[1], af[2], af[3]);
-            const uint32_t brow = (j0k + (mi & 1) * 8 + r8) * LY::PITCH;
-#pragma unroll
-            for (int np = 0; np < NT / 2; ++np) {
-                const uint32_t off = brow + (col0 + 16 * np + (mi >> 1) * 8) * 2;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(pkh_s + off, b0, b1, b2, b3);
-                mma_16816(acc[2 * np], af, b0, b1);
-                mma_16816(acc[2 * np + 1], af, b2, b3);
-                ldsm_x4_t(pkl_s + off, b0, b1, b2, b3);
-                mma_16816(acc[2 * np], af, b0, b1);
-                mma_16816(acc[2 * np + 1], af, b2, b3);
-            }
-            if (mean_warp) {  // the n8 tile of the spare columns: p, then zeros
-                uint32_t b0, b1;
-                ldsm_x2_t(pkh_s + brow + D * 2, b0, b1);
-                mma_16816(accx, af, b0, b1);
-                ldsm_x2_t(pkl_s + brow + D * 2, b0, b1);
-                mma_16816(accx, af, b0, b1);
-            }
-        }
-    }
-
-    // ---------------------------------------------------------------- covariance
-    const float l = block_sum(lpart, red);  // every warp is past its last MMA
-    const float inv_l = l > 0.f ? 1.f / l : 0.f;
-    if (mean_warp && (lane & 3) == 0) {
-        mu[16 * stripe + (lane >> 2)] = accx[0] * inv_l;
-        mu[16 * stripe + (lane >> 2) + 8] = accx[2] * inv_l;
-    }
-    __syncthreads();  // the key tiles are dead: sig takes their place
-    {
-        const int g = lane >> 2, c = 2 * (lane & 3);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int row = 16 * stripe + g + 8 * (e >> 1), col = col0 + 8 * nt + c + (e & 1);
-                sig[row * LD + col] = acc[nt][e] * inv_l - mu[row] * mu[col];
-            }
-    }
-    if (t < D) {
-        const float bt = n > 0 ? mu[t] - qv[t] : 0.f;
-        xv[t] = 0.f;
-        rv[t] = bt;
-        pv[t] = bt;
-    }
-    __syncthreads();
-
-    // ---------------------------------------------------------------- conjugate gradient
-    const int row = t / TPR, part = t % TPR;
-    float rs = block_sum(t < D ? rv[t] * rv[t] : 0.f, red);
-    const float stop = kCgTol * kCgTol * rs;
-    for (int it = 0; it < a.iters && rs > stop && rs > 0.f; ++it) {
-        float partial = 0.f;
-#pragma unroll 8
-        for (int c = part; c < D; c += TPR) partial = fmaf(sig[row * LD + c], pv[c], partial);
-#pragma unroll
-        for (int off = TPR / 2; off >= 1; off >>= 1)
-            partial += __shfl_xor_sync(kFullMask, partial, off);
-        if (part == 0) ap[row] = partial;
-        __syncthreads();
-        const float pap = block_sum(t < D ? pv[t] * ap[t] : 0.f, red);
-        if (!(pap > 0.f)) break;  // uniform; Sigma is only semi-definite
-        const float alpha = rs / pap;
-        float rn = 0.f;
         if (t < D) {
-            xv[t] = fmaf(alpha, pv[t], xv[t]);
-            rn = fmaf(-alpha, ap[t], rv[t]);
-            rv[t] = rn;
+            const float bt = n > 0 ? muk[t] - __bfloat162float(a.q[(size_t)bh * D + t]) : 0.f;
+            xv[t] = 0.f;
+            rv[t] = bt;
+            pv[t] = bt;
         }
-        const float rs_new = block_sum(rn * rn, red);
-        if (t < D) pv[t] = fmaf(rs_new / rs, pv[t], rn);
-        __syncthreads();
-        rs = rs_new;
+        named_bar_sync(1, kCompute);
+
+        // ---------------------------------------------------------------- conjugate gradient
+        constexpr int TPR = kCompute / D;  // threads per matrix row
+        const int row = t / TPR, part = t % TPR;
+        float rs = grp_sum(t < D ? rv[t] * rv[t] : 0.f, red, cw, lane);
+        const float stop = kCgTol * kCgTol * rs;
+        for (int i = 0; i < a.iters && rs > stop && rs > 0.f; ++i) {
+            float partial = 0.f;
+#pragma unroll 8
+            for (int c2 = part; c2 < D; c2 += TPR) partial = fmaf(sig[row * LY::LD + c2], pv[c2], partial);
+#pragma unroll
+            for (int off = TPR / 2; off >= 1; off >>= 1) partial += __shfl_xor_sync(kFullMask, partial, off);
+            if (part == 0) ap[row] = partial;
+            named_bar_sync(1, kCompute);
+            const float pap = grp_sum(t < D ? pv[t] * ap[t] : 0.f, red, cw, lane);
+            if (!(pap > 0.f)) break;  // uniform; Sigma is only semi-definite
+            const float alpha = rs / pap;
+            float rn = 0.f;
+            if (t < D) {
+                xv[t] = fmaf(alpha, pv[t], xv[t]);
+                rn = fmaf(-alpha, ap[t], rv[t]);
+                rv[t] = rn;
+            }
+            const float rs_new = grp_sum(rn * rn, red, cw, lane);
+            if (t < D) pv[t] = fmaf(rs_new / rs, pv[t], rn);
+            named_bar_sync(1, kCompute);
+            rs = rs_new;
+        }
+        // o = mu_v - C^T rho
+        if (t < D) {
+            float acc_o = 0.f;
+#pragma unroll 8
+            for (int f1 = 0; f1 < D; ++f1) acc_o = fmaf(ct[t * LY::LD + f1], xv[f1], acc_o);
+            a.rho[(size_t)bh * D + t] = xv[t];
+            a.o[(size_t)bh * D + t] = muv[t] - acc_o;
+        }
+        if (!ok) *abort_flag = 1;
     }
-    if (t < D) {
-        a.rho[(size_t)bh * D + t] = xv[t];
-        a.rho_bf16[(size_t)bh * D + t] = __float2bfloat16_rn(xv[t]);
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, LY::TMEM_COLS);
     }
 }
 
 template <int D>
-size_t smem_bytes() {
-    return LlaLayout<D>::SMEM_BYTES;
-}
-
-template <int D>
-cudaError_t launch(const LlaArgs& a, int BH, cudaStream_t stream) {
+cudaError_t launch(const LlaArgs& a, const void* kc, const void* vc, int BH, cudaStream_t stream) {
+    CUtensorMap mk, mv;
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.Lmax, (uint64_t)BH};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)a.Lmax * D * 2};
+    const uint32_t box[3] = {64, (uint32_t)kTile, 1};
+    if (!make_tmap_bf16(&mk, kc, 3, dims, strides, box) ||
+        !make_tmap_bf16(&mv, vc, 3, dims, strides, box))
+        return cudaErrorInvalidValue;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(lla_probe_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem_bytes<D>());
+        cudaError_t e = cudaFuncSetAttribute(
+            lla_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LlaLayout<D>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    lla_probe_kernel<D><<<BH, kThreads, smem_bytes<D>(), stream>>>(a);
+    lla_kernel<D><<<BH, kThreads, LlaLayout<D>::SMEM_BYTES, stream>>>(mk, mv, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t lla_probe_launch(const void* q, const void* kc, const int32_t* seqlens, float* rho,
-                             void* rho_bf16, int B, int H, int Lmax, int d, int iters,
-                             cudaStream_t stream) {
+cudaError_t lla_launch(const void* q, const void* kc, const void* vc, const int32_t* seqlens,
+                       float* rho, float* o, int B, int H, int Lmax, int d, int iters,
+                       cudaStream_t stream) {
     LlaArgs a;
     a.q = static_cast<const __nv_bfloat16*>(q);
-    a.kc = static_cast<const __nv_bfloat16*>(kc);
     a.seqlens = seqlens;
     a.rho = rho;
-    a.rho_bf16 = static_cast<__nv_bfloat16*>(rho_bf16);
+    a.o = o;
     a.H = H;
     a.Lmax = Lmax;
     a.iters = iters;
     a.qscale = kLog2e / sqrtf((float)d);
-    if (d == 64) return launch<64>(a, B * H, stream);
-    if (d == 128) return launch<128>(a, B * H, stream);
+    if (d == 64) return launch<64>(a, kc, vc, B * H, stream);
+    if (d == 128) return launch<128>(a, kc, vc, B * H, stream);
     return cudaErrorInvalidValue;
 }
 

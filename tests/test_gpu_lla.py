@@ -1,13 +1,14 @@
 """GPU parity of the exact local linear attention (LLA) decode against the fp64
 oracle (conjugate gradient run to convergence: d steps).
 
-The GPU forms Sigma_kk in fp32, runs CG in fp32 to a relative residual of 1e-6
-(or d steps), rounds the probe to bf16 for the Parallax decode pass.  The
-probe is compared at rel-L2 <= 1e-3 (CG residual 1e-6 times the condition
-number of Sigma_kk, which is below 25 for these draws, plus fp32 rounding of
-the d x d moments), the output at the bf16 criterion (rel-L2 <= 1e-2,
-max-abs <= 2e-2).  Sequences are long enough that Sigma_kk has full rank
-(LLA is undefined otherwise).
+The GPU forms the second moments on the tensor cores (bf16 keys times p k and
+p v carried as a bf16 high part plus residual, ~16 bits, fp32 accumulation),
+runs CG in fp32 to a relative residual of 1e-6 (or d steps) and forms
+o = mu_v - C^T rho in fp32.  The probe is compared at rel-L2 <= 1e-3 (CG
+residual 1e-6 times the condition number of Sigma_kk, which is below 25 for
+these draws, plus the ~2^-16 rounding of the moments), the output at the bf16
+criterion (rel-L2 <= 1e-2, max-abs <= 2e-2).  Sequences are long enough that
+Sigma_kk has full rank (LLA is undefined otherwise).
 """
 import numpy as np
 import pytest
