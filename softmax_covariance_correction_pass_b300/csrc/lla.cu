@@ -11,11 +11,13 @@
 //
 // lla_kernel: one CTA per (b, h), one pass over the head's keys and values.
 // Warp 0 streams 64-key tiles of K and V by TMA (3-deep ring, 128-byte
-// swizzle); warps 2-9 compute the scores, the online-softmax max (moved only
-// when a tile's max exceeds it by more than 2^8; the accumulators are then
-// rescaled), the weights p~_j, the weighted sums l = sum p~, l mu_k, l mu_v
-// (fp32), and write p~_j k_j and p~_j v_j as bf16 pairs (high part, residual)
-// into shared memory; warp 1 issues the tcgen05 MMAs
+// swizzle); warps 2-9 own one 16-byte chunk (8 features) of every key row they
+// touch: they compute the scores (a row's partial dot products summed over the
+// row's lanes), the online-softmax max (moved only when a score exceeds it by
+// more than 2^8; the accumulators are then rescaled), the weights p~_j, the
+// weighted sums l = sum p~, l mu_k, l mu_v (fp32), and write p~_j k_j and
+// p~_j v_j as bf16 pairs (high part, residual) into shared memory; warp 1
+// issues the tcgen05 MMAs
 //   G_kk += K^T (p~ K),   G_kv += K^T (p~ V)      (fp32 accumulators in TMEM)
 // with the key tile itself as the (MN-major) A operand and the two parts of
 // each product as B (so the products keep ~16 significant bits).  After the
@@ -89,6 +91,20 @@ __device__ __forceinline__ bool named_bar_and(int nthreads, bool p) {
     return r != 0;
 }
 
+// Named barrier 1 over the compute threads, returning the OR of `p` over all of them.
+__device__ __forceinline__ bool named_bar_or(int nthreads, bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, %2, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // Sum over the 256 compute threads (named barrier 1); every one gets the result.
 __device__ __forceinline__ float grp_sum(float v, float* red, int cw, int lane) {
 #pragma unroll
@@ -128,8 +144,8 @@ struct LlaLayout {
     static constexpr int CGV_OFF = MUP_OFF + RGRP * 2 * D * 4;  // 6 x [D]
     static constexpr int POST_END = CGV_OFF + 6 * D * 4;
     static constexpr int VEC_OFF = (STREAM_END > POST_END ? STREAM_END : POST_END);
-    // sc[kTile] scaled scores, wmax[8], red[8]
-    static constexpr int BAR_OFF = VEC_OFF + (kTile + 16) * 4;
+    // red[8]: reduction scratch
+    static constexpr int BAR_OFF = VEC_OFF + 64;
     // kv_full[S], kv_empty[S], b_full[2], b_empty[2], acc_full
     static constexpr int NBARS = 2 * kStages + 5;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
@@ -142,14 +158,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                const LlaArgs a) {
     using LY = LlaLayout<D>;
     constexpr int S = kStages;
-    constexpr int QPL = D / 32;  // query features per lane in the score dot products
     constexpr int ROWS_PER_T = kTile * LY::CPR / kCompute;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* sc = reinterpret_cast<float*>(smem + LY::VEC_OFF);
-    float* wmax = sc + kTile;
-    float* red = wmax + 8;
+    float* red = reinterpret_cast<float*>(smem + LY::VEC_OFF);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
     uint64_t* kv_full = bars;
     uint64_t* kv_empty = bars + S;
@@ -262,99 +275,96 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q4 = warp & 3;          // TMEM lane quarter
         const int half = cw >> 2;         // TMEM: G_kk (0) or G_kv (1)
         bool ok = !skip;
-        // the query, pre-scaled: lane l holds features QPL l .. QPL l + QPL - 1
-        float qr[QPL];
-#pragma unroll
-        for (int e = 0; e < QPL; ++e)
-            qr[e] = __bfloat162float(a.q[(size_t)bh * D + QPL * lane + e]) * a.qscale;
-        const int f0 = QPL * lane;
-        const uint32_t qoff = (uint32_t)((f0 / 64) * LY::SUBT);
-        const int qchunk = (f0 % 64) / 8, qbyte = (f0 % 8) * 2;
-        // the B-operand chunk of this thread: 8 features, ROWS_PER_T rows per tile
+        // this thread's 16-byte chunk of every key row (8 features) and its rows of each
+        // tile; the CPR threads of a row are consecutive lanes of one warp
         const int c = t % LY::CPR, rg = t / LY::CPR;
         const uint32_t coff = (uint32_t)((c / 8) * LY::SUBT);
         const int cc = c % 8;
-        float mk[8], mv[8];  // partial sums of p~ k and p~ v over this thread's rows
+        float qc[8];  // the query's features 8c .. 8c + 7, pre-scaled
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mk[e] = mv[e] = 0.f;
+        for (int e = 0; e < 8; ++e) qc[e] = __bfloat162float(a.q[(size_t)bh * D + 8 * c + e]) * a.qscale;
+        float2 mk[4], mv[4];  // partial sums of p~ k and p~ v over this thread's rows
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mk[e] = mv[e] = make_float2(0.f, 0.f);
         float lpart = 0.f, m = -INFINITY;
 
         for (int it = 0; it < ntiles; ++it) {
             const int s = it % S, buf = it & 1;
             const int nk = min(kTile, n - it * kTile);
             const bool got = ok && !*abort_flag && mbar_wait(&kv_full[s], (it / S) & 1, &g_lla_err);
-            // every compute thread leaves the loop at the same tile (the barriers below are
-            // counted); this barrier also orders the previous tile's reads of sc and wmax
-            // before this tile's writes
-            ok = named_bar_and(kCompute, __all_sync(kFullMask, got));
-            if (!ok) break;
+            ok = __all_sync(kFullMask, got);
             const uint32_t kst = sbase + s * LY::STAGE;
-            // scores: compute warp cw takes keys 8 cw .. 8 cw + 7
-            float wm = -INFINITY, mine = -INFINITY;
+            // scores of this thread's rows: 8 features here, summed over the row's CPR lanes
+            float sj[ROWS_PER_T];
+            bool need = false;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int j = 8 * cw + e;
-                const uint32_t addr = kst + qoff + j * 128 + ((qchunk ^ (j & 7)) * 16) + qbyte;
-                float dot;
-                if constexpr (QPL == 4) {
-                    uint32_t x0, x1;
-                    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(x0), "=r"(x1) : "r"(addr));
-                    dot = qr[0] * __uint_as_float(x0 << 16);
-                    dot = fmaf(qr[1], __uint_as_float(x0 & 0xffff0000u), dot);
-                    dot = fmaf(qr[2], __uint_as_float(x1 << 16), dot);
-                    dot = fmaf(qr[3], __uint_as_float(x1 & 0xffff0000u), dot);
-                } else {
-                    uint32_t x0;
-                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x0) : "r"(addr));
-                    dot = qr[0] * __uint_as_float(x0 << 16);
-                    dot = fmaf(qr[1], __uint_as_float(x0 & 0xffff0000u), dot);
+            for (int r = 0; r < ROWS_PER_T; ++r) {
+                const int j = rg + r * LY::RGRP;
+                float f[8];
+                Vec16<__nv_bfloat16>::unpack(ld_shared_16u(kst + coff + j * 128 + ((cc ^ (j & 7)) * 16)), f);
+                float d0 = qc[0] * f[0], d1 = qc[1] * f[1];
+#pragma unroll
+                for (int e = 2; e < 8; e += 2) {
+                    d0 = fmaf(qc[e], f[e], d0);
+                    d1 = fmaf(qc[e + 1], f[e + 1], d1);
                 }
+                float d = d0 + d1;
 #pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) dot += __shfl_xor_sync(kFullMask, dot, off);
-                const float sj = j < nk ? dot : -INFINITY;
-                wm = fmaxf(wm, sj);
-                if (lane == e) mine = sj;
+                for (int off = 1; off < LY::CPR; off <<= 1) d += __shfl_xor_sync(kFullMask, d, off);
+                sj[r] = j < nk ? d : -INFINITY;
+                need |= sj[r] > m + kRescale;  // true for every live row while m = -inf
             }
-            if (lane < 8) sc[8 * cw + lane] = mine;
-            if (lane == 0) wmax[cw] = wm;
-            named_bar_sync(1, kCompute);
-            float tmax = wmax[0];
+            // one barrier per tile in the common case: it also stops every compute warp at
+            // the same tile when a wait failed
+            if (named_bar_or(kCompute, need || !ok)) {
+                if (!named_bar_and(kCompute, ok)) break;
+                // the tile's max: the first one sets m, a later one rescales what is accumulated
+                float wm = sj[0];
 #pragma unroll
-            for (int w = 1; w < 8; ++w) tmax = fmaxf(tmax, wmax[w]);
-            if (m == -INFINITY) {
-                m = tmax;  // nothing accumulated yet
-            } else if (tmax > m + kRescale) {
-                // uniform: move the max and rescale everything accumulated so far, after
-                // the MMAs of the previous tile have finished
-                const float alpha = fast_exp2(m - tmax);
-                m = tmax;
-                lpart *= alpha;
+                for (int r = 1; r < ROWS_PER_T; ++r) wm = fmaxf(wm, sj[r]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    mk[e] *= alpha;
-                    mv[e] *= alpha;
-                }
-                const bool done = !*abort_flag &&
-                                  mbar_wait(&b_empty[(it - 1) & 1], ((it - 1) >> 1) & 1, &g_lla_err);
-                if (!__all_sync(kFullMask, done)) {
-                    ok = false;  // this warp stops here; the others stop at the next tile
-                    *abort_flag = 1;
-                    continue;
-                }
-                tc::fence_after_sync();
-                const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * D;
+                for (int off = 16; off >= 1; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFullMask, wm, off));
+                if (lane == 0) red[cw] = wm;
+                named_bar_sync(1, kCompute);
+                float tmax = red[0];
+#pragma unroll
+                for (int w = 1; w < kCompute / 32; ++w) tmax = fmaxf(tmax, red[w]);
+                if (m != -INFINITY) {
+                    const float alpha = fast_exp2(m - tmax);
+                    lpart *= alpha;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        mk[e] = __fmul2_rn(mk[e], make_float2(alpha, alpha));
+                        mv[e] = __fmul2_rn(mv[e], make_float2(alpha, alpha));
+                    }
+                    // after the MMAs of the previous tile, rescale the TMEM accumulators
+                    const bool done = !*abort_flag &&
+                                      mbar_wait(&b_empty[(it - 1) & 1], ((it - 1) >> 1) & 1, &g_lla_err);
+                    if (__all_sync(kFullMask, done)) {
+                        tc::fence_after_sync();
+                        const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * D;
 #pragma unroll 1
-                for (int x = 0; x < D / 32; ++x) {
-                    uint32_t u[32];
-                    tc::tmem_ld32(trow + 32 * x, u);
-                    tc::tmem_ld_wait();
+                        for (int x = 0; x < D / 32; ++x) {
+                            uint32_t u[32];
+                            tc::tmem_ld32(trow + 32 * x, u);
+                            tc::tmem_ld_wait();
 #pragma unroll
-                    for (int y = 0; y < 32; ++y) u[y] = __float_as_uint(__uint_as_float(u[y]) * alpha);
-                    tc::tmem_st32(trow + 32 * x, u);
+                            for (int y = 0; y < 32; ++y)
+                                u[y] = __float_as_uint(__uint_as_float(u[y]) * alpha);
+                            tc::tmem_st32(trow + 32 * x, u);
+                        }
+                        tc::tmem_st_wait();
+                        tc::fence_before_sync();
+                    } else {
+                        ok = false;  // every compute warp stops at the next tile's barrier
+                        *abort_flag = 1;
+                    }
                 }
-                tc::tmem_st_wait();
-                tc::fence_before_sync();
+                m = tmax;
+                // red is read by every compute thread before anyone writes it again
+                named_bar_sync(1, kCompute);
             }
+            if (!ok) continue;  // (no barrier is skipped: the next tile's first one stops all)
             // the B operands of this tile go into buffer `buf`, last read by the MMAs of it - 2
             if (it >= 2) {
                 const bool freed = !*abort_flag &&
@@ -366,39 +376,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const uint32_t bb = sbase + LY::B_OFF + buf * LY::BBUF;
+            // p~ x as a bf16 pair: the high part truncated (its bits are the top half of
+            // the fp32 word), the residual x - hi rounded to nearest
+            auto split_store = [&](const float2 (&v)[4], uint32_t dst) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const uint32_t b0 = __float_as_uint(v[h].x) & 0xffff0000u;
+                    const uint32_t b1 = __float_as_uint(v[h].y) & 0xffff0000u;
+                    hi[h] = __byte_perm(b0, b1, 0x7632);
+                    const float2 r = __fadd2_rn(v[h], make_float2(-__uint_as_float(b0), -__uint_as_float(b1)));
+                    lo[h] = pack_bf16_lla(r.x, r.y);
+                }
+                st_shared_16(dst, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_16(dst + LY::TILE, lo[0], lo[1], lo[2], lo[3]);
+            };
+            const bool full = nk == kTile;  // uniform
 #pragma unroll
             for (int r = 0; r < ROWS_PER_T; ++r) {
                 const int j = rg + r * LY::RGRP;
-                const bool live = j < nk;
-                const float p = live ? fast_exp2(sc[j] - m) : 0.f;
-                if (c == 0) lpart += p;
                 const uint32_t off = coff + j * 128 + ((cc ^ (j & 7)) * 16);
+                if (full || j < nk) {
+                    const float p = fast_exp2(sj[r] - m);
+                    if (c == 0) lpart += p;
+                    const float2 p2 = make_float2(p, p);
 #pragma unroll
-                for (int kv = 0; kv < 2; ++kv) {
-                    const uint4 raw = ld_shared_16u(kst + kv * LY::TILE + off);
-                    float f[8];
-                    Vec16<__nv_bfloat16>::unpack(raw, f);
-                    uint32_t hi[4], lo[4];
+                    for (int kv = 0; kv < 2; ++kv) {
+                        float f[8];
+                        Vec16<__nv_bfloat16>::unpack(ld_shared_16u(kst + kv * LY::TILE + off), f);
+                        float2 v[4];
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        // rows past the sequence may hold anything: select, do not multiply
-                        const float v0 = live ? p * f[2 * h] : 0.f;
-                        const float v1 = live ? p * f[2 * h + 1] : 0.f;
-                        if (kv == 0) {
-                            mk[2 * h] += v0;
-                            mk[2 * h + 1] += v1;
-                        } else {
-                            mv[2 * h] += v0;
-                            mv[2 * h + 1] += v1;
+                        for (int h = 0; h < 4; ++h) {
+                            v[h] = __fmul2_rn(p2, make_float2(f[2 * h], f[2 * h + 1]));
+                            if (kv == 0) mk[h] = __fadd2_rn(mk[h], v[h]);
+                            else mv[h] = __fadd2_rn(mv[h], v[h]);
                         }
-                        hi[h] = pack_bf16_lla(v0, v1);
-                        lo[h] = pack_bf16_lla(v0 - __uint_as_float(hi[h] << 16),
-                                              v1 - __uint_as_float(hi[h] & 0xffff0000u));
+                        split_store(v, bb + (2 * kv) * LY::TILE + off);
                     }
-                    st_shared_16(bb + (2 * kv) * LY::TILE + off, hi[0], hi[1], hi[2], hi[3]);
-                    st_shared_16(bb + (2 * kv + 1) * LY::TILE + off, lo[0], lo[1], lo[2], lo[3]);
-                    // the key tile is the A operand: rows past the sequence become zeros
-                    if (kv == 0 && !live) st_shared_16(kst + off, 0u, 0u, 0u, 0u);
+                } else {
+                    // past the sequence (the rows may hold anything): zero B rows, and zero the
+                    // key row, which is also the A operand
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) st_shared_16(bb + x * LY::TILE + off, 0u, 0u, 0u, 0u);
+                    st_shared_16(kst + off, 0u, 0u, 0u, 0u);
                 }
             }
             fence_async_smem();  // visible to the tensor core's reads
@@ -424,9 +444,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* pv = cgv + 4 * D;    // search direction
         float* ap = cgv + 5 * D;    // Sigma p
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            mup[(rg * 2 + 0) * D + 8 * c + e] = mk[e];
-            mup[(rg * 2 + 1) * D + 8 * c + e] = mv[e];
+        for (int e = 0; e < 4; ++e) {
+            mup[(rg * 2 + 0) * D + 8 * c + 2 * e] = mk[e].x;
+            mup[(rg * 2 + 0) * D + 8 * c + 2 * e + 1] = mk[e].y;
+            mup[(rg * 2 + 1) * D + 8 * c + 2 * e] = mv[e].x;
+            mup[(rg * 2 + 1) * D + 8 * c + 2 * e + 1] = mv[e].y;
         }
         named_bar_sync(1, kCompute);
         if (t < 2 * D) {
