@@ -11,7 +11,7 @@
 //
 // lla_kernel: one CTA per (b, h), one pass over the head's keys and values.
 // Warp 0 streams 64-key tiles of K and V by TMA (3-deep ring, 128-byte
-// swizzle); warps 2-9 own one 16-byte chunk (8 features) of every key row they
+// swizzle); warps 2-17 own one 16-byte chunk (8 features) of every key row they
 // touch: they compute the scores (a row's partial dot products summed over the
 // row's lanes), the online-softmax max (moved only when a score exceeds it by
 // more than 2^8; the accumulators are then rescaled), the weights p~_j, the
@@ -23,7 +23,7 @@
 // each product as B (so the products keep ~16 significant bits).  After the
 // stream: Sigma_kk = G_kk / l - mu_k mu_k^T and C = G_kv / l - mu_k mu_v^T go
 // to shared memory, conjugate gradient runs there (matrix-vector products over
-// 256 threads, dot products by group reduction), stopping after `iters` steps or
+// 512 threads, dot products by group reduction), stopping after `iters` steps or
 // at a relative residual of 1e-6, and o = mu_v - C^T rho is formed in fp32.
 #include "tcgen05.cuh"
 #include "kernels.h"
@@ -31,8 +31,9 @@
 namespace parallax {
 namespace {
 
-constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 compute
-constexpr int kCompute = 256;
+constexpr int kThreads = 576;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-17 compute
+constexpr int kCompute = 512;
+constexpr int kComputeWarps = kCompute / 32;
 constexpr int kTile = 64;       // keys per tile
 constexpr int kStages = 3;
 constexpr float kCgTol = 1e-6f;
@@ -56,21 +57,11 @@ __device__ __forceinline__ uint32_t pack_bf16_lla(float lo, float hi) {
     return r;
 }
 
-__device__ __forceinline__ void st_shared_16(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
-                                             uint32_t w) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
-                 "r"(w)
-                 : "memory");
+// Plain 16-byte shared-memory accesses (the compiler may schedule them freely).
+__device__ __forceinline__ void st16(unsigned char* p, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(x, y, z, w);
 }
-
-__device__ __forceinline__ uint4 ld_shared_16u(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
+__device__ __forceinline__ uint4 ld16(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
 
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -105,7 +96,7 @@ __device__ __forceinline__ bool named_bar_or(int nthreads, bool p) {
     return r != 0;
 }
 
-// Sum over the 256 compute threads (named barrier 1); every one gets the result.
+// Sum over the compute threads (named barrier 1); every one gets the result.
 __device__ __forceinline__ float grp_sum(float v, float* red, int cw, int lane) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
@@ -114,7 +105,7 @@ __device__ __forceinline__ float grp_sum(float v, float* red, int cw, int lane) 
     named_bar_sync(1, kCompute);
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kCompute / 32; ++w) s += red[w];
+    for (int w = 0; w < kComputeWarps; ++w) s += red[w];
     return s;
 }
 
@@ -144,8 +135,8 @@ struct LlaLayout {
     static constexpr int CGV_OFF = MUP_OFF + RGRP * 2 * D * 4;  // 6 x [D]
     static constexpr int POST_END = CGV_OFF + 6 * D * 4;
     static constexpr int VEC_OFF = (STREAM_END > POST_END ? STREAM_END : POST_END);
-    // red[8]: reduction scratch
-    static constexpr int BAR_OFF = VEC_OFF + 64;
+    // red[kComputeWarps]: reduction scratch
+    static constexpr int BAR_OFF = VEC_OFF + 4 * kComputeWarps;
     // kv_full[S], kv_empty[S], b_full[2], b_empty[2], acc_full
     static constexpr int NBARS = 2 * kStages + 5;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
@@ -166,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
     uint64_t* kv_full = bars;
     uint64_t* kv_empty = bars + S;
-    uint64_t* b_full = bars + 2 * S;   // [2] 256 arrivals
+    uint64_t* b_full = bars + 2 * S;   // [2] kCompute arrivals
     uint64_t* b_empty = bars + 2 * S + 2;
     uint64_t* acc_full = bars + 2 * S + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
@@ -270,10 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- compute
-        const int t = threadIdx.x - 64;  // 0 .. 255
-        const int cw = warp - 2;          // compute warp 0 .. 7
+        const int t = threadIdx.x - 64;  // 0 .. kCompute - 1
+        const int cw = warp - 2;          // compute warp 0 .. kComputeWarps - 1
         const int q4 = warp & 3;          // TMEM lane quarter
-        const int half = cw >> 2;         // TMEM: G_kk (0) or G_kv (1)
+        const int half = (cw >> 2) & 1;   // TMEM: G_kk (0) or G_kv (1)
+        const int chalf = cw >> 3;        // which half of its D columns
+        constexpr int CW = D / 2;         // columns per warp in TMEM passes
         bool ok = !skip;
         // this thread's 16-byte chunk of every key row (8 features) and its rows of each
         // tile; the CPR threads of a row are consecutive lanes of one warp
@@ -293,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nk = min(kTile, n - it * kTile);
             const bool got = ok && !*abort_flag && mbar_wait(&kv_full[s], (it / S) & 1, &g_lla_err);
             ok = __all_sync(kFullMask, got);
-            const uint32_t kst = sbase + s * LY::STAGE;
+            unsigned char* kst = smem + s * LY::STAGE;
             // scores of this thread's rows: 8 features here, summed over the row's CPR lanes
             float sj[ROWS_PER_T];
             bool need = false;
@@ -301,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int r = 0; r < ROWS_PER_T; ++r) {
                 const int j = rg + r * LY::RGRP;
                 float f[8];
-                Vec16<__nv_bfloat16>::unpack(ld_shared_16u(kst + coff + j * 128 + ((cc ^ (j & 7)) * 16)), f);
+                Vec16<__nv_bfloat16>::unpack(ld16(kst + coff + j * 128 + ((cc ^ (j & 7)) * 16)), f);
                 float d0 = qc[0] * f[0], d1 = qc[1] * f[1];
 #pragma unroll
                 for (int e = 2; e < 8; e += 2) {
@@ -328,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(1, kCompute);
                 float tmax = red[0];
 #pragma unroll
-                for (int w = 1; w < kCompute / 32; ++w) tmax = fmaxf(tmax, red[w]);
+                for (int w = 1; w < kComputeWarps; ++w) tmax = fmaxf(tmax, red[w]);
                 if (m != -INFINITY) {
                     const float alpha = fast_exp2(m - tmax);
                     lpart *= alpha;
@@ -342,9 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       mbar_wait(&b_empty[(it - 1) & 1], ((it - 1) >> 1) & 1, &g_lla_err);
                     if (__all_sync(kFullMask, done)) {
                         tc::fence_after_sync();
-                        const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * D;
+                        const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * D + chalf * CW;
 #pragma unroll 1
-                        for (int x = 0; x < D / 32; ++x) {
+                        for (int x = 0; x < CW / 32; ++x) {
                             uint32_t u[32];
                             tc::tmem_ld32(trow + 32 * x, u);
                             tc::tmem_ld_wait();
@@ -375,10 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
             }
-            const uint32_t bb = sbase + LY::B_OFF + buf * LY::BBUF;
+            unsigned char* bb = smem + LY::B_OFF + buf * LY::BBUF;
             // p~ x as a bf16 pair: the high part truncated (its bits are the top half of
             // the fp32 word), the residual x - hi rounded to nearest
-            auto split_store = [&](const float2 (&v)[4], uint32_t dst) {
+            auto split_store = [&](const float2 (&v)[4], unsigned char* dst) {
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
@@ -388,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float2 r = __fadd2_rn(v[h], make_float2(-__uint_as_float(b0), -__uint_as_float(b1)));
                     lo[h] = pack_bf16_lla(r.x, r.y);
                 }
-                st_shared_16(dst, hi[0], hi[1], hi[2], hi[3]);
-                st_shared_16(dst + LY::TILE, lo[0], lo[1], lo[2], lo[3]);
+                st16(dst, hi[0], hi[1], hi[2], hi[3]);
+                st16(dst + LY::TILE, lo[0], lo[1], lo[2], lo[3]);
             };
             const bool full = nk == kTile;  // uniform
 #pragma unroll
@@ -403,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {
                         float f[8];
-                        Vec16<__nv_bfloat16>::unpack(ld_shared_16u(kst + kv * LY::TILE + off), f);
+                        Vec16<__nv_bfloat16>::unpack(ld16(kst + kv * LY::TILE + off), f);
                         float2 v[4];
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
@@ -417,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // past the sequence (the rows may hold anything): zero B rows, and zero the
                     // key row, which is also the A operand
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) st_shared_16(bb + x * LY::TILE + off, 0u, 0u, 0u, 0u);
-                    st_shared_16(kst + off, 0u, 0u, 0u, 0u);
+                    for (int x = 0; x < 4; ++x) st16(bb + x * LY::TILE + off, 0u, 0u, 0u, 0u);
+                    st16(kst + off, 0u, 0u, 0u, 0u);
                 }
             }
             fence_async_smem();  // visible to the tensor core's reads
@@ -459,14 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(1, kCompute);
         {
-            // Sigma_kk (half 0) or C^T (half 1) from TMEM: lane = feature of k
+            // Sigma_kk (half 0) or C^T (half 1) from TMEM: lane = feature of k; each warp
+            // takes half of the columns
             const int f1 = 32 * q4 + lane;
-            const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * D;
+            const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * D + chalf * CW;
             const bool have = ntiles > 0 && ok;
             if (f1 < D) {
                 const float mk1 = muk[f1];
 #pragma unroll 1
-                for (int x = 0; x < D / 32; ++x) {
+                for (int x = 0; x < CW / 32; ++x) {
                     uint32_t u[32];
                     if (have) {
                         tc::tmem_ld32(trow + 32 * x, u);
@@ -477,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int y = 0; y < 32; ++y) {
-                        const int f2 = 32 * x + y;
+                        const int f2 = chalf * CW + 32 * x + y;
                         const float g = __uint_as_float(u[y]) * inv_l;
                         if (half == 0)
                             sig[f1 * LY::LD + f2] = g - mk1 * muk[f2];
