@@ -119,7 +119,8 @@ struct LlaLayout {
     static constexpr int SUBT = kTile * 128;           // [64 keys x 64 features] bf16, swizzled
     static constexpr int TILE = NCB * SUBT;            // a 64-key tile of K or V
     static constexpr int STAGE = 2 * TILE;             // K, then V
-    static constexpr int B_OFF = kStages * STAGE;      // 2 buffers of {p~K hi, lo, p~V hi, lo}
+    // 2 buffers of {p~K hi, p~V hi, p~K lo, p~V lo}: each half is one N = 2d MN-major operand
+    static constexpr int B_OFF = kStages * STAGE;
     static constexpr int BBUF = 4 * TILE;
     // d = 64: a zero block stands in for features 64..127 of the M = 128 A operand
     static constexpr int ZERO_OFF = B_OFF + 2 * BBUF;
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (!skip) {
-            constexpr uint32_t kIdesc = idesc_mn_mn(128, D);
+            constexpr uint32_t kIdesc = idesc_mn_mn(128, 2 * D);  // [G_kk | G_kv] in one MMA
             bool ok = true;
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int s = t % S, buf = t & 1;
@@ -245,10 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     const uint32_t off = (kk * 16 * 128) >> 4;
                     const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                    tc::mma_ss(tmem, dA + off, dB + off, kIdesc, acc);                       // p~K hi
-                    tc::mma_ss(tmem, dA + off, dB + kTileStep + off, kIdesc, 1u);            // p~K lo
-                    tc::mma_ss(tmem + D, dA + off, dB + 2 * kTileStep + off, kIdesc, acc);  // p~V hi
-                    tc::mma_ss(tmem + D, dA + off, dB + 3 * kTileStep + off, kIdesc, 1u);   // p~V lo
+                    tc::mma_ss(tmem, dA + off, dB + off, kIdesc, acc);                 // high parts
+                    tc::mma_ss(tmem, dA + off, dB + 2 * kTileStep + off, kIdesc, 1u);  // residuals
                 }
                 tc::commit(&b_empty[buf]);
                 tc::commit(&kv_empty[s]);
@@ -289,12 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             unsigned char* kst = smem + s * LY::STAGE;
             // scores of this thread's rows: 8 features here, summed over the row's CPR lanes
             float sj[ROWS_PER_T];
+            uint4 kraw[ROWS_PER_T];  // this thread's key chunks, reused for p~ k
             bool need = false;
 #pragma unroll
             for (int r = 0; r < ROWS_PER_T; ++r) {
                 const int j = rg + r * LY::RGRP;
                 float f[8];
-                Vec16<__nv_bfloat16>::unpack(ld16(kst + coff + j * 128 + ((cc ^ (j & 7)) * 16)), f);
+                kraw[r] = ld16(kst + coff + j * 128 + ((cc ^ (j & 7)) * 16));
+                Vec16<__nv_bfloat16>::unpack(kraw[r], f);
                 float d0 = qc[0] * f[0], d1 = qc[1] * f[1];
 #pragma unroll
                 for (int e = 2; e < 8; e += 2) {
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lo[h] = pack_bf16_lla(r.x, r.y);
                 }
                 st16(dst, hi[0], hi[1], hi[2], hi[3]);
-                st16(dst + LY::TILE, lo[0], lo[1], lo[2], lo[3]);
+                st16(dst + 2 * LY::TILE, lo[0], lo[1], lo[2], lo[3]);
             };
             const bool full = nk == kTile;  // uniform
 #pragma unroll
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {
                         float f[8];
-                        Vec16<__nv_bfloat16>::unpack(ld16(kst + kv * LY::TILE + off), f);
+                        Vec16<__nv_bfloat16>::unpack(kv == 0 ? kraw[r] : ld16(kst + LY::TILE + off), f);
                         float2 v[4];
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (kv == 0) mk[h] = __fadd2_rn(mk[h], v[h]);
                             else mv[h] = __fadd2_rn(mv[h], v[h]);
                         }
-                        split_store(v, bb + (2 * kv) * LY::TILE + off);
+                        split_store(v, bb + kv * LY::TILE + off);
                     }
                 } else {
                     // past the sequence (the rows may hold anything): zero B rows, and zero the
