@@ -370,16 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             unsigned char* bb = smem + LY::B_OFF + buf * LY::BBUF;
-            // p~ x as a bf16 pair: the high part truncated (its bits are the top half of
-            // the fp32 word), the residual x - hi rounded to nearest
+            // p~ x as a bf16 pair: the high part and the residual x - hi, each rounded to
+            // nearest (about 16 significant bits together)
             auto split_store = [&](const float2 (&v)[4], unsigned char* dst) {
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    const uint32_t b0 = __float_as_uint(v[h].x) & 0xffff0000u;
-                    const uint32_t b1 = __float_as_uint(v[h].y) & 0xffff0000u;
-                    hi[h] = __byte_perm(b0, b1, 0x7632);
-                    const float2 r = __fadd2_rn(v[h], make_float2(-__uint_as_float(b0), -__uint_as_float(b1)));
+                    hi[h] = pack_bf16_lla(v[h].x, v[h].y);
+                    const float2 r = __fadd2_rn(v[h], make_float2(-__uint_as_float(hi[h] << 16),
+                                                                  -__uint_as_float(hi[h] & 0xffff0000u)));
                     lo[h] = pack_bf16_lla(r.x, r.y);
                 }
                 st16(dst, hi[0], hi[1], hi[2], hi[3]);
