@@ -21,7 +21,7 @@
 //                   dV += W dO and dK += dS Q + dR rho (A from TMEM);
 //   bwd_q_kernel    per 64-query tile, the forward's stacked layout (TMEM lane
 //                   32g+i: query 16g+i's S row, lane 32g+16+i: its R row): MMAs
-//                   [S; R] = [Q; rho] K^T and [D; D] = [dO; dO] V^T, the compute
+//                   [S; R] = [Q; rho] K^T and D = dO V^T (M = 64: D lands in the S lanes), the compute
 //                   warps form dS, dR, MMA [dQ; drho] += [dS; dR] K.
 // Every contraction is a tcgen05.mma with bf16 operands and fp32 TMEM
 // accumulators; K, V and the query-side tiles arrive by TMA (128-byte swizzle).
@@ -547,7 +547,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 // ------------------------------------------------------------------------ dQ, drho
 // One 64-query tile per CTA (the forward's stacked lane layout), 128-key tiles
 // (K in a 4-deep TMA ring, V in a 2-deep one).  TMEM: Y = [S; R] (128 columns)
-// and [D; D] (128 columns) of the current key tile, the [dQ; drho] accumulator,
+// and D (128 columns, in the query lanes only: an M = 64 MMA) of the current key
+// tile, the [dQ; drho] accumulator,
 // the packed dS/dR operand slot, and the stacked [Q; rho] tile itself (the A
 // operand of [S; R], copied in once, which leaves shared memory to the K ring).
 // The compute warps release Y as soon as they have loaded it, so the MMAs of
@@ -563,8 +564,8 @@ template <int D>
 struct QLayout {
     static constexpr int NCB = D / 64;
     static constexpr int OPB = NCB * SUB;             // [128 x D] operand, also one K or V tile
-    static constexpr int DO_OFF = 0;                  // stacked [dO; dO] (16-row groups)
-    static constexpr int K_OFF = OPB;                 // K ring
+    static constexpr int DO_OFF = 0;                  // dO [64 x D] (the A operand of D, M = 64)
+    static constexpr int K_OFF = NCB * SUB64;         // K ring
     static constexpr int V_OFF = K_OFF + Q_KSTAGES * OPB;  // V ring
     // the stacked [Q; rho] tile lands in the last K stage, on its way to TMEM
     static constexpr int QR_OFF = K_OFF + (Q_KSTAGES - 1) * OPB;
@@ -574,7 +575,7 @@ struct QLayout {
     static constexpr int B_S = 1 + 2 * Q_KSTAGES + 2 * Q_VSTAGES;
     static constexpr int NBARS = B_S + 6;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
-    // TMEM columns: [S; R] at 0, [D; D] at YD, the accumulator at O, the packed slot at PK,
+    // TMEM columns: [S; R] at 0, D at YD, the accumulator at O, the packed slot at PK,
     // [Q; rho] (bf16 pairs) at QA
     static constexpr uint32_t YD = 128, O = 256, PK = 256 + D, QA = 256 + D + 64;
 };
@@ -654,18 +655,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && !skip) {
             bool ok = true;
             int kj = 0, vj = 0;
-            // Q (and rho) once, dO twice: 16-row boxes, NCB * SUB / 2 bytes per tensor copy
-            mbar_arrive_expect_tx(q_full, ((RHO ? 2 : 1) + 2) * LY::NCB * (SUB / 2));
+            // Q (and rho) once in 16-row boxes (the stacked layout), dO once as a 64-row box
+            mbar_arrive_expect_tx(q_full, (RHO ? 2 : 1) * LY::NCB * (SUB / 2) + LY::NCB * SUB64);
             for (int cb = 0; cb < LY::NCB; ++cb) {
                 unsigned char* qr = smem + LY::QR_OFF + cb * SUB;
-                unsigned char* d2 = smem + LY::DO_OFF + cb * SUB;
                 for (int g = 0; g < 4; ++g) {
                     const int row = q0 + 16 * g;
                     tc::tma_load_3d(qr + (32 * g) * 128, &tmQ, cb * 64, row, bh, q_full);
                     if (RHO) tc::tma_load_3d(qr + (32 * g + 16) * 128, &tmR, cb * 64, row, bh, q_full);
-                    tc::tma_load_3d(d2 + (32 * g) * 128, &tmO, cb * 64, row, bh, q_full);
-                    tc::tma_load_3d(d2 + (32 * g + 16) * 128, &tmO, cb * 64, row, bh, q_full);
                 }
+                tc::tma_load_3d(smem + LY::DO_OFF + cb * SUB64, &tmO, cb * 64, q0, bh, q_full);
             }
             for (int j = 0; j < n_t && ok; ++j) {
                 // V first: its slot frees (S|R MMAs of tile j - VS) before K's (dQ of tile j - KS)
@@ -707,6 +706,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- MMA issuer
         if (!skip) {
             constexpr uint32_t kIdesc1 = tc::idesc_bf16_f32(128, Q_KT, false);
+            // M = 64: row r of D lands in TMEM lane 32 (r / 16) + r % 16, the lane of query r's
+            // S row in the stacked layout
+            constexpr uint32_t kIdescD = tc::idesc_bf16_f32(64, Q_KT, false);
             constexpr uint32_t kIdesc2 = tc::idesc_bf16_f32(128, D, true);
             const uint32_t sbase = smem_u32(smem);
             const uint64_t dDO = tc::smem_desc_sw128(sbase + LY::DO_OFF, 16, 1024);
@@ -715,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // MN-major view of a K tile: rows = keys (the K dimension of dQ += dS K)
             const uint64_t mK0 = tc::smem_desc_sw128(sbase + LY::K_OFF, SUB, 1024);
             constexpr uint32_t kStep = LY::OPB >> 4;
-            auto issue_ab = [&](int j) -> bool {  // [S; R] and [D; D] of key tile j into Y
+            auto issue_ab = [&](int j) -> bool {  // [S; R] and D of key tile j into Y
                 const int ks = j % KS, vs = j % VS;
                 if (*abort_flag || !mbar_wait_warp(&k_full[ks], (j / KS) & 1, &g_bwd_err) ||
                     !mbar_wait_warp(&v_full[vs], (j / VS) & 1, &g_bwd_err))
@@ -729,9 +731,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::mma_ts(tmem, tmem + LY::QA + 8 * kk, dK + off, kIdesc1, kk > 0);
                 }
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // [D; D] = [dO; dO] V^T
-                    const uint32_t off = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
-                    tc::mma_ss(tmem + LY::YD, dDO + off, dV + off, kIdesc1, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk) {  // D = dO V^T
+                    const uint32_t offA = ((kk / 4) * SUB64 + (kk % 4) * 32) >> 4;
+                    const uint32_t offB = ((kk / 4) * SUB + (kk % 4) * 32) >> 4;
+                    tc::mma_ss(tmem + LY::YD, dDO + offA, dV + offB, kIdescD, kk > 0);
                 }
                 tc::commit(s_full);
                 tc::commit(&v_empty[vs]);
@@ -918,10 +921,10 @@ cudaError_t set_smem(K kern, int bytes) {
 template <int D, bool CAUSAL, bool RHO>
 cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const void* k,
                        const void* v, cudaStream_t stream) {
-    CUtensorMap q32, r32, k128, v128, o32, q16, r16, o16;
+    CUtensorMap q32, r32, k128, v128, o32, q16, r16;
     if (!make_map(&q32, q, a.BH, a.L, D, 64) || !make_map(&k128, k, a.BH, a.L, D, 128) ||
         !make_map(&v128, v, a.BH, a.L, D, 128) || !make_map(&o32, a.dout, a.BH, a.L, D, 64) ||
-        !make_map(&q16, q, a.BH, a.L, D, 16) || !make_map(&o16, a.dout, a.BH, a.L, D, 16))
+        !make_map(&q16, q, a.BH, a.L, D, 16))
         return cudaErrorInvalidValue;
     if (RHO) {
         if (!make_map(&r32, rho, a.BH, a.L, D, 64) || !make_map(&r16, rho, a.BH, a.L, D, 16))
@@ -942,7 +945,7 @@ cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const v
     bwd_kv_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_kt * a.BH), kKvThreads,
                                     KvLayout<D>::SMEM_BYTES, stream>>>(q32, r32, k128, v128, o32, a);
     bwd_q_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_qt * a.BH), kThreads,
-                                   QLayout<D>::SMEM_BYTES, stream>>>(q16, r16, k128, v128, o16, a);
+                                   QLayout<D>::SMEM_BYTES, stream>>>(q16, r16, k128, v128, o32, a);
     return cudaGetLastError();
 }
 
