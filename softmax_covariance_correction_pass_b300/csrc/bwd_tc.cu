@@ -70,14 +70,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Shared-memory load the compiler may not hoist or merge (keeps the per-query
-// statistics out of registers until the moment they are used).
-__device__ __forceinline__ float lds(const float* p) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(p)));
-    return v;
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -124,7 +116,6 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     }
 }
 
-__device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
 
 // The per-(query, key) gradient terms for two pairs at once (packed fp32x2).  In:
 // the scores s, probe scores r and D = dO.v of the pairs; the rows' statistics
