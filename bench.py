@@ -806,7 +806,7 @@ def run_serving(args):
     ms = timed(lambda: px.parallax_lla_decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens), 5)
     gram = 2.0 * d * d * n * B * H        # p-weighted second moment of the keys
     kv_bytes = 2.0 * B * H * n * d * 2    # K and V, read once
-    rows.append({"case": f"exact LLA decode B={B} H={H} ctx={n} (CG probe + Parallax decode)",
+    rows.append({"case": f"exact LLA decode B={B} H={H} ctx={n} (one pass: second moments, CG probe, output)",
                  "ms": ms, "bound": "hbm", "GB/s": kv_bytes / ms / 1e6,
                  "frac_of_hbm_peak": kv_bytes / ms / 1e6 / peaks["hbm_gbs"],
                  "gram_TFLOP/s": gram / ms / 1e9,
