@@ -156,7 +156,7 @@ parallax::DecodePlan make_plan(int B, int H, int Hkv, int Lmax, int d, int num_s
     plan.scale = 1.0f / std::sqrt((float)d);
     // grouped heads run the tensor-core decode, whose per-key cost is lower and whose
     // per-item merge costs more: half as many items, twice the keys each
-    plan.chunk = plan_chunk(B, Hkv, Lmax, num_sms, H > Hkv ? 8.0 : 16.0);
+    plan.chunk = plan_chunk(B, Hkv, Lmax, num_sms, H >= 8 * Hkv ? 4.0 : H > Hkv ? 8.0 : 16.0);
     if (page_size > 0 && plan.chunk > parallax::decode_paged_max_chunk(page_size)) plan.chunk = 4096;
     plan.nsplit = (Lmax + plan.chunk - 1) / plan.chunk;
     const long long items = (long long)B * Hkv * plan.nsplit;
