@@ -214,3 +214,63 @@ def _chunk(lib, q=FAKE, rho=None, k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, cl=FAKE, o=F
 ])
 def test_chunk_validation(lib, kw, code):
     assert _chunk(lib, **kw) == code
+
+
+def _lla(lib, q=FAKE, k=FAKE, v=FAKE, sl=FAKE, o=FAKE, rho=FAKE, B=1, H=2, Lmax=64, d=128,
+         iters=0):
+    vp = ctypes.c_void_p
+    return lib.parallax_lla_decode(vp(q), vp(k), vp(v), vp(sl), vp(o), vp(rho), B, H, Lmax, d,
+                                   iters, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(sl=0), px.PARALLAX_ERR_INVALID),
+    (dict(rho=0), px.PARALLAX_ERR_INVALID),
+    (dict(iters=-1), px.PARALLAX_ERR_INVALID),
+    (dict(d=96), px.PARALLAX_ERR_UNSUPPORTED),
+    (dict(B=0), px.PARALLAX_ERR_INVALID),
+    (dict(v=FAKE + 4), px.PARALLAX_ERR_INVALID),   # not 16-byte aligned
+])
+def test_lla_validation(lib, kw, code):
+    assert _lla(lib, **kw) == code
+    assert px.last_error() != ""
+
+
+def _train(lib, q=FAKE, rho=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, rbar=FAKE, mu=FAKE, B=1, H=1,
+           L=64, d=64, causal=1, scale=0.125):
+    vp = ctypes.c_void_p
+    return lib.parallax_attn_prefill_train(vp(q), vp(rho), vp(k), vp(v), vp(o), vp(lse), vp(rbar),
+                                           vp(mu), B, H, L, d, causal, ctypes.c_float(scale), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(lse=0), px.PARALLAX_ERR_INVALID),
+    (dict(mu=0), px.PARALLAX_ERR_INVALID),
+    (dict(rbar=FAKE + 4), px.PARALLAX_ERR_INVALID),
+    (dict(causal=2), px.PARALLAX_ERR_INVALID),
+    (dict(scale=float("nan")), px.PARALLAX_ERR_INVALID),
+    (dict(d=48), px.PARALLAX_ERR_UNSUPPORTED),
+])
+def test_prefill_train_validation(lib, kw, code):
+    assert _train(lib, **kw) == code
+
+
+def _bwd(lib, dout=FAKE, dq=FAKE, drho=FAKE, dk=FAKE, dv=FAKE, causal=1, scale=0.125, L=64, d=64):
+    vp = ctypes.c_void_p
+    f = FAKE
+    return lib.parallax_attn_prefill_backward(vp(f), vp(f), vp(f), vp(f), vp(f), vp(f), vp(f),
+                                              vp(f), vp(dout), vp(dq), vp(drho), vp(dk), vp(dv),
+                                              1, 1, L, d, causal, ctypes.c_float(scale), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dout=0), px.PARALLAX_ERR_INVALID),
+    (dict(dk=0), px.PARALLAX_ERR_INVALID),
+    (dict(dv=FAKE + 8), px.PARALLAX_ERR_INVALID),
+    (dict(causal=-1), px.PARALLAX_ERR_INVALID),
+    (dict(scale=float("inf")), px.PARALLAX_ERR_INVALID),
+    (dict(L=0), px.PARALLAX_ERR_INVALID),
+    (dict(d=256), px.PARALLAX_ERR_UNSUPPORTED),
+])
+def test_prefill_backward_validation(lib, kw, code):
+    assert _bwd(lib, **kw) == code
