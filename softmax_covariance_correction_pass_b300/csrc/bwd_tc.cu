@@ -254,13 +254,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
+        // lane 0 streams the query-side tiles, lane 1 the row statistics: each waits only on
+        // its own slots, so a statistics slot still in use never holds up a tile load
         if (lane == 0 && !skip) {
             mbar_arrive_expect_tx(kv_full, 2 * LY::OPB);
             for (int cb = 0; cb < LY::NCB; ++cb) {
                 tc::tma_load_3d(smem + LY::K_OFF + cb * SUB, &tmK, cb * 64, k0, bh, kv_full);
                 tc::tma_load_3d(smem + LY::G_OFF + cb * SUB, &tmV, cb * 64, k0, bh, kv_full);
             }
-            int issued = 0, rs_issued = 0;
+            int issued = 0;
             bool ok = true;
             for (int t = 0; t < n_t; ++t) {
                 const int st = t % S;
@@ -279,6 +281,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                                     &qr_full[st]);
                 }
                 issued = t + 1;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                mbar_wait(kv_full, 0, &g_bwd_err);
+                for (int t = issued >= S ? issued - S : 0; t < issued; ++t)
+                    mbar_wait(&qr_full[t % S], (t / S) & 1, &g_bwd_err);
+            }
+        } else if (lane == 1 && !skip) {
+            int rs_issued = 0;
+            bool ok = true;
+            for (int t = 0; t < n_t; ++t) {
                 // the 64 rows' statistics (one 256-byte copy per array) into slot t % 2, once
                 // the compute warps are done with tile t - 2
                 const int rsl = t & 1;
@@ -286,6 +299,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     ok = false;
                     break;
                 }
+                const int q0 = (qt0 + t) * 64;
                 mbar_arrive_expect_tx(&rs_full[rsl], 4 * 64 * 4);
                 for (int k = 0; k < 4; ++k)
                     bulk_g2s(smem + LY::RS_OFF + rsl * 1024 + k * 256,
@@ -294,9 +308,6 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             }
             if (!ok) {
                 *abort_flag = 1;
-                mbar_wait(kv_full, 0, &g_bwd_err);
-                for (int t = issued >= S ? issued - S : 0; t < issued; ++t)
-                    mbar_wait(&qr_full[t % S], (t / S) & 1, &g_bwd_err);
                 for (int t = rs_issued >= 2 ? rs_issued - 2 : 0; t < rs_issued; ++t)
                     mbar_wait(&rs_full[t & 1], (t >> 1) & 1, &g_bwd_err);
             }
