@@ -57,8 +57,9 @@ def test_train_forward_stats(B, H, L, d, causal, with_rho):
     assert_bf16(mu, rm, "mu_v")
 
 
+# (1, 20, 200, 64): 20 heads = one full CTA-scheduling group of 16 heads plus a partial one
 @pytest.mark.parametrize("B,H,L,d", [(1, 2, 128, 64), (2, 2, 300, 128), (1, 3, 200, 64),
-                                     (1, 1, 1, 128)])
+                                     (1, 1, 1, 128), (1, 20, 200, 64)])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("with_rho", [True, False])
 def test_backward_matches_oracle(B, H, L, d, causal, with_rho):
