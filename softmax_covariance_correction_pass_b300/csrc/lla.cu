@@ -20,7 +20,9 @@
 // issues the tcgen05 MMAs
 //   G_kk += K^T (p~ K),   G_kv += K^T (p~ V)      (fp32 accumulators in TMEM)
 // with the key tile itself as the (MN-major) A operand and the two parts of
-// each product as B (so the products keep ~16 significant bits).  After the
+// each product as B (so the products keep ~16 significant bits); even and odd
+// key tiles accumulate into two TMEM sets (the accumulation error grows with
+// the number of MMAs added into one accumulator).  After the
 // stream: Sigma_kk = G_kk / l - mu_k mu_k^T and C = G_kv / l - mu_k mu_v^T go
 // to shared memory, conjugate gradient runs there (matrix-vector products over
 // 512 threads, dot products by group reduction), stopping after `iters` steps or
@@ -141,7 +143,9 @@ struct LlaLayout {
     // kv_full[S], kv_empty[S], b_full[2], b_empty[2], acc_full
     static constexpr int NBARS = 2 * kStages + 5;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
-    static constexpr uint32_t TMEM_COLS = 2 * D;       // G_kk at 0, G_kv at D
+    // two accumulator sets [G_kk | G_kv] (even / odd key tiles) at 0 and 2D: each takes half
+    // of a head's MMAs, and the two are added at the end
+    static constexpr uint32_t TMEM_COLS = 4 * D;
 };
 
 template <int D>
@@ -245,9 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     const uint32_t off = (kk * 16 * 128) >> 4;
-                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                    tc::mma_ss(tmem, dA + off, dB + off, kIdesc, acc);                 // high parts
-                    tc::mma_ss(tmem, dA + off, dB + 2 * kTileStep + off, kIdesc, 1u);  // residuals
+                    const uint32_t acc = (t > 1 || kk > 0) ? 1u : 0u;
+                    const uint32_t dacc = tmem + (uint32_t)(t & 1) * 2 * D;
+                    tc::mma_ss(dacc, dA + off, dB + off, kIdesc, acc);                 // high parts
+                    tc::mma_ss(dacc, dA + off, dB + 2 * kTileStep + off, kIdesc, 1u);  // residuals
                 }
                 tc::commit(&b_empty[buf]);
                 tc::commit(&kv_empty[s]);
@@ -338,14 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::fence_after_sync();
                         const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + half * D + chalf * CW;
 #pragma unroll 1
-                        for (int x = 0; x < CW / 32; ++x) {
+                        for (int x = 0; x < 2 * (CW / 32); ++x) {  // both accumulator sets
+                            const uint32_t col = (x / (CW / 32)) * 2 * D + 32 * (x % (CW / 32));
                             uint32_t u[32];
-                            tc::tmem_ld32(trow + 32 * x, u);
+                            tc::tmem_ld32(trow + col, u);
                             tc::tmem_ld_wait();
 #pragma unroll
                             for (int y = 0; y < 32; ++y)
                                 u[y] = __float_as_uint(__uint_as_float(u[y]) * alpha);
-                            tc::tmem_st32(trow + 32 * x, u);
+                            tc::tmem_st32(trow + col, u);
                         }
                         tc::tmem_st_wait();
                         tc::fence_before_sync();
@@ -464,6 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t u[32];
                     if (have) {
                         tc::tmem_ld32(trow + 32 * x, u);
+                        if (ntiles > 1) {  // the odd tiles' set
+                            uint32_t u2[32];
+                            tc::tmem_ld32(trow + 2 * D + 32 * x, u2);
+                            tc::tmem_ld_wait();
+#pragma unroll
+                            for (int y = 0; y < 32; ++y)
+                                u[y] = __float_as_uint(__uint_as_float(u[y]) + __uint_as_float(u2[y]));
+                        }
                         tc::tmem_ld_wait();
                     } else {
 #pragma unroll
