@@ -293,14 +293,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             unsigned char* kst = smem + s * LY::STAGE;
             // scores of this thread's rows: 8 features here, summed over the row's CPR lanes
             float sj[ROWS_PER_T];
-            uint4 kraw[ROWS_PER_T];  // this thread's key chunks, reused for p~ k
+            float kf[ROWS_PER_T][8];  // this thread's key chunks as fp32, reused for p~ k
             bool need = false;
 #pragma unroll
             for (int r = 0; r < ROWS_PER_T; ++r) {
                 const int j = rg + r * LY::RGRP;
-                float f[8];
-                kraw[r] = ld16(kst + coff + j * 128 + ((cc ^ (j & 7)) * 16));
-                Vec16<__nv_bfloat16>::unpack(kraw[r], f);
+                float (&f)[8] = kf[r];
+                Vec16<__nv_bfloat16>::unpack(ld16(kst + coff + j * 128 + ((cc ^ (j & 7)) * 16)), f);
                 float d0 = qc[0] * f[0], d1 = qc[1] * f[1];
 #pragma unroll
                 for (int e = 2; e < 8; e += 2) {
@@ -402,7 +401,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {
                         float f[8];
-                        Vec16<__nv_bfloat16>::unpack(kv == 0 ? kraw[r] : ld16(kst + LY::TILE + off), f);
+                        if (kv == 0) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) f[e] = kf[r][e];
+                        } else {
+                            Vec16<__nv_bfloat16>::unpack(ld16(kst + LY::TILE + off), f);
+                        }
                         float2 v[4];
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
