@@ -154,9 +154,12 @@ parallax::DecodePlan make_plan(int B, int H, int Hkv, int Lmax, int d, int num_s
     plan.max_pages = max_pages;
     plan.num_pages = num_pages;
     plan.scale = 1.0f / std::sqrt((float)d);
-    // grouped heads run the tensor-core decode, whose per-key cost is lower and whose
-    // per-item merge costs more: half as many items, twice the keys each
-    plan.chunk = plan_chunk(B, Hkv, Lmax, num_sms, H >= 8 * Hkv ? 4.0 : H > Hkv ? 8.0 : 16.0);
+    // grouped heads run the tensor-core decode, whose per-item merge and combine cost more:
+    // groups of 4 or 8 take the longest chunk that still leaves at least 1.7 items per SM,
+    // groups of 2 about 8 items per SM (chunks capped at 4096 keys in every case, so ragged
+    // lengths keep splitting).  Measured at B=64, H=16, 8192 keys, forced chunks 256..8192:
+    // H_kv = 2 and 4 run fastest at 4096 keys among the chunks this allows, H_kv = 8 at 2048.
+    plan.chunk = plan_chunk(B, Hkv, Lmax, num_sms, H >= 4 * Hkv ? 1.7 : H > Hkv ? 8.0 : 16.0);
     if (page_size > 0 && plan.chunk > parallax::decode_paged_max_chunk(page_size)) plan.chunk = 4096;
     plan.nsplit = (Lmax + plan.chunk - 1) / plan.chunk;
     const long long items = (long long)B * Hkv * plan.nsplit;
