@@ -262,11 +262,28 @@ int parallax_attn_qkvr_projection(const void* x, const void* w, void* q, void* k
 
 /*
  * Keys per split-KV chunk that parallax_attn_decode{,_f32} would use for this
- * shape (elem_bytes = 2 for bf16, 4 for fp32); with shared key/value heads
- * pass H = H_kv.  Returns a negative
+ * shape (elem_bytes = 2 for bf16, 4 for fp32; one query head per key/value
+ * head).  Returns a negative
  * parallax_status for invalid arguments.  A result >= Lmax means no split.
  */
 int parallax_attn_decode_chunk_keys(int B, int H, int Lmax, int d, int elem_bytes);
+
+/*
+ * Keys per work item that parallax_attn_decode, parallax_attn_decode_gqa
+ * (page_size = 0) or parallax_attn_decode_paged (page_size > 0, Lmax =
+ * page_size * max_pages) would use for this shape.  The plan depends on the
+ * group size H / H_kv: one query head per key/value head aims at about 16
+ * items per SM, groups of 2 at about 8, groups of 4 and 8 take the longest
+ * chunk that leaves at least 1.7 items per SM; chunks are 256..4096 keys, and
+ * grouped heads on a paged cache take at most 2048.  A forced chunk
+ * (parallax_attn_set_decode_chunk_keys) takes precedence.  Host-only: no
+ * device work; without a device the SM count is taken as 148.
+ * Errors: PARALLAX_ERR_INVALID for B, H, Lmax < 1, H not a multiple of H_kv
+ * or page_size < 0; PARALLAX_ERR_UNSUPPORTED for d not 64 or 128, group sizes
+ * other than 1, 2, 4, 8, or page_size not a multiple of 16.
+ * A result >= Lmax means no split.
+ */
+int parallax_attn_decode_plan_keys(int B, int H, int H_kv, int Lmax, int d, int page_size);
 
 /*
  * Force the decode chunk size (keys, a positive multiple of 256) for later

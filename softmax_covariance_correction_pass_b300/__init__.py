@@ -63,6 +63,7 @@ def load_library() -> ctypes.CDLL:
     lib.parallax_attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                i32, i32, i32, vp]
     lib.parallax_attn_decode_chunk_keys.argtypes = [i32, i32, i32, i32, i32]
+    lib.parallax_attn_decode_plan_keys.argtypes = [i32] * 6
     lib.parallax_attn_qkvr_projection.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                   vp]
     lib.parallax_attn_set_decode_chunk_keys.argtypes = [i32]
@@ -75,6 +76,7 @@ def load_library() -> ctypes.CDLL:
                  "parallax_attn_prefill_train", "parallax_attn_prefill_backward",
                  "parallax_lla_decode",
                  "parallax_attn_decode_f32", "parallax_attn_decode_chunk_keys",
+                 "parallax_attn_decode_plan_keys",
                  "parallax_attn_set_decode_chunk_keys", "parallax_attn_release_workspace",
                  "parallax_check_device_error", "parallax_version"):
         getattr(lib, name).restype = ctypes.c_int
@@ -351,6 +353,15 @@ def parallax_attn_qkvr_projection(x, w, H: int, d: int, q=None, k=None, v=None, 
 
 def parallax_attn_decode_chunk_keys(B: int, H: int, Lmax: int, d: int, elem_bytes: int) -> int:
     rc = load_library().parallax_attn_decode_chunk_keys(B, H, Lmax, d, elem_bytes)
+    if rc < 0:
+        raise ParallaxError(rc, last_error())
+    return rc
+
+
+def parallax_attn_decode_plan_keys(B: int, H: int, H_kv: int, Lmax: int, d: int,
+                                   page_size: int = 0) -> int:
+    """Keys per work item of the decode plan (plain, grouped-query or paged decode)."""
+    rc = load_library().parallax_attn_decode_plan_keys(B, H, H_kv, Lmax, d, page_size)
     if rc < 0:
         raise ParallaxError(rc, last_error())
     return rc

@@ -464,6 +464,24 @@ int parallax_attn_decode_chunk_keys(int B, int H, int Lmax, int d, int elem_byte
     return plan_chunk(B, H, Lmax, num_sms);
 }
 
+int parallax_attn_decode_plan_keys(int B, int H, int H_kv, int Lmax, int d, int page_size) {
+    if (B <= 0 || H <= 0 || Lmax <= 0)
+        return fail(PARALLAX_ERR_INVALID, "B, H, Lmax must be >= 1");
+    if (d != 64 && d != 128) return fail(PARALLAX_ERR_UNSUPPORTED, "d=%d", d);
+    int rc = validate_groups(H, H_kv);
+    if (rc != PARALLAX_OK) return rc;
+    if (page_size < 0) return fail(PARALLAX_ERR_INVALID, "page_size=%d must be >= 0", page_size);
+    if (page_size % 16 != 0)
+        return fail(PARALLAX_ERR_UNSUPPORTED, "page_size=%d must be a multiple of 16", page_size);
+    int num_sms = 148;
+    if (DeviceState* ds = device_state(nullptr)) num_sms = ds->num_sms;
+    const int max_pages = page_size > 0 ? (Lmax + page_size - 1) / page_size : 0;
+    const parallax::DecodePlan plan =
+        make_plan(B, H, H_kv, Lmax, d, num_sms, page_size, max_pages, page_size > 0 ? 1 : 0);
+    succeed();
+    return plan.chunk;
+}
+
 int parallax_attn_set_decode_chunk_keys(int keys) {
     if (keys < 0 || keys % 256 != 0)
         return fail(PARALLAX_ERR_INVALID, "chunk keys %d must be 0 or a positive multiple of 256",

@@ -123,6 +123,52 @@ def test_chunk_plan(lib):
         f(1, 16, 128, 128, 3)
 
 
+def test_decode_plan_by_group_size(lib):
+    """The plan of the plain, grouped-query and paged decode (host logic, 148 SMs without a
+    device): plain decode aims at ~16 items per SM, groups of 2 at ~8, groups of 4 and 8 take
+    the longest chunk leaving >= 1.7 items per SM, grouped heads on a paged cache stop at 2048
+    keys; chunks stay within 256..4096 keys or cover the whole cache."""
+    f = px.parallax_attn_decode_plan_keys
+    sms = 148
+    # one query head per key/value head: the same plan as parallax_attn_decode_chunk_keys
+    for B, H, L in ((64, 16, 8192), (1, 16, 32768), (512, 16, 16384), (2048, 16, 1024)):
+        assert f(B, H, H, L, 128) == px.parallax_attn_decode_chunk_keys(B, H, L, 128, 2)
+    # B=64, H=16, 8192 keys: H_kv = 8 / 4 / 2 (groups of 2 / 4 / 8)
+    assert f(64, 16, 8, 8192, 128) == 2048
+    assert f(64, 16, 4, 8192, 128) == 4096
+    assert f(64, 16, 2, 8192, 128) == 4096
+    assert f(8, 16, 2, 8192, 128) == 512
+    for B in (1, 4, 8, 16, 32, 64, 128):
+        for Hkv in (4, 2):
+            c = f(B, 16, Hkv, 8192, 128)
+            items = B * Hkv * -(-8192 // c)
+            assert 256 <= c <= 4096
+            # the longest chunk that keeps >= 1.7 items per SM (or the shortest chunk)
+            assert items >= 1.7 * sms or c == 256
+            assert c == 4096 or B * Hkv * -(-8192 // (2 * c)) < 1.7 * sms
+    # paged: grouped heads at most 2048 keys per item, one head per group as contiguous
+    assert f(512, 16, 4, 16384, 128, 256) == 2048
+    assert f(512, 16, 16, 16384, 128, 256) == f(512, 16, 16, 16384, 128, 0) == 4096
+    assert f(1, 16, 2, 300, 128, 16) == 256
+    # a forced chunk wins, also over the paged cap
+    px.parallax_attn_set_decode_chunk_keys(4096)
+    try:
+        assert f(512, 16, 4, 16384, 128, 256) == 4096
+        assert f(64, 16, 2, 8192, 64) == 4096
+        assert f(1, 16, 2, 1000, 128) == 1000  # >= Lmax: no split
+    finally:
+        px.parallax_attn_set_decode_chunk_keys(0)
+    for args, code in (((0, 16, 2, 128, 128), px.PARALLAX_ERR_INVALID),
+                       ((1, 16, 3, 128, 128), px.PARALLAX_ERR_INVALID),
+                       ((1, 16, 1, 128, 128), px.PARALLAX_ERR_UNSUPPORTED),   # groups of 16
+                       ((1, 16, 2, 128, 96), px.PARALLAX_ERR_UNSUPPORTED),
+                       ((1, 16, 2, 128, 128, 20), px.PARALLAX_ERR_UNSUPPORTED),
+                       ((1, 16, 2, 128, 128, -16), px.PARALLAX_ERR_INVALID)):
+        with pytest.raises(px.ParallaxError) as ei:
+            f(*args)
+        assert ei.value.code == code, args
+
+
 def test_forced_chunk_validation(lib):
     with pytest.raises(px.ParallaxError):
         px.parallax_attn_set_decode_chunk_keys(100)
