@@ -915,11 +915,6 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int L, int D, int box_ro
     return make_tmap_bf16(m, base, 3, dims, strides, box);
 }
 
-template <typename K>
-cudaError_t set_smem(K kern, int bytes) {
-    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
-
 template <int D, bool CAUSAL, bool RHO>
 cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const void* k,
                        const void* v, cudaStream_t stream) {
@@ -935,13 +930,12 @@ cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const v
         r32 = q32;
         r16 = q16;
     }
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = set_smem(bwd_kv_kernel<D, CAUSAL, RHO>, KvLayout<D>::SMEM_BYTES);
-        if (e == cudaSuccess) e = set_smem(bwd_q_kernel<D, CAUSAL, RHO>, QLayout<D>::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> kv_smem_set{0}, q_smem_set{0};
+    cudaError_t e = ensure_dynamic_smem(bwd_kv_kernel<D, CAUSAL, RHO>, KvLayout<D>::SMEM_BYTES,
+                                        kv_smem_set);
+    if (e == cudaSuccess)
+        e = ensure_dynamic_smem(bwd_q_kernel<D, CAUSAL, RHO>, QLayout<D>::SMEM_BYTES, q_smem_set);
+    if (e != cudaSuccess) return e;
     const size_t rows = (size_t)a.BH * a.Lp;
     bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
     bwd_kv_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_kt * a.BH), kKvThreads,

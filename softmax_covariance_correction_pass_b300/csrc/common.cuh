@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/parallax_attn.h"
 
 namespace parallax {
@@ -18,6 +20,26 @@ constexpr unsigned kFullMask = 0xffffffffu;
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+
+// ----------------------------------------------------------------------------
+// host: per-device one-time kernel set-up
+// ----------------------------------------------------------------------------
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device, once per
+// device: the attribute is held by each device's context, so a process that launches on
+// several devices sets it on each.  `done` is the kernel's own mask of devices already set
+// (devices 0..63; a later device sets it on every launch).  Threads racing on a first
+// launch may both set it, which is harmless.
+template <typename Kernel>
+inline cudaError_t ensure_dynamic_smem(Kernel kern, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // ----------------------------------------------------------------------------
 // error word: one per translation unit, read and cleared by the host

@@ -637,13 +637,8 @@ template <int D, bool RHO, bool SPLIT, int G, bool PAGED>
 cudaError_t launch_decode_mma_kernel(const DecodeArgs& a, int grid, cudaStream_t stream) {
     using MS = MmaShape<D>;
     auto kern = decode_mma_kernel<D, RHO, SPLIT, G, PAGED>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)MS::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = ensure_dynamic_smem(kern, (int)MS::SMEM_BYTES, smem_set)) return e;
     // the caches as [rows, D] bf16 tensors: (b, h_kv, key) -> row (b*H_kv + h_kv)*Lmax + key,
     // or, paged, (page, h_kv, row) -> (page*H_kv + h_kv)*page_size + row
     const uint64_t rows = PAGED ? (uint64_t)a.num_pages * a.Hkv * a.page_size
@@ -663,13 +658,8 @@ template <typename T, int D, bool RHO, bool SPLIT, int G, bool PAGED>
 cudaError_t launch_decode_kernel(const DecodeArgs& a, int grid, cudaStream_t stream) {
     using SH = DecodeShape<T, D, G>;
     auto kern = decode_kernel<T, D, RHO, SPLIT, G, PAGED>;
-    static bool configured = false;  // per process; the attribute is per function
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SH::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = ensure_dynamic_smem(kern, (int)SH::SMEM_BYTES, smem_set)) return e;
     kern<<<grid, kThreads, SH::SMEM_BYTES, stream>>>(a);
     return cudaGetLastError();
 }

@@ -562,13 +562,9 @@ cudaError_t launch(const LlaArgs& a, const void* kc, const void* vc, int BH, cud
     if (!make_tmap_bf16(&mk, kc, 3, dims, strides, box) ||
         !make_tmap_bf16(&mv, vc, 3, dims, strides, box))
         return cudaErrorInvalidValue;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(
-            lla_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LlaLayout<D>::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = ensure_dynamic_smem(lla_kernel<D>, (int)LlaLayout<D>::SMEM_BYTES, smem_set))
+        return e;
     lla_kernel<D><<<BH, kThreads, LlaLayout<D>::SMEM_BYTES, stream>>>(mk, mv, a);
     return cudaGetLastError();
 }

@@ -705,13 +705,8 @@ cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mr, const CUtensorM
                    const CUtensorMap& mv, const TcArgs& a, cudaStream_t stream) {
     using LY = PairLayout<D, RHO>;
     auto kern = prefill_pair_kernel<D, CAUSAL, RHO>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             LY::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = ensure_dynamic_smem(kern, (int)LY::SMEM_BYTES, smem_set)) return e;
     const unsigned grid = (unsigned)((size_t)a.n_qb * a.BH);
     kern<<<grid, kThreads, LY::SMEM_BYTES, stream>>>(mq, mr, mk, mv, a);
     return cudaGetLastError();

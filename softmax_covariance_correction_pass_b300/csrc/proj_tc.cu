@@ -240,13 +240,8 @@ cudaError_t launch(const CUtensorMap& mx, const CUtensorMap& mw, const ProjArgs&
                    cudaStream_t stream) {
     using LY = ProjLayout<BN>;
     auto kern = proj_kernel<BN, D>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             LY::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = ensure_dynamic_smem(kern, (int)LY::SMEM_BYTES, smem_set)) return e;
     const int grid = a.n_tiles < num_sms ? a.n_tiles : num_sms;
     kern<<<grid, kThreads, LY::SMEM_BYTES, stream>>>(mx, mw, a);
     return cudaGetLastError();
