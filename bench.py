@@ -215,6 +215,11 @@ def cpu_oracle_decode_sample(inp, target_s: float, max_batches: int = 64):
 
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
+    """The oracle timed on the host cores, on the same step as the CUDA arm: per step a bounded
+    sample of the decode workload (the H heads of one sequence) and of the layer-shaped causal
+    prefill (query rows of one head spread over the causal range), both with the explicit d x d
+    covariance in fp64.  `value` is the decode part's KV-stream GB/s, as in the CUDA arm; the
+    prefill part's TFLOP/s (8 d flop per visible (query, key) pair) is reported beside it."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
@@ -226,40 +231,66 @@ def run_reference(args):
 
     c = configs.DECODE_UNIFORM
     B, H, d, n = c["B"], c["H"], c["d"], c["ctx"]
-    # the same seeded workload, drawn on the host
+    # the same seeded recipes, drawn on the host
     inp = configs.decode_inputs(B, H, d, n, n, c["seed"], c["rho_std"], device="cpu")
     q = inp.q.double().numpy()
     rho = inp.rho.double().numpy()
-    # per step: one sequence (H heads) of the workload, cycling through the batch;
-    # keep the whole run to about two minutes
+    pc = configs.LAYER_PREFILL
+    pin = configs.layer_prefill_inputs(device="cpu", B=1)
+    PH, PL, Pd = pc["H"], pc["L"], pc["d"]
+    pq, pr = pin.q[0].double().numpy(), pin.rho[0].double().numpy()
+    pk, pv = pin.k[0].double().numpy(), pin.v[0].double().numpy()
+    # about two minutes for the whole run, half for each part
+    budget = 60.0 / max(1, args.steps + args.warmup)
     t0 = time.perf_counter()
     oracle.decode(q[:1], rho[:1], inp.k_cache[:1].double().numpy(),
                   inp.v_cache[:1].double().numpy(), inp.seqlens[:1].numpy(), form="explicit")
     t_one = time.perf_counter() - t0
-    heads_per_step = H
-    budget = 120.0 / max(1, args.steps + args.warmup)
     keys = n if t_one <= budget else max(256, int(n * budget / t_one) // 256 * 256)
     kh = [inp.k_cache[b:b + 1, :, :keys].double().numpy() for b in range(min(B, 8))]
     vh = [inp.v_cache[b:b + 1, :, :keys].double().numpy() for b in range(min(B, 8))]
     sl = np.full(1, keys, dtype=np.int32)
-    times = []
+
+    def prefill_rows(step, R):
+        h = step % PH
+        idx = (np.arange(R, dtype=np.int64) * PL // R + 7 * step) % PL
+        return h, idx
+
+    h, idx = prefill_rows(0, 16)
+    t0 = time.perf_counter()
+    oracle.rows(pq[h, idx], pr[h, idx], pk[h], pv[h], idx + 1, pin.scale, form="explicit")
+    t16 = time.perf_counter() - t0
+    R = int(min(1024, max(8, 16 * budget / max(t16, 1e-4))) // 8 * 8)
+
+    dec_t, pre_t, pre_flops = [], [], 0.0
     for s in range(args.warmup + args.steps):
         b = s % len(kh)
         t0 = time.perf_counter()
         oracle.decode(q[b:b + 1], rho[b:b + 1], kh[b], vh[b], sl, form="explicit")
+        t1 = time.perf_counter()
+        h, idx = prefill_rows(s, R)
+        oracle.rows(pq[h, idx], pr[h, idx], pk[h], pv[h], idx + 1, pin.scale, form="explicit")
+        t2 = time.perf_counter()
         if s >= args.warmup:
-            times.append(time.perf_counter() - t0)
+            dec_t.append(t1 - t0)
+            pre_t.append(t2 - t1)
+            pre_flops += 8.0 * Pd * float((idx + 1).sum())
     _, per_step = decode_bytes(1, H, keys, d)
-    total_t = sum(times)
-    value = per_step * len(times) / total_t / 1e9
-    sample = (f"per step {heads_per_step} heads x {keys} keys of the B=64 H=16 d=128 ctx=8192 "
-              "decode workload (explicit covariance, fp64)")
+    value = per_step * len(dec_t) / sum(dec_t) / 1e9
+    pre_tflops = pre_flops / sum(pre_t) / 1e12
+    sample = (f"per step: decode {H} heads x {keys} keys of one sequence of the B={B} decode "
+              f"workload; prefill {R} query rows (keys 0..row) of one head of a B=1 draw of the "
+              f"layer-shaped causal prefill; explicit d x d covariance, fp64")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * total_t / len(times), "higher_is_better": True,
+        "ms_per_step": 1e3 * (sum(dec_t) + sum(pre_t)) / len(dec_t), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": configs.DECODE_UNIFORM["name"], "sample": sample},
+        "config": {"workload": c["name"] + " + " + pc["name"], "sample": sample},
+        "decode": {"metric": "decode KV-stream GB/s", "value": value, "unit": "GB/s",
+                   "ms_per_call": 1e3 * sum(dec_t) / len(dec_t)},
+        "prefill": {"metric": "causal prefill TFLOP/s", "value": pre_tflops, "unit": "TFLOP/s",
+                    "rows_per_step": R, "ms_per_step": 1e3 * sum(pre_t) / len(pre_t)},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -267,6 +298,7 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
 
 def time_projection(args, dev, peaks, max_over_ranks, n_rep=20):
     """The layer-shaped projection x [B, L, 2048] -> q, k, v, rho [B, H, L, d] (one tcgen05

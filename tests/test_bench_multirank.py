@@ -74,3 +74,32 @@ def test_reference_arm_other_ranks_exit_without_work():
                        text=True, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""  # only rank 0 prints the line
+
+
+def test_reference_arm_line_on_rank0():
+    """Rank 0 of the reference arm times the oracle on the host cores on the CUDA arm's
+    workload (decode + layer-shaped prefill) and prints one JSON line with the same metric,
+    unit and workload name as the CUDA arm."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from softmax_covariance_correction_pass_b300 import configs
+
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "1"], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference"
+    assert j["metric"] == bench.METRIC and j["unit"] == "GB/s" and j["higher_is_better"] is True
+    assert j["config"]["workload"] == (configs.DECODE_UNIFORM["name"] + " + "
+                                       + configs.LAYER_PREFILL["name"])
+    assert j["steps"] == 2 and j["warmup"] == 1 and j["value"] > 0
+    assert j["decode"]["value"] == j["value"] and j["prefill"]["value"] > 0
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["value"] == j["value"]
+    assert j["cpu_baseline"]["cores"] >= 1
+    assert j["e2e"] == {"value": j["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert j["gpu_launches"] == 0
