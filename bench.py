@@ -537,6 +537,29 @@ def run_ours(args):
         torch.cuda.synchronize()
         f0[name] = units / (a.elapsed_time(b) / 20 * 1e-3)
 
+    # ---- torch's scaled_dot_product_attention (a library kernel, not this path) on the same
+    # decode and prefill tensors, softmax attention only, for context beside the W_R = 0 paths
+    sdpa = {}
+    if not args.only:
+        try:
+            attn = torch.nn.functional.scaled_dot_product_attention
+            qd = dinp.q.unsqueeze(2)
+            for name, fn, units in (
+                    ("decode_gbs", lambda: attn(qd, dinp.k_cache, dinp.v_cache), dec_bytes / 1e9),
+                    ("prefill_tflops_softmax_only", lambda: attn(
+                        pinp.q, pinp.k, pinp.v, is_causal=True, scale=pinp.scale),
+                     pre_flops / 2 / 1e12)):
+                fn()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(20):
+                    fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                sdpa[name] = units / (a.elapsed_time(b) / 20 * 1e-3)
+        except Exception as e:  # context only: never fail the bench on it
+            sdpa = {"error": f"{type(e).__name__}: {e}"[:300]}
+
     # ---- q/k/v/probe projection of the layer-shaped workload (one tcgen05 GEMM), timed alone
     proj = None
     if not args.only and not args.no_projection:
@@ -632,6 +655,7 @@ def run_ours(args):
                 "metric": "decode KV-stream GB/s", "value": value, "unit": "GB/s",
                 "frac_of_peak": roof_dec["frac"], "ms_per_call": dec_ms},
             "w_r_zero_fast_path": f0,
+            "torch_sdpa_w_r_zero": sdpa,
             "roofline_projection": proj,
             "roofline_backward": bwd,
             "e2e": e2e,
