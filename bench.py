@@ -45,6 +45,13 @@ TRAFFIC_BYTES = {
     "projection": 177.38e6 + 497.77e6,
     "backward": None,
 }
+# The backward call is three kernels; the ncu capture (B=2, profiles/) measured the two
+# tensor-core kernels, scaled here by 4 to the B=8 launch (work and traffic grow with the
+# heads).  bwd_pre_kernel's traffic was not captured, so the call's total stays None above.
+TRAFFIC_BACKWARD_KERNELS = {
+    "bwd_kv_kernel": 4 * (178.9e6 + 89.4e6),
+    "bwd_q_kernel": 4 * (171.3e6 + 94.4e6),
+}
 
 
 def parse_args(argv=None):
@@ -382,6 +389,7 @@ def time_backward(args, dev, peaks, max_over_ranks, n_rep=10):
     tf = flops / (ms * 1e-3) / 1e12
     return {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": tf / peaks["bf16_tflops"], "traffic": TRAFFIC_BYTES.get("backward"),
+            "traffic_by_kernel": TRAFFIC_BACKWARD_KERNELS,
             "kernel": "bwd_pre_kernel + bwd_kv_kernel + bwd_q_kernel",
             "algorithmic_flops_per_launch": flops, "avg_launch_ms": ms, "launches": n_rep,
             "shape": f"causal prefill backward B={B} H={H} L={L} d={d}, bf16 in, fp32 grads",
