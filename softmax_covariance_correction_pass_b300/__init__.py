@@ -2,8 +2,10 @@
 
 Thin ctypes binding over ``libparallax_attn.so`` (C ABI declared in
 ``include/parallax_attn.h``).  This module only marshals arguments: every step
-of the computation runs in the library's CUDA kernels.  There is no CPU path;
-if the library is missing the import of the binding fails loudly.
+of the computation runs in the library's CUDA kernels.  There is no CPU path:
+the library is loaded on the first call (so that the build step can import this
+package before the library exists), and if it is missing that call raises
+ImportError.
 
 Functions carry the C names (``parallax_attn_prefill``, ...), with short
 aliases ``prefill`` / ``decode``.

@@ -320,3 +320,19 @@ def _bwd(lib, dout=FAKE, dq=FAKE, drho=FAKE, dk=FAKE, dv=FAKE, causal=1, scale=0
 ])
 def test_prefill_backward_validation(lib, kw, code):
     assert _bwd(lib, **kw) == code
+
+
+def test_no_cpu_path(lib, monkeypatch, tmp_path):
+    """Nothing computes on the CPU: host tensors are refused, and without the CUDA library
+    every call raises."""
+    import torch
+
+    x = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        px.parallax_attn_prefill(x, None, x, x)
+    monkeypatch.setattr(px, "LIB_PATH", str(tmp_path / "libparallax_attn.so"))
+    monkeypatch.setattr(px, "_lib", None)
+    with pytest.raises(ImportError, match="no CPU fallback"):
+        px.parallax_attn_decode_plan_keys(1, 1, 1, 128, 64)
+    with pytest.raises(ImportError):
+        px.parallax_version()
