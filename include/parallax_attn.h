@@ -25,6 +25,10 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     never frees or retains them.  Every tensor is dense row-major.
  *   - Every pointer must be 16-byte aligned.
+ *   - Every pointer and `stream` belong to the calling thread's current CUDA
+ *     device (cudaSetDevice): the library launches there and keeps its
+ *     workspaces per device.  The library does not check where a pointer lives;
+ *     the Python binding refuses tensors on another device.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream) and never
  *     synchronise, except parallax_check_device_error().
  *   - Return value: PARALLAX_OK or a negative parallax_status.  Argument errors

@@ -102,12 +102,23 @@ def _ptr(t):
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
+    elif isinstance(getattr(stream, "device", None), torch.device):
+        dev = torch.cuda.current_device()
+        if stream.device.index != dev:
+            raise ValueError(f"stream belongs to {stream.device}, but the library launches on "
+                             f"the current device cuda:{dev}")
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
 def _need(t, name, dtype, shape):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    dev = torch.cuda.current_device()
+    if t.get_device() != dev:
+        # the library launches on the current device; a pointer into another device's
+        # memory would be dereferenced there
+        raise ValueError(f"{name} is on cuda:{t.get_device()}, but the library launches on the "
+                         f"current device cuda:{dev} (use torch.cuda.device(...))")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):

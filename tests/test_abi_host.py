@@ -336,3 +336,36 @@ def test_no_cpu_path(lib, monkeypatch, tmp_path):
         px.parallax_attn_decode_plan_keys(1, 1, 1, 128, 64)
     with pytest.raises(ImportError):
         px.parallax_version()
+
+
+def test_binding_refuses_tensors_on_another_device(monkeypatch):
+    """The library launches on the current device; the binding refuses a tensor or a stream of
+    another device (emulated on the CPU: a tensor subclass that reports a CUDA device)."""
+    import torch
+
+    class FakeCuda(torch.Tensor):
+        @property
+        def is_cuda(self):
+            return True
+
+        def get_device(self):
+            return self.fake_index
+
+    def on(index):
+        t = torch.zeros(2, 3).as_subclass(FakeCuda)
+        t.fake_index = index
+        return t
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    px._need(on(0), "q", torch.float32, (2, 3))          # the current device: accepted
+    with pytest.raises(ValueError, match="cuda:1.*current device cuda:0"):
+        px._need(on(1), "q", torch.float32, (2, 3))
+
+    class FakeStream:
+        device = torch.device("cuda", 1)
+        cuda_stream = 0
+
+    with pytest.raises(ValueError, match="stream belongs to cuda:1"):
+        px._stream(FakeStream())
+    FakeStream.device = torch.device("cuda", 0)
+    assert px._stream(FakeStream()).value is None        # the null stream handle
