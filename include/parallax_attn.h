@@ -172,8 +172,9 @@ int parallax_attn_decode_f32(const void* q, const void* rho, const void* k_cache
  *   k_cache, v_cache  : bf16 [B, H_kv, Lmax, d]   query head h reads head h / (H / H_kv)
  *   seqlens, o        : as in parallax_attn_decode
  * H / H_kv must be 1, 2, 4 or 8 (PARALLAX_ERR_UNSUPPORTED otherwise); each key
- * and value row is read from HBM once for the whole group.  Workspace, split
- * plan (keyed on B, H_kv, Lmax) and concurrency rules of parallax_attn_decode.
+ * and value row is read from HBM once for the whole group.  Workspace and
+ * concurrency rules of parallax_attn_decode; the split plan depends on the group
+ * size (parallax_attn_decode_plan_keys).
  * The Parallax pages do not discuss head sharing; the result is, per query
  * head, exactly parallax_attn_decode against that head's key/value head.
  */
