@@ -8,7 +8,6 @@ Covered: split-KV decode (bf16 and fp32, automatic plan and forced 256-key chunk
 grouped-query decode on the warp-level MMA kernel, paged decode (SIMT and MMA
 kernels), exact LLA decode.  Tolerances as in the parity tests of each path.
 """
-import numpy as np
 import pytest
 import torch
 

@@ -1,6 +1,4 @@
 """Prefill parity: the CUDA path (through the C ABI) against the fp64 oracle."""
-import math
-
 import numpy as np
 import pytest
 import torch
