@@ -103,3 +103,30 @@ def test_reference_arm_line_on_rank0():
     assert j["e2e"] == {"value": j["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert j["gpu_launches"] == 0
+
+
+def test_clock_sampler_summary():
+    """The clock record that decides whether a timed run stands: median SM clock under load,
+    the maximum clock, and every throttle reason seen Active (nvidia-smi csv, no units)."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    s = bench.ClockSampler("0")
+    s.out = "\n".join([
+        "0, 1920, 2032, 150.2, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2032, 540.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1935, 2032, 610.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1950, 2032, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active",  # skipped
+        "garbage line",
+    ])
+    r = s.summary()
+    assert r["samples"] == 3
+    assert r["sm_mhz"] == 1957.5             # median of the two samples above 250 W
+    assert r["sm_max_mhz"] == 2032.0
+    assert r["reasons"] == ["sw_power_cap"]
+    assert r["power_w_max"] == 610.5
+    s.out = "0, 1200, 2032, 500, 0x8, Active, Not Active, Active, Not Active"
+    assert s.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    s.out = ""
+    assert s.summary(max_mhz_hint=2032) == {"sm_mhz": None, "sm_max_mhz": 2032, "reasons": [],
+                                            "samples": 0}
