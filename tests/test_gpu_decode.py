@@ -133,15 +133,35 @@ def test_uniform_workload_full_size():
     assert_bf16(o0, sdpa, "rho=NULL vs sdpa")
 
 
-@pytest.mark.parametrize("B,L", [(1, 32768), (8, 8192), (2048, 128), (64, 1024)])
+def _sweep_params():
+    """Every cell of the decode sweep (batch x context, caches up to 64e9 bytes), plus the
+    (256, 32768) cell whose cache is exactly 64 GiB, flagged by its id."""
+    cells = configs.decode_sweep_cells()
+    out = [pytest.param(B, L, id=f"B{B}-L{L}") for B, L in cells]
+    out += [pytest.param(B, L, id=f"B{B}-L{L}-64GiB-boundary")
+            for B, L in configs.decode_sweep_cells(include_boundary=True) if (B, L) not in cells]
+    return out
+
+
+@pytest.mark.parametrize("B,L", _sweep_params())
 def test_sweep_cells_full_size(B, L):
+    """One sweep cell at full size through the launch configuration the plan picks for it:
+    the first and last head of the first and last sequence plus random heads (32 in all,
+    fewer when the cell has fewer) against the oracle."""
     inp = configs.decode_sweep_inputs(B, L, DEV)
     o = _run(inp)
+    assert torch.isfinite(o).all()
     rng = np.random.default_rng(B + L)
-    n = min(32, B * 16)
-    heads = [(int(rng.integers(B)), int(rng.integers(16))) for _ in range(n)]
+    heads = list(dict.fromkeys([(0, 0), (0, 15), (B - 1, 0), (B - 1, 15)]))
+    while len(heads) < min(32, B * 16):
+        bh = (int(rng.integers(B)), int(rng.integers(16)))
+        if bh not in heads:
+            heads.append(bh)
     got = np.stack([o[b, h].double().cpu().numpy() for b, h in heads])
-    assert_bf16(got, _ref_heads(inp, heads), f"sweep cell B={B} L={L}")
+    rel, mx = assert_bf16(got, _ref_heads(inp, heads), f"sweep cell B={B} L={L}")
+    print(f"sweep cell B={B} L={L}: rel-L2 {rel:.3e} max-abs {mx:.3e} over {len(heads)} heads")
+    del inp, o
+    torch.cuda.empty_cache()
 
 
 def test_ragged_workload_full_size():

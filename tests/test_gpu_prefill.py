@@ -132,6 +132,29 @@ def test_layer_prefill_full_size_sampled():
     print(f"layer prefill sampled rows: rel-L2 {rel:.3e} max-abs {mx:.3e} over {len(got)} rows")
 
 
+def test_layer_prefill_full_size_whole_heads():
+    """Full layer shape: eight whole heads -- (0, 0) and one random head of every other
+    sequence, all 4096 rows of each -- against the oracle's contracted form (the same
+    function as the explicit covariance form, pinned to it on the CPU), so the max-abs
+    bound is checked on every row of those heads, not on a sample."""
+    inp = configs.layer_prefill_inputs(DEV)
+    o = _run(inp)
+    B, H, L, d = inp.q.shape
+    rng = np.random.default_rng(55)
+    heads = [(0, 0)] + [(b, int(rng.integers(H))) for b in range(1, B)]
+    got, want = [], []
+    for b, h in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.prefill(inp.q[sl], inp.rho[sl], inp.k[sl], inp.v[sl], causal=True,
+                             scale=inp.scale, form="contracted")
+        got.append(o[sl].double().cpu().numpy())
+        want.append(ref)
+        rel_h, mx_h = errors(got[-1], ref)
+        print(f"layer prefill head ({b},{h}): rel-L2 {rel_h:.3e} max-abs {mx_h:.3e}")
+    rel, mx = assert_bf16(np.concatenate(got), np.concatenate(want), "layer prefill whole heads")
+    print(f"layer prefill whole heads: rel-L2 {rel:.3e} max-abs {mx:.3e} over {len(heads) * L} rows")
+
+
 def test_layer_prefill_full_size_properties():
     """Whole-tensor checks at full size: every element written and finite, and the
     rho = NULL path equals torch's SDPA on the same bf16 tensors."""
