@@ -30,27 +30,83 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode KV-stream GB/s (% B300 HBM peak); causal prefill TFLOP/s (% TC peak)"
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# bench-size launch, from the ncu captures summarised in profiles/ (taken on
-# smaller cases and scaled by the units processed; see those files).  None when
-# the kernel has changed since its counters were taken.
-TRAFFIC_BYTES = {
-    # B=8 capture: 536.97 MB read (x8 at B=64) + 4.8 MB of partials and o at B=64
-    "decode": 8 * 536.97e6 + 4.8e6,
-    # B=2 capture: 135.47 MB read (x4 at B=8) + the 268.4 MB fp32 output written
-    "prefill": 4 * 135.47e6 + 268.4e6,
-    # full-size capture: 177.38 MB read + 497.77 MB written (the rest of the 536.9 MB
-    # output was still in L2 when the kernel ended)
-    "projection": 177.38e6 + 497.77e6,
-    "backward": None,
-}
-# The backward call is three kernels; the ncu capture (B=2, profiles/) measured the two
-# tensor-core kernels, scaled here by 4 to the B=8 launch (work and traffic grow with the
-# heads).  bwd_pre_kernel's traffic was not captured, so the call's total stays None above.
-TRAFFIC_BACKWARD_KERNELS = {
-    "bwd_kv_kernel": 4 * (178.9e6 + 89.4e6),
-    "bwd_q_kernel": 4 * (171.3e6 + 94.4e6),
-}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) comes from the ncu
+# captures listed in profiles/dram_traffic.md, one table row per kernel: the captured case, its
+# bytes, the factor that scales it to the bench's launch (units processed), and a hash of the
+# kernel's source file and the csrc headers it includes at capture time.  A figure whose hash no
+# longer matches the source is reported as null: the kernel has changed since the counters were
+# taken.
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+CSRC = os.path.join(ROOT, "softmax_covariance_correction_pass_b300", "csrc")
+
+
+def source_hash(cu_name: str) -> str:
+    """sha256 (first 16 hex digits) of csrc/<cu_name> followed by the csrc headers (.cuh) it
+    includes, transitively, in include order."""
+    import hashlib
+    import re
+
+    seen, order = set(), []
+
+    def walk(name):
+        if name in seen:
+            return
+        seen.add(name)
+        order.append(name)
+        with open(os.path.join(CSRC, name), "rb") as f:
+            text = f.read().decode()
+        for inc in re.findall(r'#include\s+"([^"/]+\.cuh)"', text):
+            walk(inc)
+
+    walk(cu_name)
+    h = hashlib.sha256()
+    for name in order:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(path: str = TRAFFIC_TABLE) -> dict:
+    """kernel -> {"bytes": scaled read+write bytes per bench launch or None, ...} from the
+    table in profiles/dram_traffic.md (rows whose first cell is a kernel name)."""
+    out = {}
+    try:
+        with open(path) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return out
+    for line in lines:
+        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+        if len(cells) < 7 or not cells[0].endswith("_kernel"):
+            continue
+        try:
+            kernel, src, case = cells[0], cells[1], cells[2]
+            rd, wr, scale = float(cells[3]), float(cells[4]), float(cells[5])
+            sha = cells[6]
+        except ValueError:
+            continue
+        try:
+            fresh = source_hash(src) == sha
+        except OSError:
+            fresh = False
+        out[kernel] = {"bytes": (rd + wr) * scale if fresh else None,
+                       "captured": case, "scale": scale, "source": src,
+                       "note": "profiles/dram_traffic.md" if fresh else
+                       f"stale: {src} changed since the capture (profiles/dram_traffic.md)"}
+    return out
+
+
+def traffic_of(table: dict, *kernels: str):
+    """Summed traffic of the kernels of one call, or None if any of them has no fresh figure."""
+    vals = [table.get(k, {}).get("bytes") for k in kernels]
+    return None if any(v is None for v in vals) else sum(vals)
+
+
+def traffic_notes(table: dict, *kernels: str) -> dict:
+    return {k: table.get(k, {"note": "not captured"}) for k in kernels}
+
+
+TRAFFIC = load_traffic()
 
 
 def parse_args(argv=None):
@@ -340,7 +396,8 @@ def time_projection(args, dev, peaks, max_over_ranks, n_rep=20):
     proj_tf = proj_flops / (proj_ms * 1e-3) / 1e12
     return {"bound": "tensor", "achieved": proj_tf, "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s", "frac": proj_tf / peaks["bf16_tflops"],
-            "traffic": TRAFFIC_BYTES.get("projection"), "kernel": "proj_kernel",
+            "traffic": traffic_of(TRAFFIC, "proj_kernel"),
+            "traffic_source": traffic_notes(TRAFFIC, "proj_kernel"), "kernel": "proj_kernel",
             "algorithmic_flops_per_launch": proj_flops, "avg_launch_ms": proj_ms,
             "launches": n_rep,
             "shape": f"x [{PB},{PL},{width}] x W^T [{width},{4 * PH * Pd}] -> q,k,v,rho "
@@ -387,8 +444,10 @@ def time_backward(args, dev, peaks, max_over_ranks, n_rep=10):
         raise RuntimeError("device error in the backward pass")
     tf = flops / (ms * 1e-3) / 1e12
     return {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": tf / peaks["bf16_tflops"], "traffic": TRAFFIC_BYTES.get("backward"),
-            "traffic_by_kernel": TRAFFIC_BACKWARD_KERNELS,
+            "frac": tf / peaks["bf16_tflops"],
+            "traffic": traffic_of(TRAFFIC, "bwd_pre_kernel", "bwd_kv_kernel", "bwd_q_kernel"),
+            "traffic_source": traffic_notes(TRAFFIC, "bwd_pre_kernel", "bwd_kv_kernel",
+                                            "bwd_q_kernel"),
             "kernel": "bwd_pre_kernel + bwd_kv_kernel + bwd_q_kernel",
             "algorithmic_flops_per_launch": flops, "avg_launch_ms": ms, "launches": n_rep,
             "shape": f"causal prefill backward B={B} H={H} L={L} d={d}, bf16 in, fp32 grads",
@@ -509,17 +568,23 @@ def run_ours(args):
     value = whole_job_rate(ws, dec_bytes, dec_ms) / 1e9  # all replicas' bytes / slowest time
 
     roof_dec = {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": dec_gbs / peaks["hbm_gbs"], "traffic": TRAFFIC_BYTES["decode"],
+                "frac": dec_gbs / peaks["hbm_gbs"],
+                "traffic": traffic_of(TRAFFIC, "decode_kernel", "combine_kernel"),
+                "traffic_source": traffic_notes(TRAFFIC, "decode_kernel", "combine_kernel"),
                 "kernel": "decode_kernel (+ combine_kernel)",
                 "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_ms,
                 "peak_source": peaks["source"]}
-    roof_pre = {"bound": "tensor", "achieved": pre_tflops, "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": pre_tflops / peaks["bf16_tflops_sustained"],
-                "traffic": TRAFFIC_BYTES["prefill"], "kernel": "prefill_pair_kernel",
+    # the prefill launches take about a millisecond each inside a timed region of tens of
+    # milliseconds: the burst peak is the denominator (the sustained one is reported beside it)
+    roof_pre = {"bound": "tensor", "achieved": pre_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": pre_tflops / peaks["bf16_tflops"],
+                "traffic": traffic_of(TRAFFIC, "prefill_pair_kernel"),
+                "traffic_source": traffic_notes(TRAFFIC, "prefill_pair_kernel"),
+                "kernel": "prefill_pair_kernel",
                 "algorithmic_flops_per_launch": pre_flops, "avg_launch_ms": pre_ms,
-                "peak_burst": peaks["bf16_tflops"],
-                "frac_burst": pre_tflops / peaks["bf16_tflops"],
-                "peak_source": peaks["source"] + " (sustained)"}
+                "peak_sustained": peaks["bf16_tflops_sustained"],
+                "frac_sustained": pre_tflops / peaks["bf16_tflops_sustained"],
+                "peak_source": peaks["source"] + " (burst)"}
     if not run_decode:
         roof_dec = None
     if not run_prefill:
