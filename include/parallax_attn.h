@@ -63,6 +63,8 @@ typedef enum {
                                                   [0, num_pages); page 0 was read */
 #define PARALLAX_DEVERR_SMEM_MISALIGNED 0x8u /* a kernel's dynamic shared memory was not
                                                 1024-byte aligned; it did no work (bug) */
+#define PARALLAX_DEVERR_BOUNDS 0x10u /* debug builds only: a global write or copy would have
+                                        left its tensor; it was skipped or redirected (bug) */
 
 /*
  * Causal or full prefill, bf16 inputs, fp32 output.
@@ -126,8 +128,8 @@ int parallax_attn_prefill_train(const void* q, const void* rho, const void* k, c
  *   dq, drho, dk, dv  : fp32 [B, H, L, d], written in full (drho unused if rho == NULL)
  * The contractions run on the tcgen05 tensor cores with bf16 operands (p-weighted
  * terms rounded to bf16) and fp32 accumulation.  Uses a library-owned per-device
- * workspace of 16 B per query row (grown on demand with cudaMalloc, which
- * synchronises the device; same concurrency rules as the decode workspace).
+ * workspace of 16 B per query row, grown in stream order like the decode
+ * workspace (same concurrency rules).
  */
 int parallax_attn_prefill_backward(const void* q, const void* rho, const void* k, const void* v,
                                    const float* o, const float* mu_v, const float* lse,
@@ -152,9 +154,13 @@ int parallax_attn_prefill_f32(const void* q, const void* rho, const void* k, con
  * Long caches are split into fixed-size key chunks processed in parallel
  * (split-KV); the per-chunk partial states are merged by a log-sum-exp combine
  * kernel.  The partials live in a library-owned device workspace, one per
- * device, grown on demand (cudaMalloc; growing synchronises the device).  The
- * workspace is shared by all calls on a device: calls issued concurrently from
- * several host threads, or on several streams that may overlap, race on it.
+ * device, grown on demand in stream order: a call that needs more space frees
+ * the old buffer with cudaFreeAsync and allocates the new one with
+ * cudaMallocAsync on `stream`, after making `stream` wait for the last call
+ * that used the old buffer (whatever its stream), so growing never
+ * synchronises the device.  The workspace is shared by all calls on a device:
+ * calls issued concurrently from several host threads, or on several streams
+ * that may overlap, race on its contents.
  */
 int parallax_attn_decode(const void* q, const void* rho, const void* k_cache,
                          const void* v_cache, const int32_t* seqlens, void* o, int B, int H,
@@ -300,7 +306,10 @@ int parallax_attn_set_decode_chunk_keys(int keys);
 /* Bytes currently held by the calling device's decode workspace. */
 size_t parallax_attn_workspace_bytes(void);
 
-/* Free the calling device's decode and backward workspaces (synchronises the device). */
+/*
+ * Free the calling device's decode and backward workspaces.  Synchronises the
+ * device first, so no call in flight still uses them.
+ */
 int parallax_attn_release_workspace(void);
 
 /*
@@ -312,13 +321,55 @@ const char* parallax_last_error(void);
 /*
  * Synchronise `stream`, then read and clear the device error word of the
  * current device.  Returns PARALLAX_OK if it was zero, PARALLAX_ERR_DEVICE if
- * not (the bits, PARALLAX_DEVERR_*, are stored to *bits when bits != NULL), or
- * PARALLAX_ERR_CUDA if the synchronisation failed.
+ * not, or PARALLAX_ERR_CUDA if the synchronisation failed.  The bits that were
+ * set (PARALLAX_DEVERR_*) stay available on the calling host thread through
+ * parallax_last_device_error_bits() until its next check.
  */
-int parallax_check_device_error(cudaStream_t stream, unsigned int* bits);
+int parallax_check_device_error(cudaStream_t stream);
+
+/*
+ * PARALLAX_DEVERR_* bits read by the calling thread's last
+ * parallax_check_device_error() (0 if none were set, or if that check failed
+ * before reading them).  Host-only.
+ */
+unsigned int parallax_last_device_error_bits(void);
+
+/*
+ * Overrun check of the library-owned workspaces (decode split-KV partials,
+ * backward row statistics) of the current device.  Each workspace sits between
+ * two 4 KB guard bands filled with 0xA5 when it is allocated; this call
+ * synchronises the device and returns 1 if every band of every workspace still
+ * holds that pattern, 0 if one was overwritten, or a negative parallax_status.
+ * A debugging and test aid; it copies 8 KB per workspace to the host.
+ */
+int parallax_workspace_guards_intact(void);
+
+/*
+ * Test hook for the failure path of the bounded pipeline waits.  Every wait in
+ * the library's kernels gives up after a time limit instead of spinning forever;
+ * it then raises PARALLAX_DEVERR_WAIT_TIMEOUT in its kernel family's device
+ * error word, and CTAs launched later in that family see the bit and return
+ * without work until parallax_check_device_error() clears it.  This call launches
+ * one thread that waits, with a limit of limit_us microseconds (1 .. 1000000), on
+ * an mbarrier nothing arrives on, in the error word of `family`:
+ *   PARALLAX_SELFTEST_DECODE  (0): the decode kernels (plain, grouped, paged)
+ *   PARALLAX_SELFTEST_PREFILL (1): the tensor-core prefill kernels
+ * Nothing faults and nothing hangs: the kernel ends after about limit_us.
+ * Asynchronous on `stream`; read the result with parallax_check_device_error().
+ */
+#define PARALLAX_SELFTEST_DECODE 0
+#define PARALLAX_SELFTEST_PREFILL 1
+int parallax_selftest_wait_timeout(int family, unsigned int limit_us, cudaStream_t stream);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int parallax_version(void);
+
+/*
+ * 1 if this library was built with device-side bounds checks (the debug build,
+ * libparallax_attn_debug.so: a global write or copy that would leave its tensor is
+ * skipped or redirected and raises PARALLAX_DEVERR_BOUNDS), 0 for the release build.
+ */
+int parallax_debug_checks(void);
 
 #ifdef __cplusplus
 }

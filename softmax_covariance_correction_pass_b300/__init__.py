@@ -19,7 +19,10 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libparallax_attn.so")
+# PARALLAX_LIBRARY=debug selects the build with device-side bounds checks
+# (`python -m softmax_covariance_correction_pass_b300.build --debug`)
+LIB_PATH = os.path.join(_HERE, "libparallax_attn_debug.so"
+                        if os.environ.get("PARALLAX_LIBRARY") == "debug" else "libparallax_attn.so")
 
 PARALLAX_OK = 0
 PARALLAX_ERR_INVALID = -1
@@ -30,6 +33,7 @@ DEVERR_SEQLEN_CLAMPED = 0x1
 DEVERR_WAIT_TIMEOUT = 0x2
 DEVERR_PAGE_OUT_OF_RANGE = 0x4
 DEVERR_SMEM_MISALIGNED = 0x8
+DEVERR_BOUNDS = 0x10
 
 _lib = None
 
@@ -48,7 +52,8 @@ def load_library() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is missing: build it with "
-            "`python -m softmax_covariance_correction_pass_b300.build` (no CPU fallback exists)")
+            "`python -m softmax_covariance_correction_pass_b300.build` (add --debug for the "
+            "checked build; no CPU fallback exists)")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.parallax_attn_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
@@ -71,7 +76,11 @@ def load_library() -> ctypes.CDLL:
     lib.parallax_attn_set_decode_chunk_keys.argtypes = [i32]
     lib.parallax_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.parallax_last_error.restype = ctypes.c_char_p
-    lib.parallax_check_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.parallax_check_device_error.argtypes = [vp]
+    lib.parallax_last_device_error_bits.argtypes = []
+    lib.parallax_last_device_error_bits.restype = ctypes.c_uint
+    lib.parallax_selftest_wait_timeout.argtypes = [i32, ctypes.c_uint, vp]
+    lib.parallax_workspace_guards_intact.argtypes = []
     for name in ("parallax_attn_prefill", "parallax_attn_prefill_f32", "parallax_attn_decode",
                  "parallax_attn_qkvr_projection", "parallax_attn_decode_gqa",
                  "parallax_attn_decode_paged", "parallax_attn_prefill_chunk",
@@ -80,7 +89,9 @@ def load_library() -> ctypes.CDLL:
                  "parallax_attn_decode_f32", "parallax_attn_decode_chunk_keys",
                  "parallax_attn_decode_plan_keys",
                  "parallax_attn_set_decode_chunk_keys", "parallax_attn_release_workspace",
-                 "parallax_check_device_error", "parallax_version"):
+                 "parallax_check_device_error", "parallax_version",
+                 "parallax_selftest_wait_timeout", "parallax_workspace_guards_intact",
+                 "parallax_debug_checks"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -394,15 +405,41 @@ def parallax_attn_release_workspace() -> None:
 
 def parallax_check_device_error(stream=None) -> int:
     """Synchronise ``stream`` and return (and clear) the device error bits (0 = none)."""
-    bits = ctypes.c_uint(0)
-    rc = load_library().parallax_check_device_error(_stream(stream), ctypes.byref(bits))
+    lib = load_library()
+    rc = lib.parallax_check_device_error(_stream(stream))
     if rc not in (PARALLAX_OK, PARALLAX_ERR_DEVICE):
         raise ParallaxError(rc, last_error())
-    return int(bits.value)
+    return int(lib.parallax_last_device_error_bits())
+
+
+def parallax_workspace_guards_intact() -> bool:
+    """Synchronise the device and report whether the guard bands around the library's own
+    workspaces are intact (no kernel wrote past either end of its workspace)."""
+    rc = load_library().parallax_workspace_guards_intact()
+    if rc < 0:
+        raise ParallaxError(rc, last_error())
+    return rc == 1
+
+
+SELFTEST_DECODE = 0
+SELFTEST_PREFILL = 1
+
+
+def parallax_selftest_wait_timeout(family: int, limit_us: int, stream=None) -> None:
+    """Launch one thread that waits, with a limit of ``limit_us`` microseconds, on a barrier
+    nothing arrives on, in the error word of ``family`` (SELFTEST_DECODE or
+    SELFTEST_PREFILL); the wait gives up and raises DEVERR_WAIT_TIMEOUT there."""
+    _check(load_library().parallax_selftest_wait_timeout(int(family), int(limit_us),
+                                                          _stream(stream)))
 
 
 def parallax_version() -> int:
     return int(load_library().parallax_version())
+
+
+def parallax_debug_checks() -> bool:
+    """True if the loaded library is the build with device-side bounds checks."""
+    return bool(load_library().parallax_debug_checks())
 
 
 prefill = parallax_attn_prefill

@@ -1,12 +1,18 @@
 """Build libparallax_attn.so in-tree with nvcc for sm_103a.
 
-    python -m softmax_covariance_correction_pass_b300.build [--force] [--verbose]
+    python -m softmax_covariance_correction_pass_b300.build [--force] [--verbose] [--debug]
 
 Each ``csrc/*.cu`` is compiled to an object in ``_build/`` (in parallel), then
 linked into ``softmax_covariance_correction_pass_b300/libparallax_attn.so``
 with the CUDA runtime linked statically, so the library loads without a GPU
 and without a CUDA runtime on the loader path.  ``-Xptxas -v`` output (registers,
 spills, shared memory per kernel) is kept in ``_build/ptxas.log``.
+
+``--debug`` builds ``libparallax_attn_debug.so`` instead (objects in ``_build/debug``)
+with ``-DPARALLAX_DEBUG_CHECKS``: every global write and bulk copy the kernels guard is
+checked against the extent of its tensor on the device, and a failed check raises
+PARALLAX_DEVERR_BOUNDS in the device error word instead of touching memory outside the
+tensor.  The binding loads it when ``PARALLAX_LIBRARY=debug`` is set.
 """
 from __future__ import annotations
 
@@ -24,6 +30,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libparallax_attn.so")
+DEBUG_LIB = os.path.join(PKG, "libparallax_attn_debug.so")
+DEBUG_FLAGS = ["-DPARALLAX_DEBUG_CHECKS"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
@@ -46,16 +54,16 @@ def _deps():
         os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def _compile(src: str) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, build_dir: str, extra: tuple = ()) -> tuple[str, str]:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -92,34 +100,39 @@ def check_registers(log: str) -> None:
                                f"the register hand-over needs exactly {want}")
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    lib = DEBUG_LIB if debug else LIB
+    if not force and up_to_date(lib):
+        return lib
+    build_dir = os.path.join(BUILD, "debug") if debug else BUILD
+    extra = tuple(DEBUG_FLAGS) if debug else ()
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        results = list(ex.map(_compile, srcs))
+        results = list(ex.map(lambda p: _compile(p, build_dir, extra), srcs))
     log = "\n".join(r[1] for r in results)
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+    with open(os.path.join(build_dir, "ptxas.log"), "w") as f:
         f.write(log)
     check_registers(log)
     if verbose:
         print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[r[0] for r in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
+    ap.add_argument("--debug", action="store_true",
+                    help="build libparallax_attn_debug.so with device-side bounds checks")
     args = ap.parse_args(argv)
-    print(build(force=args.force, verbose=args.verbose))
+    print(build(force=args.force, verbose=args.verbose, debug=args.debug))
     return 0
 
 

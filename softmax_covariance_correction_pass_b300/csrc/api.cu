@@ -16,6 +16,7 @@
 namespace {
 
 thread_local std::string t_last_error;
+thread_local unsigned t_last_bits = 0;  // device error bits of this thread's last check
 
 int fail(int code, const char* fmt, ...) {
     char buf[512];
@@ -40,16 +41,37 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 std::atomic<int> g_chunk_override{0};
 
+// A library-owned device buffer, grown in stream order.  `last_use` is recorded on the
+// stream of every launch that reads or writes the buffer, so that a later call that grows
+// it (on any stream) frees the old buffer only after that launch.  The usable bytes
+// [ptr, ptr + bytes) sit between two guard bands of kGuardBytes filled with kGuardFill,
+// which parallax_workspace_guards_intact() checks (a kernel that overran its workspace
+// would have changed them).
+constexpr size_t kGuardBytes = 4096;
+constexpr unsigned char kGuardFill = 0xA5;
+
+struct Workspace {
+    void* ptr = nullptr;  // usable region (base + kGuardBytes)
+    size_t bytes = 0;
+    cudaEvent_t last_use = nullptr;
+    bool used = false;  // last_use has been recorded since the buffer was allocated
+    unsigned char* base() const { return static_cast<unsigned char*>(ptr) - kGuardBytes; }
+};
+
 struct DeviceState {
-    void* ws = nullptr;  // decode split-KV partials
-    size_t ws_bytes = 0;
-    void* bws = nullptr;  // prefill backward row statistics
-    size_t bws_bytes = 0;
+    Workspace ws;   // decode split-KV partials
+    Workspace bws;  // prefill backward row statistics
     int num_sms = 0;
 };
 
-// Grow a per-device buffer to `need` bytes (cudaMalloc; growing synchronises the device).
-int grow(void*& buf, size_t& have, size_t need, const char* what);
+// Make `w` at least `need` bytes for a launch on `stream`: the old buffer is freed with
+// cudaFreeAsync on `stream` after `stream` has waited for the buffer's last use, and the new
+// one comes from cudaMallocAsync on `stream`; nothing synchronises the device.  Call with
+// g_mu held, and keep holding it until the launch that uses the buffer is recorded.
+int grow(Workspace& w, size_t need, cudaStream_t stream, const char* what);
+// Record the launch just issued on `stream` as the buffer's last use (g_mu held).  A call
+// captured into a CUDA graph is not recorded: its launches run when the graph does.
+int mark_used(Workspace& w, cudaStream_t stream, const char* what);
 std::mutex g_mu;
 std::vector<DeviceState> g_dev;
 
@@ -69,11 +91,10 @@ DeviceState* device_state(int* dev_out) {
     return &s;
 }
 
-// Keys per split-KV chunk.  Aim for about 16 work items per SM so the
-// persistent CTAs balance well (also for ragged lengths), with chunks of
-// 256..4096 keys: long enough that the 1 KB partial state per chunk is noise
-// next to the chunk's K/V bytes.
-int plan_chunk(int B, int H, int Lmax, int num_sms, double items_per_sm = 16.0) {
+// Keys per split-KV chunk for grouped heads: about `items_per_sm` work items per SM, with
+// chunks of 256..4096 keys (long enough that the 1 KB partial state per chunk is noise next
+// to the chunk's K/V bytes).
+int plan_chunk(int B, int H, int Lmax, int num_sms, double items_per_sm) {
     const int forced = g_chunk_override.load();
     int c;
     if (forced > 0) {
@@ -86,21 +107,82 @@ int plan_chunk(int B, int H, int Lmax, int num_sms, double items_per_sm = 16.0) 
     return c >= Lmax ? Lmax : c;
 }
 
-int grow(void*& buf, size_t& have, size_t need, const char* what) {
-    if (have >= need) return PARALLAX_OK;
-    if (buf) {
-        cudaError_t e = cudaFree(buf);  // synchronises the device
-        buf = nullptr;
-        have = 0;
+// One query head per key/value head: the longest chunk (256..4096 keys, powers of two) that
+// still leaves about one work item per resident CTA (at least 85% of them).  Every item ends
+// with a merge of its warps' states, and every split adds partial states for the combine
+// kernel, so few long items beat many short ones as long as the CTAs stay busy; heads of at
+// most 1024 keys are not split at all (their stream is shorter than a second launch costs).
+// Measured at H=16, d=128 over chunks 256..4096: B=1 with 32768 keys runs best at 2048-key
+// items (256 items), B=8 with 8192 keys at 4096 (256 items), B=1 with 8192 keys at 512-1024,
+// B=8 with 1024 keys unsplit.  The 4096-key cap keeps ragged batches splitting.
+int plan_chunk_single(int B, int H, int Lmax, int ctas) {
+    const int forced = g_chunk_override.load();
+    if (forced > 0) return forced >= Lmax ? Lmax : forced;
+    if (Lmax <= 1024) return Lmax;
+    const long long heads = (long long)B * H;
+    const double target = 0.85 * ctas;
+    int c = 4096;
+    while (c > 256 && (double)heads * ((Lmax + c - 1) / c) < target) c /= 2;
+    return c >= Lmax ? Lmax : c;
+}
+
+int grow(Workspace& w, size_t need, cudaStream_t stream, const char* what) {
+    if (w.bytes >= need) return PARALLAX_OK;
+    cudaError_t e;
+    if (!w.last_use) {
+        e = cudaEventCreateWithFlags(&w.last_use, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            w.last_use = nullptr;
+            return cuda_fail(e, what);
+        }
+    }
+    if (w.ptr) {
+        if (w.used) {
+            e = cudaStreamWaitEvent(stream, w.last_use, 0);
+            if (e != cudaSuccess) return cuda_fail(e, what);
+        }
+        e = cudaFreeAsync(w.base(), stream);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        w.used = false;
         if (e != cudaSuccess) return cuda_fail(e, what);
     }
-    cudaError_t e = cudaMalloc(&buf, need);
+    void* base = nullptr;
+    e = cudaMallocAsync(&base, need + 2 * kGuardBytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    unsigned char* b = static_cast<unsigned char*>(base);
+    e = cudaMemsetAsync(b, kGuardFill, kGuardBytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(b + kGuardBytes + need, kGuardFill, kGuardBytes, stream);
     if (e != cudaSuccess) {
-        buf = nullptr;
+        cudaFreeAsync(base, stream);
         return cuda_fail(e, what);
     }
-    have = need;
+    w.ptr = b + kGuardBytes;
+    w.bytes = need;
     return PARALLAX_OK;
+}
+
+int mark_used(Workspace& w, cudaStream_t stream, const char* what) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    if (cap != cudaStreamCaptureStatusNone) return PARALLAX_OK;
+    e = cudaEventRecord(w.last_use, stream);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    w.used = true;
+    return PARALLAX_OK;
+}
+
+// Free a buffer after the whole device has finished with it (release path).
+int release(Workspace& w, const char* what) {
+    if (!w.ptr) return PARALLAX_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaFreeAsync(w.base(), nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    w.ptr = nullptr;
+    w.bytes = 0;
+    w.used = false;
+    return e == cudaSuccess ? PARALLAX_OK : cuda_fail(e, what);
 }
 
 int validate_common(const void* q, const void* k, const void* v, const void* o, const void* rho,
@@ -160,7 +242,9 @@ parallax::DecodePlan make_plan(int B, int H, int Hkv, int Lmax, int d, int num_s
     // groups of 2 about 8 items per SM (chunks capped at 4096 keys in every case, so ragged
     // lengths keep splitting).  Measured at B=64, H=16, 8192 keys, forced chunks 256..8192:
     // H_kv = 2 and 4 run fastest at 4096 keys among the chunks this allows, H_kv = 8 at 2048.
-    plan.chunk = plan_chunk(B, Hkv, Lmax, num_sms, H >= 4 * Hkv ? 1.7 : H > Hkv ? 8.0 : 16.0);
+    const int ctas = num_sms * parallax::decode_ctas_per_sm();
+    plan.chunk = H == Hkv ? plan_chunk_single(B, H, Lmax, ctas)
+                          : plan_chunk(B, Hkv, Lmax, num_sms, H >= 4 * Hkv ? 1.7 : 8.0);
     // a paged cache usually holds a ragged batch, which balances better on shorter items:
     // grouped heads on a paged cache take at most 2048 keys per item (B=512, lengths
     // U{128..16384}, page 256, H=16, H_kv=4: 1.39 ms at 2048 keys, 1.45 ms at 4096)
@@ -169,38 +253,38 @@ parallax::DecodePlan make_plan(int B, int H, int Hkv, int Lmax, int d, int num_s
     if (page_size > 0 && plan.chunk > parallax::decode_paged_max_chunk(page_size)) plan.chunk = 4096;
     plan.nsplit = (Lmax + plan.chunk - 1) / plan.chunk;
     const long long items = (long long)B * Hkv * plan.nsplit;
-    plan.grid = (int)std::min<long long>(items, (long long)num_sms * parallax::decode_ctas_per_sm());
+    plan.grid = (int)std::min<long long>(items, (long long)ctas);
+    // One query head per key/value head (bf16): the tensor-core decode streams faster once
+    // every CTA has at least two items of 512 keys or more (B=64, 8192 keys: 7.1 against
+    // 6.8 TB/s; B=2048, 1024 keys: 7.2 against 6.9); with fewer, shorter items the SIMT
+    // decode's deeper per-CTA pipeline wins (B=8, 8192 keys: 6.3 against 6.1 TB/s; 128-key
+    // heads: 6.3 against 5.8).
+    plan.mma = items >= 2LL * ctas && plan.chunk >= 512;
     return plan;
 }
 
-int decode_run(const parallax::DecodePlan& plan, int dev, DeviceState* ds, const void* q,
-               const void* rho, const void* kc, const void* vc, const int32_t* seqlens, void* o,
+int decode_run(const parallax::DecodePlan& plan, int dev, const void* q, const void* rho,
+               const void* kc, const void* vc, const int32_t* seqlens, void* o,
                cudaStream_t stream, bool bf16, const int32_t* block_table) {
-    (void)ds;
     const size_t need = parallax::decode_workspace_bytes(plan);
-    void* ws = nullptr;
-    if (need > 0) {
-        std::lock_guard<std::mutex> lock(g_mu);
-        DeviceState& s = g_dev[dev];
-        if (s.ws_bytes < need) {
-            if (s.ws) {
-                cudaError_t e = cudaFree(s.ws);  // synchronises the device
-                s.ws = nullptr;
-                s.ws_bytes = 0;
-                if (e != cudaSuccess) return cuda_fail(e, "workspace free");
-            }
-            cudaError_t e = cudaMalloc(&s.ws, need);
-            if (e != cudaSuccess) {
-                s.ws = nullptr;
-                return cuda_fail(e, "workspace allocation");
-            }
-            s.ws_bytes = need;
-        }
-        ws = s.ws;
+    if (need == 0) {
+        cudaError_t e = parallax::decode_launch(plan, bf16, q, rho, kc, vc, seqlens,
+                                                static_cast<float*>(o), nullptr, stream,
+                                                block_table);
+        if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+        return succeed();
     }
+    // the buffer is grown, used and marked under one lock, so that another thread's call
+    // cannot free it between this call's growth and its launch
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace& w = g_dev[dev].ws;
+    int rc = grow(w, need, stream, "decode workspace");
+    if (rc != PARALLAX_OK) return rc;
     cudaError_t e = parallax::decode_launch(plan, bf16, q, rho, kc, vc, seqlens,
-                                            static_cast<float*>(o), ws, stream, block_table);
+                                            static_cast<float*>(o), w.ptr, stream, block_table);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    rc = mark_used(w, stream, "decode workspace");
+    if (rc != PARALLAX_OK) return rc;
     return succeed();
 }
 
@@ -228,7 +312,7 @@ int decode_common(const void* q, const void* rho, const void* kc, const void* vc
     DeviceState* ds = device_state(&dev);
     if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
     const parallax::DecodePlan plan = make_plan(B, H, Hkv, Lmax, d, ds->num_sms);
-    return decode_run(plan, dev, ds, q, rho, kc, vc, seqlens, o, stream, bf16, nullptr);
+    return decode_run(plan, dev, q, rho, kc, vc, seqlens, o, stream, bf16, nullptr);
 }
 
 }  // namespace
@@ -286,19 +370,17 @@ int parallax_attn_prefill_backward(const void* q, const void* rho, const void* k
     int dev = 0;
     DeviceState* ds = device_state(&dev);
     if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
-    void* ws = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        DeviceState& st = g_dev[dev];
-        rc = grow(st.bws, st.bws_bytes, parallax::prefill_backward_workspace_bytes(B, H, L),
-                  "backward workspace");
-        if (rc != PARALLAX_OK) return rc;
-        ws = st.bws;
-    }
     parallax::PrefillShape s{B, H, L, d, causal, scale};
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace& w = g_dev[dev].bws;
+    rc = grow(w, parallax::prefill_backward_workspace_bytes(B, H, L), stream,
+              "backward workspace");
+    if (rc != PARALLAX_OK) return rc;
     cudaError_t e = parallax::prefill_backward_launch(s, q, rho, k, v, o, mu_v, lse, rbar, dout,
-                                                      dq, drho, dk, dv, ws, stream);
+                                                      dq, drho, dk, dv, w.ptr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    rc = mark_used(w, stream, "backward workspace");
+    if (rc != PARALLAX_OK) return rc;
     return succeed();
 }
 
@@ -352,7 +434,7 @@ int parallax_attn_decode_paged(const void* q, const void* rho, const void* k_pag
     if (!ds) return fail(PARALLAX_ERR_CUDA, "no usable CUDA device");
     const parallax::DecodePlan plan =
         make_plan(B, H, H_kv, Lmax, d, ds->num_sms, page_size, max_pages, num_pages);
-    return decode_run(plan, dev, ds, q, rho, k_pages, v_pages, seqlens, o, stream, true,
+    return decode_run(plan, dev, q, rho, k_pages, v_pages, seqlens, o, stream, true,
                       block_table);
 }
 
@@ -460,8 +542,9 @@ int parallax_attn_decode_chunk_keys(int B, int H, int Lmax, int d, int elem_byte
         return fail(PARALLAX_ERR_INVALID, "elem_bytes=%d must be 2 or 4", elem_bytes);
     int num_sms = 148;
     if (DeviceState* ds = device_state(nullptr)) num_sms = ds->num_sms;
+    const parallax::DecodePlan plan = make_plan(B, H, H, Lmax, d, num_sms);
     succeed();
-    return plan_chunk(B, H, Lmax, num_sms);
+    return plan.chunk;
 }
 
 int parallax_attn_decode_plan_keys(int B, int H, int H_kv, int Lmax, int d, int page_size) {
@@ -494,7 +577,7 @@ size_t parallax_attn_workspace_bytes(void) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     std::lock_guard<std::mutex> lock(g_mu);
-    return (int)g_dev.size() > dev ? g_dev[dev].ws_bytes : 0;
+    return (int)g_dev.size() > dev ? g_dev[dev].ws.bytes : 0;
 }
 
 int parallax_attn_release_workspace(void) {
@@ -502,34 +585,80 @@ int parallax_attn_release_workspace(void) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     std::lock_guard<std::mutex> lock(g_mu);
-    if ((int)g_dev.size() > dev && g_dev[dev].ws) {
-        e = cudaFree(g_dev[dev].ws);
-        g_dev[dev].ws = nullptr;
-        g_dev[dev].ws_bytes = 0;
-        if (e != cudaSuccess) return cuda_fail(e, "workspace free");
-    }
-    if ((int)g_dev.size() > dev && g_dev[dev].bws) {
-        e = cudaFree(g_dev[dev].bws);
-        g_dev[dev].bws = nullptr;
-        g_dev[dev].bws_bytes = 0;
-        if (e != cudaSuccess) return cuda_fail(e, "workspace free");
+    if ((int)g_dev.size() > dev) {
+        int rc = release(g_dev[dev].ws, "workspace free");
+        if (rc != PARALLAX_OK) return rc;
+        rc = release(g_dev[dev].bws, "workspace free");
+        if (rc != PARALLAX_OK) return rc;
     }
     return succeed();
 }
 
 const char* parallax_last_error(void) { return t_last_error.c_str(); }
 
-int parallax_check_device_error(cudaStream_t stream, unsigned int* bits) {
+int parallax_check_device_error(cudaStream_t stream) {
+    t_last_bits = 0;
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     const unsigned v = parallax::decode_take_error() | parallax::prefill_simt_take_error() |
                        parallax::prefill_tc_take_error() | parallax::proj_tc_take_error() |
                        parallax::prefill_backward_take_error() | parallax::lla_take_error();
-    if (bits) *bits = v;
+    t_last_bits = v;
     if (v) return fail(PARALLAX_ERR_DEVICE, "device error word 0x%x", v);
     return succeed();
 }
 
+unsigned int parallax_last_device_error_bits(void) { return t_last_bits; }
+
+int parallax_workspace_guards_intact(void) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((int)g_dev.size() <= dev) {
+        succeed();
+        return 1;
+    }
+    std::vector<unsigned char> band(kGuardBytes);
+    for (Workspace* w : {&g_dev[dev].ws, &g_dev[dev].bws}) {
+        if (!w->ptr) continue;
+        for (unsigned char* g : {w->base(), static_cast<unsigned char*>(w->ptr) + w->bytes}) {
+            e = cudaMemcpy(band.data(), g, kGuardBytes, cudaMemcpyDeviceToHost);
+            if (e != cudaSuccess) return cuda_fail(e, "guard band copy");
+            for (unsigned char c : band)
+                if (c != kGuardFill) {
+                    succeed();
+                    return 0;
+                }
+        }
+    }
+    succeed();
+    return 1;
+}
+
+int parallax_selftest_wait_timeout(int family, unsigned int limit_us, cudaStream_t stream) {
+    if (family != PARALLAX_SELFTEST_DECODE && family != PARALLAX_SELFTEST_PREFILL)
+        return fail(PARALLAX_ERR_INVALID, "kernel family %d (0: decode, 1: tensor-core prefill)",
+                    family);
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(PARALLAX_ERR_INVALID, "limit_us=%u must lie in [1, 1000000]", limit_us);
+    const uint64_t ns = 1000ull * limit_us;
+    cudaError_t e = family == PARALLAX_SELFTEST_DECODE ? parallax::decode_wait_selftest(ns, stream)
+                                                      : parallax::prefill_tc_wait_selftest(ns, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "wait self-test launch");
+    return succeed();
+}
+
 int parallax_version(void) { return 100; }
+
+int parallax_debug_checks(void) {
+#ifdef PARALLAX_DEBUG_CHECKS
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 }  // extern "C"

@@ -89,6 +89,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     if (prow >= (size_t)a.BH * a.Lp) return;
     const int bh = (int)(prow / a.Lp), i = (int)(prow - (size_t)bh * a.Lp);
     float* out = a.rs + (size_t)bh * 4 * a.Lp + i;
+    if (!in_bounds(&g_bwd_err, (size_t)bh * 4 * a.Lp + 3 * (size_t)a.Lp + i + 1,
+                   (size_t)a.BH * 4 * a.Lp))
+        return;
     if (i >= a.L) {  // padding rows: zeros, so that tiles past L read finite values
         if (lane < 4) out[(size_t)lane * a.Lp] = 0.f;
         return;
@@ -520,12 +523,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             // half 0 stores dV, half 1 dK
             float* orow = (c == 0 ? a.dv : a.dk) + ((size_t)bh * a.L + j) * D;
             const uint32_t base = trow + (c == 0 ? LY::DV : LY::DK);
+            const bool row_ok =
+                j < a.L && in_bounds(&g_bwd_err, ((size_t)bh * a.L + j + 1) * D, (size_t)a.BH * a.L * D);
 #pragma unroll 1
             for (int b = 0; b < D / 32; ++b) {
                 uint32_t u[32];
                 tc::tmem_ld32(base + 32 * b, u);
                 tc::tmem_ld_wait();
-                if (j < a.L) {
+                if (row_ok) {
 #pragma unroll
                     for (int x = 0; x < 32; x += 4)
                         *reinterpret_cast<float4*>(orow + 32 * b + x) =
@@ -880,12 +885,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (set == 0 || RHO) {
                 float* orow = (set == 0 ? a.dq : a.drho) + ((size_t)bh * a.L + i) * D + h * (D / 2);
                 const uint32_t base = (set == 0 ? rowS : rowR) + LY::O;
+                const bool row_ok = i < a.L && in_bounds(&g_bwd_err, ((size_t)bh * a.L + i + 1) * D,
+                                                         (size_t)a.BH * a.L * D);
 #pragma unroll 1
                 for (int b = 0; b < D / 64; ++b) {
                     uint32_t u[32];
                     tc::tmem_ld32_split<D / 2>(base + 32 * b, u);
                     tc::tmem_ld_wait();
-                    if (i < a.L) {
+                    if (row_ok) {
 #pragma unroll
                         for (int x = 0; x < 32; x += 4)
                             *reinterpret_cast<float4*>(orow + 32 * b + x) =

@@ -46,6 +46,23 @@ inline cudaError_t ensure_dynamic_smem(Kernel kern, int bytes, std::atomic<uint6
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) { atomicOr(err, bits); }
 
+// Debug builds (-DPARALLAX_DEBUG_CHECKS; `build.py --debug`) check, before each global
+// write and bulk copy they cover, that the element range [begin, end) lies inside its
+// tensor of `extent` elements.  A failed check raises PARALLAX_DEVERR_BOUNDS in the kernel's
+// error word; the caller then skips the write, or points a copy at the start of its tensor
+// so that every byte count the pipeline waits for still arrives.  Release builds compile
+// the checks away.
+#ifdef PARALLAX_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+__device__ __forceinline__ bool in_bounds(unsigned* err, size_t end, size_t extent) {
+    if (!kDebugChecks || end <= extent) return true;
+    raise_error(err, PARALLAX_DEVERR_BOUNDS);
+    return false;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -91,14 +108,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and
-// raises the timeout bit) if it did not complete within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+// raises the timeout bit) if it did not complete within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     uint32_t n = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((++n & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+        if ((++n & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
             raise_error(err, PARALLAX_DEVERR_WAIT_TIMEOUT);
             return false;
         }
@@ -139,32 +157,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// 2^x for a pair of x <= 0 (-inf allowed) on the FMA/ALU pipes, to take part of
-// the exponentials off the SFU.  Method: Cody-Waite style split x = n + f with
-// n = round(x) (added to a 1.5 * 2^23 bias, whose low mantissa bits then hold
-// n) and f in [-1/2, 1/2]; 2^f from a degree-3 polynomial whose coefficients
-// are a minimax fit of the relative error on [-1/2, 1/2] (Lawson's iteratively
-// reweighted least squares, computed offline); 2^n is added to the exponent
-// field.  Maximum relative error 7.5e-5 (the product path rounds P to bf16,
-// 3.9e-3).  x is clamped to -125, so 2^x underflows to ~2.4e-38, not to 0.
-constexpr float kExp2C0 = 0.99992806f;
-constexpr float kExp2C1 = 0.69326097f;
-constexpr float kExp2C2 = 0.24261114f;
-constexpr float kExp2C3 = 0.055171669f;
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 bias = make_float2(12582912.f, 12582912.f);  // 1.5 * 2^23
-    const float2 j = __fadd2_rn(x, bias);
-    const float2 n = __fadd2_rn(j, make_float2(-12582912.f, -12582912.f));
-    const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
-    float2 p = __ffma2_rn(f, make_float2(kExp2C3, kExp2C3), make_float2(kExp2C2, kExp2C2));
-    p = __ffma2_rn(p, f, make_float2(kExp2C1, kExp2C1));
-    p = __ffma2_rn(p, f, make_float2(kExp2C0, kExp2C0));
-    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(j.x) << 23)),
-                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(j.y) << 23)));
 }
 
 // max(a, b, c) in one instruction (three-input max of the sm_100 family).

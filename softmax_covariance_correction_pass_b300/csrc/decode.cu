@@ -165,17 +165,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
                     T* dv = stage_v + (size_t)s * SH::STAGE_KEYS * D;
                     if (!PAGED) {
                         const uint32_t bytes = (uint32_t)nk * KL::ROW_BYTES;
-                        bulk_copy_g2s(dk, static_cast<const T*>(a.kc) + (head + t0) * D, bytes,
-                                      &full[s], pol);
-                        bulk_copy_g2s(dv, static_cast<const T*>(a.vc) + (head + t0) * D, bytes,
-                                      &full[s], pol);
+                        const size_t src =
+                            in_bounds(&g_decode_err, (head + t0 + nk) * D, (size_t)BHkv * a.Lmax * D)
+                                ? (head + t0) * D : 0;
+                        bulk_copy_g2s(dk, static_cast<const T*>(a.kc) + src, bytes, &full[s], pol);
+                        bulk_copy_g2s(dv, static_cast<const T*>(a.vc) + src, bytes, &full[s], pol);
                     } else {
                         // one copy per page the stage touches
                         for (int t = t0; t < t0 + nk;) {
                             const int pg = t / a.page_size, row = t - pg * a.page_size;
                             const int seg = min(a.page_size - row, t0 + nk - t);
-                            const size_t src =
+                            size_t src =
                                 (((size_t)page_ids[pg - p0] * a.Hkv + hk) * a.page_size + row) * D;
+                            if (!in_bounds(&g_decode_err, src + (size_t)seg * D,
+                                           (size_t)a.num_pages * a.Hkv * a.page_size * D))
+                                src = 0;
                             const uint32_t bytes = (uint32_t)seg * KL::ROW_BYTES;
                             bulk_copy_g2s(dk + (size_t)(t - t0) * D,
                                           static_cast<const T*>(a.kc) + src, bytes, &full[s], pol);
@@ -275,10 +279,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
                 const int bq = bh * G + h2;
                 if (SPLIT) {
                     const size_t idx2 = (size_t)bq * a.nsplit + ch;
-                    a.ws_uw[idx2 * 2 * D + c] = U;
-                    a.ws_uw[idx2 * 2 * D + D + c] = W;
-                    if (c == 0) a.ws_stats[idx2] = make_float4(M, l, A, 0.f);
-                } else {
+                    if (in_bounds(&g_decode_err, idx2 + 1, (size_t)a.B * a.H * a.nsplit)) {
+                        a.ws_uw[idx2 * 2 * D + c] = U;
+                        a.ws_uw[idx2 * 2 * D + D + c] = W;
+                        if (c == 0) a.ws_stats[idx2] = make_float4(M, l, A, 0.f);
+                    }
+                } else if (in_bounds(&g_decode_err, (size_t)bq * D + c + 1, (size_t)a.B * a.H * D)) {
                     const float inv_l = l > 0.f ? 1.f / l : 0.f;
                     const float mu = U * inv_l;
                     a.o[(size_t)bq * D + c] = RHO ? mu - (W * inv_l - (A * inv_l) * mu) : mu;
@@ -289,27 +295,71 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     }
 }
 
+// One CTA of D threads per query head.  The chunks' maxima are reduced in parallel, then
+// the chunks are taken D at a time: thread t forms the weight 2^(m_t - M) of chunk t of the
+// batch (and its l, A terms) into shared memory, and thread c sums column c of U and W over
+// the batch with independent, unrolled loads.
 template <int D, bool RHO>
 __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a) {
-    const int bh = blockIdx.x, c = threadIdx.x;
+    __shared__ float s_f[D];
+    __shared__ float s_red[3][D / 32];
+    const int bh = blockIdx.x, c = threadIdx.x, w = c / 32, lane = c % 32;
     const int n = clamp_seqlen(a.seqlens, bh / a.H, a.Lmax);
-    const int nch = (n + a.chunk - 1) / a.chunk;
+    int nch = (n + a.chunk - 1) / a.chunk;
+    if (!in_bounds(&g_decode_err, (size_t)nch, (size_t)a.nsplit)) nch = a.nsplit;
     const float4* stats = a.ws_stats + (size_t)bh * a.nsplit;
     const float* uw = a.ws_uw + (size_t)bh * a.nsplit * 2 * D;
     float M = -INFINITY;
-    for (int k = 0; k < nch; ++k) M = fmaxf(M, stats[k].x);
+    for (int k = c; k < nch; k += D) M = fmaxf(M, stats[k].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
+    if (lane == 0) s_red[0][w] = M;
+    __syncthreads();
+    M = s_red[0][0];
+#pragma unroll
+    for (int i = 1; i < D / 32; ++i) M = fmaxf(M, s_red[0][i]);
     float l = 0.f, A = 0.f, U = 0.f, W = 0.f;
-    for (int k = 0; k < nch; ++k) {
-        const float4 s = stats[k];
-        const float f = fast_exp2(s.x - M);
-        l = fmaf(f, s.y, l);
-        A = fmaf(f, s.z, A);
-        U = fmaf(f, uw[(size_t)k * 2 * D + c], U);
-        if (RHO) W = fmaf(f, uw[(size_t)k * 2 * D + D + c], W);
+    for (int k0 = 0; k0 < nch; k0 += D) {
+        const int nb = min(D, nch - k0);
+        __syncthreads();  // s_f of the previous batch has been read
+        if (c < nb) {
+            const float4 st = stats[k0 + c];
+            const float f = M > -INFINITY ? fast_exp2(st.x - M) : 0.f;
+            s_f[c] = f;
+            l = fmaf(f, st.y, l);
+            A = fmaf(f, st.z, A);
+        }
+        __syncthreads();
+        const float* col = uw + (size_t)k0 * 2 * D + c;
+#pragma unroll 8
+        for (int k = 0; k < nb; ++k) {
+            const float f = s_f[k];
+            U = fmaf(f, __ldg(col + (size_t)k * 2 * D), U);
+            if (RHO) W = fmaf(f, __ldg(col + (size_t)k * 2 * D + D), W);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        l += __shfl_xor_sync(kFullMask, l, o);
+        A += __shfl_xor_sync(kFullMask, A, o);
+    }
+    __syncthreads();
+    if (lane == 0) {
+        s_red[1][w] = l;
+        s_red[2][w] = A;
+    }
+    __syncthreads();
+    l = 0.f;
+    A = 0.f;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+        l += s_red[1][i];
+        A += s_red[2][i];
     }
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     const float mu = U * inv_l;
-    a.o[(size_t)bh * D + c] = RHO ? mu - (W * inv_l - (A * inv_l) * mu) : mu;
+    if (in_bounds(&g_decode_err, (size_t)bh * D + c + 1, (size_t)a.B * a.H * D))
+        a.o[(size_t)bh * D + c] = RHO ? mu - (W * inv_l - (A * inv_l) * mu) : mu;
 }
 
 // ---------------------------------------------------------------------------
@@ -338,9 +388,8 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a) {
 // workspace and combine kernel).
 constexpr int kMmaWarps = 4;
 constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
-constexpr int kMmaStages = 2;
 
-template <int D>
+template <int D, int G>
 struct MmaShape {
     static constexpr int STAGE_KEYS = kStageRowBytes / (D * 2);
     static constexpr int NCB = D / 64;                  // 64-column (128-byte) blocks per row
@@ -348,10 +397,14 @@ struct MmaShape {
     static constexpr int KPW = STAGE_KEYS / kMmaWarps;  // keys per warp per stage
     static_assert(KPW % 16 == 0, "16-key blocks");
     static constexpr int STAGE_BYTES = NCB * CB_BYTES;
-    static constexpr int SLOT_FLOATS = 8 * (2 * D + 4);  // per warp: 8 heads x (U, W, m, l, A)
-    static constexpr int MERGE_OFF = 2 * kMmaStages * STAGE_BYTES;
+    // three stages while two CTAs still fit an SM (groups of 1 and 2: small merge slots),
+    // two for the groups of 4 and 8, whose merge slots take the room of a third
+    static constexpr int STAGES = G <= 2 ? 3 : 2;
+    static constexpr int SLOT_FLOATS = G * (2 * D + 4);  // per warp: G heads x (U, W, m, l, A)
+    static constexpr int MERGE_OFF = 2 * STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = MERGE_OFF + kMmaWarps * SLOT_FLOATS * 4;
-    static constexpr size_t SMEM_BYTES = BAR_OFF + 2 * kMmaStages * 8 + 16 + 1024;
+    static constexpr size_t SMEM_BYTES = BAR_OFF + 2 * STAGES * 8 + 16 + 1024;
+    static_assert(2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -387,7 +440,7 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 // within each 64-column block.
 template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int c16) {
-    using MS = MmaShape<D>;
+    using MS = MmaShape<D, 1>;
     return (uint32_t)((c16 >> 3) * MS::CB_BYTES + row * 128 + (((c16 & 7) ^ (row & 7)) << 4));
 }
 
@@ -395,7 +448,8 @@ template <int D, bool RHO, bool SPLIT, int G, bool PAGED>
 __global__ void __launch_bounds__(kMmaThreads, 2)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const DecodeArgs a) {
-    using MS = MmaShape<D>;
+    using MS = MmaShape<D, G>;
+    constexpr int kMmaStages = MS::STAGES;
     using T = __nv_bfloat16;
     constexpr int ROW_BYTES = D * 2;
     extern __shared__ unsigned char smem_raw[];
@@ -584,17 +638,20 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
         l += __shfl_xor_sync(kFullMask, l, 2);
         A += __shfl_xor_sync(kFullMask, A, 1);
         A += __shfl_xor_sync(kFullMask, A, 2);
-        float* hs = slot + g * (2 * D + 4);
-        if (t == 0) {
-            hs[0] = m;
-            hs[1] = l;
-            hs[2] = A;
-        }
+        if (g < G) {  // rows past the group are padding
+            float* hs = slot + g * (2 * D + 4);
+            if (t == 0) {
+                hs[0] = m;
+                hs[1] = l;
+                hs[2] = A;
+            }
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-            *reinterpret_cast<float2*>(hs + 4 + 8 * nt + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<float2*>(hs + 4 + D + 8 * nt + 2 * t) =
-                make_float2(acc[nt][2], acc[nt][3]);
+            for (int nt = 0; nt < D / 8; ++nt) {
+                *reinterpret_cast<float2*>(hs + 4 + 8 * nt + 2 * t) =
+                    make_float2(acc[nt][0], acc[nt][1]);
+                *reinterpret_cast<float2*>(hs + 4 + D + 8 * nt + 2 * t) =
+                    make_float2(acc[nt][2], acc[nt][3]);
+            }
         }
         named_bar_sync(1, kMmaWarps * 32);
         if (ok && !*abort_flag) {
@@ -619,10 +676,12 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
                 const int bq = bh * G + h2;
                 if (SPLIT) {
                     const size_t idx2 = (size_t)bq * a.nsplit + ch;
-                    a.ws_uw[idx2 * 2 * D + c] = U;
-                    a.ws_uw[idx2 * 2 * D + D + c] = W;
-                    if (c == 0) a.ws_stats[idx2] = make_float4(M, ls, As, 0.f);
-                } else {
+                    if (in_bounds(&g_decode_err, idx2 + 1, (size_t)a.B * a.H * a.nsplit)) {
+                        a.ws_uw[idx2 * 2 * D + c] = U;
+                        a.ws_uw[idx2 * 2 * D + D + c] = W;
+                        if (c == 0) a.ws_stats[idx2] = make_float4(M, ls, As, 0.f);
+                    }
+                } else if (in_bounds(&g_decode_err, (size_t)bq * D + c + 1, (size_t)a.B * a.H * D)) {
                     const float inv_l = ls > 0.f ? 1.f / ls : 0.f;
                     const float mu = U * inv_l;
                     a.o[(size_t)bq * D + c] = RHO ? mu - (W * inv_l - (As * inv_l) * mu) : mu;
@@ -635,7 +694,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
 
 template <int D, bool RHO, bool SPLIT, int G, bool PAGED>
 cudaError_t launch_decode_mma_kernel(const DecodeArgs& a, int grid, cudaStream_t stream) {
-    using MS = MmaShape<D>;
+    using MS = MmaShape<D, G>;
     auto kern = decode_mma_kernel<D, RHO, SPLIT, G, PAGED>;
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = ensure_dynamic_smem(kern, (int)MS::SMEM_BYTES, smem_set)) return e;
@@ -691,9 +750,10 @@ cudaError_t run_decode(const DecodePlan& plan, const void* q, const void* rho, c
     a.ws_uw = reinterpret_cast<float*>(static_cast<char*>(ws) + BH * plan.nsplit * sizeof(float4));
     cudaError_t e = cudaSuccess;
     // grouped heads: the tensor-core decode (a paged cache only when every stage lies in one page)
-    constexpr bool kMmaOk = sizeof(T) == 2 && G >= 2;
-    const bool mma = kMmaOk && (!PAGED || (plan.page_size % MmaShape<D>::STAGE_KEYS == 0 &&
-                                           plan.chunk % MmaShape<D>::STAGE_KEYS == 0));
+    constexpr bool kMmaOk = sizeof(T) == 2;
+    const bool mma = kMmaOk && (G >= 2 || plan.mma) &&
+                     (!PAGED || (plan.page_size % MmaShape<D, G>::STAGE_KEYS == 0 &&
+                                 plan.chunk % MmaShape<D, G>::STAGE_KEYS == 0));
     if (plan.nsplit > 1) {
         if constexpr (kMmaOk) {
             if (mma) e = launch_decode_mma_kernel<D, RHO, true, G, PAGED>(a, plan.grid, stream);
@@ -827,6 +887,26 @@ cudaError_t decode_launch_noalloc(const DecodePlan& plan, bool bf16, const void*
         ptr = g_noalloc_addr[dev];
     }
     return decode_launch(plan, bf16, q, rho, kc, vc, seqlens, o, ptr, stream, nullptr);
+}
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing ever
+// arrives on, with a wait limit of limit_ns; the wait gives up, raises
+// PARALLAX_DEVERR_WAIT_TIMEOUT in the decode kernels' error word and the kernel returns.
+// Until the host clears the word, later decode launches see the bit and exit at once.
+namespace {
+__global__ void decode_wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait(&bar, 0, &g_decode_err, limit_ns);
+    }
+}
+}  // namespace
+
+cudaError_t decode_wait_selftest(uint64_t limit_ns, cudaStream_t stream) {
+    decode_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 unsigned decode_take_error() {

@@ -19,6 +19,9 @@ struct DecodePlan {
     int nsplit;  // ceil(Lmax / chunk); 1 = no split, no combine kernel
     int grid;    // persistent CTAs
     float scale;
+    // bf16, one query head per key/value head: run the tensor-core decode kernel (the
+    // grouped kernels always do when their cache layout allows it)
+    bool mma;
 };
 
 size_t decode_workspace_bytes(const DecodePlan& plan);
@@ -31,6 +34,8 @@ cudaError_t decode_launch(const DecodePlan& plan, bool bf16, const void* q, cons
 // Largest chunk (keys) whose page ids fit the per-item table of the paged decode.
 int decode_paged_max_chunk(int page_size);
 unsigned decode_take_error();
+// One thread waits, with the given limit, on an mbarrier nothing arrives on (test hook).
+cudaError_t decode_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 // Same as decode_launch with the split-KV partials in a fixed device array
 // (no allocation).  Fails with cudaErrorInvalidValue if the plan needs more
 // than decode_noalloc_capacity() bytes.
@@ -63,6 +68,7 @@ cudaError_t prefill_tc_launch(const PrefillShape& s, const void* q, const void* 
                               const void* k, const void* v, float* o, int num_sms,
                               cudaStream_t stream, const TrainStats& ts = TrainStats{});
 unsigned prefill_tc_take_error();
+cudaError_t prefill_tc_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 // Chunked prefill: append k_new / v_new [B, H, L, d] to the caches [B, H, Lmax, d] at
 // rows cache_lens[b].., then causal attention of the chunk's queries over the cache.
 cudaError_t prefill_tc_chunk_launch(const PrefillShape& s, const void* q, const void* rho,

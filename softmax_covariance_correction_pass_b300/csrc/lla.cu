@@ -48,6 +48,7 @@ struct LlaArgs {
     float* o;    // [B*H, D]
     int H, Lmax, iters;
     float qscale;  // scale * log2(e)
+    size_t out_elems;  // B * H * D (debug bounds checks)
 };
 
 __device__ unsigned g_lla_err = 0;
@@ -539,8 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             float acc_o = 0.f;
 #pragma unroll 8
             for (int f1 = 0; f1 < D; ++f1) acc_o = fmaf(ct[t * LY::LD + f1], xv[f1], acc_o);
-            a.rho[(size_t)bh * D + t] = xv[t];
-            a.o[(size_t)bh * D + t] = muv[t] - acc_o;
+            if (in_bounds(&g_lla_err, (size_t)bh * D + t + 1, a.out_elems)) {
+                a.rho[(size_t)bh * D + t] = xv[t];
+                a.o[(size_t)bh * D + t] = muv[t] - acc_o;
+            }
         }
         if (!ok) *abort_flag = 1;
     }
@@ -583,6 +586,7 @@ cudaError_t lla_launch(const void* q, const void* kc, const void* vc, const int3
     a.Lmax = Lmax;
     a.iters = iters;
     a.qscale = kLog2e / sqrtf((float)d);
+    a.out_elems = (size_t)B * H * d;
     if (d == 64) return launch<64>(a, kc, vc, B * H, stream);
     if (d == 128) return launch<128>(a, kc, vc, B * H, stream);
     return cudaErrorInvalidValue;

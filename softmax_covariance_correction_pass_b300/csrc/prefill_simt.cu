@@ -26,6 +26,7 @@ struct SimtArgs {
     float* o;
     int L;
     float qscale;
+    size_t o_elems;  // B * H * L * D (debug bounds checks)
 };
 
 template <typename T, int D, bool RHO, bool CAUSAL>
@@ -79,7 +80,8 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const SimtArgs a
             warp_block<T, D, RHO>(st, qf, rf, sK, sV, kb, nvalid, lane);
     }
     warp_merge_groups<T, D, RHO>(st);
-    if (i < L && lane < KL::LPK)
+    if (i < L && lane < KL::LPK &&
+        in_bounds(&g_simt_err, head + (size_t)i * D + (e + 1) * VEC, a.o_elems))
         finish_slice<T, D, RHO>(st, a.o + head + (size_t)i * D + e * VEC);
 }
 
@@ -95,7 +97,7 @@ cudaError_t run(const PrefillShape& s, const SimtArgs& a, cudaStream_t stream) {
 
 cudaError_t prefill_simt_launch(const PrefillShape& s, bool bf16, const void* q, const void* rho,
                                 const void* k, const void* v, float* o, cudaStream_t stream) {
-    SimtArgs a{q, rho, k, v, o, s.L, s.scale * kLog2e};
+    SimtArgs a{q, rho, k, v, o, s.L, s.scale * kLog2e, (size_t)s.B * s.H * s.L * s.d};
     const bool r = rho != nullptr;
 #define PARALLAX_SIMT_CASE(T, DD)                                           \
     if (s.d == DD) return r ? run<T, DD, true>(s, a, stream) : run<T, DD, false>(s, a, stream);

@@ -51,8 +51,6 @@
 //  * the running max m is only moved when a tile's max exceeds it by more
 //    than 2^8 (lazy rescale); the final normalisation uses the same m, so the
 //    result is exact in exact arithmetic.
-// A quarter of the exponentials are evaluated by a polynomial on the FMA
-// pipes (exp2_poly2) to take load off the SFU.
 #include "tcgen05.cuh"
 #include "kernels.h"
 
@@ -125,15 +123,15 @@ __device__ __forceinline__ int cached_keys(const TcArgs& a, int bh, unsigned* er
 }
 
 // p = 2^(s*qs - m) for 32 consecutive values (in place), their sum into ls0/ls1,
-// and the bf16 pairs into pk; one pair in four through exp2_poly2, the rest on
-// the SFU.
+// and the bf16 pairs into pk.  Every exponential runs on the SFU: on sm_103a its
+// ex2 rate (measured: about 32 per clock per SM) leaves the SFU far from busy.
 __device__ __forceinline__ void exp_block32(uint32_t (&v)[32], float2 qs2, float2 nm2,
                                             float2& ls0, float2& ls1, uint32_t (&pk)[16]) {
 #pragma unroll
     for (int y = 0; y < 16; ++y) {
         const float2 t = __ffma2_rn(
             make_float2(__uint_as_float(v[2 * y]), __uint_as_float(v[2 * y + 1])), qs2, nm2);
-        const float2 p2 = (y & 3) == 3 ? exp2_poly2(t) : make_float2(fast_exp2(t.x), fast_exp2(t.y));
+        const float2 p2 = make_float2(fast_exp2(t.x), fast_exp2(t.y));
         v[2 * y] = __float_as_uint(p2.x);
         v[2 * y + 1] = __float_as_uint(p2.y);
         if (y & 1) ls1 = __fadd2_rn(ls1, p2);
@@ -544,13 +542,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float inv_l = 1.f / lt;
                 const float gain = 1.f + At * inv_l;
                 float* orow = a.o + ((size_t)bh * a.L + i) * D + h * (D / 2);
+                const bool row_ok =
+                    i < a.L && in_bounds(&g_tc_err, ((size_t)bh * a.L + i + 1) * D, (size_t)a.BH * a.L * D);
 #pragma unroll 1
                 for (int b = 0; b < D / 64; ++b) {
                     uint32_t u[32], w[32];
                     tc::tmem_ld32_split<D / 2>(tU + 32 * b, u);
                     tc::tmem_ld32_split<D / 2>(tW + 32 * b, w);
                     tc::tmem_ld_wait();
-                    if (i < a.L) {
+                    if (row_ok) {
 #pragma unroll
                         for (int x = 0; x < 32; x += 4) {
                             float out[4];
@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (a.lse && h == 0 && i < a.L) {
+                if (a.lse && h == 0 && row_ok) {
                     a.lse[(size_t)bh * a.L + i] = (m + __log2f(lt)) * kLn2;
                     a.rbar[(size_t)bh * a.L + i] = At * inv_l + c;
                 }
@@ -655,12 +655,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_after_sync();
                 const float inv_l = 1.f / l;
                 float* orow = a.o + ((size_t)bh * a.L + i) * D;
+                const bool row_ok =
+                    i < a.L && in_bounds(&g_tc_err, ((size_t)bh * a.L + i + 1) * D, (size_t)a.BH * a.L * D);
 #pragma unroll 1
                 for (int b = 0; b < D / 32; ++b) {
                     uint32_t u[32];
                     tc::tmem_ld32(tU + 32 * b, u);
                     tc::tmem_ld_wait();
-                    if (i < a.L) {
+                    if (row_ok) {
 #pragma unroll
                         for (int x = 0; x < 32; x += 4) {
                             const float4 v4 = make_float4(
@@ -672,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (a.lse && i < a.L) {
+                if (a.lse && row_ok) {
                     a.lse[(size_t)bh * a.L + i] = (m + __log2f(l)) * kLn2;
                     a.rbar[(size_t)bh * a.L + i] = 0.f;
                 }
@@ -770,6 +772,7 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4* __restrict__ k
         int off = __ldg(cache_lens + bh / H);
         off = off < 0 ? 0 : (off > Lcap - L ? Lcap - L : off);
         const size_t dst = ((size_t)bh * Lcap + off + i) * vec_per_row + c;
+        if (!in_bounds(&g_tc_err, dst + 1, total_vec / rows * Lcap)) continue;
         if (i < L) {
             const size_t src = ((size_t)bh * L + i) * vec_per_row + c;
             k_cache[dst] = k_new[src];
@@ -807,6 +810,25 @@ cudaError_t prefill_tc_chunk_launch(const PrefillShape& s, const void* q, const 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_any(s, q, rho, k_cache, v_cache, o, cache_lens, Lmax, stream);
+}
+
+// Self-test of the bounded wait for the tensor-core prefill's error word (see
+// decode_wait_selftest); later prefill CTAs see the bit, skip their work, free their
+// TMEM and return.
+namespace {
+__global__ void tc_wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait(&bar, 0, &g_tc_err, limit_ns);
+    }
+}
+}  // namespace
+
+cudaError_t prefill_tc_wait_selftest(uint64_t limit_ns, cudaStream_t stream) {
+    tc_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 unsigned prefill_tc_take_error() {

@@ -52,6 +52,7 @@ struct ProjArgs {
     int m_tiles_per_b;  // ceil(L / 128)
     int n_tiles;        // all tiles
     int kblocks;        // ceil(width / 64)
+    size_t out_elems;   // B * H * L * d per output (debug bounds checks)
 };
 
 template <int BN, int D>
@@ -209,8 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t(&r)[32] = e ? r1 : r0;
                         const int f = f0 + 32 * (ch + e);
                         const int h = f / D, c = f % D;
-                        uint4* dst = reinterpret_cast<uint4*>(
-                            base + (((size_t)b * a.H + h) * a.L + l) * D + c);
+                        const size_t at = (((size_t)b * a.H + h) * a.L + l) * D + c;
+                        if (!in_bounds(&g_proj_err, at + 32, a.out_elems)) continue;
+                        uint4* dst = reinterpret_cast<uint4*>(base + at);
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
                             dst[v] = make_uint4(
@@ -279,6 +281,7 @@ cudaError_t proj_tc_launch(const ProjShape& s, const void* x, const void* w, voi
     if (tiles > 2147483647LL) return cudaErrorInvalidValue;
     a.n_tiles = (int)tiles;
     a.kblocks = (s.width + BK - 1) / BK;
+    a.out_elems = (size_t)s.B * s.H * s.L * s.d;
     if (BN == 256)
         return s.d == 64 ? launch<256, 64>(mx, mw, a, num_sms, stream)
                          : launch<256, 128>(mx, mw, a, num_sms, stream);

@@ -34,6 +34,47 @@ def test_header_declares_the_boundary():
         assert required in names
 
 
+def _declaration(name):
+    """The declaration of `name` in the header, comments and preprocessor lines stripped,
+    whitespace collapsed."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = "\n".join(l for l in text.splitlines() if not l.lstrip().startswith("#"))
+    for stmt in re.split(r"[;{}]", text):
+        if re.search(r"\b" + name + r"\s*\(", stmt):
+            return " ".join(stmt.split())
+    raise AssertionError(f"{name} is not declared")
+
+
+# The boundary's own signatures (argument names, order and types), as the hot-path scope
+# defines them: prefill(q, rho, k, v, o, B, H, L, d, causal, scale, stream),
+# decode(q, rho, k_cache, v_cache, seqlens, o, B, H, Lmax, d, stream) and a device-error
+# check that takes the stream alone.
+BOUNDARY = {
+    "parallax_attn_prefill":
+        "int parallax_attn_prefill(const void* q, const void* rho, const void* k, const void* v, "
+        "void* o, int B, int H, int L, int d, int causal, float scale, cudaStream_t stream)",
+    "parallax_attn_decode":
+        "int parallax_attn_decode(const void* q, const void* rho, const void* k_cache, "
+        "const void* v_cache, const int32_t* seqlens, void* o, int B, int H, int Lmax, int d, "
+        "cudaStream_t stream)",
+    "parallax_attn_prefill_f32":
+        "int parallax_attn_prefill_f32(const void* q, const void* rho, const void* k, "
+        "const void* v, void* o, int B, int H, int L, int d, int causal, float scale, "
+        "cudaStream_t stream)",
+    "parallax_attn_decode_f32":
+        "int parallax_attn_decode_f32(const void* q, const void* rho, const void* k_cache, "
+        "const void* v_cache, const int32_t* seqlens, void* o, int B, int H, int Lmax, int d, "
+        "cudaStream_t stream)",
+    "parallax_last_error": "const char* parallax_last_error(void)",
+    "parallax_check_device_error": "int parallax_check_device_error(cudaStream_t stream)",
+}
+
+
+@pytest.mark.parametrize("name", sorted(BOUNDARY))
+def test_boundary_signatures(name):
+    assert _declaration(name) == BOUNDARY[name]
+
+
 def test_library_exports_every_declared_symbol(lib):
     missing = [n for n in _declared() if not hasattr(lib, n)]
     assert not missing, missing
@@ -109,14 +150,25 @@ def test_last_error_is_thread_local(lib):
 
 
 def test_chunk_plan(lib):
-    # split-KV plan: chunk is a multiple of 256 keys (or the whole cache), more
-    # splits for few heads and long caches, none when every head is short
+    # split-KV plan with one query head per key/value head (148 SMs, 2 CTAs each, without a
+    # device): the longest chunk of 256..4096 keys that leaves at least 0.85 items per CTA;
+    # heads of at most 1024 keys are never split
     f = px.parallax_attn_decode_chunk_keys
-    assert f(64, 16, 8192, 128, 2) % 256 == 0
+    ctas = 2 * 148
     assert f(1, 16, 128, 128, 2) == 128                      # no split: whole cache
-    assert f(1, 16, 32768, 128, 2) == 256                    # few heads: smallest chunks
+    assert f(8, 16, 1024, 128, 2) == 1024                    # short heads: no split
     assert f(2048, 16, 1024, 128, 2) == 1024                 # many heads: no split
-    assert 256 <= f(512, 16, 16384, 128, 2) <= 4096
+    assert f(1, 16, 32768, 128, 2) == 2048                   # 16 heads x 16 chunks
+    assert f(8, 16, 8192, 128, 2) == 4096                    # 128 heads x 2 chunks
+    assert f(1, 16, 8192, 128, 2) == 512                     # 16 heads x 16 chunks
+    assert f(64, 16, 8192, 128, 2) == 4096
+    assert f(512, 16, 16384, 128, 2) == 4096                 # the 4096-key cap
+    for B, L in ((1, 2048), (1, 100000), (4, 5000), (32, 2049), (3, 65536)):
+        c = f(B, 16, L, 128, 2)
+        items = B * 16 * -(-L // c)
+        assert c == L or (256 <= c <= 4096 and c & (c - 1) == 0)
+        assert items >= 0.85 * ctas or c == 256
+        assert c >= 4096 or c == L or B * 16 * -(-L // (2 * c)) < 0.85 * ctas
     with pytest.raises(px.ParallaxError):
         f(0, 16, 128, 128, 2)
     with pytest.raises(px.ParallaxError):
@@ -125,7 +177,7 @@ def test_chunk_plan(lib):
 
 def test_decode_plan_by_group_size(lib):
     """The plan of the plain, grouped-query and paged decode (host logic, 148 SMs without a
-    device): plain decode aims at ~16 items per SM, groups of 2 at ~8, groups of 4 and 8 take
+    device): plain decode as above, groups of 2 aim at ~8 items per SM, groups of 4 and 8 take
     the longest chunk leaving >= 1.7 items per SM, grouped heads on a paged cache stop at 2048
     keys; chunks stay within 256..4096 keys or cover the whole cache."""
     f = px.parallax_attn_decode_plan_keys
