@@ -120,7 +120,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["decode", "prefill", "projection", "backward", "gqa", "lla"],
+    ap.add_argument("--only", choices=["decode", "prefill", "projection", "backward", "gqa", "lla",
+                                       "chunk"],
                     default=None,
                     help="time one kernel alone (profiling runs); the default times both")
     ap.add_argument("--decode-batch", type=int, default=None,
@@ -130,6 +131,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-projection", action="store_true",
                     help="skip the q/k/v/probe projection leg")
     ap.add_argument("--no-backward", action="store_true", help="skip the prefill backward leg")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the decode sweep grid reported beside the step")
     ap.add_argument("--wr-zero", action="store_true",
                     help="time the W_R = 0 path (rho = NULL) in the step instead of the "
                          "correction path (profiling runs)")
@@ -697,6 +700,16 @@ def run_ours(args):
                        "ms_per_step": ep_ms}
         del hp, dp
 
+    # ---- the decode sweep grid (17 cells, batch 1-2048 x context 128-32768) and the ragged
+    # batch, each timed alone; reported beside the step, not part of it
+    sweep = None
+    if not args.only and not args.no_sweep:
+        sweep = [{"B": r["B"], "context": r["context"], "GB/s": round(r["GB/s"], 1),
+                  "frac_of_hbm_peak": round(r["frac_of_hbm_peak"], 4), "ms": round(r["ms"], 5),
+                  "chunk_keys": r["chunk_keys"], "l2": r["l2"]}
+                 for r in sweep_rows(dev, peaks, include_boundary=False, include_ragged=True,
+                                     quiet=True)]
+
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -730,6 +743,7 @@ def run_ours(args):
             "torch_sdpa_w_r_zero": sdpa,
             "roofline_projection": proj,
             "roofline_backward": bwd,
+            "decode_sweep": sweep,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks.summary(),
@@ -742,27 +756,26 @@ def run_ours(args):
 
 
 # ----------------------------------------------------------------------------- decode sweep
-def run_sweep(args):
-    """Decode over the sweep grid (batch x context, caches up to 64e9 bytes, plus the
-    64 GiB boundary cell, flagged) and the ragged batch.  Each case is timed with CUDA
-    events per call; caches smaller than twice the L2 are evicted before every call by
-    writing a 512 MB buffer (not timed), larger ones are timed back to back."""
+def sweep_rows(dev, peaks, include_boundary=True, include_ragged=True, quiet=False):
+    """Decode over the sweep grid (batch x context, caches up to 64e9 bytes; optionally the
+    64 GiB boundary cell, flagged) and the ragged batch.  Each case is timed with CUDA events
+    per call; caches smaller than twice the L2 are evicted before every call by writing a
+    512 MB buffer (not timed), larger ones are timed back to back."""
     import torch
 
     import softmax_covariance_correction_pass_b300 as px
     from softmax_covariance_correction_pass_b300 import configs
 
-    dev = torch.device("cuda", torch.cuda.current_device())
-    px.load_library()
-    peaks = load_peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     sw = configs.DECODE_SWEEP
     cases = [("sweep", B, L, False) for B, L in configs.decode_sweep_cells()]
-    cases += [("sweep", B, L, True) for B, L in configs.decode_sweep_cells(include_boundary=True)
-              if (B, L) not in configs.decode_sweep_cells()]
-    cases.append(("ragged", configs.DECODE_RAGGED["B"], configs.DECODE_RAGGED["hi"], False))
+    if include_boundary:
+        cases += [("sweep", B, L, True) for B, L in configs.decode_sweep_cells(include_boundary=True)
+                  if (B, L) not in configs.decode_sweep_cells()]
+    if include_ragged:
+        cases.append(("ragged", configs.DECODE_RAGGED["B"], configs.DECODE_RAGGED["hi"], False))
     rows = []
     for kind, B, L, boundary in cases:
         if kind == "sweep":
@@ -803,9 +816,25 @@ def run_sweep(args):
                "chunk_keys": chunk, "l2": "evicted before each call" if cold else "larger than L2",
                "boundary_cell_64GiB": boundary}
         rows.append(row)
-        print(json.dumps(row), flush=True)
+        if not quiet:
+            print(json.dumps(row), flush=True)
         del inp, o
         torch.cuda.empty_cache()
+    del flush
+    torch.cuda.empty_cache()
+    return rows
+
+
+def run_sweep(args):
+    """--sweep: every decode sweep cell (plus the 64 GiB boundary cell) and the ragged batch,
+    one JSON line per case, and a markdown table on stderr."""
+    import torch
+
+    import softmax_covariance_correction_pass_b300 as px
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    px.load_library()
+    rows = sweep_rows(dev, load_peaks())
     print("| case | B | context | KV bytes | ms | GB/s | % of HBM peak | tokens/s | chunk |",
           file=sys.stderr)
     print("|---|---|---|---|---|---|---|---|---|", file=sys.stderr)
@@ -852,6 +881,30 @@ def run_serving_one(args):
     print(json.dumps({"case": args.only, "B": B, "ms": a.elapsed_time(b) / args.steps}),
           flush=True)
     return 0
+
+
+def time_chunk(args, dev, peaks, timed, reps):
+    """Chunked prefill of the layer-shaped workload: 3072 tokens cached, the last 1024 of each
+    sequence appended (append_kernel) and attended (prefill_pair_kernel with offsets)."""
+    import torch
+
+    import softmax_covariance_correction_pass_b300 as px
+    from softmax_covariance_correction_pass_b300 import configs
+
+    full = configs.layer_prefill_inputs(dev, B=args.prefill_batch)
+    B, H, L, d = full.q.shape
+    off, Lq = 3072, 1024
+    kc, vc = full.k.clone(), full.v.clone()
+    cl = torch.full((B,), off, dtype=torch.int32, device=dev)
+    sl_ = slice(off, L)
+    qn, rn, kn, vn = (t[:, :, sl_].contiguous() for t in (full.q, full.rho, full.k, full.v))
+    o = torch.empty((B, H, Lq, d), dtype=torch.float32, device=dev)
+    ms = timed(lambda: px.parallax_attn_prefill_chunk(qn, rn, kn, vn, kc, vc, cl, o), reps)
+    pairs = B * H * sum(off + i + 1 for i in range(Lq))
+    flops = 8.0 * d * pairs
+    return {"case": f"chunked prefill B={B} H={H} cached={off} chunk={Lq}", "ms": ms,
+            "TFLOP/s": flops / ms / 1e9, "frac_of_tensor_peak_burst":
+                flops / ms / 1e9 / peaks["bf16_tflops"], "tokens_per_s": B * Lq / (ms * 1e-3)}
 
 
 def run_serving(args):
@@ -911,21 +964,7 @@ def run_serving(args):
                      "kv_bytes": 2 * keys * Hkv * d * 2, "tokens_per_s": B / (ms * 1e-3)})
         del inp, o, bt
         torch.cuda.empty_cache()
-    full = configs.layer_prefill_inputs(dev)
-    B, H, L, _ = full.q.shape
-    off, Lq = 3072, 1024
-    kc, vc = full.k.clone(), full.v.clone()
-    cl = torch.full((B,), off, dtype=torch.int32, device=dev)
-    sl_ = slice(off, L)
-    qn, rn, kn, vn = (t[:, :, sl_].contiguous() for t in (full.q, full.rho, full.k, full.v))
-    o = torch.empty((B, H, Lq, d), dtype=torch.float32, device=dev)
-    ms = timed(lambda: px.parallax_attn_prefill_chunk(qn, rn, kn, vn, kc, vc, cl, o), 20)
-    pairs = B * H * sum(off + i + 1 for i in range(Lq))
-    flops = 8.0 * d * pairs
-    rows.append({"case": f"chunked prefill B={B} H={H} cached={off} chunk={Lq}", "ms": ms,
-                 "TFLOP/s": flops / ms / 1e9, "frac_of_tensor_peak_burst":
-                     flops / ms / 1e9 / peaks["bf16_tflops"], "tokens_per_s": B * Lq / (ms * 1e-3)})
-    del full, kc, vc, qn, rn, kn, vn, o
+    rows.append(time_chunk(args, dev, peaks, timed, 20))
     torch.cuda.empty_cache()
     # exact local linear attention decode (comparison workload) at the uniform decode shape
     dc = configs.DECODE_UNIFORM
@@ -957,6 +996,31 @@ def main(argv=None):
         return run_projection_only(args)
     if args.only in ("gqa", "lla"):
         return run_serving_one(args)
+    if args.only == "chunk":
+        import torch
+
+        import softmax_covariance_correction_pass_b300 as px
+
+        px.load_library()
+        dev = torch.device("cuda", torch.cuda.current_device())
+        stream = torch.cuda.current_stream()
+
+        def timed(call, reps):
+            for _ in range(max(args.warmup, 3)):
+                call()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if px.parallax_check_device_error() != 0:
+                raise RuntimeError("device error")
+            return a.elapsed_time(b) / reps
+
+        print(json.dumps(time_chunk(args, dev, load_peaks(), timed, args.steps)), flush=True)
+        return 0
     if args.only == "backward":
         import torch
 

@@ -36,6 +36,9 @@
  *     available from parallax_last_error() on the calling thread.
  *   - Head dimension d must be 64 or 128 (PARALLAX_ERR_UNSUPPORTED otherwise).
  *   - Attention outputs o are always fp32 (the projection writes bf16).
+ *   - The library keeps per-device state (workspaces, the no-allocation array's
+ *     address, kernel attributes) for the life of the process: do not use it
+ *     across a cudaDeviceReset() of a device it has run on.
  */
 #ifndef PARALLAX_ATTN_H
 #define PARALLAX_ATTN_H
@@ -245,8 +248,13 @@ int parallax_lla_decode(const void* q, const void* k_cache, const void* v_cache,
  * needs more returns PARALLAX_ERR_UNSUPPORTED before anything is launched
  * (parallax_attn_decode handles it).  The first call on a device looks up
  * the array's device address (no allocation); make that first call before
- * any stream capture.  All calls on a device share the array, so calls that
- * may overlap on the GPU (other streams, other host threads) race on it.
+ * any stream capture.  The array, like the decode kernels' code, is placed in
+ * device memory when the library's decode module is first loaded on a device:
+ * under CUDA's default lazy module loading that can be this entry point's first
+ * call (or the first decode of any kind), so make one call -- or run one decode
+ * -- on each device before reserving the rest of its memory for a cache pool.
+ * All calls on a device share the array, so calls that may overlap on the GPU
+ * (other streams, other host threads) race on it.
  */
 int parallax_attn_decode_noalloc(const void* q, const void* rho, const void* k_cache,
                                  const void* v_cache, const int32_t* seqlens, void* o, int B,

@@ -73,6 +73,11 @@ constexpr int kRegsSoftmax = 216;
 static_assert(128 * kRegsSupport + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register hand-over exceeds the launch allocation");
 constexpr int kHeadGroup = 16;  // heads per CTA-scheduling group (keeps their K/V in L2)
+// K tiles are needed half a tile step before V tiles (S of tile j+1 is computed while P of
+// tile j is pending), so the K ring is one stage deeper than the V ring; K and V are loaded
+// by two producer warps so that neither ring's wait holds up the other's loads.
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 
 template <int D, bool RHO>
 struct PairLayout {
@@ -82,12 +87,21 @@ struct PairLayout {
     static constexpr int NCB = D / 64;                  // 64-column blocks per row
     static constexpr int OP_BYTES = NCB * SUB_BYTES;    // one 128 x D bf16 operand
     static constexpr int QR_OFF = 0;                    // A operands of MMA-1, sub-tiles 0 and 1
-    static constexpr int K_OFF = 2 * OP_BYTES;          // K ring, 2 stages
-    static constexpr int V_OFF = K_OFF + 2 * OP_BYTES;  // V ring, 2 stages
-    static constexpr int BAR_OFF = V_OFF + 2 * OP_BYTES;
-    // q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2], p_full[2], o_full
-    static constexpr int NBARS = 14;
+    static constexpr int K_OFF = 2 * OP_BYTES;                     // K ring
+    static constexpr int V_OFF = K_OFF + kKStages * OP_BYTES;      // V ring
+    static constexpr int BAR_OFF = V_OFF + kVStages * OP_BYTES;
+    // q_full, k_full[kKStages], v_full[kVStages], k_empty[kKStages], v_empty[kVStages],
+    // s_full[2], p_full[2], o_full
+    static constexpr int B_KFULL = 1;
+    static constexpr int B_VFULL = B_KFULL + kKStages;
+    static constexpr int B_KEMPTY = B_VFULL + kVStages;
+    static constexpr int B_VEMPTY = B_KEMPTY + kKStages;
+    static constexpr int B_SFULL = B_VEMPTY + kVStages;
+    static constexpr int B_PFULL = B_SFULL + 2;
+    static constexpr int B_OFULL = B_PFULL + 2;
+    static constexpr int NBARS = B_OFULL + 1;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     __host__ __device__ static constexpr uint32_t dcol(int sub) { return 128u * sub; }
     __host__ __device__ static constexpr uint32_t ocol(int sub) { return 256u + (uint32_t)(D * sub); }
 };
@@ -140,6 +154,23 @@ __device__ __forceinline__ void exp_block32(uint32_t (&v)[32], float2 qs2, float
     }
 }
 
+// Maximum of the 128 values of v[4][32] (or 64 of v[2][32]) in eight independent chains of
+// three-input max, then a short tree.
+template <int NB>
+__device__ __forceinline__ float max_blocks(const uint32_t (&v)[NB][32]) {
+    float c[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) c[k] = -INFINITY;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int x = 0; x < 32; x += 16)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                c[k] = fmax3(c[k], __uint_as_float(v[b][x + 2 * k]), __uint_as_float(v[b][x + 2 * k + 1]));
+    return fmaxf(fmaxf(fmax3(c[0], c[1], c[2]), fmax3(c[3], c[4], c[5])), fmaxf(c[6], c[7]));
+}
+
 // bf16 rounding residual of the 32 values packed in pk.
 __device__ __forceinline__ void residual_block32(const uint32_t (&v)[32], uint32_t (&pk)[16]) {
 #pragma unroll
@@ -159,13 +190,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
     uint64_t* q_full = bars;
-    uint64_t* k_full = bars + 1;
-    uint64_t* v_full = bars + 3;
-    uint64_t* k_empty = bars + 5;
-    uint64_t* v_empty = bars + 7;
-    uint64_t* s_full = bars + 9;
-    uint64_t* p_full = bars + 11;
-    uint64_t* o_full = bars + 13;
+    uint64_t* k_full = bars + LY::B_KFULL;
+    uint64_t* v_full = bars + LY::B_VFULL;
+    uint64_t* k_empty = bars + LY::B_KEMPTY;
+    uint64_t* v_empty = bars + LY::B_VEMPTY;
+    uint64_t* s_full = bars + LY::B_SFULL;
+    uint64_t* p_full = bars + LY::B_PFULL;
+    uint64_t* o_full = bars + LY::B_OFULL;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -195,7 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool precise = RHO && n1 == 1;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < LY::NBARS; ++b) mbar_init(&bars[b], (b == 11 || b == 12) ? 128 : 1);
+        for (int b = 0; b < LY::NBARS; ++b)
+            mbar_init(&bars[b], (b == LY::B_PFULL || b == LY::B_PFULL + 1) ? 128 : 1);
         *abort_flag = (*(volatile unsigned*)&g_tc_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
         fence_mbar_init();
     }
@@ -214,11 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) {
         tc::setmaxnreg_dec<kRegsSupport>();
         if (warp == 0) {
-            // ------------------------------------------------------------ TMA producer
+            // ------------------------------------------------------------ TMA producer: Q, K
             if (lane == 0 && !skip) {
                 const int z = bh;
                 bool ok = true;
-                int kj = 0, vj = 0;  // K / V tiles issued
+                int kj = 0;  // K tiles issued
                 mbar_arrive_expect_tx(q_full, 2 * LY::OP_BYTES);
                 for (int sub = 0; sub < 2; ++sub)
                     for (int cb = 0; cb < LY::NCB; ++cb) {
@@ -234,9 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc::tma_load_3d(dst, &tmQ, cb * 64, q0 + 128 * sub, z, q_full);
                         }
                     }
-                for (int j = 0; j < n1 && ok; ++j) {
-                    const int st = j & 1;
-                    if (j >= 2 && !mbar_wait(&k_empty[st], ((j >> 1) - 1) & 1, &g_tc_err)) {
+                for (int j = 0; j < n1; ++j) {
+                    const int st = j % kKStages;
+                    if (j >= kKStages &&
+                        !mbar_wait(&k_empty[st], (j / kKStages - 1) & 1, &g_tc_err)) {
                         ok = false;
                         break;
                     }
@@ -245,24 +278,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::tma_load_3d(smem + LY::K_OFF + st * LY::OP_BYTES + cb * LY::SUB_BYTES,
                                         &tmK, cb * 64, j * BN, z, &k_full[st]);
                     kj = j + 1;
-                    if (j >= 2 && !mbar_wait(&v_empty[st], ((j >> 1) - 1) & 1, &g_tc_err)) {
+                }
+                if (!ok) {
+                    *abort_flag = 1;
+                    // wait (bounded) for the copies already issued into this CTA's shared memory
+                    mbar_wait(q_full, 0, &g_tc_err);
+                    for (int k = (kj >= kKStages ? kj - kKStages : 0); k < kj; ++k)
+                        mbar_wait(&k_full[k % kKStages], (k / kKStages) & 1, &g_tc_err);
+                }
+            }
+        } else if (warp == 2) {
+            // ------------------------------------------------------------ TMA producer: V
+            if (lane == 0 && !skip) {
+                bool ok = true;
+                int vj = 0;  // V tiles issued
+                for (int j = 0; j < n1; ++j) {
+                    const int st = j % kVStages;
+                    if (j >= kVStages &&
+                        !mbar_wait(&v_empty[st], (j / kVStages - 1) & 1, &g_tc_err)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&v_full[st], LY::OP_BYTES);
                     for (int cb = 0; cb < LY::NCB; ++cb)
                         tc::tma_load_3d(smem + LY::V_OFF + st * LY::OP_BYTES + cb * LY::SUB_BYTES,
-                                        &tmV, cb * 64, j * BN, z, &v_full[st]);
+                                        &tmV, cb * 64, j * BN, bh, &v_full[st]);
                     vj = j + 1;
                 }
                 if (!ok) {
                     *abort_flag = 1;
-                    // wait (bounded) for the copies already issued into this CTA's shared memory
-                    mbar_wait(q_full, 0, &g_tc_err);
-                    for (int k = (kj >= 2 ? kj - 2 : 0); k < kj; ++k)
-                        mbar_wait(&k_full[k & 1], (k >> 1) & 1, &g_tc_err);
-                    for (int k = (vj >= 2 ? vj - 2 : 0); k < vj; ++k)
-                        mbar_wait(&v_full[k & 1], (k >> 1) & 1, &g_tc_err);
+                    for (int k = (vj >= kVStages ? vj - kVStages : 0); k < vj; ++k)
+                        mbar_wait(&v_full[k % kVStages], (k / kVStages) & 1, &g_tc_err);
                 }
             }
         } else if (warp == 1) {
@@ -322,10 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::commit(&k_empty[0]);
                 }
                 for (int j = 0; j < n1 && ok; ++j) {
-                    const int st = j & 1;
+                    const int vs = j % kVStages, ks = (j + 1) % kKStages;  // V of j, K of j + 1
                     const bool do0 = j < n0, more0 = j + 1 < n0, more1 = j + 1 < n1;
                     // V first: it is normally resident long before P is ready
-                    if (!mbar_wait_warp(&v_full[st], (j >> 1) & 1, &g_tc_err)) {
+                    if (!mbar_wait_warp(&v_full[vs], (j / kVStages) & 1, &g_tc_err)) {
                         ok = false;
                         break;
                     }
@@ -335,15 +381,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc::fence_after_sync();
-                        mma2(0, st, j == 0);
+                        mma2(0, vs, j == 0);
                     }
-                    if (more1 && !mbar_wait_warp(&k_full[st ^ 1], ((j + 1) >> 1) & 1, &g_tc_err)) {
+                    if (more1 &&
+                        !mbar_wait_warp(&k_full[ks], ((j + 1) / kKStages) & 1, &g_tc_err)) {
                         ok = false;
                         break;
                     }
                     if (more0) {
                         tc::fence_after_sync();
-                        mma1(0, st ^ 1);  // in order after mma2(0): P_0 is read before D_0 is rewritten
+                        mma1(0, ks);  // in order after mma2(0): P_0 is read before D_0 is rewritten
                         tc::commit(&s_full[0]);
                     }
                     if (!mbar_wait_warp(&p_full[1], j & 1, &g_tc_err)) {
@@ -351,12 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc::fence_after_sync();
-                    mma2(1, st, j == 0);
-                    tc::commit(&v_empty[st]);
+                    mma2(1, vs, j == 0);
+                    tc::commit(&v_empty[vs]);
                     if (more1) {
-                        mma1(1, st ^ 1);
+                        mma1(1, ks);
                         tc::commit(&s_full[1]);
-                        tc::commit(&k_empty[st ^ 1]);
+                        tc::commit(&k_empty[ks]);
                     }
                 }
                 tc::commit(o_full);
@@ -416,18 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 sv[b][x] = __float_as_uint(-INFINITY);
                         }
                 }
-                // row max: four independent chains of three-input max
-                float c0 = -INFINITY, c1 = -INFINITY, c2 = -INFINITY, c3 = -INFINITY;
-#pragma unroll
-                for (int b = 0; b < 2; ++b)
-#pragma unroll
-                    for (int x = 0; x < 32; x += 8) {
-                        c0 = fmax3(c0, __uint_as_float(sv[b][x]), __uint_as_float(sv[b][x + 1]));
-                        c1 = fmax3(c1, __uint_as_float(sv[b][x + 2]), __uint_as_float(sv[b][x + 3]));
-                        c2 = fmax3(c2, __uint_as_float(sv[b][x + 4]), __uint_as_float(sv[b][x + 5]));
-                        c3 = fmax3(c3, __uint_as_float(sv[b][x + 6]), __uint_as_float(sv[b][x + 7]));
-                    }
-                float mx = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3));
+                // row max: this thread's half of the row, then the other half's
+                float mx = max_blocks<2>(sv);
                 mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16)) * qs;
                 if (it == 0) {
                     m = mx;
@@ -607,17 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 sv[b][x] = __float_as_uint(-INFINITY);
                         }
                 }
-                float c0 = -INFINITY, c1 = -INFINITY, c2 = -INFINITY, c3 = -INFINITY;
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-#pragma unroll
-                    for (int x = 0; x < 32; x += 8) {
-                        c0 = fmax3(c0, __uint_as_float(sv[b][x]), __uint_as_float(sv[b][x + 1]));
-                        c1 = fmax3(c1, __uint_as_float(sv[b][x + 2]), __uint_as_float(sv[b][x + 3]));
-                        c2 = fmax3(c2, __uint_as_float(sv[b][x + 4]), __uint_as_float(sv[b][x + 5]));
-                        c3 = fmax3(c3, __uint_as_float(sv[b][x + 6]), __uint_as_float(sv[b][x + 7]));
-                    }
-                const float mx = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * qs;
+                const float mx = max_blocks<4>(sv) * qs;
                 if (it == 0) {
                     m = mx;
                 } else if (__any_sync(kFullMask, mx > m + kRescaleThreshold)) {
