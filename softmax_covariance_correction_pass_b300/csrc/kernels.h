@@ -99,6 +99,9 @@ unsigned lla_take_error();
 // box `box`, 128-byte swizzle, out-of-range elements read as zero.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                     const uint64_t* strides_bytes, const uint32_t* box);
+// The same for an fp32 tensor (box[0] * 4 bytes must be 128: one swizzle row).
+bool make_tmap_f32(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box);
 
 // ---------------------------------------------------------------- q/k/v/probe projection
 struct ProjShape {

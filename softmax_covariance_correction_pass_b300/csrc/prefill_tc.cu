@@ -99,7 +99,14 @@ struct PairLayout {
     static constexpr int B_SFULL = B_VEMPTY + kVStages;
     static constexpr int B_PFULL = B_SFULL + 2;
     static constexpr int B_OFULL = B_PFULL + 2;
-    static constexpr int NBARS = B_OFULL + 1;
+    static constexpr int B_STAGED = B_OFULL + 1;  // [2]: a sub-tile's output is in shared memory
+    static constexpr int NBARS = B_STAGED + 2;
+    // Epilogue: once every MMA has completed, the K/V rings are free and hold each sub-tile's
+    // fp32 output as boxes of [QROWS rows x 32 columns] (128 bytes a row, 128-byte swizzle),
+    // which TMA stores write to o.
+    static constexpr int OUT_BOX = QROWS * 128;
+    static constexpr int OUT_OFF = K_OFF;
+    static_assert(2 * (D / 32) * OUT_BOX <= BAR_OFF - K_OFF, "output staging fits the rings");
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     __host__ __device__ static constexpr uint32_t dcol(int sub) { return 128u * sub; }
@@ -183,7 +190,7 @@ template <int D, bool CAUSAL, bool RHO>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmR,
                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                        const TcArgs a) {
+                        const __grid_constant__ CUtensorMap tmO, const TcArgs a) {
     using LY = PairLayout<D, RHO>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -197,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* s_full = bars + LY::B_SFULL;
     uint64_t* p_full = bars + LY::B_PFULL;
     uint64_t* o_full = bars + LY::B_OFULL;
+    uint64_t* staged = bars + LY::B_STAGED;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -227,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < LY::NBARS; ++b)
-            mbar_init(&bars[b], (b == LY::B_PFULL || b == LY::B_PFULL + 1) ? 128 : 1);
+            mbar_init(&bars[b], (b == LY::B_PFULL || b == LY::B_PFULL + 1 || b == LY::B_STAGED ||
+                                 b == LY::B_STAGED + 1) ? 128 : 1);
         *abort_flag = (*(volatile unsigned*)&g_tc_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
         fence_mbar_init();
     }
@@ -236,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (RHO) tc::prefetch_tmap(&tmR);
         tc::prefetch_tmap(&tmK);
         tc::prefetch_tmap(&tmV);
+        tc::prefetch_tmap(&tmO);
     }
     if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
     tc::fence_before_sync();
@@ -572,13 +582,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---- epilogue: o = U/l - (W/l - (A/l)(U/l)) = ((U (1 + A/l)) - W) / l
             const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_tc_err);
+            const int rl = 16 * g + (lane & 15);  // row within the sub-tile
+            unsigned char* stage = smem + LY::OUT_OFF + sub * (D / 32) * LY::OUT_BOX;
             if (__all_sync(kFullMask, done)) {
                 tc::fence_after_sync();
                 const float lt = l + __shfl_xor_sync(kFullMask, l, 16);
                 const float At = A + __shfl_xor_sync(kFullMask, A, 16);
                 const float inv_l = 1.f / lt;
                 const float gain = 1.f + At * inv_l;
-                float* orow = a.o + ((size_t)bh * a.L + i) * D + h * (D / 2);
                 const bool row_ok =
                     i < a.L && in_bounds(&g_tc_err, ((size_t)bh * a.L + i + 1) * D, (size_t)a.BH * a.L * D);
 #pragma unroll 1
@@ -587,25 +598,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::tmem_ld32_split<D / 2>(tU + 32 * b, u);
                     tc::tmem_ld32_split<D / 2>(tW + 32 * b, w);
                     tc::tmem_ld_wait();
-                    if (row_ok) {
+                    // columns h D/2 + 32 b .. : 32-column box h (D/64) + b
+                    unsigned char* box = stage + (h * (D / 64) + b) * LY::OUT_BOX + rl * 128;
 #pragma unroll
-                        for (int x = 0; x < 32; x += 4) {
-                            float out[4];
+                    for (int x = 0; x < 8; ++x) {
+                        float out[4];
 #pragma unroll
-                            for (int y = 0; y < 4; ++y)
-                                out[y] = (__uint_as_float(u[x + y]) * gain - __uint_as_float(w[x + y])) *
-                                         inv_l;
-                            *reinterpret_cast<float4*>(orow + 32 * b + x) =
-                                make_float4(out[0], out[1], out[2], out[3]);
-                        }
-                        if (a.mu) {
-                            float* mrow = a.mu + ((size_t)bh * a.L + i) * D + h * (D / 2);
+                        for (int y = 0; y < 4; ++y)
+                            out[y] = (__uint_as_float(u[4 * x + y]) * gain - __uint_as_float(w[4 * x + y])) *
+                                     inv_l;
+                        *reinterpret_cast<float4*>(box + ((x ^ (rl & 7)) << 4)) =
+                            make_float4(out[0], out[1], out[2], out[3]);
+                    }
+                    if (a.mu && row_ok) {
+                        float* mrow = a.mu + ((size_t)bh * a.L + i) * D + h * (D / 2);
 #pragma unroll
-                            for (int x = 0; x < 32; x += 4)
-                                *reinterpret_cast<float4*>(mrow + 32 * b + x) = make_float4(
-                                    __uint_as_float(u[x]) * inv_l, __uint_as_float(u[x + 1]) * inv_l,
-                                    __uint_as_float(u[x + 2]) * inv_l, __uint_as_float(u[x + 3]) * inv_l);
-                        }
+                        for (int x = 0; x < 32; x += 4)
+                            *reinterpret_cast<float4*>(mrow + 32 * b + x) = make_float4(
+                                __uint_as_float(u[x]) * inv_l, __uint_as_float(u[x + 1]) * inv_l,
+                                __uint_as_float(u[x + 2]) * inv_l, __uint_as_float(u[x + 3]) * inv_l);
                     }
                 }
                 if (a.lse && h == 0 && row_ok) {
@@ -614,6 +625,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 *abort_flag = 1;
+            }
+            // every thread of the sub-tile arrives, whichever way it went; one thread then
+            // stores the sub-tile's rows (rows past L are clipped by the tensor map)
+            tc::fence_proxy_async_smem();
+            mbar_arrive(&staged[sub]);
+            if (g == 0 && lane == 0 && mbar_wait(&staged[sub], 0, &g_tc_err) && !*abort_flag) {
+#pragma unroll 1
+                for (int cb = 0; cb < D / 32; ++cb)
+                    tc::tma_store_3d(&tmO, 32 * cb, first_row, bh, stage + cb * LY::OUT_BOX);
+                tc::bulk_commit_group();
+                tc::bulk_wait_group_read0();
             }
         } else {
             // ------------------------------------------------ W_R = 0: one query row per thread
@@ -678,10 +700,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // ---- epilogue: o = U / l
             const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_tc_err);
+            const int rl = 32 * g + lane;  // row within the sub-tile
+            unsigned char* stage = smem + LY::OUT_OFF + sub * (D / 32) * LY::OUT_BOX;
             if (__all_sync(kFullMask, done)) {
                 tc::fence_after_sync();
                 const float inv_l = 1.f / l;
-                float* orow = a.o + ((size_t)bh * a.L + i) * D;
                 const bool row_ok =
                     i < a.L && in_bounds(&g_tc_err, ((size_t)bh * a.L + i + 1) * D, (size_t)a.BH * a.L * D);
 #pragma unroll 1
@@ -689,16 +712,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t u[32];
                     tc::tmem_ld32(tU + 32 * b, u);
                     tc::tmem_ld_wait();
-                    if (row_ok) {
+                    unsigned char* box = stage + b * LY::OUT_BOX + rl * 128;
 #pragma unroll
-                        for (int x = 0; x < 32; x += 4) {
-                            const float4 v4 = make_float4(
-                                __uint_as_float(u[x]) * inv_l, __uint_as_float(u[x + 1]) * inv_l,
-                                __uint_as_float(u[x + 2]) * inv_l, __uint_as_float(u[x + 3]) * inv_l);
-                            *reinterpret_cast<float4*>(orow + 32 * b + x) = v4;
-                            if (a.mu)
-                                *reinterpret_cast<float4*>(a.mu + ((size_t)bh * a.L + i) * D + 32 * b + x) = v4;
-                        }
+                    for (int x = 0; x < 8; ++x) {
+                        const float4 v4 = make_float4(
+                            __uint_as_float(u[4 * x]) * inv_l, __uint_as_float(u[4 * x + 1]) * inv_l,
+                            __uint_as_float(u[4 * x + 2]) * inv_l, __uint_as_float(u[4 * x + 3]) * inv_l);
+                        *reinterpret_cast<float4*>(box + ((x ^ (rl & 7)) << 4)) = v4;
+                        if (a.mu && row_ok)
+                            *reinterpret_cast<float4*>(a.mu + ((size_t)bh * a.L + i) * D + 32 * b + 4 * x) = v4;
                     }
                 }
                 if (a.lse && row_ok) {
@@ -707,6 +729,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 *abort_flag = 1;
+            }
+            tc::fence_proxy_async_smem();
+            mbar_arrive(&staged[sub]);
+            if (g == 0 && lane == 0 && mbar_wait(&staged[sub], 0, &g_tc_err) && !*abort_flag) {
+#pragma unroll 1
+                for (int cb = 0; cb < D / 32; ++cb)
+                    tc::tma_store_3d(&tmO, 32 * cb, first_row, bh, stage + cb * LY::OUT_BOX);
+                tc::bulk_commit_group();
+                tc::bulk_wait_group_read0();
             }
         }
     }
@@ -731,13 +762,14 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int L, int D, int box_ro
 
 template <int D, bool CAUSAL, bool RHO>
 cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mr, const CUtensorMap& mk,
-                   const CUtensorMap& mv, const TcArgs& a, cudaStream_t stream) {
+                   const CUtensorMap& mv, const CUtensorMap& mo, const TcArgs& a,
+                   cudaStream_t stream) {
     using LY = PairLayout<D, RHO>;
     auto kern = prefill_pair_kernel<D, CAUSAL, RHO>;
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = ensure_dynamic_smem(kern, (int)LY::SMEM_BYTES, smem_set)) return e;
     const unsigned grid = (unsigned)((size_t)a.n_qb * a.BH);
-    kern<<<grid, kThreads, LY::SMEM_BYTES, stream>>>(mq, mr, mk, mv, a);
+    kern<<<grid, kThreads, LY::SMEM_BYTES, stream>>>(mq, mr, mk, mv, mo, a);
     return cudaGetLastError();
 }
 
@@ -749,8 +781,14 @@ cudaError_t launch_d(const PrefillShape& s, const CUtensorMap& mq, const CUtenso
     using LY = PairLayout<D, RHO>;
     const TcArgs a{o,      cache_lens, s.L,    Lcap,  s.H,  s.B * s.H, (s.L + LY::BLOCK - 1) / LY::BLOCK,
                    s.scale * kLog2e, ts.lse, ts.rbar, ts.mu};
-    return s.causal ? launch<D, true, RHO>(mq, mr, mk, mv, a, stream)
-                    : launch<D, false, RHO>(mq, mr, mk, mv, a, stream);
+    // o [B*H, L, D] fp32 for the TMA stores of the epilogue: boxes of 32 columns x QROWS rows
+    CUtensorMap mo;
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)s.L, (uint64_t)s.B * s.H};
+    const uint64_t strides[2] = {(uint64_t)D * 4, (uint64_t)s.L * D * 4};
+    const uint32_t box[3] = {32, (uint32_t)LY::QROWS, 1};
+    if (!make_tmap_f32(&mo, o, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    return s.causal ? launch<D, true, RHO>(mq, mr, mk, mv, mo, a, stream)
+                    : launch<D, false, RHO>(mq, mr, mk, mv, mo, a, stream);
 }
 
 // Query-side maps (q, rho: L rows per head) and key-side maps (k, v: Lcap rows per head).

@@ -26,6 +26,31 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int
         : "memory");
 }
 
+// 3-D tiled store of box {x, y, z} from shared memory (bulk async group; elements of the
+// box that fall outside the tensor are not written).  The shared-memory writes it reads
+// must be made visible to the async proxy first (fence_proxy_async_smem).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, int x, int y, int z,
+                                             const void* src) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(m),
+        "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until the committed bulk stores have read their shared memory (the CTA may then
+// reuse it, or exit).
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 2-D tiled load of box {x, y} into shared memory.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int x, int y,
                                             uint64_t* bar) {

@@ -1,5 +1,5 @@
-// Tensor-map (TMA descriptor) encoding for the bf16 operands of the tcgen05
-// kernels.  cuTensorMapEncodeTiled is a driver entry point; it is looked up
+// Tensor-map (TMA descriptor) encoding for the bf16 operands and the fp32
+// outputs of the tcgen05 kernels.  cuTensorMapEncodeTiled is a driver entry point; it is looked up
 // once through the runtime so that the library does not link libcuda.
 #include <cuda.h>
 
@@ -28,8 +28,9 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                    const uint64_t* strides_bytes, const uint32_t* box) {
+namespace {
+bool make_tmap(CUtensorMapDataType dtype, CUtensorMap* m, const void* base, int rank,
+               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
     EncodeTiledFn fn = encode_fn();
     if (!fn || rank < 1 || rank > 5) return false;
     cuuint64_t d[5], s[4];
@@ -40,9 +41,20 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* 
         e[i] = 1;
         if (i + 1 < rank) s[i] = strides_bytes[i];
     }
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, s,
-              b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return fn(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, e,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box) {
+    return make_tmap(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m, base, rank, dims, strides_bytes, box);
+}
+
+bool make_tmap_f32(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box) {
+    return make_tmap(CU_TENSOR_MAP_DATA_TYPE_FLOAT32, m, base, rank, dims, strides_bytes, box);
 }
 
 }  // namespace parallax
