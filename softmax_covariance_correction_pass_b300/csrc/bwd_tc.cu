@@ -179,8 +179,13 @@ struct KvLayout {
     static constexpr int RS_OFF = G_OFF + 3 * SUB;
     static constexpr int BAR_OFF = RS_OFF + 2 * 1024;
     // kv_full, v_ready, qr_full[S], qr_empty[S], s_full, y_free, p_full, g_done, o_full,
-    // rs_full[2], rs_free[2]
-    static constexpr int NBARS = 2 + 2 * kKvStages + 9;
+    // rs_full[2], rs_free[2], staged
+    static constexpr int B_STAGED = 2 + 2 * kKvStages + 9;
+    static constexpr int NBARS = B_STAGED + 1;
+    // Epilogue: once every MMA has completed, the query-side ring holds dV and dK as
+    // [128 keys x 32 columns] fp32 boxes (128-byte swizzle) for TMA stores.
+    static constexpr int OUT_BOX = 128 * 128;
+    static_assert(2 * (D / 32) * OUT_BOX <= kKvStages * STAGE, "dK/dV staging fits the ring");
     // the buffers start at the (1024-byte aligned) base of dynamic shared memory
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16;
     static_assert(OPB <= 3 * SUB, "the V tile must fit in the gradient-operand area");
@@ -192,7 +197,8 @@ template <int D, bool CAUSAL, bool RHO>
 __global__ void __launch_bounds__(kKvThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmR,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmO, const BwdArgs a) {
+                  const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmDV,
+                  const __grid_constant__ CUtensorMap tmDK, const BwdArgs a) {
     using LY = KvLayout<D>;
     constexpr int S = kKvStages;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -214,6 +220,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     uint64_t* o_full = bars + 6 + 2 * S;
     uint64_t* rs_full = bars + 7 + 2 * S;  // [2] statistics slot loaded
     uint64_t* rs_free = bars + 9 + 2 * S;  // [2] statistics slot read (256 arrivals)
+    uint64_t* staged = bars + LY::B_STAGED;  // dV, dK staged for the TMA stores (256 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -234,7 +241,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         for (int b = 0; b < LY::NBARS; ++b) {
             uint32_t count = 1;
             if (b == 1) count = 128;
-            if (b == 3 + 2 * S || b == 4 + 2 * S || b == 9 + 2 * S || b == 10 + 2 * S)
+            if (b == 3 + 2 * S || b == 4 + 2 * S || b == 9 + 2 * S || b == 10 + 2 * S ||
+                b == LY::B_STAGED)
                 count = kComputeThreads;
             mbar_init(&bars[b], count);
         }
@@ -247,6 +255,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tc::prefetch_tmap(&tmK);
         tc::prefetch_tmap(&tmV);
         tc::prefetch_tmap(&tmO);
+        tc::prefetch_tmap(&tmDV);
+        tc::prefetch_tmap(&tmDK);
     }
     if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
     tc::fence_before_sync();
@@ -518,28 +528,38 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mbar_arrive(p_full);
         }
         const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
+        // half 0 stages dV, half 1 dK, each row into [128 keys x 32 columns] boxes
+        unsigned char* stage = smem + LY::ST_OFF + c * (D / 32) * LY::OUT_BOX;
         if (__all_sync(kFullMask, done)) {
             tc::fence_after_sync();
-            // half 0 stores dV, half 1 dK
-            float* orow = (c == 0 ? a.dv : a.dk) + ((size_t)bh * a.L + j) * D;
             const uint32_t base = trow + (c == 0 ? LY::DV : LY::DK);
-            const bool row_ok =
-                j < a.L && in_bounds(&g_bwd_err, ((size_t)bh * a.L + j + 1) * D, (size_t)a.BH * a.L * D);
 #pragma unroll 1
             for (int b = 0; b < D / 32; ++b) {
                 uint32_t u[32];
                 tc::tmem_ld32(base + 32 * b, u);
                 tc::tmem_ld_wait();
-                if (row_ok) {
+                unsigned char* box = stage + b * LY::OUT_BOX + row * 128;
 #pragma unroll
-                    for (int x = 0; x < 32; x += 4)
-                        *reinterpret_cast<float4*>(orow + 32 * b + x) =
-                            make_float4(__uint_as_float(u[x]), __uint_as_float(u[x + 1]),
-                                        __uint_as_float(u[x + 2]), __uint_as_float(u[x + 3]));
-                }
+                for (int x = 0; x < 8; ++x)
+                    st_shared_v4(smem_u32(box + ((x ^ (row & 7)) << 4)), u[4 * x], u[4 * x + 1],
+                                 u[4 * x + 2], u[4 * x + 3]);
             }
         } else {
             *abort_flag = 1;
+        }
+        // every compute thread arrives, whichever way it went; one thread then stores the
+        // tile's dV and dK rows (rows past L are clipped by the tensor maps)
+        fence_proxy_async_smem();
+        mbar_arrive(staged);
+        if (warp == 2 && lane == 0 && mbar_wait(staged, 0, &g_bwd_err) && !*abort_flag) {
+            unsigned char* st0 = smem + LY::ST_OFF;
+#pragma unroll 1
+            for (int b = 0; b < D / 32; ++b) {
+                tc::tma_store_3d(&tmDV, 32 * b, k0, bh, st0 + b * LY::OUT_BOX);
+                tc::tma_store_3d(&tmDK, 32 * b, k0, bh, st0 + (D / 32 + b) * LY::OUT_BOX);
+            }
+            tc::bulk_commit_group();
+            tc::bulk_wait_group_read0();
         }
     }
 
@@ -578,9 +598,13 @@ struct QLayout {
     static constexpr int QR_OFF = K_OFF + (Q_KSTAGES - 1) * OPB;
     static constexpr int BAR_OFF = V_OFF + Q_VSTAGES * OPB;
     // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full, y_free, p_full,
-    // pk_empty, o_full, qr_in
+    // pk_empty, o_full, qr_in, staged
     static constexpr int B_S = 1 + 2 * Q_KSTAGES + 2 * Q_VSTAGES;
-    static constexpr int NBARS = B_S + 6;
+    static constexpr int NBARS = B_S + 7;
+    // Epilogue: once every MMA has completed, the K ring holds dQ and drho as
+    // [64 queries x 32 columns] fp32 boxes (128-byte swizzle) for TMA stores.
+    static constexpr int OUT_BOX = 64 * 128;
+    static_assert(2 * (D / 32) * OUT_BOX <= (Q_KSTAGES + Q_VSTAGES) * OPB, "dQ staging fits the rings");
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
     // TMEM columns: [S; R] at 0, D at YD, the accumulator at O, the packed slot at PK,
     // [Q; rho] (bf16 pairs) at QA
@@ -591,7 +615,8 @@ template <int D, bool CAUSAL, bool RHO>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmR,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                 const __grid_constant__ CUtensorMap tmO, const BwdArgs a) {
+                 const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmDQ,
+                 const __grid_constant__ CUtensorMap tmDR, const BwdArgs a) {
     using LY = QLayout<D>;
     constexpr int KS = Q_KSTAGES, VS = Q_VSTAGES;
     extern __shared__ unsigned char smem_raw[];
@@ -609,6 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* pk_empty = bars + LY::B_S + 3;  // packed slot read by its dQ MMAs
     uint64_t* o_full = bars + LY::B_S + 4;
     uint64_t* qr_in = bars + LY::B_S + 5;     // [Q; rho] copied to TMEM (128 arrivals)
+    uint64_t* staged = bars + LY::B_S + 6;    // dQ, drho staged for the TMA stores (256 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -627,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < LY::NBARS; ++b) {
             uint32_t count = 1;
-            if (b == LY::B_S + 1 || b == LY::B_S + 2) count = kComputeThreads;
+            if (b == LY::B_S + 1 || b == LY::B_S + 2 || b == LY::B_S + 6) count = kComputeThreads;
             if (b == LY::B_S + 5) count = 128;
             mbar_init(&bars[b], count);
         }
@@ -879,30 +905,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(p_full);
         }
         const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_bwd_err);
+        // set 0 stages dQ (query lanes), set 1 drho (probe lanes): columns h D/2 + 32 b of
+        // row rl go to the [64 queries x 32 columns] box h (D/64) + b of the set
+        const int rl = 16 * g + (lane & 15);
+        unsigned char* stage = smem + LY::K_OFF + set * (D / 32) * LY::OUT_BOX;
         if (__all_sync(kFullMask, done)) {
             tc::fence_after_sync();
-            // set 0 stores dQ (query lanes), set 1 drho (probe lanes)
             if (set == 0 || RHO) {
-                float* orow = (set == 0 ? a.dq : a.drho) + ((size_t)bh * a.L + i) * D + h * (D / 2);
                 const uint32_t base = (set == 0 ? rowS : rowR) + LY::O;
-                const bool row_ok = i < a.L && in_bounds(&g_bwd_err, ((size_t)bh * a.L + i + 1) * D,
-                                                         (size_t)a.BH * a.L * D);
 #pragma unroll 1
                 for (int b = 0; b < D / 64; ++b) {
                     uint32_t u[32];
                     tc::tmem_ld32_split<D / 2>(base + 32 * b, u);
                     tc::tmem_ld_wait();
-                    if (row_ok) {
+                    unsigned char* box = stage + (h * (D / 64) + b) * LY::OUT_BOX + rl * 128;
 #pragma unroll
-                        for (int x = 0; x < 32; x += 4)
-                            *reinterpret_cast<float4*>(orow + 32 * b + x) =
-                                make_float4(__uint_as_float(u[x]), __uint_as_float(u[x + 1]),
-                                            __uint_as_float(u[x + 2]), __uint_as_float(u[x + 3]));
-                    }
+                    for (int x = 0; x < 8; ++x)
+                        st_shared_v4(smem_u32(box + ((x ^ (rl & 7)) << 4)), u[4 * x], u[4 * x + 1],
+                                     u[4 * x + 2], u[4 * x + 3]);
                 }
             }
         } else {
             *abort_flag = 1;
+        }
+        // every compute thread arrives, whichever way it went; one thread then stores the
+        // tile's rows (rows past L are clipped by the tensor maps)
+        fence_proxy_async_smem();
+        mbar_arrive(staged);
+        if (warp == 4 && lane == 0 && mbar_wait(staged, 0, &g_bwd_err) && !*abort_flag) {
+            unsigned char* st0 = smem + LY::K_OFF;
+#pragma unroll 1
+            for (int b = 0; b < D / 32; ++b) {
+                tc::tma_store_3d(&tmDQ, 32 * b, q0, bh, st0 + b * LY::OUT_BOX);
+                if (RHO) tc::tma_store_3d(&tmDR, 32 * b, q0, bh, st0 + (D / 32 + b) * LY::OUT_BOX);
+            }
+            tc::bulk_commit_group();
+            tc::bulk_wait_group_read0();
         }
     }
 
@@ -937,6 +975,18 @@ cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const v
         r32 = q32;
         r16 = q16;
     }
+    // the fp32 gradients [BH, L, D] for the epilogues' TMA stores: boxes of 32 columns x 128
+    // keys (dK, dV) or x 64 queries (dQ, drho)
+    CUtensorMap dk128, dv128, dq64, dr64;
+    auto grad_map = [&](CUtensorMap* m, const float* base, int rows) {
+        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.L, (uint64_t)a.BH};
+        const uint64_t strides[2] = {(uint64_t)D * 4, (uint64_t)a.L * D * 4};
+        const uint32_t box[3] = {32, (uint32_t)rows, 1};
+        return make_tmap_f32(m, base, 3, dims, strides, box);
+    };
+    if (!grad_map(&dk128, a.dk, 128) || !grad_map(&dv128, a.dv, 128) ||
+        !grad_map(&dq64, a.dq, 64) || !grad_map(&dr64, RHO ? a.drho : a.dq, 64))
+        return cudaErrorInvalidValue;
     static std::atomic<uint64_t> kv_smem_set{0}, q_smem_set{0};
     cudaError_t e = ensure_dynamic_smem(bwd_kv_kernel<D, CAUSAL, RHO>, KvLayout<D>::SMEM_BYTES,
                                         kv_smem_set);
@@ -946,9 +996,11 @@ cudaError_t launch_all(const BwdArgs& a, const void* q, const void* rho, const v
     const size_t rows = (size_t)a.BH * a.Lp;
     bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
     bwd_kv_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_kt * a.BH), kKvThreads,
-                                    KvLayout<D>::SMEM_BYTES, stream>>>(q32, r32, k128, v128, o32, a);
+                                    KvLayout<D>::SMEM_BYTES, stream>>>(q32, r32, k128, v128, o32,
+                                                                       dv128, dk128, a);
     bwd_q_kernel<D, CAUSAL, RHO><<<(unsigned)((size_t)a.n_qt * a.BH), kThreads,
-                                   QLayout<D>::SMEM_BYTES, stream>>>(q16, r16, k128, v128, o32, a);
+                                   QLayout<D>::SMEM_BYTES, stream>>>(q16, r16, k128, v128, o32,
+                                                                     dq64, dr64, a);
     return cudaGetLastError();
 }
 
