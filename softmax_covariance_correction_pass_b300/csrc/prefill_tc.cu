@@ -233,19 +233,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n0 = CAUSAL ? min(n1, (off + q0 + LY::QROWS - 1) / BN + 1) : n_all;
     const bool precise = RHO && n1 == 1;
 
+    // The first Q, K and V loads go out before the CTA-wide set-up (TMEM allocation and
+    // the barrier below): thread 0 initialises the barriers and issues them, and the
+    // producer loops continue after these tiles.
+    const int k_pre = min(n1, kKStages), v_pre = min(n1, kVStages);
     if (threadIdx.x == 0) {
         for (int b = 0; b < LY::NBARS; ++b)
             mbar_init(&bars[b], (b == LY::B_PFULL || b == LY::B_PFULL + 1 || b == LY::B_STAGED ||
                                  b == LY::B_STAGED + 1) ? 128 : 1);
-        *abort_flag = (*(volatile unsigned*)&g_tc_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
+        const bool abort0 = (*(volatile unsigned*)&g_tc_err & PARALLAX_DEVERR_WAIT_TIMEOUT) != 0;
+        *abort_flag = abort0 ? 1 : 0;
         fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tmQ);
         if (RHO) tc::prefetch_tmap(&tmR);
         tc::prefetch_tmap(&tmK);
         tc::prefetch_tmap(&tmV);
         tc::prefetch_tmap(&tmO);
+        if (!abort0) {
+            mbar_arrive_expect_tx(q_full, 2 * LY::OP_BYTES);
+            for (int sub = 0; sub < 2; ++sub)
+                for (int cb = 0; cb < LY::NCB; ++cb) {
+                    unsigned char* dst = smem + LY::QR_OFF + sub * LY::OP_BYTES + cb * LY::SUB_BYTES;
+                    if (RHO) {
+                        for (int g = 0; g < 4; ++g) {
+                            const int row = q0 + 64 * sub + 16 * g;
+                            tc::tma_load_3d(dst + (32 * g) * 128, &tmQ, cb * 64, row, bh, q_full);
+                            tc::tma_load_3d(dst + (32 * g + 16) * 128, &tmR, cb * 64, row, bh, q_full);
+                        }
+                    } else {
+                        tc::tma_load_3d(dst, &tmQ, cb * 64, q0 + 128 * sub, bh, q_full);
+                    }
+                }
+            for (int j = 0; j < k_pre; ++j) {
+                mbar_arrive_expect_tx(&k_full[j], LY::OP_BYTES);
+                for (int cb = 0; cb < LY::NCB; ++cb)
+                    tc::tma_load_3d(smem + LY::K_OFF + j * LY::OP_BYTES + cb * LY::SUB_BYTES, &tmK,
+                                    cb * 64, j * BN, bh, &k_full[j]);
+            }
+            for (int j = 0; j < v_pre; ++j) {
+                mbar_arrive_expect_tx(&v_full[j], LY::OP_BYTES);
+                for (int cb = 0; cb < LY::NCB; ++cb)
+                    tc::tma_load_3d(smem + LY::V_OFF + j * LY::OP_BYTES + cb * LY::SUB_BYTES, &tmV,
+                                    cb * 64, j * BN, bh, &v_full[j]);
+            }
+        }
     }
     if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
     tc::fence_before_sync();
@@ -256,27 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) {
         tc::setmaxnreg_dec<kRegsSupport>();
         if (warp == 0) {
-            // ------------------------------------------------------------ TMA producer: Q, K
+            // ------------------------------------------------------------ TMA producer: K
+            // (Q and the first k_pre K tiles went out at set-up)
             if (lane == 0 && !skip) {
                 const int z = bh;
                 bool ok = true;
-                int kj = 0;  // K tiles issued
-                mbar_arrive_expect_tx(q_full, 2 * LY::OP_BYTES);
-                for (int sub = 0; sub < 2; ++sub)
-                    for (int cb = 0; cb < LY::NCB; ++cb) {
-                        unsigned char* dst = smem + LY::QR_OFF + sub * LY::OP_BYTES + cb * LY::SUB_BYTES;
-                        if (RHO) {
-                            for (int g = 0; g < 4; ++g) {
-                                const int row = q0 + 64 * sub + 16 * g;
-                                tc::tma_load_3d(dst + (32 * g) * 128, &tmQ, cb * 64, row, z, q_full);
-                                tc::tma_load_3d(dst + (32 * g + 16) * 128, &tmR, cb * 64, row, z,
-                                                q_full);
-                            }
-                        } else {
-                            tc::tma_load_3d(dst, &tmQ, cb * 64, q0 + 128 * sub, z, q_full);
-                        }
-                    }
-                for (int j = 0; j < n1; ++j) {
+                int kj = k_pre;  // K tiles issued
+                for (int j = k_pre; j < n1; ++j) {
                     const int st = j % kKStages;
                     if (j >= kKStages &&
                         !mbar_wait(&k_empty[st], (j / kKStages - 1) & 1, &g_tc_err)) {
@@ -299,10 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (warp == 2) {
             // ------------------------------------------------------------ TMA producer: V
+            // (the first v_pre V tiles went out at set-up)
             if (lane == 0 && !skip) {
                 bool ok = true;
-                int vj = 0;  // V tiles issued
-                for (int j = 0; j < n1; ++j) {
+                int vj = v_pre;  // V tiles issued
+                for (int j = v_pre; j < n1; ++j) {
                     const int st = j % kVStages;
                     if (j >= kVStages &&
                         !mbar_wait(&v_empty[st], (j / kVStages - 1) & 1, &g_tc_err)) {
@@ -632,8 +650,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&staged[sub]);
             if (g == 0 && lane == 0 && mbar_wait(&staged[sub], 0, &g_tc_err) && !*abort_flag) {
 #pragma unroll 1
+                const uint64_t pol = l2_evict_first_policy();
                 for (int cb = 0; cb < D / 32; ++cb)
-                    tc::tma_store_3d(&tmO, 32 * cb, first_row, bh, stage + cb * LY::OUT_BOX);
+                    tc::tma_store_3d_hint(&tmO, 32 * cb, first_row, bh, stage + cb * LY::OUT_BOX, pol);
                 tc::bulk_commit_group();
                 tc::bulk_wait_group_read0();
             }
@@ -734,8 +753,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&staged[sub]);
             if (g == 0 && lane == 0 && mbar_wait(&staged[sub], 0, &g_tc_err) && !*abort_flag) {
 #pragma unroll 1
+                const uint64_t pol = l2_evict_first_policy();
                 for (int cb = 0; cb < D / 32; ++cb)
-                    tc::tma_store_3d(&tmO, 32 * cb, first_row, bh, stage + cb * LY::OUT_BOX);
+                    tc::tma_store_3d_hint(&tmO, 32 * cb, first_row, bh, stage + cb * LY::OUT_BOX, pol);
                 tc::bulk_commit_group();
                 tc::bulk_wait_group_read0();
             }

@@ -37,6 +37,17 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, int x, int y,
         : "memory");
 }
 
+// The same with an L2 cache-eviction policy (e.g. evict-first for outputs nothing reads
+// back soon, so that their dirty lines leave L2 early instead of crowding later work).
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* m, int x, int y, int z,
+                                                  const void* src, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint "
+        "[%0, {%1, %2, %3}], [%4], %5;" ::"l"(m),
+        "r"(x), "r"(y), "r"(z), "r"(smem_u32(src)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

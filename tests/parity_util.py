@@ -24,14 +24,22 @@ def errors(got, ref):
     return rel, float(np.abs(diff).max()) if diff.size else 0.0
 
 
+def report(what, rel, mx, ref=None):
+    """One line per comparison, for the parity record a `pytest -s` run prints."""
+    top = f" max|ref| {float(np.abs(to_np(ref)).max()):.3g}" if ref is not None else ""
+    print(f"PARITY {what}: rel-L2 {rel:.3e} max-abs {mx:.3e}{top}")
+
+
 def assert_f32(got, ref, what=""):
     rel, mx = errors(got, ref)
+    report(what, rel, mx, ref)
     assert rel <= TOL_F32_REL, f"{what}: rel-L2 {rel:.3e} > {TOL_F32_REL} (max-abs {mx:.3e})"
     return rel, mx
 
 
 def assert_bf16(got, ref, what=""):
     rel, mx = errors(got, ref)
+    report(what, rel, mx, ref)
     assert rel <= TOL_BF16_REL and mx <= TOL_BF16_ABS, \
         f"{what}: rel-L2 {rel:.3e} (<= {TOL_BF16_REL}), max-abs {mx:.3e} (<= {TOL_BF16_ABS})"
     return rel, mx

@@ -52,6 +52,7 @@ def test_lla_decode_layer_size_sampled():
             sl = (slice(int(b), int(b) + 1), slice(int(h), int(h) + 1))
             ro, rr = oracle.lla_decode(inp.q[sl], inp.k_cache[sl], inp.v_cache[sl],
                                        inp.seqlens[int(b):int(b) + 1])
-            rel, _ = errors(rho[sl], rr)
+            rel, mxr = errors(rho[sl], rr)
+            print(f"PARITY lla probe b={b} h={h}: rel-L2 {rel:.3e} max-abs {mxr:.3e}")
             assert rel <= 1e-3, f"probe b={b} h={h} rel-L2 {rel:.3e}"
             assert_bf16(o[sl], ro, f"lla o b={b} h={h}")
