@@ -511,6 +511,8 @@ def run_ours(args):
         pre_flops /= 2
     chunk = px.parallax_attn_decode_chunk_keys(B, H, n, d, 2)
     dec_launches = 2 if chunk < n else 1
+    dec_kernel = px.parallax_attn_decode_plan_kernel(B, H, H, n, d)
+    dec_kernels = (dec_kernel, "combine_kernel") if chunk < n else (dec_kernel,)
 
     run_decode = args.only in (None, "decode")
     run_prefill = args.only in (None, "prefill")
@@ -572,9 +574,9 @@ def run_ours(args):
 
     roof_dec = {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": dec_gbs / peaks["hbm_gbs"],
-                "traffic": traffic_of(TRAFFIC, "decode_kernel", "combine_kernel"),
-                "traffic_source": traffic_notes(TRAFFIC, "decode_kernel", "combine_kernel"),
-                "kernel": "decode_kernel (+ combine_kernel)",
+                "traffic": traffic_of(TRAFFIC, *dec_kernels),
+                "traffic_source": traffic_notes(TRAFFIC, *dec_kernels),
+                "kernel": " + ".join(dec_kernels),
                 "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_ms,
                 "peak_source": peaks["source"]}
     # the prefill launches take about a millisecond each inside a timed region of tens of

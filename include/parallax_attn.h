@@ -305,6 +305,15 @@ int parallax_attn_decode_chunk_keys(int B, int H, int Lmax, int d, int elem_byte
 int parallax_attn_decode_plan_keys(int B, int H, int H_kv, int Lmax, int d, int page_size);
 
 /*
+ * Which kernel the bf16 decode entry points run for this shape (same arguments and
+ * errors as parallax_attn_decode_plan_keys): 1 for the tensor-core kernel (warp-level
+ * MMAs on the stacked [q; rho] operand of a head group; grouped heads, and one head per
+ * key/value head when every CTA gets at least two work items of 512 keys or more), 0 for
+ * the SIMT kernel.  fp32 inputs always take the SIMT kernel.  Host-only.
+ */
+int parallax_attn_decode_plan_kernel(int B, int H, int H_kv, int Lmax, int d, int page_size);
+
+/*
  * Force the decode chunk size (keys, a positive multiple of 256) for later
  * calls in this process, or restore the automatic choice with 0.  Meant for
  * tests that exercise the combine path at small sizes.

@@ -71,6 +71,7 @@ def load_library() -> ctypes.CDLL:
                                                i32, i32, i32, vp]
     lib.parallax_attn_decode_chunk_keys.argtypes = [i32, i32, i32, i32, i32]
     lib.parallax_attn_decode_plan_keys.argtypes = [i32] * 6
+    lib.parallax_attn_decode_plan_kernel.argtypes = [i32] * 6
     lib.parallax_attn_qkvr_projection.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                   vp]
     lib.parallax_attn_set_decode_chunk_keys.argtypes = [i32]
@@ -87,7 +88,7 @@ def load_library() -> ctypes.CDLL:
                  "parallax_attn_prefill_train", "parallax_attn_prefill_backward",
                  "parallax_lla_decode",
                  "parallax_attn_decode_f32", "parallax_attn_decode_chunk_keys",
-                 "parallax_attn_decode_plan_keys",
+                 "parallax_attn_decode_plan_keys", "parallax_attn_decode_plan_kernel",
                  "parallax_attn_set_decode_chunk_keys", "parallax_attn_release_workspace",
                  "parallax_check_device_error", "parallax_version",
                  "parallax_selftest_wait_timeout", "parallax_workspace_guards_intact",
@@ -389,6 +390,16 @@ def parallax_attn_decode_plan_keys(B: int, H: int, H_kv: int, Lmax: int, d: int,
     if rc < 0:
         raise ParallaxError(rc, last_error())
     return rc
+
+
+def parallax_attn_decode_plan_kernel(B: int, H: int, H_kv: int, Lmax: int, d: int,
+                                     page_size: int = 0) -> str:
+    """The decode kernel the bf16 entry points run for this shape: "decode_mma_kernel" (tensor
+    cores) or "decode_kernel" (SIMT).  Host-only."""
+    rc = load_library().parallax_attn_decode_plan_kernel(B, H, H_kv, Lmax, d, page_size)
+    if rc < 0:
+        raise ParallaxError(rc, last_error())
+    return "decode_mma_kernel" if rc == 1 else "decode_kernel"
 
 
 def parallax_attn_set_decode_chunk_keys(keys: int) -> None:

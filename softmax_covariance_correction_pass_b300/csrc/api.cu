@@ -565,6 +565,18 @@ int parallax_attn_decode_plan_keys(int B, int H, int H_kv, int Lmax, int d, int 
     return plan.chunk;
 }
 
+int parallax_attn_decode_plan_kernel(int B, int H, int H_kv, int Lmax, int d, int page_size) {
+    const int chunk = parallax_attn_decode_plan_keys(B, H, H_kv, Lmax, d, page_size);
+    if (chunk < 0) return chunk;
+    int num_sms = 148;
+    if (DeviceState* ds = device_state(nullptr)) num_sms = ds->num_sms;
+    const int max_pages = page_size > 0 ? (Lmax + page_size - 1) / page_size : 0;
+    const parallax::DecodePlan plan =
+        make_plan(B, H, H_kv, Lmax, d, num_sms, page_size, max_pages, page_size > 0 ? 1 : 0);
+    succeed();
+    return parallax::decode_uses_mma(plan, true) ? 1 : 0;
+}
+
 int parallax_attn_set_decode_chunk_keys(int keys) {
     if (keys < 0 || keys % 256 != 0)
         return fail(PARALLAX_ERR_INVALID, "chunk keys %d must be 0 or a positive multiple of 256",

@@ -246,10 +246,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 count = kComputeThreads;
             mbar_init(&bars[b], count);
         }
-        *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
+        const bool abort0 = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) != 0;
+        *abort_flag = abort0 ? 1 : 0;
         fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tmQ);
         if (RHO) tc::prefetch_tmap(&tmR);
         tc::prefetch_tmap(&tmK);
@@ -257,6 +256,27 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tc::prefetch_tmap(&tmO);
         tc::prefetch_tmap(&tmDV);
         tc::prefetch_tmap(&tmDK);
+        // the key tile, V and the first query-side tiles go out before the CTA-wide set-up
+        // (TMEM allocation and the barrier below); the producer loop continues after them
+        if (!abort0) {
+            mbar_arrive_expect_tx(kv_full, 2 * LY::OPB);
+            for (int cb = 0; cb < LY::NCB; ++cb) {
+                tc::tma_load_3d(smem + LY::K_OFF + cb * SUB, &tmK, cb * 64, k0, bh, kv_full);
+                tc::tma_load_3d(smem + LY::G_OFF + cb * SUB, &tmV, cb * 64, k0, bh, kv_full);
+            }
+            for (int t = 0; t < min(n_t, S); ++t) {
+                const int q0 = (qt0 + t) * 64;
+                unsigned char* stage = smem + LY::ST_OFF + t * LY::STAGE;
+                mbar_arrive_expect_tx(&qr_full[t], (RHO ? 2 : 1) * LY::NCB * SUB64 + LY::DO_BYTES);
+                for (int cb = 0; cb < LY::NCB; ++cb) {
+                    tc::tma_load_3d(stage + cb * SUB, &tmQ, cb * 64, q0, bh, &qr_full[t]);
+                    if (RHO)
+                        tc::tma_load_3d(stage + cb * SUB + SUB64, &tmR, cb * 64, q0, bh, &qr_full[t]);
+                    tc::tma_load_3d(stage + LY::QR_BYTES + cb * SUB64, &tmO, cb * 64, q0, bh,
+                                    &qr_full[t]);
+                }
+            }
+        }
     }
     if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
     tc::fence_before_sync();
@@ -269,15 +289,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // ---------------------------------------------------------------- TMA producer
         // lane 0 streams the query-side tiles, lane 1 the row statistics: each waits only on
         // its own slots, so a statistics slot still in use never holds up a tile load
+        // (the key tile, V and the first min(n_t, S) query-side tiles went out at set-up)
         if (lane == 0 && !skip) {
-            mbar_arrive_expect_tx(kv_full, 2 * LY::OPB);
-            for (int cb = 0; cb < LY::NCB; ++cb) {
-                tc::tma_load_3d(smem + LY::K_OFF + cb * SUB, &tmK, cb * 64, k0, bh, kv_full);
-                tc::tma_load_3d(smem + LY::G_OFF + cb * SUB, &tmV, cb * 64, k0, bh, kv_full);
-            }
-            int issued = 0;
+            int issued = min(n_t, S);
             bool ok = true;
-            for (int t = 0; t < n_t; ++t) {
+            for (int t = issued; t < n_t; ++t) {
                 const int st = t % S;
                 if (t >= S && !mbar_wait(&qr_empty[st], ((t / S) - 1) & 1, &g_bwd_err)) {
                     ok = false;
@@ -533,11 +549,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (__all_sync(kFullMask, done)) {
             tc::fence_after_sync();
             const uint32_t base = trow + (c == 0 ? LY::DV : LY::DK);
-#pragma unroll 1
+            uint32_t uu[D / 32][32];  // the whole row behind one wait
+#pragma unroll
+            for (int b = 0; b < D / 32; ++b) tc::tmem_ld32(base + 32 * b, uu[b]);
+            tc::tmem_ld_wait();
+#pragma unroll
             for (int b = 0; b < D / 32; ++b) {
-                uint32_t u[32];
-                tc::tmem_ld32(base + 32 * b, u);
-                tc::tmem_ld_wait();
+                const uint32_t(&u)[32] = uu[b];
                 unsigned char* box = stage + b * LY::OUT_BOX + row * 128;
 #pragma unroll
                 for (int x = 0; x < 8; ++x)
@@ -657,37 +675,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (b == LY::B_S + 5) count = 128;
             mbar_init(&bars[b], count);
         }
-        *abort_flag = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) ? 1 : 0;
+        const bool abort0 = (*(volatile unsigned*)&g_bwd_err & PARALLAX_DEVERR_WAIT_TIMEOUT) != 0;
+        *abort_flag = abort0 ? 1 : 0;
         fence_mbar_init();
-    }
-    if (!RHO && (warp == 2 || warp == 3)) {
-        // no probe: the rho rows of the stacked operand are zero (R = 0)
-        for (int i = threadIdx.x - 64; i < LY::NCB * 64 * 8; i += 64) {
-            const int cb = i / 512, rem = i % 512, g = rem / 128, w = rem % 128;
-            reinterpret_cast<uint4*>(smem + LY::QR_OFF + cb * SUB + (32 * g + 16) * 128)[w] =
-                make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-    }
-    if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tmQ);
         if (RHO) tc::prefetch_tmap(&tmR);
         tc::prefetch_tmap(&tmK);
         tc::prefetch_tmap(&tmV);
         tc::prefetch_tmap(&tmO);
-    }
-    if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-    const bool skip = *abort_flag != 0;
-
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0 && !skip) {
-            bool ok = true;
-            int kj = 0, vj = 0;
+        // Q (and rho), dO and the first key tiles go out before the CTA-wide set-up (TMEM
+        // allocation and the barrier below); the producer loop continues after them
+        if (!abort0) {
             // Q (and rho) once in 16-row boxes (the stacked layout), dO once as a 64-row box
             mbar_arrive_expect_tx(q_full, (RHO ? 2 : 1) * LY::NCB * (SUB / 2) + LY::NCB * SUB64);
             for (int cb = 0; cb < LY::NCB; ++cb) {
@@ -699,7 +697,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::tma_load_3d(smem + LY::DO_OFF + cb * SUB64, &tmO, cb * 64, q0, bh, q_full);
             }
-            for (int j = 0; j < n_t && ok; ++j) {
+            for (int j = 0; j < min(n_t, KS - 1); ++j) {
+                mbar_arrive_expect_tx(&v_full[j], LY::OPB);
+                for (int cb = 0; cb < LY::NCB; ++cb)
+                    tc::tma_load_3d(smem + LY::V_OFF + j * LY::OPB + cb * SUB, &tmV, cb * 64,
+                                    j * Q_KT, bh, &v_full[j]);
+                mbar_arrive_expect_tx(&k_full[j], LY::OPB);
+                for (int cb = 0; cb < LY::NCB; ++cb)
+                    tc::tma_load_3d(smem + LY::K_OFF + j * LY::OPB + cb * SUB, &tmK, cb * 64,
+                                    j * Q_KT, bh, &k_full[j]);
+            }
+        }
+    }
+    if (!RHO && (warp == 2 || warp == 3)) {
+        // no probe: the rho rows of the stacked operand are zero (R = 0)
+        for (int i = threadIdx.x - 64; i < LY::NCB * 64 * 8; i += 64) {
+            const int cb = i / 512, rem = i % 512, g = rem / 128, w = rem % 128;
+            reinterpret_cast<uint4*>(smem + LY::QR_OFF + cb * SUB + (32 * g + 16) * 128)[w] =
+                make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort_flag != 0;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        // (Q, rho, dO and the key tiles before min(n_t, KS - 1) went out at set-up)
+        if (lane == 0 && !skip) {
+            bool ok = true;
+            int kj = min(n_t, KS - 1), vj = kj;
+            for (int j = kj; j < n_t && ok; ++j) {
                 // V first: its slot frees (S|R MMAs of tile j - VS) before K's (dQ of tile j - KS)
                 const int vs = j % VS, ks = j % KS;
                 if (j >= VS && !mbar_wait(&v_empty[vs], ((j / VS) - 1) & 1, &g_bwd_err)) {
@@ -913,11 +945,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after_sync();
             if (set == 0 || RHO) {
                 const uint32_t base = (set == 0 ? rowS : rowR) + LY::O;
-#pragma unroll 1
+                uint32_t uu[D / 64][32];  // this thread's half row behind one wait
+#pragma unroll
+                for (int b = 0; b < D / 64; ++b) tc::tmem_ld32_split<D / 2>(base + 32 * b, uu[b]);
+                tc::tmem_ld_wait();
+#pragma unroll
                 for (int b = 0; b < D / 64; ++b) {
-                    uint32_t u[32];
-                    tc::tmem_ld32_split<D / 2>(base + 32 * b, u);
-                    tc::tmem_ld_wait();
+                    const uint32_t(&u)[32] = uu[b];
                     unsigned char* box = stage + (h * (D / 64) + b) * LY::OUT_BOX + rl * 128;
 #pragma unroll
                     for (int x = 0; x < 8; ++x)

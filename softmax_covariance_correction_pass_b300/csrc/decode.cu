@@ -751,9 +751,7 @@ cudaError_t run_decode(const DecodePlan& plan, const void* q, const void* rho, c
     cudaError_t e = cudaSuccess;
     // grouped heads: the tensor-core decode (a paged cache only when every stage lies in one page)
     constexpr bool kMmaOk = sizeof(T) == 2;
-    const bool mma = kMmaOk && (G >= 2 || plan.mma) &&
-                     (!PAGED || (plan.page_size % MmaShape<D, G>::STAGE_KEYS == 0 &&
-                                 plan.chunk % MmaShape<D, G>::STAGE_KEYS == 0));
+    const bool mma = kMmaOk && decode_uses_mma(plan, true);
     if (plan.nsplit > 1) {
         if constexpr (kMmaOk) {
             if (mma) e = launch_decode_mma_kernel<D, RHO, true, G, PAGED>(a, plan.grid, stream);
@@ -803,6 +801,15 @@ cudaError_t run_decode_any(const DecodePlan& plan, const void* q, const void* rh
 }
 
 }  // namespace
+
+bool decode_uses_mma(const DecodePlan& plan, bool bf16) {
+    if (!bf16 || plan.Hkv <= 0) return false;
+    const int G = plan.H / plan.Hkv;
+    const int stage_keys = kStageRowBytes / (plan.d * 2);  // MmaShape<D, G>::STAGE_KEYS
+    const bool pages_fit = plan.page_size == 0 || (plan.page_size % stage_keys == 0 &&
+                                                   plan.chunk % stage_keys == 0);
+    return (G >= 2 || plan.mma) && pages_fit;
+}
 
 size_t decode_workspace_bytes(const DecodePlan& plan) {
     if (plan.nsplit <= 1) return 0;

@@ -25,6 +25,9 @@ struct DecodePlan {
 };
 
 size_t decode_workspace_bytes(const DecodePlan& plan);
+// Whether a decode with this plan runs the tensor-core kernel (decode_mma_kernel) rather than
+// the SIMT kernel (decode_kernel); every launch decides with this function.
+bool decode_uses_mma(const DecodePlan& plan, bool bf16);
 int decode_stage_keys(int d, int elem_bytes);
 int decode_threads();
 int decode_ctas_per_sm();  // resident decode CTAs per SM the kernel is built for

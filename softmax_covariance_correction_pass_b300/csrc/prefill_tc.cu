@@ -610,12 +610,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float gain = 1.f + At * inv_l;
                 const bool row_ok =
                     i < a.L && in_bounds(&g_tc_err, ((size_t)bh * a.L + i + 1) * D, (size_t)a.BH * a.L * D);
-#pragma unroll 1
+                // all of this thread's U and W columns behind one wait
+                uint32_t uu[D / 64][32], ww[D / 64][32];
+#pragma unroll
                 for (int b = 0; b < D / 64; ++b) {
-                    uint32_t u[32], w[32];
-                    tc::tmem_ld32_split<D / 2>(tU + 32 * b, u);
-                    tc::tmem_ld32_split<D / 2>(tW + 32 * b, w);
-                    tc::tmem_ld_wait();
+                    tc::tmem_ld32_split<D / 2>(tU + 32 * b, uu[b]);
+                    tc::tmem_ld32_split<D / 2>(tW + 32 * b, ww[b]);
+                }
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int b = 0; b < D / 64; ++b) {
+                    const uint32_t(&u)[32] = uu[b];
+                    const uint32_t(&w)[32] = ww[b];
                     // columns h D/2 + 32 b .. : 32-column box h (D/64) + b
                     unsigned char* box = stage + (h * (D / 64) + b) * LY::OUT_BOX + rl * 128;
 #pragma unroll
@@ -726,11 +732,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float inv_l = 1.f / l;
                 const bool row_ok =
                     i < a.L && in_bounds(&g_tc_err, ((size_t)bh * a.L + i + 1) * D, (size_t)a.BH * a.L * D);
-#pragma unroll 1
+                // all of this thread's U columns behind one wait
+                uint32_t uu[D / 32][32];
+#pragma unroll
+                for (int b = 0; b < D / 32; ++b) tc::tmem_ld32(tU + 32 * b, uu[b]);
+                tc::tmem_ld_wait();
+#pragma unroll
                 for (int b = 0; b < D / 32; ++b) {
-                    uint32_t u[32];
-                    tc::tmem_ld32(tU + 32 * b, u);
-                    tc::tmem_ld_wait();
+                    const uint32_t(&u)[32] = uu[b];
                     unsigned char* box = stage + b * LY::OUT_BOX + rl * 128;
 #pragma unroll
                     for (int x = 0; x < 8; ++x) {

@@ -221,6 +221,26 @@ def test_decode_plan_by_group_size(lib):
         assert ei.value.code == code, args
 
 
+def test_decode_plan_kernel(lib):
+    """Which decode kernel a bf16 shape runs (host logic, 148 SMs and 2 CTAs each without a
+    device): grouped heads always take the tensor-core kernel; one head per key/value head
+    takes it when every CTA gets at least two items of 512 keys or more."""
+    f = px.parallax_attn_decode_plan_kernel
+    assert f(64, 16, 16, 8192, 128) == "decode_mma_kernel"     # 2048 items of 4096 keys
+    assert f(2048, 16, 16, 1024, 128) == "decode_mma_kernel"   # unsplit 1024-key items
+    assert f(8, 16, 16, 8192, 128) == "decode_kernel"          # 256 items: too few
+    assert f(256, 16, 16, 128, 128) == "decode_kernel"         # 128-key items: too short
+    assert f(1, 16, 16, 32768, 128) == "decode_kernel"
+    for Hkv in (8, 4, 2):
+        assert f(8, 16, Hkv, 1024, 128) == "decode_mma_kernel"
+    # paged: the tensor-core kernel maps a stage (64 keys at d = 128, 128 at d = 64) to a page
+    assert f(512, 16, 4, 16384, 128, 256) == "decode_mma_kernel"
+    assert f(512, 16, 4, 16384, 128, 48) == "decode_kernel"
+    assert f(512, 16, 4, 16384, 64, 64) == "decode_kernel"
+    with pytest.raises(px.ParallaxError):
+        f(1, 16, 3, 128, 128)
+
+
 def test_forced_chunk_validation(lib):
     with pytest.raises(px.ParallaxError):
         px.parallax_attn_set_decode_chunk_keys(100)
