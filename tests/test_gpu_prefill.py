@@ -71,6 +71,27 @@ def test_bf16_large_probe(d):
     rel, mx = assert_bf16(_run(inp), _ref(inp, form="contracted"), "large probe")
 
 
+@pytest.mark.parametrize("kind", ["ramp", "tile_steps"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("rho", [True, False])
+def test_bf16_growing_scores(kind, causal, rho):
+    # Scores that grow along the keys, so that the running row maximum moves by more
+    # than the lazy-rescale threshold after the first key tile: "ramp" raises it inside
+    # every tile (both halves of a tile exceed the maximum so far), "tile_steps" raises
+    # it once at the start of every 128-key tile.
+    inp = configs.prefill_inputs(1, 2, 640, 128, seed=303, device=DEV, dtype=torch.bfloat16)
+    q, k = inp.q.float().clone(), inp.k.float().clone() * 0.5
+    q[..., 0] = 8.0
+    j = torch.arange(640, device=DEV, dtype=torch.float32)
+    # per key, in log2 units of the softmax: 8 * k0 * scale * log2(e)
+    k[..., 0] = 0.245 * j if kind == "ramp" else 12.0 * torch.div(j, 128, rounding_mode="floor")
+    rh = inp.rho.clone()
+    rh[..., 0] = 0  # keeps r = rho.k of ordinary size
+    inp = configs.PrefillInputs(q.bfloat16(), k.bfloat16(), inp.v, rh, inp.scale)
+    assert_bf16(_run(inp, causal, rho), _ref(inp, causal, rho, form="contracted"),
+                f"{kind} causal={causal} rho={rho}")
+
+
 def test_bf16_rho_zero_is_softmax():
     inp = configs.prefill_inputs(2, 4, 700, 128, seed=301, device=DEV, dtype=torch.bfloat16)
     inp.rho = torch.zeros_like(inp.rho)
