@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
 // ------------------------------------------------------------------------ dQ, drho
 // One 64-query tile per CTA (the forward's stacked lane layout), 128-key tiles
-// (K in a 4-deep TMA ring, V in a 2-deep one).  TMEM: Y = [S; R] (128 columns)
+// (K and V in 3-deep TMA rings).  TMEM: Y = [S; R] (128 columns)
 // and D (128 columns, in the query lanes only: an M = 64 MMA) of the current key
 // tile, the [dQ; drho] accumulator,
 // the packed dS/dR operand slot, and the stacked [Q; rho] tile itself (the A
