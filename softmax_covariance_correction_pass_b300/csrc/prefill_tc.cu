@@ -676,47 +676,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::fence_after_sync();
                 uint32_t sv[4][32];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) tc::tmem_ld32(tS + 32 * b, sv[b]);
-                tc::tmem_ld_wait();
                 const bool need_mask = CAUSAL ? k0 + BN - 1 > off + first_row : k0 + BN > Lk;
-                if (need_mask) {
-                    const int lim = CAUSAL ? off + i : Lk - 1;
+                // S of the tile into registers, masked
+                auto load_s = [&]() {
 #pragma unroll
-                    for (int b = 0; b < 4; ++b)
+                    for (int b = 0; b < 4; ++b) tc::tmem_ld32(tS + 32 * b, sv[b]);
+                    tc::tmem_ld_wait();
+                    if (need_mask) {
+                        const int lim = CAUSAL ? off + i : Lk - 1;
 #pragma unroll
-                        for (int x = 0; x < 32; ++x) {
-                            const int key = k0 + 32 * b + x;
-                            if (key > lim)
-                                sv[b][x] = __float_as_uint(-INFINITY);
-                        }
-                }
-                const float mx = max_blocks<4>(sv) * qs;
-                if (it == 0) {
-                    m = mx;
-                } else if (__any_sync(kFullMask, mx > m + kRescaleThreshold)) {
-                    const float m_new = fmaxf(m, mx);
-                    const float alpha = fast_exp2(m - m_new);
-                    l *= alpha;
-#pragma unroll 1
-                    for (int b = 0; b < D / 32; ++b) {
-                        uint32_t u[32];
-                        tc::tmem_ld32(tU + 32 * b, u);
-                        tc::tmem_ld_wait();
+                        for (int b = 0; b < 4; ++b)
 #pragma unroll
-                        for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
-                        tc::tmem_st32(tU + 32 * b, u);
+                            for (int x = 0; x < 32; ++x)
+                                if (k0 + 32 * b + x > lim) sv[b][x] = __float_as_uint(-INFINITY);
                     }
-                    m = m_new;
-                }
-                const float2 nm2 = make_float2(-m, -m);
-                float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
+                };
+                float2 ls0, ls1;
+                uint32_t pk[4][16];  // P as bf16 pairs: keys 32b.. -> packed columns 16b..
+                auto exps = [&]() {
+                    const float2 nm2 = make_float2(-m, -m);
+                    ls0 = ls1 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    uint32_t pk[16];
-                    exp_block32(sv[b], qs2, nm2, ls0, ls1, pk);
-                    tc::tmem_st16(tS + 16 * b, pk);  // packed: keys 32b.. -> columns 16b..
+                    for (int b = 0; b < 4; ++b) exp_block32(sv[b], qs2, nm2, ls0, ls1, pk[b]);
+                };
+                // the row maximum sets m (first tile) or, when it exceeds m by more than the
+                // lazy-rescale threshold, moves m and rescales U and l
+                auto max_pass = [&]() {
+                    const float mx = max_blocks<4>(sv) * qs;
+                    if (it == 0) {
+                        m = mx;
+                    } else if (__any_sync(kFullMask, mx > m + kRescaleThreshold)) {
+                        const float m_new = fmaxf(m, mx);
+                        const float alpha = fast_exp2(m - m_new);
+                        l *= alpha;
+#pragma unroll 1
+                        for (int b = 0; b < D / 32; ++b) {
+                            uint32_t u[32];
+                            tc::tmem_ld32(tU + 32 * b, u);
+                            tc::tmem_ld_wait();
+#pragma unroll
+                            for (int x = 0; x < 32; ++x) u[x] = __float_as_uint(__uint_as_float(u[x]) * alpha);
+                            tc::tmem_st32(tU + 32 * b, u);
+                        }
+                        m = m_new;
+                    }
+                };
+                load_s();
+                if (it == 0) {
+                    max_pass();
+                    exps();
+                } else {
+                    // Later tiles skip the row maximum: P is taken against the running m,
+                    // and a row whose P sums to at most 2^8 has no p above 2^8, i.e. its
+                    // maximum has not passed m by more than the lazy-rescale threshold and
+                    // these are the values the maximum would have given.  Otherwise (rare)
+                    // the maximum is formed from S, reloaded from TMEM (P is stored below).
+                    exps();
+                    const float2 lt = __fadd2_rn(ls0, ls1);
+                    if (__any_sync(kFullMask, lt.x + lt.y > 256.f)) {
+                        load_s();
+                        max_pass();
+                        exps();
+                    }
                 }
+#pragma unroll
+                for (int b = 0; b < 4; ++b) tc::tmem_st16(tS + 16 * b, pk[b]);
                 const float2 ls = __fadd2_rn(ls0, ls1);
                 l += ls.x + ls.y;
                 tc::tmem_st_wait();

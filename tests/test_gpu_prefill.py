@@ -71,20 +71,23 @@ def test_bf16_large_probe(d):
     rel, mx = assert_bf16(_run(inp), _ref(inp, form="contracted"), "large probe")
 
 
-@pytest.mark.parametrize("kind", ["ramp", "tile_steps"])
+@pytest.mark.parametrize("kind", ["ramp", "tile_steps", "small_steps"])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("rho", [True, False])
 def test_bf16_growing_scores(kind, causal, rho):
     # Scores that grow along the keys, so that the running row maximum moves by more
     # than the lazy-rescale threshold after the first key tile: "ramp" raises it inside
     # every tile (both halves of a tile exceed the maximum so far), "tile_steps" raises
-    # it once at the start of every 128-key tile.
+    # it once at the start of every 128-key tile; "small_steps" raises it by ~3 (log2
+    # units) per tile, so that a tile's weights sum to more than 2^8 while its maximum is
+    # still within the threshold of the running one (until the steps add up).
     inp = configs.prefill_inputs(1, 2, 640, 128, seed=303, device=DEV, dtype=torch.bfloat16)
     q, k = inp.q.float().clone(), inp.k.float().clone() * 0.5
     q[..., 0] = 8.0
     j = torch.arange(640, device=DEV, dtype=torch.float32)
     # per key, in log2 units of the softmax: 8 * k0 * scale * log2(e)
-    k[..., 0] = 0.245 * j if kind == "ramp" else 12.0 * torch.div(j, 128, rounding_mode="floor")
+    step = {"tile_steps": 12.0, "small_steps": 3.0}.get(kind, 0.0)
+    k[..., 0] = 0.245 * j if kind == "ramp" else step * torch.div(j, 128, rounding_mode="floor")
     rh = inp.rho.clone()
     rh[..., 0] = 0  # keeps r = rho.k of ordinary size
     inp = configs.PrefillInputs(q.bfloat16(), k.bfloat16(), inp.v, rh, inp.scale)
