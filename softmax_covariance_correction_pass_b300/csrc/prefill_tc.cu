@@ -99,12 +99,13 @@ struct PairLayout {
     static constexpr int B_SFULL = B_VEMPTY + kVStages;
     static constexpr int B_PFULL = B_SFULL + 2;
     static constexpr int B_OFULL = B_PFULL + 2;
-    static constexpr int B_STAGED = B_OFULL + 1;  // [2]: a sub-tile's output is in shared memory
-    static constexpr int NBARS = B_STAGED + 2;
+    static constexpr int NBARS = B_OFULL + 1;
     // Epilogue: once every MMA has completed, the K/V rings are free and hold each sub-tile's
-    // fp32 output as boxes of [QROWS rows x 32 columns] (128 bytes a row, 128-byte swizzle),
-    // which TMA stores write to o.
+    // fp32 output as boxes of [QROWS rows x 32 columns] (128 bytes a row, 128-byte swizzle).
+    // Each softmax warp writes its WROWS rows there and stores them with its own TMA tensor
+    // stores (boxes of [WROWS rows x 32 columns]), without waiting for the other warps.
     static constexpr int OUT_BOX = QROWS * 128;
+    static constexpr int WROWS = QROWS / 4;
     static constexpr int OUT_OFF = K_OFF;
     static_assert(2 * (D / 32) * OUT_BOX <= BAR_OFF - K_OFF, "output staging fits the rings");
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
@@ -204,7 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* s_full = bars + LY::B_SFULL;
     uint64_t* p_full = bars + LY::B_PFULL;
     uint64_t* o_full = bars + LY::B_OFULL;
-    uint64_t* staged = bars + LY::B_STAGED;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -239,8 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int k_pre = min(n1, kKStages), v_pre = min(n1, kVStages);
     if (threadIdx.x == 0) {
         for (int b = 0; b < LY::NBARS; ++b)
-            mbar_init(&bars[b], (b == LY::B_PFULL || b == LY::B_PFULL + 1 || b == LY::B_STAGED ||
-                                 b == LY::B_STAGED + 1) ? 128 : 1);
+            mbar_init(&bars[b], (b == LY::B_PFULL || b == LY::B_PFULL + 1) ? 128 : 1);
         const bool abort0 = (*(volatile unsigned*)&g_tc_err & PARALLAX_DEVERR_WAIT_TIMEOUT) != 0;
         *abort_flag = abort0 ? 1 : 0;
         fence_mbar_init();
@@ -650,15 +649,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 *abort_flag = 1;
             }
-            // every thread of the sub-tile arrives, whichever way it went; one thread then
-            // stores the sub-tile's rows (rows past L are clipped by the tensor map)
+            // this warp's rows, once all of its threads have written them (rows past L are
+            // clipped by the tensor map)
             tc::fence_proxy_async_smem();
-            mbar_arrive(&staged[sub]);
-            if (g == 0 && lane == 0 && mbar_wait(&staged[sub], 0, &g_tc_err) && !*abort_flag) {
-#pragma unroll 1
+            __syncwarp();
+            if (lane == 0 && !*abort_flag) {
                 const uint64_t pol = l2_evict_first_policy();
+#pragma unroll 1
                 for (int cb = 0; cb < D / 32; ++cb)
-                    tc::tma_store_3d_hint(&tmO, 32 * cb, first_row, bh, stage + cb * LY::OUT_BOX, pol);
+                    tc::tma_store_3d_hint(&tmO, 32 * cb, first_row + LY::WROWS * g, bh,
+                                          stage + cb * LY::OUT_BOX + LY::WROWS * g * 128, pol);
                 tc::bulk_commit_group();
                 tc::bulk_wait_group_read0();
             }
@@ -782,13 +782,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 *abort_flag = 1;
             }
+            // this warp's rows, once all of its threads have written them (rows past L are
+            // clipped by the tensor map)
             tc::fence_proxy_async_smem();
-            mbar_arrive(&staged[sub]);
-            if (g == 0 && lane == 0 && mbar_wait(&staged[sub], 0, &g_tc_err) && !*abort_flag) {
-#pragma unroll 1
+            __syncwarp();
+            if (lane == 0 && !*abort_flag) {
                 const uint64_t pol = l2_evict_first_policy();
+#pragma unroll 1
                 for (int cb = 0; cb < D / 32; ++cb)
-                    tc::tma_store_3d_hint(&tmO, 32 * cb, first_row, bh, stage + cb * LY::OUT_BOX, pol);
+                    tc::tma_store_3d_hint(&tmO, 32 * cb, first_row + LY::WROWS * g, bh,
+                                          stage + cb * LY::OUT_BOX + LY::WROWS * g * 128, pol);
                 tc::bulk_commit_group();
                 tc::bulk_wait_group_read0();
             }
@@ -834,11 +837,12 @@ cudaError_t launch_d(const PrefillShape& s, const CUtensorMap& mq, const CUtenso
     using LY = PairLayout<D, RHO>;
     const TcArgs a{o,      cache_lens, s.L,    Lcap,  s.H,  s.B * s.H, (s.L + LY::BLOCK - 1) / LY::BLOCK,
                    s.scale * kLog2e, ts.lse, ts.rbar, ts.mu};
-    // o [B*H, L, D] fp32 for the TMA stores of the epilogue: boxes of 32 columns x QROWS rows
+    // o [B*H, L, D] fp32 for the TMA stores of the epilogue: boxes of 32 columns x WROWS rows
+    // (one softmax warp's rows)
     CUtensorMap mo;
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)s.L, (uint64_t)s.B * s.H};
     const uint64_t strides[2] = {(uint64_t)D * 4, (uint64_t)s.L * D * 4};
-    const uint32_t box[3] = {32, (uint32_t)LY::QROWS, 1};
+    const uint32_t box[3] = {32, (uint32_t)LY::WROWS, 1};
     if (!make_tmap_f32(&mo, o, 3, dims, strides, box)) return cudaErrorInvalidValue;
     return s.causal ? launch<D, true, RHO>(mq, mr, mk, mv, mo, a, stream)
                     : launch<D, false, RHO>(mq, mr, mk, mv, mo, a, stream);
