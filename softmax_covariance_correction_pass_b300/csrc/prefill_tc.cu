@@ -91,7 +91,7 @@ struct PairLayout {
     static constexpr int V_OFF = K_OFF + kKStages * OP_BYTES;      // V ring
     static constexpr int BAR_OFF = V_OFF + kVStages * OP_BYTES;
     // q_full, k_full[kKStages], v_full[kVStages], k_empty[kKStages], v_empty[kVStages],
-    // s_full[2], p_full[2], o_full
+    // s_full[2], p_full[2], o_full, o_full0 (sub-tile 0's last P.V has completed)
     static constexpr int B_KFULL = 1;
     static constexpr int B_VFULL = B_KFULL + kKStages;
     static constexpr int B_KEMPTY = B_VFULL + kVStages;
@@ -99,15 +99,23 @@ struct PairLayout {
     static constexpr int B_SFULL = B_VEMPTY + kVStages;
     static constexpr int B_PFULL = B_SFULL + 2;
     static constexpr int B_OFULL = B_PFULL + 2;
-    static constexpr int NBARS = B_OFULL + 1;
-    // Epilogue: once every MMA has completed, the K/V rings are free and hold each sub-tile's
-    // fp32 output as boxes of [QROWS rows x 32 columns] (128 bytes a row, 128-byte swizzle).
-    // Each softmax warp writes its WROWS rows there and stores them with its own TMA tensor
-    // stores (boxes of [WROWS rows x 32 columns]), without waiting for the other warps.
+    static constexpr int B_OFULL0 = B_OFULL + 1;
+    static constexpr int NBARS = B_OFULL0 + 1;
+    // Epilogue: each sub-tile's fp32 output is staged as boxes of [QROWS rows x 32 columns]
+    // (128 bytes a row, 128-byte swizzle) and each softmax warp stores its WROWS rows with its
+    // own TMA tensor stores (boxes of [WROWS rows x 32 columns]), without waiting for the other
+    // warps.  With W_R = 0 a causal sub-tile 1 has one key tile more than sub-tile 0, and
+    // sub-tile 0 stages as soon as its own last P.V has completed, into the two K stages that
+    // sub-tile 1's last S does not read (n1 % 3 and (n1 + 1) % 3: their tiles were consumed by
+    // MMAs that completed before that P.V, and no load targets them any more); sub-tile 1
+    // stages into the V ring once every MMA has completed.  On the correction path, whose
+    // sub-tiles end together, both stage into the rings from K_OFF once every MMA has completed.
     static constexpr int OUT_BOX = QROWS * 128;
     static constexpr int WROWS = QROWS / 4;
-    static constexpr int OUT_OFF = K_OFF;
+    static constexpr int BOXES_PER_K_STAGE = OP_BYTES / OUT_BOX;
+    static_assert(kKStages == 3 && D / 32 <= 2 * BOXES_PER_K_STAGE, "sub-tile 0 staging fits two K stages");
     static_assert(2 * (D / 32) * OUT_BOX <= BAR_OFF - K_OFF, "output staging fits the rings");
+    static_assert((D / 32) * OUT_BOX <= kVStages * OP_BYTES, "sub-tile 1 staging fits the V ring");
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     __host__ __device__ static constexpr uint32_t dcol(int sub) { return 128u * sub; }
@@ -205,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* s_full = bars + LY::B_SFULL;
     uint64_t* p_full = bars + LY::B_PFULL;
     uint64_t* o_full = bars + LY::B_OFULL;
+    uint64_t* o_full0 = bars + LY::B_OFULL0;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + LY::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -394,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::commit(&s_full[1]);
                     tc::commit(&k_empty[0]);
                 }
+                bool o0_committed = false;
                 for (int j = 0; j < n1 && ok; ++j) {
                     const int vs = j % kVStages, ks = (j + 1) % kKStages;  // V of j, K of j + 1
                     const bool do0 = j < n0, more0 = j + 1 < n0, more1 = j + 1 < n1;
@@ -409,6 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc::fence_after_sync();
                         mma2(0, vs, j == 0);
+                        if constexpr (!RHO) {  // sub-tile 0's output may be staged early
+                            if (j + 1 == n0) {
+                                tc::commit(o_full0);
+                                o0_committed = true;
+                            }
+                        }
                     }
                     if (more1 &&
                         !mbar_wait_warp(&k_full[ks], ((j + 1) / kKStages) & 1, &g_tc_err)) {
@@ -433,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::commit(&k_empty[ks]);
                     }
                 }
+                if (!RHO && !o0_committed) tc::commit(o_full0);
                 tc::commit(o_full);
                 if (!ok) {
                     *abort_flag = 1;
@@ -600,7 +617,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- epilogue: o = U/l - (W/l - (A/l)(U/l)) = ((U (1 + A/l)) - W) / l
             const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_tc_err);
             const int rl = 16 * g + (lane & 15);  // row within the sub-tile
-            unsigned char* stage = smem + LY::OUT_OFF + sub * (D / 32) * LY::OUT_BOX;
+            // 32-column box cb of this sub-tile's staged output: the two sub-tiles have the same
+            // number of key tiles here, so both stage into the K/V rings once every MMA has
+            // completed
+            auto box_at = [&](int cb) -> unsigned char* {
+                return smem + LY::K_OFF + (sub * (D / 32) + cb) * LY::OUT_BOX;
+            };
             if (__all_sync(kFullMask, done)) {
                 tc::fence_after_sync();
                 const float lt = l + __shfl_xor_sync(kFullMask, l, 16);
@@ -622,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t(&u)[32] = uu[b];
                     const uint32_t(&w)[32] = ww[b];
                     // columns h D/2 + 32 b .. : 32-column box h (D/64) + b
-                    unsigned char* box = stage + (h * (D / 64) + b) * LY::OUT_BOX + rl * 128;
+                    unsigned char* box = box_at(h * (D / 64) + b) + rl * 128;
 #pragma unroll
                     for (int x = 0; x < 8; ++x) {
                         float out[4];
@@ -658,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                 for (int cb = 0; cb < D / 32; ++cb)
                     tc::tma_store_3d_hint(&tmO, 32 * cb, first_row + LY::WROWS * g, bh,
-                                          stage + cb * LY::OUT_BOX + LY::WROWS * g * 128, pol);
+                                          box_at(cb) + LY::WROWS * g * 128, pol);
                 tc::bulk_commit_group();
                 tc::bulk_wait_group_read0();
             }
@@ -748,9 +770,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&p_full[sub]);
             }
             // ---- epilogue: o = U / l
-            const bool done = ok && !*abort_flag && mbar_wait(o_full, 0, &g_tc_err);
+            const bool done = ok && !*abort_flag && mbar_wait(sub ? o_full : o_full0, 0, &g_tc_err);
             const int rl = 32 * g + lane;  // row within the sub-tile
-            unsigned char* stage = smem + LY::OUT_OFF + sub * (D / 32) * LY::OUT_BOX;
+            // 32-column box cb of this sub-tile's staged output
+            auto box_at = [&](int cb) -> unsigned char* {
+                return sub ? smem + LY::V_OFF + cb * LY::OUT_BOX
+                           : smem + LY::K_OFF +
+                                 ((n1 + cb / LY::BOXES_PER_K_STAGE) % kKStages) * LY::OP_BYTES +
+                                 (cb % LY::BOXES_PER_K_STAGE) * LY::OUT_BOX;
+            };
             if (__all_sync(kFullMask, done)) {
                 tc::fence_after_sync();
                 const float inv_l = 1.f / l;
@@ -764,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int b = 0; b < D / 32; ++b) {
                     const uint32_t(&u)[32] = uu[b];
-                    unsigned char* box = stage + b * LY::OUT_BOX + rl * 128;
+                    unsigned char* box = box_at(b) + rl * 128;
 #pragma unroll
                     for (int x = 0; x < 8; ++x) {
                         const float4 v4 = make_float4(
@@ -791,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                 for (int cb = 0; cb < D / 32; ++cb)
                     tc::tma_store_3d_hint(&tmO, 32 * cb, first_row + LY::WROWS * g, bh,
-                                          stage + cb * LY::OUT_BOX + LY::WROWS * g * 128, pol);
+                                          box_at(cb) + LY::WROWS * g * 128, pol);
                 tc::bulk_commit_group();
                 tc::bulk_wait_group_read0();
             }
